@@ -1,0 +1,266 @@
+"""Pins of the fp64 oracle to things other than itself (CPU only).
+
+- torch.nn.LSTMCell / GRUCell / RNNCell in float64 (independent library
+  implementations of the textbook cells), forward and autograd backward;
+- hand-worked single steps (tests/golden/hand_steps.json);
+- central finite differences of every gradient for all four cells;
+- sLSTM: the unstabilised closed form, the stabiliser invariants and the
+  shift invariance of the stabiliser;
+- sequence-level invariants (chunked continuation, batch permutation, T=0).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_steps.json")
+FNS = ["lstm", "gru", "elman", "slstm"]
+
+
+def rand_problem(fn, B, T, N, D, seed, rscale=1.0):
+    rng = np.random.default_rng(seed)
+    G, S = oracle.GATES[fn], oracle.STATES[fn]
+    Wx = rng.normal(size=(B, T, G, N, D))
+    R = rng.normal(size=(G, N, D, D)) * rscale / math.sqrt(D)
+    b = rng.normal(size=(G, N, D))
+    s0 = rng.normal(size=(S, B, 1, N, D))
+    if fn == "slstm":
+        s0[2] = np.abs(s0[2]) + 0.5  # normaliser must be positive
+        s0[3] = rng.normal(size=s0[3].shape) * 0.5
+    return Wx, R, b, s0
+
+
+# ---------------------------------------------------------------- golden steps
+@pytest.mark.parametrize("case", json.load(open(GOLDEN))["cases"], ids=lambda c: c["name"])
+def test_hand_steps(case):
+    fn, D = case["fn"], case["D"]
+    G, S = oracle.GATES[fn], oracle.STATES[fn]
+    Wx = np.array(case["Wx"], dtype=np.float64).reshape(1, 1, G, 1, D)
+    R = np.array(case["R"], dtype=np.float64).reshape(G, 1, D, D)
+    b = np.array(case["b"], dtype=np.float64).reshape(G, 1, D)
+    s0 = np.array(case["s0"], dtype=np.float64).reshape(S, 1, 1, 1, D)
+    states, last = oracle.fwd(fn, Wx, R, b, s0)
+    exp = np.array(case["expect"], dtype=np.float64).reshape(S, D)
+    np.testing.assert_allclose(states[:, 0, 0, 0, :], exp, rtol=1e-14, atol=1e-15)
+    np.testing.assert_array_equal(last[:, 0, 0], states[:, 0, -1])
+
+
+# ------------------------------------------------------------ torch.nn cells
+def _torch_cell(fn, D, G, R, b, n):
+    kw = dict(dtype=torch.float64)
+    if fn == "lstm":
+        cell = torch.nn.LSTMCell(G * D, D, **kw)
+    elif fn == "gru":
+        cell = torch.nn.GRUCell(G * D, D, **kw)
+    else:
+        cell = torch.nn.RNNCell(G * D, D, nonlinearity="tanh", **kw)
+    with torch.no_grad():
+        cell.weight_ih.copy_(torch.eye(G * D, dtype=torch.float64))
+        cell.bias_ih.zero_()
+        # torch computes W_hh @ h; row (g, j), column i  <->  R[g, n, i, j]
+        cell.weight_hh.copy_(torch.from_numpy(R[:, n].transpose(0, 2, 1).reshape(G * D, D)))
+        cell.bias_hh.copy_(torch.from_numpy(b[:, n].reshape(G * D)))
+    return cell
+
+
+@pytest.mark.parametrize("fn", ["lstm", "gru", "elman"])
+@pytest.mark.parametrize("shape", [(3, 5, 2, 4), (2, 7, 1, 5)])
+def test_against_torch_cells(fn, shape):
+    B, T, N, D = shape
+    G, S = oracle.GATES[fn], oracle.STATES[fn]
+    Wx, R, b, s0 = rand_problem(fn, B, T, N, D, seed=11 + D, rscale=1.5)
+    rng = np.random.default_rng(5)
+    dst = rng.normal(size=(S, B, T, N, D))
+    dl = rng.normal(size=(S, B, 1, N, D))
+    states, last = oracle.fwd(fn, Wx, R, b, s0)
+    dWx, dR, db, ds0 = oracle.bwd(fn, Wx, R, b, s0, dst, dl)
+
+    for n in range(N):
+        cell = _torch_cell(fn, D, G, R, b, n)
+        x = torch.from_numpy(Wx[:, :, :, n, :].reshape(B, T, G * D).copy()).requires_grad_(True)
+        h = torch.from_numpy(s0[0, :, 0, n, :].copy()).requires_grad_(True)
+        c0 = c = torch.from_numpy(s0[1, :, 0, n, :].copy()).requires_grad_(True) if fn == "lstm" else None
+        h0 = h
+        outs_h, outs_c = [], []
+        for t in range(T):
+            if fn == "lstm":
+                h, c = cell(x[:, t], (h, c))
+                outs_c.append(c)
+            else:
+                h = cell(x[:, t], h)
+            outs_h.append(h)
+        Hs = torch.stack(outs_h, 1)  # [B,T,D]
+        np.testing.assert_allclose(states[0, :, :, n, :], Hs.detach().numpy(), rtol=1e-12, atol=1e-13)
+        loss = (Hs * torch.from_numpy(dst[0, :, :, n, :])).sum() + (h * torch.from_numpy(dl[0, :, 0, n, :])).sum()
+        if fn == "lstm":
+            Cs = torch.stack(outs_c, 1)
+            np.testing.assert_allclose(states[1, :, :, n, :], Cs.detach().numpy(), rtol=1e-12, atol=1e-13)
+            loss = loss + (Cs * torch.from_numpy(dst[1, :, :, n, :])).sum() + (c * torch.from_numpy(dl[1, :, 0, n, :])).sum()
+        loss.backward()
+        np.testing.assert_allclose(dWx[:, :, :, n, :].reshape(B, T, G * D), x.grad.numpy(), rtol=1e-10, atol=1e-12)
+        tdR = cell.weight_hh.grad.numpy().reshape(G, D, D).transpose(0, 2, 1)
+        np.testing.assert_allclose(dR[:, n], tdR, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(db[:, n], cell.bias_hh.grad.numpy().reshape(G, D), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(ds0[0, :, 0, n, :], h0.grad.numpy(), rtol=1e-10, atol=1e-12)
+        if fn == "lstm":
+            np.testing.assert_allclose(ds0[1, :, 0, n, :], c0.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+# ------------------------------------------------------- finite differences
+def _loss(fn, Wx, R, b, s0, W1, W2):
+    st, last = oracle.fwd(fn, Wx, R, b, s0)
+    return float((st * W1).sum() + (last * W2).sum())
+
+
+@pytest.mark.parametrize("fn", FNS)
+def test_finite_differences(fn):
+    B, T, N, D = 2, 4, 2, 3
+    Wx, R, b, s0 = rand_problem(fn, B, T, N, D, seed=3, rscale=1.2)
+    rng = np.random.default_rng(9)
+    S = oracle.STATES[fn]
+    W1 = rng.normal(size=(S, B, T, N, D))
+    W2 = rng.normal(size=(S, B, 1, N, D))
+    grads = oracle.bwd(fn, Wx, R, b, s0, W1, W2)
+    eps = 1e-6
+    for name, arr, g in zip(["Wx", "R", "b", "s0"], [Wx, R, b, s0], grads):
+        fd = np.zeros_like(arr)
+        flat, fflat = arr.reshape(-1), fd.reshape(-1)
+        for k in range(flat.size):
+            keep = flat[k]
+            flat[k] = keep + eps
+            lp = _loss(fn, Wx, R, b, s0, W1, W2)
+            flat[k] = keep - eps
+            lm = _loss(fn, Wx, R, b, s0, W1, W2)
+            flat[k] = keep
+            fflat[k] = (lp - lm) / (2 * eps)
+        scale = max(1.0, np.abs(fd).max())
+        np.testing.assert_allclose(g, fd, rtol=0, atol=2e-7 * scale, err_msg=f"{fn} d{name}")
+
+
+# ------------------------------------------------------------------- sLSTM
+def _preacts(Wx, R, b, h_prev):
+    """a[b,t,g,n,j] = Wx + h_{t-1} . R[g,n] + b, via numpy einsum."""
+    return Wx + np.einsum("btni,gnij->btgnj", h_prev, R) + b[None, None]
+
+
+def test_slstm_unstabilised_closed_form():
+    """Stabilised states times exp(m) equal the plain exponential-gating
+    recurrence c~ = e^{a_f} c~ + e^{a_i} tanh(a_z), n~ likewise; h = sig(a_o) c~/n~."""
+    B, T, N, D = 2, 12, 2, 3
+    Wx, R, b, s0 = rand_problem("slstm", B, T, N, D, seed=21)
+    st, _ = oracle.fwd("slstm", Wx, R, b, s0)
+    h_prev = np.concatenate([s0[0], st[0, :, :-1]], axis=1)
+    a = _preacts(Wx, R, b, h_prev)
+    ct = s0[1, :, 0] * np.exp(s0[3, :, 0])
+    nt = s0[2, :, 0] * np.exp(s0[3, :, 0])
+    for t in range(T):
+        ai, af, az, ao = (a[:, t, g] for g in range(4))
+        ct = np.exp(af) * ct + np.exp(ai) * np.tanh(az)
+        nt = np.exp(af) * nt + np.exp(ai)
+        h = ct / nt / (1 + np.exp(-ao))
+        np.testing.assert_allclose(st[0, :, t], h, rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(st[1, :, t] * np.exp(st[3, :, t]), ct, rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(st[2, :, t] * np.exp(st[3, :, t]), nt, rtol=1e-11, atol=1e-13)
+
+
+def test_slstm_stabiliser_invariants():
+    B, T, N, D = 3, 40, 2, 4
+    Wx, R, b, s0 = rand_problem("slstm", B, T, N, D, seed=8, rscale=2.0)
+    Wx *= 3.0  # large gate values: the unstabilised form would overflow soon
+    s0[2] = 1.0
+    s0[3] = 0.0
+    st, _ = oracle.fwd("slstm", Wx, R, b, s0)
+    assert np.all(np.isfinite(st))
+    h_prev = np.concatenate([s0[0], st[0, :, :-1]], axis=1)
+    m_prev = np.concatenate([s0[3], st[3, :, :-1]], axis=1)
+    a = _preacts(Wx, R, b, h_prev)
+    ig = np.exp(a[:, :, 0] - st[3])
+    fg = np.exp(a[:, :, 1] + m_prev - st[3])
+    # a is recomputed here in another summation order: allow rounding only
+    assert np.all(ig <= 1.0 + 1e-12) and np.all(fg <= 1.0 + 1e-12)
+    np.testing.assert_allclose(np.maximum(ig, fg), 1.0, rtol=0, atol=1e-12)
+    assert np.all(st[2] >= 1.0 - 1e-12)  # n_t >= 1 when n_0 = 1
+    # |c/n| <= max(|c0/n0|, 1): c/n is a convex combination of c0/n0 and tanh values
+    bound = np.maximum(np.abs(s0[1] / s0[2]), 1.0)
+    assert np.all(np.abs(st[1] / st[2]) <= bound + 1e-12)
+
+
+def test_slstm_shift_invariance():
+    B, T, N, D = 2, 10, 1, 3
+    Wx, R, b, s0 = rand_problem("slstm", B, T, N, D, seed=13)
+    st, _ = oracle.fwd("slstm", Wx, R, b, s0)
+    k = 0.7
+    s1 = s0.copy()
+    s1[3] += k
+    s1[1] *= math.exp(-k)
+    s1[2] *= math.exp(-k)
+    st2, _ = oracle.fwd("slstm", Wx, R, b, s1)
+    np.testing.assert_allclose(st2[0], st[0], rtol=1e-12, atol=1e-13)
+
+
+# --------------------------------------------------------------- sequences
+def test_lstm_gru_elman_bounds():
+    for fn in ["lstm", "elman", "gru"]:
+        Wx, R, b, s0 = rand_problem(fn, 2, 30, 2, 4, seed=2, rscale=2.0)
+        s0[0] = np.clip(s0[0], -0.99, 0.99)
+        st, _ = oracle.fwd(fn, Wx * 3, R, b, s0)
+        if fn in ("lstm", "elman"):
+            assert np.all(np.abs(st[0]) < 1.0)
+        if fn == "gru":
+            assert np.all(np.abs(st[0]) <= np.maximum(np.abs(s0[0]).max(), 1.0) + 1e-12)
+        if fn == "lstm":
+            t = np.arange(1, 31)[None, :, None, None]
+            assert np.all(np.abs(st[1]) <= np.abs(s0[1]) + t + 1e-12)
+
+
+@pytest.mark.parametrize("fn", FNS)
+def test_chunked_continuation(fn):
+    B, T, N, D = 2, 9, 2, 3
+    Wx, R, b, s0 = rand_problem(fn, B, T, N, D, seed=4)
+    st, last = oracle.fwd(fn, Wx, R, b, s0)
+    st1, l1 = oracle.fwd(fn, Wx[:, :4], R, b, s0)
+    st2, l2 = oracle.fwd(fn, Wx[:, 4:], R, b, l1)
+    np.testing.assert_allclose(np.concatenate([st1, st2], axis=2), st, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(l2, last, rtol=1e-13, atol=1e-14)
+
+
+@pytest.mark.parametrize("fn", FNS)
+def test_batch_permutation(fn):
+    B, T, N, D = 4, 5, 2, 3
+    Wx, R, b, s0 = rand_problem(fn, B, T, N, D, seed=6)
+    perm = np.array([2, 0, 3, 1])
+    st, _ = oracle.fwd(fn, Wx, R, b, s0)
+    stp, _ = oracle.fwd(fn, Wx[perm], R, b, s0[:, perm])
+    np.testing.assert_allclose(stp, st[:, perm], rtol=1e-14, atol=0)
+
+
+@pytest.mark.parametrize("fn", FNS)
+def test_zero_length_and_zero_initial(fn):
+    G, S = oracle.GATES[fn], oracle.STATES[fn]
+    Wx, R, b, s0 = rand_problem(fn, 2, 0, 1, 3, seed=1)
+    st, last = oracle.fwd(fn, Wx, R, b, s0)
+    assert st.shape == (S, 2, 0, 1, 3)
+    np.testing.assert_array_equal(last, s0)
+    dl = np.random.default_rng(0).normal(size=s0.shape)
+    dWx, dR, db, ds0 = oracle.bwd(fn, Wx, R, b, s0, None, dl)
+    np.testing.assert_array_equal(ds0, dl)
+    assert not dR.any() and not db.any()
+    # states0 = None means zeros
+    Wx, R, b, _ = rand_problem(fn, 2, 3, 1, 3, seed=1)
+    a, _ = oracle.fwd(fn, Wx, R, b, None)
+    z, _ = oracle.fwd(fn, Wx, R, b, np.zeros((S, 2, 1, 1, 3)))
+    np.testing.assert_array_equal(a, z)
+
+
+def test_threads_do_not_change_results():
+    Wx, R, b, s0 = rand_problem("lstm", 3, 6, 2, 4, seed=31)
+    d = np.random.default_rng(1).normal(size=(2, 3, 6, 2, 4))
+    a = oracle.bwd("lstm", Wx, R, b, s0, d, nthreads=1)
+    c = oracle.bwd("lstm", Wx, R, b, s0, d, nthreads=4)
+    for x, y in zip(a, c):
+        np.testing.assert_allclose(x, y, rtol=1e-13, atol=1e-14)
