@@ -1,0 +1,371 @@
+#!/usr/bin/env python
+"""Benchmark of the head-wise recurrent scan on one GB300 (or N replicas).
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+the forward scan (writing states and the backward's tape) followed by the
+backward through time (reverse scan, dWx, dstates0, and the dR / db
+reduction). Default workload: LSTM, bf16 storage / fp32 arithmetic, B=8,
+T=1024, N=3 heads, D=256 (the FlashRNN announcement's usage example).
+
+Prints ONE JSON line (rank 0). value = timesteps*batch per second of the
+forward + backward step, summed over all ranks (weak scaling: every rank runs
+the full workload). --impl reference times the fp64 CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "timesteps·batch/s fwd and fwd+bwd; % of per-step roofline (1 GB300)"
+UNIT = "timesteps*batch/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--function", default=None, help="override the workload's cell (workload 3: gru|elman)")
+    ap.add_argument("--path", default="auto", choices=["auto", "fused", "alternating", "simt"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d.get("bf16_tflops_sustained"),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+def algorithmic(w, fn, esize):
+    """Algorithmic work of one step per (b, n, t): forward F = 2 G D^2 flops,
+    (G + S) D e bytes (Wx read, states written); backward F = 4 G D^2,
+    (2S + 2G) D e bytes (dstates, states, gates read; dWx written)."""
+    from recurrent_networks_gb300.synth import GATES, STATES
+    G, S, D = GATES[fn], STATES[fn], w["D"]
+    units = w["B"] * w["T"] * w["N"]
+    return dict(units=units,
+                fwd_flops=2.0 * G * D * D * units, fwd_bytes=float((G + S) * D * esize * units),
+                bwd_flops=4.0 * G * D * D * units, bwd_bytes=float((2 * S + 2 * G) * D * esize * units))
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9 and parts[1].isdigit():
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [int(r[1]) for r in rows]
+        smax = max(int(r[2]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ oracle
+def cpu_oracle_step(fn, inp, nthreads, sample_b):
+    """One forward + backward of the oracle over the first sample_b batch rows."""
+    from oracle import oracle
+    sub = {k: (v[:sample_b] if k == "Wx" else v) for k, v in inp.items()}
+    sub["states0"] = inp["states0"][:, :sample_b]
+    sub["dstates"] = inp["dstates"][:, :sample_b] if inp["dstates"] is not None else None
+    t0 = time.perf_counter()
+    oracle.fwd(fn, sub["Wx"], sub["R"], sub["b"], sub["states0"], nthreads=nthreads)
+    oracle.bwd(fn, sub["Wx"], sub["R"], sub["b"], sub["states0"], sub["dstates"], nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def oracle_sample_rows(w, fn):
+    """Batch rows timed so that one oracle step takes ~10-30 s of CPU work."""
+    from recurrent_networks_gb300.synth import GATES
+    G, D, T, N = GATES[fn], w["D"], w["T"], w["N"]
+    flops_per_row = 3 * 2.0 * G * D * D * T * N  # fwd + ~2x for bwd, fp64 loops
+    budget = 20e9 * 1.0  # ~1 GFLOP/s per core x 20 core-seconds
+    return max(1, min(w["B"], int(budget // flops_per_row) or 1))
+
+
+def run_reference(args, w, fn):
+    from recurrent_networks_gb300.synth import workload_inputs
+    cores = host_cores()
+    inp = workload_inputs(args.workload, function=fn, with_grads=True)
+    rows = oracle_sample_rows(w, fn)
+    times = []
+    for k in range(args.warmup + args.steps):
+        dt = cpu_oracle_step(fn, inp, cores, rows)
+        if k >= args.warmup:
+            times.append(dt)
+    per_step = sum(times) / len(times)
+    value = rows * w["T"] / per_step
+    sample = f"{fn} fwd+bwd over {rows} of {w['B']} batch rows, all T={w['T']}, N={w['N']}, D={w['D']}, fp64"
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w["name"], "function": fn},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------ ours
+def main():
+    args = parse()
+    from recurrent_networks_gb300.synth import WORKLOADS
+    w = WORKLOADS[args.workload]
+    fn = args.function or w["fns"][0]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, w, fn)), flush=True)
+        return
+
+    import torch.distributed as dist
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+
+    from recurrent_networks_gb300 import _lib
+    from recurrent_networks_gb300.synth import workload_inputs
+    _lib.load()
+    dtype = w["dtype"]
+    esize = 2 if dtype == torch.bfloat16 else 4
+    B, T, N, D = w["B"], w["T"], w["N"], w["D"]
+    backward = w["backward"]
+    host = workload_inputs(args.workload, function=fn, with_grads=backward)
+    inp = {k: (v.to(dev) if v is not None else None) for k, v in host.items()}
+    S = _lib.rnn_num_states(fn)
+    dims = _lib.make_dims(B, T, N, D, fn, dtype, args.path)
+    _, plan_f = _lib.rnn_plan_describe(dims, False)
+    _, plan_b = _lib.rnn_plan_describe(dims, True)
+    states = torch.empty((S, B, T, N, D), dtype=dtype, device=dev)
+    last = torch.empty((S, B, 1, N, D), dtype=dtype, device=dev)
+    tape = torch.empty(_lib.rnn_tape_size(dims), dtype=torch.uint8, device=dev) if backward else None
+    ws = torch.empty(_lib.rnn_workspace_size(dims, _lib.WS_BWD if backward else _lib.WS_FWD),
+                     dtype=torch.uint8, device=dev)
+    if backward:
+        dWx, dR, db, ds0 = (torch.empty_like(inp[k]) for k in ("Wx", "R", "b", "states0"))
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        _lib.rnn_fwd(dims, inp["Wx"], inp["R"], inp["b"], inp["states0"], states, last, tape, ws)
+        if backward:
+            _lib.rnn_bwd(dims, inp["Wx"], inp["R"], inp["b"], inp["states0"], states, tape, inp["dstates"],
+                         None, dWx, dR, db, ds0, ws)
+
+    ev = {k: torch.cuda.Event(enable_timing=True) for k in ("f0", "f1", "b0", "b1")}
+    for e in ev.values():
+        e.record()  # creates the underlying cudaEvent_t
+    _lib.rnn_profile_events(0, ev["f0"], ev["f1"])
+    if backward:
+        _lib.rnn_profile_events(1, ev["b0"], ev["b1"])
+
+    for _ in range(args.warmup):
+        step()
+    _lib.rnn_check_status(ws)
+    torch.cuda.synchronize()
+
+    # timed region: per-step events; L2 flushed before every step, outside the event window
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    fscan, bscan = [], []
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = _lib.rnn_kernel_launches()
+    with ClockSampler(dev.index) as clk:
+        for k in range(args.steps):
+            flush.zero_()
+            starts[k].record()
+            _lib.rnn_fwd(dims, inp["Wx"], inp["R"], inp["b"], inp["states0"], states, last, tape, ws)
+            mids[k].record()
+            if backward:
+                _lib.rnn_bwd(dims, inp["Wx"], inp["R"], inp["b"], inp["states0"], states, tape, inp["dstates"],
+                             None, dWx, dR, db, ds0, ws)
+            ends[k].record()
+            # the scan-kernel events are re-recorded every step: read them now
+            ends[k].synchronize()
+            fscan.append(ev["f0"].elapsed_time(ev["f1"]))
+            if backward:
+                bscan.append(ev["b0"].elapsed_time(ev["b1"]))
+        torch.cuda.synchronize()
+    launches = _lib.rnn_kernel_launches() - launches0
+    if world > 1:
+        dist.barrier()
+    _lib.rnn_check_status(ws)
+    _lib.rnn_profile_events(0, None, None)
+    _lib.rnn_profile_events(1, None, None)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    fwd_ms = [s.elapsed_time(m) for s, m in zip(starts, mids)]
+    tot_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([tot_ms, sum(fwd_ms)], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms, fwd_tot = float(t[0]), float(t[1])
+    else:
+        fwd_tot = sum(fwd_ms)
+    ms_per_step = tot_ms / args.steps
+    value = world * B * T / (ms_per_step / 1e3)
+    fwd_value = world * B * T / (fwd_tot / args.steps / 1e3)
+
+    pk = peaks()
+    alg = algorithmic(w, fn, esize)
+    f_ms = statistics.mean(fscan)
+    b_ms = statistics.mean(bscan) if bscan else 0.0
+    # per-step roofline of the method (max of tensor time and HBM time), per the metric
+    roof_f = max(alg["fwd_flops"] / (pk["bf16"] * 1e12), alg["fwd_bytes"] / (pk["hbm"] * 1e9))
+    roof_b = max(alg["bwd_flops"] / (pk["bf16"] * 1e12), alg["bwd_bytes"] / (pk["hbm"] * 1e9)) if backward else 0
+    dom_bwd = backward and b_ms > f_ms
+    kms = b_ms if dom_bwd else f_ms
+    kbytes = alg["bwd_bytes"] if dom_bwd else alg["fwd_bytes"]
+    kflops = alg["bwd_flops"] if dom_bwd else alg["fwd_flops"]
+    hbm_bound = kbytes / (pk["hbm"] * 1e9) >= kflops / (pk["bf16"] * 1e12)
+    if hbm_bound:
+        achieved = kbytes / (kms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                "frac": achieved / pk["hbm"], "traffic": None}
+    else:
+        achieved = kflops / (kms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16"], "traffic": None}
+    roof.update({"kernel": "bwd_scan" if dom_bwd else "fwd_scan", "kernel_ms": kms,
+                 "peak_source": f"{pk['source']} (MEASURED_PEAKS.json, burst)" if pk["source"] == "measured"
+                 else "fallback"})
+
+    result = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+              "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+              "vs_baseline": None, "dtype": "bf16" if dtype == torch.bfloat16 else "f32",
+              "data": "synthetic",
+              "config": {"workload": w["name"], "function": fn, "B": B, "T": T, "N": N, "D": D,
+                         "backward": backward, "plan_fwd": plan_f, "plan_bwd": plan_b,
+                         "l2": "flushed (256 MiB write) before every step, outside the event window",
+                         "parallelism": f"replicas x{world}"},
+              "fwd_value": fwd_value, "fwd_ms": fwd_tot / args.steps,
+              "scan_ms": {"fwd": f_ms, "bwd": b_ms},
+              "per_step_roofline": {"fwd_ns": roof_f / T * 1e9, "fwd_frac": roof_f / (f_ms / 1e3),
+                                    "bwd_ns": roof_b / T * 1e9,
+                                    "bwd_frac": (roof_b / (b_ms / 1e3)) if backward else None,
+                                    "step_frac": (roof_f + roof_b) / (ms_per_step / 1e3)},
+              "step_latency_ns": {"fwd": f_ms * 1e6 / T, "bwd": (b_ms * 1e6 / T) if backward else None},
+              "roofline": roof, "gpu_launches": launches}
+    result["clocks"] = clk.summary()
+
+    # ---- e2e through the C ABI with host buffers (pinned), copies inside the window
+    if not args.no_e2e:
+        hin = {k: v.pin_memory() for k, v in host.items() if v is not None}
+        outs = [states, last] + ([dWx, dR, db, ds0] if backward else [])
+        hout = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+        h2d = sum(v.numel() * v.element_size() for v in hin.values())
+        d2h = sum(o.numel() * o.element_size() for o in outs)
+        dev_in = {k: torch.empty_like(v, device=dev) for k, v in hin.items()}
+
+        def e2e_step():
+            for k, v in hin.items():
+                dev_in[k].copy_(v, non_blocking=True)
+            _lib.rnn_fwd(dims, dev_in["Wx"], dev_in["R"], dev_in["b"], dev_in["states0"], states, last, tape, ws)
+            if backward:
+                _lib.rnn_bwd(dims, dev_in["Wx"], dev_in["R"], dev_in["b"], dev_in["states0"], states, tape,
+                             dev_in["dstates"], None, dWx, dR, db, ds0, ws)
+            for o, h in zip(outs, hout):
+                h.copy_(o, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / args.steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t[0])
+        result["e2e"] = {"value": world * B * T / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                         "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    # ---- the oracle on the host cores (rank 0, N=1 only), bounded sample
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and backward:
+        cores = host_cores()
+        rows = oracle_sample_rows(w, fn)
+        dt = cpu_oracle_step(fn, host, cores, rows)
+        result["cpu_baseline"] = {"value": rows * T / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                  "sample": f"{fn} fwd+bwd, {rows} of {B} batch rows, all T={T}, N={N}, "
+                                            f"D={D}, fp64, {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

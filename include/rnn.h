@@ -1,0 +1,146 @@
+/*
+ * rnn.h: C ABI of the GB300 head-wise recurrent scan library (librnn_gb300.so).
+ *
+ * The operation is the one the FlashRNN announcement (hottg.com/neural/9889,
+ * "FlashRNN: optimising RNNs on modern hardware", usage example) exposes as
+ *     states, last_states = flashrnn(Wx, R, b, states=states_initial, function=...)
+ * with Wx[B,T,G,N,D], R[G,N,D,D], b[G,N,D], states_initial[S,B,1,N,D] and the
+ * result states[S,B,T,N,D]: N independent heads of size D; per step t and head n
+ *     rec_g = h_{t-1} . R[g,n] + b[g,n]      (row vector h, D x D block, g < G)
+ *     a_g   = Wx[b,t,g,n,:] + rec_g           (GRU: a_n = Wx_n + r * rec_n)
+ * then the pointwise update of the chosen cell. The LSTM cell (gates i,f,g,o;
+ * c = f c + i g; h = o tanh c) and the row-vector orientation are those of
+ * developnotes "deep learning operators", section 5.3 LSTM (MyLSTM.forward).
+ * GRU (gates r,z,n; h' = (1-z) n + z h), Elman (h' = tanh a) and sLSTM (gates
+ * i,f,z,o; states h,c,n,m; exponential gating with stabiliser m) follow the
+ * readings documented in the repository's design notes.
+ *
+ * Conventions shared by every call
+ *  - All tensor pointers are DEVICE pointers to dense, contiguous, row-major
+ *    arrays in the order given, 16-byte aligned, of element type `dtype`
+ *    (RNN_BF16: bfloat16 storage with fp32 arithmetic and fp32 carried c,n,m;
+ *    RNN_F32: float32 throughout). The caller owns and allocates all memory;
+ *    the library allocates nothing and never synchronises the stream except
+ *    in rnn_check_status. Every call is asynchronous on `stream`
+ *    (a cudaStream_t; NULL = legacy default stream).
+ *  - Return value: RNN_OK (0) or a status below. Host-side validation errors
+ *    are returned before anything is enqueued. Device-side errors (a bounded
+ *    wait that ran out) are recorded in the workspace and reported by
+ *    rnn_check_status.
+ *  - B = 0 is an error (RNN_EINVAL). T = 0 is not: the last states equal the
+ *    initial states and the backward passes dlast through to dstates0.
+ */
+#ifndef RNN_GB300_H
+#define RNN_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes -------------------------------------------------------- */
+#define RNN_OK 0
+#define RNN_EINVAL 1      /* bad dimensions, NULL required pointer, misalignment */
+#define RNN_EUNSUPPORTED 2 /* no feasible kernel plan for the requested path */
+#define RNN_ENOSPC 3      /* workspace smaller than rnn_workspace_size() */
+#define RNN_ETIMEOUT 4    /* a device-side wait gave up (reported by rnn_check_status) */
+#define RNN_ECUDA 5       /* a CUDA runtime call or launch failed */
+
+/* ---- enumerations ---------------------------------------------------------- */
+typedef enum { RNN_LSTM = 0, RNN_GRU = 1, RNN_ELMAN = 2, RNN_SLSTM = 3 } rnn_function_t;
+/* (G, S) = (4, 2) LSTM, (3, 1) GRU, (1, 1) Elman, (4, 4) sLSTM.
+ * State order: LSTM h,c; GRU h; Elman h; sLSTM h,c,n,m. */
+typedef enum { RNN_F32 = 0, RNN_BF16 = 1 } rnn_dtype_t;
+typedef enum {
+  RNN_PATH_AUTO = 0,        /* the planner picks */
+  RNN_PATH_FUSED = 1,       /* persistent thread-block-cluster kernel, R resident on chip */
+  RNN_PATH_ALTERNATING = 2, /* persistent grid kernel for R too large for one cluster */
+  RNN_PATH_SIMT = 3         /* plain per-head kernel, any size; the fp32 path */
+} rnn_path_t;
+
+typedef struct {
+  int B, T, N, D;
+  int function; /* rnn_function_t */
+  int dtype;    /* rnn_dtype_t */
+  int path;     /* rnn_path_t */
+} rnn_dims_t;
+
+/* Workspace kinds for rnn_workspace_size. */
+#define RNN_WS_FWD 0          /* rnn_fwd */
+#define RNN_WS_BWD 1          /* rnn_bwd given the forward's tape */
+#define RNN_WS_BWD_RECOMPUTE 2 /* rnn_bwd with tape == NULL (re-runs the forward) */
+
+int rnn_num_gates(int function);  /* G, or -1 for an unknown function */
+int rnn_num_states(int function); /* S, or -1 */
+
+/* Bytes of the forward tape (fp32 gate pre-activations and carried states of
+ * every step, [T][B][N][K][D] floats) that rnn_bwd reads; 0 for invalid dims. */
+size_t rnn_tape_size(const rnn_dims_t *dims);
+
+/* Bytes of scratch the call of the given kind needs (a multiple of 256;
+ * at least 256). 0 for invalid dims. */
+size_t rnn_workspace_size(const rnn_dims_t *dims, int kind);
+
+/*
+ * Forward scan (FlashRNN announcement, usage example: the flashrnn call).
+ *   Wx      [B,T,G,N,D]  input pre-activations                         (in)
+ *   R       [G,N,D,D]    recurrent blocks, R[g,n,i,j], i = input unit    (in)
+ *   b       [G,N,D]      bias                                           (in)
+ *   states0 [S,B,1,N,D]  initial states, or NULL = all zeros            (in)
+ *   states  [S,B,T,N,D]  state after every step (initial state excluded)(out)
+ *   last    [S,B,1,N,D]  state after the last step, or NULL             (out)
+ *   tape    rnn_tape_size() bytes, or NULL; written for rnn_bwd         (out)
+ *   workspace / ws_bytes: at least rnn_workspace_size(dims, RNN_WS_FWD)
+ * Errors: RNN_EINVAL, RNN_EUNSUPPORTED, RNN_ENOSPC, RNN_ECUDA.
+ */
+int rnn_fwd(const rnn_dims_t *dims, const void *Wx, const void *R, const void *b,
+            const void *states0, void *states, void *last, void *tape,
+            void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Backward through time of rnn_fwd (the gradient of sum(states*dstates) +
+ * sum(last*dlast) with respect to every input).
+ *   Wx, R, b, states0  the forward's inputs (states0 may be NULL = zeros)
+ *   states             the forward's output [S,B,T,N,D]
+ *   tape               the tape rnn_fwd wrote for these inputs, or NULL to have
+ *                      it rebuilt inside the workspace (one extra forward)
+ *   dstates [S,B,T,N,D] upstream gradient, or NULL = zero
+ *   dlast   [S,B,1,N,D] upstream gradient of `last`, or NULL = zero
+ *   dWx [B,T,G,N,D], dR [G,N,D,D], db [G,N,D], dstates0 [S,B,1,N,D]: outputs,
+ *                      each may be NULL when not wanted
+ *   workspace / ws_bytes: at least rnn_workspace_size(dims, RNN_WS_BWD) with a
+ *                      tape, RNN_WS_BWD_RECOMPUTE without
+ * Errors: as rnn_fwd.
+ */
+int rnn_bwd(const rnn_dims_t *dims, const void *Wx, const void *R, const void *b,
+            const void *states0, const void *states, const void *tape,
+            const void *dstates, const void *dlast, void *dWx, void *dR, void *db,
+            void *dstates0, void *workspace, size_t ws_bytes, void *stream);
+
+/* Synchronises `stream`, reads and clears the device status word that kernels
+ * running on `workspace` recorded. Returns RNN_OK, RNN_ETIMEOUT or RNN_ECUDA. */
+int rnn_check_status(void *workspace, void *stream);
+
+/* Writes a one-line description of the plan chosen for dims (path, cluster
+ * size, tiles) or the reason none fits into buf (NUL-terminated, truncated to
+ * len). Returns RNN_OK, RNN_EINVAL or RNN_EUNSUPPORTED. */
+int rnn_plan_describe(const rnn_dims_t *dims, int for_backward, char *buf, size_t len);
+
+const char *rnn_strerror(int status);
+
+/* Number of CUDA kernels this library has enqueued since it was loaded
+ * (all streams, all devices). A diagnostic counter for benchmarks. */
+unsigned long long rnn_kernel_launches(void);
+
+/* Benchmarking aid. Registers two CUDA events (cudaEvent_t, or NULL to clear)
+ * that rnn_fwd (which = 0) or rnn_bwd (which = 1) record on the call's stream
+ * immediately before and after launching its recurrent-scan kernel, so that
+ * the scan kernel can be timed inside a longer step. Process-global and not
+ * thread-safe. Returns RNN_OK or RNN_EINVAL. */
+int rnn_profile_events(int which, void *before, void *after);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RNN_GB300_H */

@@ -1,0 +1,150 @@
+"""Thin ctypes binding of librnn_gb300.so: the C ABI of include/rnn.h, name for
+name. Arguments are marshalled from torch tensors (device pointers, the current
+CUDA stream); every computation happens in the library's CUDA kernels. There is
+no fallback: if the library cannot be built or loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import torch
+
+from . import build as _build
+
+RNN_OK, RNN_EINVAL, RNN_EUNSUPPORTED, RNN_ENOSPC, RNN_ETIMEOUT, RNN_ECUDA = range(6)
+FUNCTIONS = {"lstm": 0, "gru": 1, "elman": 2, "slstm": 3}
+DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+PATHS = {"auto": 0, "fused": 1, "alternating": 2, "simt": 3}
+WS_FWD, WS_BWD, WS_BWD_RECOMPUTE = 0, 1, 2
+
+EXPORTS = ["rnn_num_gates", "rnn_num_states", "rnn_tape_size", "rnn_workspace_size", "rnn_fwd",
+           "rnn_bwd", "rnn_check_status", "rnn_plan_describe", "rnn_strerror", "rnn_kernel_launches",
+           "rnn_profile_events"]
+
+
+class RnnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {rnn_strerror(status)} (status {status})")
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("N", ctypes.c_int), ("D", ctypes.c_int),
+                ("function", ctypes.c_int), ("dtype", ctypes.c_int), ("path", ctypes.c_int)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the CUDA library; raises if impossible."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(path or _build.build())
+            vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+            dp = ctypes.POINTER(Dims)
+            lib.rnn_num_gates.argtypes = [i]
+            lib.rnn_num_states.argtypes = [i]
+            lib.rnn_tape_size.argtypes = [dp]
+            lib.rnn_tape_size.restype = sz
+            lib.rnn_workspace_size.argtypes = [dp, i]
+            lib.rnn_workspace_size.restype = sz
+            lib.rnn_fwd.argtypes = [dp] + [vp] * 8 + [sz, vp]
+            lib.rnn_bwd.argtypes = [dp] + [vp] * 13 + [sz, vp]
+            lib.rnn_check_status.argtypes = [vp, vp]
+            lib.rnn_plan_describe.argtypes = [dp, i, ctypes.c_char_p, sz]
+            lib.rnn_strerror.argtypes = [i]
+            lib.rnn_strerror.restype = ctypes.c_char_p
+            lib.rnn_kernel_launches.argtypes = []
+            lib.rnn_kernel_launches.restype = ctypes.c_ulonglong
+            lib.rnn_profile_events.argtypes = [i, vp, vp]
+            _lib = lib
+    return _lib
+
+
+def make_dims(B, T, N, D, function="lstm", dtype=torch.bfloat16, path="auto") -> Dims:
+    fn = FUNCTIONS[function] if isinstance(function, str) else int(function)
+    dt = DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    pa = PATHS[path] if isinstance(path, str) else int(path)
+    return Dims(int(B), int(T), int(N), int(D), fn, dt, pa)
+
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(rc: int, where: str) -> int:
+    if rc != RNN_OK:
+        raise RnnError(rc, where)
+    return rc
+
+
+# ---- the C ABI, name for name -------------------------------------------------
+def rnn_num_gates(function) -> int:
+    return load().rnn_num_gates(FUNCTIONS.get(function, function) if isinstance(function, str) else function)
+
+
+def rnn_num_states(function) -> int:
+    return load().rnn_num_states(FUNCTIONS.get(function, function) if isinstance(function, str) else function)
+
+
+def rnn_tape_size(dims: Dims) -> int:
+    return load().rnn_tape_size(ctypes.byref(dims))
+
+
+def rnn_workspace_size(dims: Dims, kind: int = WS_FWD) -> int:
+    return load().rnn_workspace_size(ctypes.byref(dims), kind)
+
+
+def rnn_fwd(dims: Dims, Wx, R, b, states0, states, last, tape, workspace, stream=None) -> int:
+    rc = load().rnn_fwd(ctypes.byref(dims), _p(Wx), _p(R), _p(b), _p(states0), _p(states), _p(last),
+                        _p(tape), _p(workspace), workspace.numel() * workspace.element_size(),
+                        _stream(stream))
+    return _check(rc, "rnn_fwd")
+
+
+def rnn_bwd(dims: Dims, Wx, R, b, states0, states, tape, dstates, dlast, dWx, dR, db, dstates0,
+            workspace, stream=None) -> int:
+    rc = load().rnn_bwd(ctypes.byref(dims), _p(Wx), _p(R), _p(b), _p(states0), _p(states), _p(tape),
+                        _p(dstates), _p(dlast), _p(dWx), _p(dR), _p(db), _p(dstates0), _p(workspace),
+                        workspace.numel() * workspace.element_size(), _stream(stream))
+    return _check(rc, "rnn_bwd")
+
+
+def rnn_check_status(workspace, stream=None) -> int:
+    return _check(load().rnn_check_status(_p(workspace), _stream(stream)), "rnn_check_status")
+
+
+def rnn_plan_describe(dims: Dims, for_backward: bool = False) -> tuple[int, str]:
+    buf = ctypes.create_string_buffer(512)
+    rc = load().rnn_plan_describe(ctypes.byref(dims), int(for_backward), buf, 512)
+    return rc, buf.value.decode()
+
+
+def rnn_strerror(status: int) -> str:
+    return load().rnn_strerror(status).decode()
+
+
+def rnn_kernel_launches() -> int:
+    return int(load().rnn_kernel_launches())
+
+
+def rnn_profile_events(which: int, before=None, after=None) -> int:
+    """which: 0 = forward scan kernel, 1 = backward scan kernel; torch.cuda.Event
+    objects (recorded by the library around that kernel) or None to clear."""
+    b = ctypes.c_void_p(before.cuda_event) if before is not None else None
+    a = ctypes.c_void_p(after.cuda_event) if after is not None else None
+    return _check(load().rnn_profile_events(which, b, a), "rnn_profile_events")

@@ -1,0 +1,268 @@
+// C ABI of the head-wise recurrent scan library: validation, workspace layout,
+// path selection and launches. Declarations and argument documentation are in
+// include/rnn.h.
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "kernels.cuh"
+#include "plan.h"
+#include "rnn.h"
+
+namespace rnn {
+
+static std::atomic<unsigned long long> g_launches{0};
+void note_launch(int count) { g_launches.fetch_add((unsigned long long)count); }
+
+// Optional events recorded around the scan kernel (rnn_profile_events).
+static cudaEvent_t g_prof[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};
+static void prof_mark(int which, int edge, cudaStream_t st) {
+  if (g_prof[which][edge]) cudaEventRecord(g_prof[which][edge], st);
+}
+
+static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct Sizes {
+  int G, S, K;
+  size_t esize, wx, r, bias, st, st0, tape, dr;
+};
+
+static bool dims_ok(const rnn_dims_t* d) {
+  return d && d->B >= 1 && d->T >= 0 && d->N >= 1 && d->D >= 1 && d->function >= 0 &&
+         d->function <= 3 && (d->dtype == RNN_F32 || d->dtype == RNN_BF16) && d->path >= 0 &&
+         d->path <= 3 && (size_t)d->B * d->N * d->D < ((size_t)1 << 40);
+}
+
+static Sizes sizes_of(const rnn_dims_t* d) {
+  Sizes z;
+  z.G = fn_gates(d->function);
+  z.S = fn_states(d->function);
+  z.K = fn_tape(d->function);
+  z.esize = d->dtype == RNN_BF16 ? 2 : 4;
+  const size_t B = d->B, T = d->T, N = d->N, D = d->D;
+  z.wx = B * T * z.G * N * D;
+  z.r = (size_t)z.G * N * D * D;
+  z.bias = (size_t)z.G * N * D;
+  z.st = (size_t)z.S * B * T * N * D;
+  z.st0 = (size_t)z.S * B * N * D;
+  z.tape = T * B * N * z.K * D * sizeof(float);
+  z.dr = z.wx * z.esize;
+  return z;
+}
+
+static bool aligned(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Workspace layout: [status 256 B][path scratch][dr buffer (bwd)][tape (bwd recompute)]
+struct WsLayout {
+  size_t status, path, dr, tape, total;
+};
+
+static WsLayout ws_layout(const rnn_dims_t* d, int kind, const Plan& plan) {
+  WsLayout w;
+  Sizes z = sizes_of(d);
+  w.status = 0;
+  w.path = 256;
+  size_t off = w.path + align256(plan.scratch_bytes);
+  w.dr = off;
+  if (kind != RNN_WS_FWD) off += align256(z.dr);
+  w.tape = off;
+  if (kind == RNN_WS_BWD_RECOMPUTE) off += align256(z.tape);
+  w.total = off;
+  return w;
+}
+
+static int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return RNN_OK;
+  fprintf(stderr, "librnn_gb300: CUDA error: %s\n", cudaGetErrorString(e));
+  return RNN_ECUDA;
+}
+
+static int choose(const rnn_dims_t* d, bool bwd, Plan* plan) {
+  PlanRequest q{d->B, d->T, d->N, d->D, d->function, d->dtype, d->path, bwd};
+  return plan_select(q, plan);
+}
+
+// Runs the forward kernels (states/last/tape each optional).
+static int run_forward(const rnn_dims_t* d, const Plan& plan, const void* Wx, const void* R,
+                       const void* b, const void* s0, void* states, void* last, float* tape,
+                       char* ws, cudaStream_t st) {
+  SimtArgs a{};
+  a.B = d->B; a.T = d->T; a.N = d->N; a.D = d->D;
+  a.Wx = Wx; a.R = R; a.bias = b; a.s0 = s0;
+  a.states = states; a.last = last; a.tape = tape;
+  (void)ws;
+  int rc = RNN_EUNSUPPORTED;
+  prof_mark(0, 0, st);
+  switch (plan.path) {
+    case RNN_PATH_SIMT:
+      rc = cuda_status(simt_run(d->function, d->dtype, a, false, st));
+      break;
+  }
+  prof_mark(0, 1, st);
+  return rc;
+}
+
+}  // namespace rnn
+
+using namespace rnn;
+
+extern "C" {
+
+int rnn_num_gates(int function) { return function >= 0 && function <= 3 ? fn_gates(function) : -1; }
+int rnn_num_states(int function) { return function >= 0 && function <= 3 ? fn_states(function) : -1; }
+
+size_t rnn_tape_size(const rnn_dims_t* d) {
+  if (!dims_ok(d)) return 0;
+  return sizes_of(d).tape;
+}
+
+size_t rnn_workspace_size(const rnn_dims_t* d, int kind) {
+  if (!dims_ok(d) || kind < 0 || kind > 2) return 0;
+  Plan plan;
+  if (choose(d, kind != RNN_WS_FWD, &plan) != RNN_OK) {
+    // size for the plain path so that callers can still allocate
+    plan = Plan{};
+    plan.path = RNN_PATH_SIMT;
+  }
+  if (kind == RNN_WS_BWD_RECOMPUTE) {
+    Plan fplan;
+    if (choose(d, false, &fplan) == RNN_OK && fplan.scratch_bytes > plan.scratch_bytes)
+      plan.scratch_bytes = fplan.scratch_bytes;
+  }
+  return ws_layout(d, kind, plan).total;
+}
+
+int rnn_fwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
+            const void* states0, void* states, void* last, void* tape, void* workspace,
+            size_t ws_bytes, void* stream) {
+  if (!dims_ok(d)) return RNN_EINVAL;
+  if (!R || !b || !workspace || (d->T > 0 && (!Wx || !states))) return RNN_EINVAL;
+  const void* ptrs[] = {Wx, R, b, states0, states, last, tape, workspace};
+  for (const void* p : ptrs)
+    if (p && !aligned(p)) return RNN_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  Sizes z = sizes_of(d);
+  Plan plan;
+  int rc = choose(d, false, &plan);
+  if (rc != RNN_OK) return rc;
+  WsLayout w = ws_layout(d, RNN_WS_FWD, plan);
+  if (ws_bytes < w.total) return RNN_ENOSPC;
+  char* ws = (char*)workspace;
+  rc = cuda_status(cudaMemsetAsync(ws + w.status, 0, 256, st));
+  if (rc) return rc;
+  if (d->T == 0) {
+    if (!last) return RNN_OK;
+    if (states0) return cuda_status(cudaMemcpyAsync(last, states0, z.st0 * z.esize, cudaMemcpyDeviceToDevice, st));
+    return cuda_status(cudaMemsetAsync(last, 0, z.st0 * z.esize, st));
+  }
+  return run_forward(d, plan, Wx, R, b, states0, states, last, (float*)tape, ws + w.path, st);
+}
+
+int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
+            const void* states0, const void* states, const void* tape, const void* dstates,
+            const void* dlast, void* dWx, void* dR, void* db, void* dstates0, void* workspace,
+            size_t ws_bytes, void* stream) {
+  if (!dims_ok(d)) return RNN_EINVAL;
+  if (!R || !b || !workspace || (d->T > 0 && (!Wx || !states))) return RNN_EINVAL;
+  const void* ptrs[] = {Wx, R, b, states0, states, tape, dstates, dlast, dWx, dR, db, dstates0, workspace};
+  for (const void* p : ptrs)
+    if (p && !aligned(p)) return RNN_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  Sizes z = sizes_of(d);
+  Plan plan;
+  int rc = choose(d, true, &plan);
+  if (rc != RNN_OK) return rc;
+  const int kind = tape ? RNN_WS_BWD : RNN_WS_BWD_RECOMPUTE;
+  size_t need = rnn_workspace_size(d, kind);
+  if (ws_bytes < need) return RNN_ENOSPC;
+  WsLayout w = ws_layout(d, kind, plan);
+  char* ws = (char*)workspace;
+  rc = cuda_status(cudaMemsetAsync(ws + w.status, 0, 256, st));
+  if (rc) return rc;
+  if (d->T == 0) {
+    if (dstates0) {
+      rc = dlast ? cuda_status(cudaMemcpyAsync(dstates0, dlast, z.st0 * z.esize, cudaMemcpyDeviceToDevice, st))
+                 : cuda_status(cudaMemsetAsync(dstates0, 0, z.st0 * z.esize, st));
+      if (rc) return rc;
+    }
+    if (dR && (rc = cuda_status(cudaMemsetAsync(dR, 0, z.r * z.esize, st)))) return rc;
+    if (db && (rc = cuda_status(cudaMemsetAsync(db, 0, z.bias * z.esize, st)))) return rc;
+    return RNN_OK;
+  }
+  const float* tp = (const float*)tape;
+  if (!tp) {
+    Plan fplan;
+    rc = choose(d, false, &fplan);
+    if (rc != RNN_OK) return rc;
+    float* t2 = (float*)(ws + w.tape);
+    rc = run_forward(d, fplan, Wx, R, b, states0, nullptr, nullptr, t2, ws + w.path, st);
+    if (rc) return rc;
+    tp = t2;
+  }
+  SimtArgs a{};
+  a.B = d->B; a.T = d->T; a.N = d->N; a.D = d->D;
+  a.R = R; a.s0 = states0; a.tape = (float*)tp;
+  a.dstates = dstates; a.dlast = dlast; a.dWx = dWx; a.dr = ws + w.dr; a.ds0 = dstates0;
+  rc = RNN_EUNSUPPORTED;
+  prof_mark(1, 0, st);
+  switch (plan.path) {
+    case RNN_PATH_SIMT:
+      rc = cuda_status(simt_run(d->function, d->dtype, a, true, st));
+      break;
+  }
+  prof_mark(1, 1, st);
+  if (rc) return rc;
+  if (dR || db) {
+    WgradArgs g{d->B, d->T, d->N, d->D, z.G, states, states0, ws + w.dr, dR, db};
+    rc = cuda_status(wgrad_run(d->dtype, g, st));
+  }
+  return rc;
+}
+
+int rnn_check_status(void* workspace, void* stream) {
+  if (!workspace) return RNN_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned int h = 0;
+  cudaError_t e = cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (h != STATUS_OK) {
+    e = cudaMemsetAsync(workspace, 0, sizeof(h), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_status(e);
+    return RNN_ETIMEOUT;
+  }
+  return RNN_OK;
+}
+
+int rnn_plan_describe(const rnn_dims_t* d, int for_backward, char* buf, size_t len) {
+  if (!dims_ok(d) || !buf || len == 0) return RNN_EINVAL;
+  Plan plan;
+  int rc = choose(d, for_backward != 0, &plan);
+  plan_describe(plan, rc, buf, len);
+  return rc;
+}
+
+unsigned long long rnn_kernel_launches(void) { return g_launches.load(); }
+
+int rnn_profile_events(int which, void* before, void* after) {
+  if (which < 0 || which > 1) return RNN_EINVAL;
+  g_prof[which][0] = (cudaEvent_t)before;
+  g_prof[which][1] = (cudaEvent_t)after;
+  return RNN_OK;
+}
+
+const char* rnn_strerror(int status) {
+  switch (status) {
+    case RNN_OK: return "ok";
+    case RNN_EINVAL: return "invalid argument (dimensions, null pointer or alignment)";
+    case RNN_EUNSUPPORTED: return "no feasible kernel plan for the requested path";
+    case RNN_ENOSPC: return "workspace too small";
+    case RNN_ETIMEOUT: return "a device-side wait timed out";
+    case RNN_ECUDA: return "CUDA runtime error";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

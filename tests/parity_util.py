@@ -1,0 +1,95 @@
+"""Shared helpers of the parity tests: run the CUDA path through the C ABI,
+run the oracle, compare with the stated tolerances.
+
+Tolerances (stated once, used by every parity test):
+  fp32 storage: max |err| <= 1e-4 on every state; gradients normwise-max
+                relative error max|g - g*| / max|g*| <= 1e-3.
+  bf16 storage (fp32 arithmetic): max |err| <= 3e-2 on h; other states
+                |err| <= 3e-2 * max(1, |ref|) (bf16 keeps 8 significant bits);
+                gradients normwise-max relative <= 5e-2 and cosine >= 0.999.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import oracle
+from recurrent_networks_gb300 import _lib
+
+TOL = {
+    torch.float32: dict(h=1e-4, states=1e-4, states_rel=False, grad=1e-3, cos=None),
+    torch.bfloat16: dict(h=3e-2, states=3e-2, states_rel=True, grad=5e-2, cos=0.999),
+}
+
+
+def run_fwd(fn, inp, path="auto", want_tape=True, stream=None):
+    Wx, R, b, s0 = (inp[k] for k in ("Wx", "R", "b", "states0"))
+    B, T, G, N, D = Wx.shape
+    S = _lib.rnn_num_states(fn)
+    dims = _lib.make_dims(B, T, N, D, fn, Wx.dtype, path)
+    states = torch.full((S, B, T, N, D), float("nan"), dtype=Wx.dtype, device=Wx.device)
+    last = torch.full((S, B, 1, N, D), float("nan"), dtype=Wx.dtype, device=Wx.device)
+    tape = torch.empty(_lib.rnn_tape_size(dims), dtype=torch.uint8, device=Wx.device) if want_tape else None
+    ws = torch.empty(_lib.rnn_workspace_size(dims, _lib.WS_FWD), dtype=torch.uint8, device=Wx.device)
+    _lib.rnn_fwd(dims, Wx, R, b, s0, states, last, tape, ws, stream)
+    _lib.rnn_check_status(ws, stream)
+    return states, last, tape
+
+
+def run_bwd(fn, inp, states, tape, path="auto", dlast=None):
+    Wx, R, b, s0, dst = (inp[k] for k in ("Wx", "R", "b", "states0", "dstates"))
+    B, T, G, N, D = Wx.shape
+    dims = _lib.make_dims(B, T, N, D, fn, Wx.dtype, path)
+    kind = _lib.WS_BWD if tape is not None else _lib.WS_BWD_RECOMPUTE
+    ws = torch.empty(_lib.rnn_workspace_size(dims, kind), dtype=torch.uint8, device=Wx.device)
+    dWx = torch.full_like(Wx, float("nan"))
+    dR = torch.full_like(R, float("nan"))
+    db = torch.full_like(b, float("nan"))
+    ds0 = torch.full_like(s0, float("nan")) if s0 is not None else None
+    _lib.rnn_bwd(dims, Wx, R, b, s0, states, tape, dst, dlast, dWx, dR, db, ds0, ws)
+    _lib.rnn_check_status(ws)
+    return dWx, dR, db, ds0
+
+
+def to_np(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def check_states(fn, dtype, got, ref, what="states"):
+    tol = TOL[dtype]
+    got = to_np(got)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    err_h = np.abs(got[0] - ref[0]).max() if got[0].size else 0.0
+    assert err_h <= tol["h"], f"{fn} {what} h: max abs err {err_h:.3g} > {tol['h']}"
+    for s in range(1, got.shape[0]):
+        e = np.abs(got[s] - ref[s])
+        if tol["states_rel"]:
+            e = e / np.maximum(1.0, np.abs(ref[s]))
+        m = e.max() if e.size else 0.0
+        assert m <= tol["states"], f"{fn} {what} state {s}: err {m:.3g} > {tol['states']}"
+    return err_h
+
+
+def check_grad(name, dtype, got, ref):
+    tol = TOL[dtype]
+    got = to_np(got)
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    scale = np.abs(ref).max()
+    if scale == 0:
+        assert np.abs(got).max() == 0, f"{name}: expected zeros"
+        return 0.0
+    rel = np.abs(got - ref).max() / scale
+    assert rel <= tol["grad"], f"{name}: normwise-max relative err {rel:.3g} > {tol['grad']}"
+    if tol["cos"] is not None and got.size > 1:
+        cos = float((got * ref).sum() / (np.linalg.norm(got) * np.linalg.norm(ref) + 1e-300))
+        assert cos >= tol["cos"], f"{name}: cosine {cos:.6f} < {tol['cos']}"
+    return rel
+
+
+def oracle_fwd(fn, inp, nthreads=8):
+    return oracle.fwd(fn, inp["Wx"], inp["R"], inp["b"], inp["states0"], nthreads=nthreads)
+
+
+def oracle_bwd(fn, inp, dlast=None, nthreads=8):
+    return oracle.bwd(fn, inp["Wx"], inp["R"], inp["b"], inp["states0"], inp["dstates"], dlast,
+                      nthreads=nthreads)

@@ -1,0 +1,91 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle,
+element by element, at sizes the oracle finishes in seconds (several tiles and
+ragged tails). Tolerances are those of tests/parity_util.py."""
+import numpy as np
+import pytest
+import torch
+
+from recurrent_networks_gb300 import _lib
+from recurrent_networks_gb300.synth import make_inputs
+
+from parity_util import (check_grad, check_states, oracle_bwd, oracle_fwd, run_bwd, run_fwd)
+
+pytestmark = pytest.mark.gpu
+
+FNS = ["lstm", "gru", "elman", "slstm"]
+DTYPES = [torch.float32, torch.bfloat16]
+SMALL = [(3, 37, 2, 48), (1, 5, 1, 16), (9, 20, 3, 64)]
+
+
+def _inputs(fn, shape, dtype, seed):
+    B, T, N, D = shape
+    return make_inputs(fn, B, T, N, D, dtype, seed=seed, device="cuda")
+
+
+def _full_check(fn, inp, dtype, path, backward=True, recompute=False):
+    st, last, tape = run_fwd(fn, inp, path)
+    ref_st, ref_last = oracle_fwd(fn, inp)
+    check_states(fn, dtype, st, ref_st)
+    check_states(fn, dtype, last, ref_last, "last")
+    if not backward:
+        return
+    dWx, dR, db, ds0 = run_bwd(fn, inp, st, None if recompute else tape, path)
+    rdWx, rdR, rdb, rds0 = oracle_bwd(fn, inp)
+    check_grad(f"{fn} dWx", dtype, dWx, rdWx)
+    check_grad(f"{fn} dR", dtype, dR, rdR)
+    check_grad(f"{fn} db", dtype, db, rdb)
+    check_grad(f"{fn} dstates0", dtype, ds0, rds0)
+
+
+@pytest.mark.parametrize("fn", FNS)
+@pytest.mark.parametrize("dtype", DTYPES, ids=["f32", "bf16"])
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "B%dT%dN%dD%d" % s)
+def test_simt_parity(fn, dtype, shape):
+    inp = _inputs(fn, shape, dtype, seed=100 * FNS.index(fn) + SMALL.index(shape))
+    _full_check(fn, inp, dtype, "simt")
+
+
+@pytest.mark.parametrize("fn", FNS)
+def test_backward_recomputes_tape(fn):
+    inp = _inputs(fn, (2, 9, 1, 32), torch.float32, seed=77)
+    _full_check(fn, inp, torch.float32, "auto", recompute=True)
+
+
+@pytest.mark.parametrize("fn", FNS)
+def test_zero_length_and_null_initial_state(fn):
+    inp = _inputs(fn, (2, 0, 1, 32), torch.float32, seed=3)
+    st, last, tape = run_fwd(fn, inp, "auto")
+    assert st.numel() == 0
+    torch.testing.assert_close(last, inp["states0"], rtol=0, atol=0)
+    dl = torch.randn_like(inp["states0"])
+    dWx, dR, db, ds0 = run_bwd(fn, inp, st, tape, "auto", dlast=dl)
+    torch.testing.assert_close(ds0, dl, rtol=0, atol=0)
+    assert not dR.any() and not db.any()
+    # states0 = NULL means zeros
+    inp = _inputs(fn, (2, 6, 1, 32), torch.float32, seed=4)
+    st1, _, _ = run_fwd(fn, dict(inp, states0=None), "auto", want_tape=False)
+    st2, _, _ = run_fwd(fn, dict(inp, states0=torch.zeros_like(inp["states0"])), "auto", want_tape=False)
+    torch.testing.assert_close(st1, st2, rtol=0, atol=0)
+
+
+def test_workload_1_full():
+    """LSTM fp32, B=2 T=16 N=1 D=32: every element of every output."""
+    from recurrent_networks_gb300.synth import workload_inputs
+    inp = workload_inputs(1, device="cuda")
+    _full_check("lstm", inp, torch.float32, "auto")
+
+
+def test_autograd_function_matches_abi():
+    from recurrent_networks_gb300 import flashrnn
+    inp = _inputs("lstm", (3, 11, 2, 32), torch.float32, seed=5)
+    leaves = {k: inp[k].clone().requires_grad_(True) for k in ("Wx", "R", "b", "states0")}
+    st, last = flashrnn(leaves["Wx"], leaves["R"], leaves["b"], leaves["states0"], function="lstm")
+    dl = torch.randn_like(last)
+    ((st * inp["dstates"]).sum() + (last * dl).sum()).backward()
+    ref_st, _ = oracle_fwd("lstm", inp)
+    rdWx, rdR, rdb, rds0 = oracle_bwd("lstm", inp, dlast=dl.cpu().double().numpy())
+    check_states("lstm", torch.float32, st, ref_st)
+    check_grad("dWx", torch.float32, leaves["Wx"].grad, rdWx)
+    check_grad("dR", torch.float32, leaves["R"].grad, rdR)
+    check_grad("db", torch.float32, leaves["b"].grad, rdb)
+    check_grad("ds0", torch.float32, leaves["states0"].grad, rds0)
