@@ -50,8 +50,8 @@ def _load():
         lib = ctypes.CDLL(build())
         dp = ctypes.POINTER(ctypes.c_double)
         i = ctypes.c_int
-        lib.oracle_fwd.argtypes = [i, i, i, i, i, dp, dp, dp, dp, dp, dp, i]
-        lib.oracle_bwd.argtypes = [i, i, i, i, i, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, i]
+        lib.oracle_fwd.argtypes = [i, i, i, i, i, dp, dp, dp, dp, dp, dp, i, i]
+        lib.oracle_bwd.argtypes = [i, i, i, i, i, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, i, i]
         lib.oracle_fwd.restype = i
         lib.oracle_bwd.restype = i
         _lib = lib
@@ -73,9 +73,13 @@ def _f64(a):
     return np.ascontiguousarray(a, dtype=np.float64)
 
 
-def fwd(function: str, Wx, R, b, states0=None, nthreads: int = 1):
+ROUND_BF16 = 1
+
+
+def fwd(function: str, Wx, R, b, states0=None, nthreads: int = 1, round_bf16: bool = False):
     """Forward scan. Wx [B,T,G,N,D], R [G,N,D,D], b [G,N,D], states0 [S,B,1,N,D]
-    (None = zeros). Returns (states [S,B,T,N,D], last [S,B,1,N,D]) in fp64."""
+    (None = zeros). Returns (states [S,B,T,N,D], last [S,B,1,N,D]) in fp64.
+    round_bf16: the bfloat16 storage mode (contraction operands rounded to bf16)."""
     Wx, R, b, s0 = _f64(Wx), _f64(R), _f64(b), _f64(states0)
     B, T, G, N, D = Wx.shape
     S = STATES[function]
@@ -85,13 +89,15 @@ def fwd(function: str, Wx, R, b, states0=None, nthreads: int = 1):
     states = np.zeros((S, B, T, N, D))
     last = np.zeros((S, B, 1, N, D))
     rc = _load().oracle_fwd(FUNCTIONS[function], B, T, N, D, _ptr(Wx), _ptr(R), _ptr(b),
-                            _ptr(s0), _ptr(states), _ptr(last), nthreads)
+                            _ptr(s0), _ptr(states), _ptr(last), ROUND_BF16 if round_bf16 else 0,
+                            nthreads)
     if rc != 0:
         raise ValueError("oracle_fwd rejected its arguments")
     return states, last
 
 
-def bwd(function: str, Wx, R, b, states0=None, dstates=None, dlast=None, nthreads: int = 1):
+def bwd(function: str, Wx, R, b, states0=None, dstates=None, dlast=None, nthreads: int = 1,
+        round_bf16: bool = False):
     """Backward through time. Returns (dWx, dR, db, dstates0) in fp64."""
     Wx, R, b, s0 = _f64(Wx), _f64(R), _f64(b), _f64(states0)
     dst, dl = _f64(dstates), _f64(dlast)
@@ -108,7 +114,7 @@ def bwd(function: str, Wx, R, b, states0=None, dstates=None, dlast=None, nthread
     ds0 = np.zeros((S, B, 1, N, D))
     rc = _load().oracle_bwd(FUNCTIONS[function], B, T, N, D, _ptr(Wx), _ptr(R), _ptr(b),
                             _ptr(s0), _ptr(dst), _ptr(dl), _ptr(dWx), _ptr(dR), _ptr(db),
-                            _ptr(ds0), nthreads)
+                            _ptr(ds0), ROUND_BF16 if round_bf16 else 0, nthreads)
     if rc != 0:
         raise ValueError("oracle_bwd rejected its arguments")
     return dWx, dR, db, ds0

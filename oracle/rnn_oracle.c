@@ -30,6 +30,7 @@
 
 #include <math.h>
 #include <pthread.h>
+#include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -185,7 +186,7 @@ static void cell_bwd(int fn, const double *x, const double *rec,
 /* ---- one (b, n) sequence -------------------------------------------------- */
 
 typedef struct {
-  int fn, B, T, N, D, G, S;
+  int fn, B, T, N, D, G, S, flags;
   const double *Wx, *R, *bias, *s0, *dstates, *dlast;
   double *states, *last, *dWx, *dR, *db, *ds0;
 } problem_t;
@@ -199,6 +200,26 @@ typedef struct {
 #define IDX_ST(p, TT, s, b, t, n, j) \
   ((((((size_t)(s) * (p)->B + (b)) * (TT) + (t)) * (p)->N + (n)) * (p)->D) + (j))
 
+/* bfloat16 storage mode (ORACLE_ROUND_BF16): the operands of the recurrent
+ * contractions are bfloat16 values, the arithmetic stays exact (fp64 here).
+ * The value is first rounded to binary32 (as an fp32 computation would hold
+ * it) and then to bfloat16 with round-to-nearest-even on the 16 dropped bits. */
+static double round_bf16(double v) {
+  float f = (float)v;
+  uint32_t u;
+  memcpy(&u, &f, sizeof(u));
+  if ((u & 0x7f800000u) != 0x7f800000u) { /* finite: round, else keep */
+    u += 0x7fffu + ((u >> 16) & 1u);
+    u &= 0xffff0000u;
+  }
+  memcpy(&f, &u, sizeof(f));
+  return (double)f;
+}
+
+static double operand(const problem_t *p, double v) {
+  return (p->flags & ORACLE_ROUND_BF16) ? round_bf16(v) : v;
+}
+
 /* rec[g*D + j] = h . R[g,n][:, j] + bias[g,n,j] */
 static void recurrent_branch(const problem_t *p, int n, const double *h,
                              double *rec) {
@@ -206,7 +227,7 @@ static void recurrent_branch(const problem_t *p, int n, const double *h,
   for (g = 0; g < p->G; ++g) {
     for (j = 0; j < D; ++j) rec[g * D + j] = p->bias[IDX_B(p, g, n, j)];
     for (i = 0; i < D; ++i) {
-      double hi = h[i];
+      double hi = operand(p, h[i]);
       const double *row = p->R + IDX_R(p, g, n, i, 0);
       for (j = 0; j < D; ++j) rec[g * D + j] += hi * row[j];
     }
@@ -296,15 +317,15 @@ static void seq_bwd(const problem_t *p, int b, int n, double *dR_acc,
       cell_bwd(p->fn, xg, rg, sp, sn, dsn, dxg, drg, dsp);
       for (g = 0; g < G; ++g) {
         if (p->dWx) p->dWx[IDX_WX(p, b, t, g, n, j)] = dxg[g];
-        drec[g * D + j] = drg[g];
-        db_acc[IDX_B(p, g, n, j)] += drg[g];
+        drec[g * D + j] = operand(p, drg[g]);
+        db_acc[IDX_B(p, g, n, j)] += drec[g * D + j];
       }
       for (s = 0; s < S; ++s) ncarry[s * D + j] = dsp[s];
     }
     /* through the recurrent branch: dR += h_{t-1}^T drec ; dh_{t-1} += drec . R^T */
     for (g = 0; g < G; ++g)
       for (i = 0; i < D; ++i) {
-        double hi = prev[i]; /* s = 0 is h */
+        double hi = operand(p, prev[i]); /* s = 0 is h */
         const double *row = p->R + IDX_R(p, g, n, i, 0);
         double *drow = dR_acc + IDX_R(p, g, n, i, 0);
         double acc = 0.0;
@@ -397,8 +418,9 @@ static int run(problem_t *p, int backward, int nthreads) {
   return 0;
 }
 
-static int setup(problem_t *p, int fn, int B, int T, int N, int D) {
+static int setup(problem_t *p, int fn, int B, int T, int N, int D, int flags) {
   memset(p, 0, sizeof(*p));
+  p->flags = flags;
   if (fn < 0 || fn > 3 || B < 0 || T < 0 || N < 0 || D < 0) return -1;
   p->fn = fn;
   p->B = B;
@@ -412,9 +434,9 @@ static int setup(problem_t *p, int fn, int B, int T, int N, int D) {
 
 int oracle_fwd(int fn, int B, int T, int N, int D, const double *Wx,
                const double *R, const double *bias, const double *s0,
-               double *states, double *last, int nthreads) {
+               double *states, double *last, int flags, int nthreads) {
   problem_t p;
-  if (setup(&p, fn, B, T, N, D)) return -1;
+  if (setup(&p, fn, B, T, N, D, flags)) return -1;
   if ((T > 0 && !Wx) || !R || !bias) return -1;
   p.Wx = Wx;
   p.R = R;
@@ -428,9 +450,9 @@ int oracle_fwd(int fn, int B, int T, int N, int D, const double *Wx,
 int oracle_bwd(int fn, int B, int T, int N, int D, const double *Wx,
                const double *R, const double *bias, const double *s0,
                const double *dstates, const double *dlast, double *dWx,
-               double *dR, double *db, double *ds0, int nthreads) {
+               double *dR, double *db, double *ds0, int flags, int nthreads) {
   problem_t p;
-  if (setup(&p, fn, B, T, N, D)) return -1;
+  if (setup(&p, fn, B, T, N, D, flags)) return -1;
   if ((T > 0 && !Wx) || !R || !bias) return -1;
   p.Wx = Wx;
   p.R = R;

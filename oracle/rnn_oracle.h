@@ -37,17 +37,25 @@ extern "C" {
 
 enum { ORACLE_LSTM = 0, ORACLE_GRU = 1, ORACLE_ELMAN = 2, ORACLE_SLSTM = 3 };
 
+/* flags: ORACLE_ROUND_BF16 = the bfloat16 storage mode, in which the operands
+ * of every recurrent contraction (h_{t-1} in h.R, the recurrent-branch
+ * gradient in dh = dr.R^T and in dR, db) are bfloat16 values; arithmetic and
+ * carried states stay fp64. 0 = plain fp64 throughout. */
+enum { ORACLE_ROUND_BF16 = 1 };
+
 int oracle_num_gates(int fn);
 int oracle_num_states(int fn);
 
 int oracle_fwd(int fn, int B, int T, int N, int D,
                const double *Wx, const double *R, const double *bias,
-               const double *s0, double *states, double *last, int nthreads);
+               const double *s0, double *states, double *last, int flags,
+               int nthreads);
 
 int oracle_bwd(int fn, int B, int T, int N, int D,
                const double *Wx, const double *R, const double *bias,
                const double *s0, const double *dstates, const double *dlast,
-               double *dWx, double *dR, double *db, double *ds0, int nthreads);
+               double *dWx, double *dR, double *db, double *ds0, int flags,
+               int nthreads);
 
 #ifdef __cplusplus
 }

@@ -3,10 +3,16 @@ run the oracle, compare with the stated tolerances.
 
 Tolerances (stated once, used by every parity test):
   fp32 storage: max |err| <= 1e-4 on every state; gradients normwise-max
-                relative error max|g - g*| / max|g*| <= 1e-3.
-  bf16 storage (fp32 arithmetic): max |err| <= 3e-2 on h; other states
-                |err| <= 3e-2 * max(1, |ref|) (bf16 keeps 8 significant bits);
-                gradients normwise-max relative <= 5e-2 and cosine >= 0.999.
+                relative error max|g - g*| / max|g*| <= 1e-3; reference = the
+                plain fp64 oracle.
+  bf16 storage (fp32 arithmetic): states against the plain fp64 oracle:
+                max |err| <= 3e-2 on h, other states |err| <= 3e-2 * max(1,|ref|)
+                (bf16 keeps 8 significant bits). Gradients against the oracle
+                in its bfloat16-operand mode (the contraction operands h and
+                dr rounded to bf16, as the kernels' tensor-core operands are):
+                normwise-max relative <= 2e-2 and cosine >= 0.9995. Against the
+                plain oracle the bf16 rounding of h alone moves sLSTM gradients
+                by ~6% on short sequences, which says nothing about the kernels.
 """
 from __future__ import annotations
 
@@ -18,7 +24,7 @@ from recurrent_networks_gb300 import _lib
 
 TOL = {
     torch.float32: dict(h=1e-4, states=1e-4, states_rel=False, grad=1e-3, cos=None),
-    torch.bfloat16: dict(h=3e-2, states=3e-2, states_rel=True, grad=5e-2, cos=0.999),
+    torch.bfloat16: dict(h=3e-2, states=3e-2, states_rel=True, grad=2e-2, cos=0.9995),
 }
 
 
@@ -86,10 +92,18 @@ def check_grad(name, dtype, got, ref):
     return rel
 
 
-def oracle_fwd(fn, inp, nthreads=8):
-    return oracle.fwd(fn, inp["Wx"], inp["R"], inp["b"], inp["states0"], nthreads=nthreads)
+def is_bf16(inp):
+    return inp["Wx"].dtype == torch.bfloat16
 
 
-def oracle_bwd(fn, inp, dlast=None, nthreads=8):
+def oracle_fwd(fn, inp, nthreads=8, round_bf16=False):
+    return oracle.fwd(fn, inp["Wx"], inp["R"], inp["b"], inp["states0"], nthreads=nthreads,
+                      round_bf16=round_bf16)
+
+
+def oracle_bwd(fn, inp, dlast=None, nthreads=8, round_bf16=None):
+    """Gradients; for bf16 inputs the oracle runs in its bfloat16-operand mode."""
+    if round_bf16 is None:
+        round_bf16 = is_bf16(inp)
     return oracle.bwd(fn, inp["Wx"], inp["R"], inp["b"], inp["states0"], inp["dstates"], dlast,
-                      nthreads=nthreads)
+                      nthreads=nthreads, round_bf16=round_bf16)

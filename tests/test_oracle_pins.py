@@ -264,3 +264,74 @@ def test_threads_do_not_change_results():
     c = oracle.bwd("lstm", Wx, R, b, s0, d, nthreads=4)
     for x, y in zip(a, c):
         np.testing.assert_allclose(x, y, rtol=1e-13, atol=1e-14)
+
+
+# --------------------------------------------------- bfloat16 operand mode
+def _bf16(x):
+    """binary32 then bfloat16 (round to nearest even), by torch's conversions."""
+    return x.float().bfloat16().double()
+
+
+class _Bf16OperandBranch(torch.autograd.Function):
+    """The recurrent branch y = bf16(h) @ W + b with bfloat16 operands and exact
+    accumulation. Its backward takes bfloat16 operands too:
+    dh = bf16(dy) @ W^T, dW = bf16(h)^T bf16(dy), db = sum bf16(dy)."""
+
+    @staticmethod
+    def forward(ctx, h, W, b):
+        hb = _bf16(h)
+        ctx.save_for_backward(hb, W)
+        return hb @ W + b
+
+    @staticmethod
+    def backward(ctx, dy):
+        hb, W = ctx.saved_tensors
+        dyb = _bf16(dy)
+        return dyb @ W.T, hb.T @ dyb, dyb.sum(0)
+
+
+@pytest.mark.parametrize("fn", ["lstm", "elman"])
+def test_bf16_operand_mode_against_torch_autograd(fn):
+    """The oracle's bfloat16 mode equals torch autograd of the same cell with a
+    bfloat16-operand recurrent matmul (gates and derivatives by torch)."""
+    B, T, N, D = 3, 8, 1, 6
+    G, S = oracle.GATES[fn], oracle.STATES[fn]
+    Wx, R, b, s0 = rand_problem(fn, B, T, N, D, seed=17, rscale=1.5)
+    rng = np.random.default_rng(2)
+    dst = rng.normal(size=(S, B, T, N, D))
+    states, _ = oracle.fwd(fn, Wx, R, b, s0, round_bf16=True)
+    dWx, dR, db, ds0 = oracle.bwd(fn, Wx, R, b, s0, dst, round_bf16=True)
+    plain, _ = oracle.fwd(fn, Wx, R, b, s0)
+    assert np.abs(plain - states).max() > 1e-6  # the mode changes the result
+
+    x = torch.from_numpy(Wx[:, :, :, 0, :].copy()).requires_grad_(True)        # [B,T,G,D]
+    W = torch.from_numpy(R[:, 0].transpose(1, 0, 2).reshape(D, G * D).copy()).requires_grad_(True)
+    bb = torch.from_numpy(b[:, 0].reshape(G * D).copy()).requires_grad_(True)
+    h = torch.from_numpy(s0[0, :, 0, 0].copy()).requires_grad_(True)
+    c = torch.from_numpy(s0[1, :, 0, 0].copy()).requires_grad_(True) if fn == "lstm" else None
+    h0, c0 = h, c
+    hs, cs = [], []
+    for t in range(T):
+        a = x[:, t].reshape(B, G * D) + _Bf16OperandBranch.apply(h, W, bb)
+        if fn == "lstm":
+            i, f, g, o = a.split(D, dim=1)
+            c = torch.sigmoid(f) * c + torch.sigmoid(i) * torch.tanh(g)
+            h = torch.sigmoid(o) * torch.tanh(c)
+            cs.append(c)
+        else:
+            h = torch.tanh(a)
+        hs.append(h)
+    H = torch.stack(hs, 1)
+    loss = (H * torch.from_numpy(dst[0, :, :, 0])).sum()
+    np.testing.assert_allclose(states[0, :, :, 0], H.detach().numpy(), rtol=1e-12, atol=1e-13)
+    if fn == "lstm":
+        Cs = torch.stack(cs, 1)
+        loss = loss + (Cs * torch.from_numpy(dst[1, :, :, 0])).sum()
+    loss.backward()
+    np.testing.assert_allclose(dWx[:, :, :, 0], x.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dR[:, 0], W.grad.numpy().reshape(D, G, D).transpose(1, 0, 2),
+                               rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(db[:, 0], bb.grad.numpy().reshape(G, D), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(ds0[0, :, 0, 0], h0.grad.numpy(), rtol=1e-10, atol=1e-12)
+    if fn == "lstm":
+        np.testing.assert_allclose(ds0[1, :, 0, 0], c0.grad.numpy(), rtol=1e-10, atol=1e-12)
