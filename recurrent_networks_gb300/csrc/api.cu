@@ -83,7 +83,11 @@ static int choose(const rnn_dims_t* d, bool bwd, Plan* plan) {
   return plan_select(q, plan);
 }
 
-// Runs the forward kernels (states/last/tape each optional).
+// Upper bound of every device-side wait (rnn_set_wait_limit).
+static unsigned long long g_wait_limit_ns = 2000000000ull;
+
+// Runs the forward kernels (states/last/tape each optional); ws is the
+// workspace base (status word at offset 0).
 static int run_forward(const rnn_dims_t* d, const Plan& plan, const void* Wx, const void* R,
                        const void* b, const void* s0, void* states, void* last, float* tape,
                        char* ws, cudaStream_t st) {
@@ -91,13 +95,23 @@ static int run_forward(const rnn_dims_t* d, const Plan& plan, const void* Wx, co
   a.B = d->B; a.T = d->T; a.N = d->N; a.D = d->D;
   a.Wx = Wx; a.R = R; a.bias = b; a.s0 = s0;
   a.states = states; a.last = last; a.tape = tape;
-  (void)ws;
   int rc = RNN_EUNSUPPORTED;
   prof_mark(0, 0, st);
   switch (plan.path) {
     case RNN_PATH_SIMT:
       rc = cuda_status(simt_run(d->function, d->dtype, a, false, st));
       break;
+    case RNN_PATH_FUSED: {
+      FusedArgs f{};
+      f.B = d->B; f.T = d->T; f.N = d->N; f.D = d->D;
+      f.C = plan.fs.C; f.U = plan.fs.U; f.KS = plan.fs.KS;
+      f.Wx = Wx; f.R = R; f.bias = b; f.s0 = s0;
+      f.states = states; f.last = last; f.tape = tape;
+      f.status = (unsigned int*)ws;
+      f.wait_limit_ns = g_wait_limit_ns;
+      rc = cuda_status(fused_fwd_run(d->function, plan.fs, f, st));
+      break;
+    }
   }
   prof_mark(0, 1, st);
   return rc;
@@ -156,7 +170,7 @@ int rnn_fwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
     if (states0) return cuda_status(cudaMemcpyAsync(last, states0, z.st0 * z.esize, cudaMemcpyDeviceToDevice, st));
     return cuda_status(cudaMemsetAsync(last, 0, z.st0 * z.esize, st));
   }
-  return run_forward(d, plan, Wx, R, b, states0, states, last, (float*)tape, ws + w.path, st);
+  return run_forward(d, plan, Wx, R, b, states0, states, last, (float*)tape, ws, st);
 }
 
 int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
@@ -196,7 +210,7 @@ int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
     rc = choose(d, false, &fplan);
     if (rc != RNN_OK) return rc;
     float* t2 = (float*)(ws + w.tape);
-    rc = run_forward(d, fplan, Wx, R, b, states0, nullptr, nullptr, t2, ws + w.path, st);
+    rc = run_forward(d, fplan, Wx, R, b, states0, nullptr, nullptr, t2, ws, st);
     if (rc) return rc;
     tp = t2;
   }

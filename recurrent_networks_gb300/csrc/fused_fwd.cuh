@@ -1,0 +1,301 @@
+// Persistent thread-block-cluster forward scan (bf16 storage, fp32 arithmetic).
+//
+// The "fused" design of the FlashRNN announcement (matrix product and
+// pointwise cell in one kernel, recurrent weights kept in registers),
+// re-planned for sm_103a:
+//  - one cluster of C CTAs runs one head n for a group of up to BC = 8*NT batch
+//    rows over the whole sequence; CTA c owns units [c*U, (c+1)*U), U = D/C;
+//  - its slice of R (all G gates of its U units, all D inputs) lives in
+//    registers as mma.sync A fragments for the whole kernel; the step's
+//    contraction is the transposed product  rec^T[(g,j), b] = R[g,:,j]^T h[b,:],
+//    M = G*U, N = batch, K = D, split over warps along M (16-unit groups) and K;
+//  - h_{t-1} (bf16, all D units) sits in shared memory; after the pointwise
+//    update every CTA pushes its U-slice of h_t into every peer's buffer with
+//    st.async, whose mbarrier transaction count is the step's only
+//    synchronisation (no cluster-wide barrier inside the time loop);
+//  - Wx[:, t] for the CTA's slice streams in through a TMA ring NS steps ahead;
+//  - the cell update runs in the epilogue with c, n, m carried in fp32 in
+//    shared memory; states and the backward's tape are written straight out.
+#pragma once
+#include <cuda.h>
+
+#include "kernels.cuh"
+#include "layout.h"
+#include "ptx.cuh"
+
+namespace rnn {
+
+template <int FN, int NT, int KT>
+__global__ void __launch_bounds__(256, 1)
+    fused_fwd_kernel(const __grid_constant__ CUtensorMap wxmap, FusedArgs a) {
+  constexpr int G = FnInfo<FN>::G, S = FnInfo<FN>::S, P = FnInfo<FN>::P, K = P + S;
+  constexpr int BC = 8 * NT;
+  const int C = a.C, U = a.U, D = a.D, KS = a.KS, TT = a.T, N = a.N, B = a.B;
+  const int HS = D + 8;  // row stride (elements) of the h buffers
+  const uint32_t rank = cluster_ctarank();
+  const int grp = blockIdx.x / C;
+  const int n = grp % N;
+  const int b0 = (grp / N) * BC;
+  const int nb = min(BC, B - b0);
+  const int u0 = (int)rank * U;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int mg = warp / KS, ks = warp - mg * KS;
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  const FusedSmem L = FusedSmem::make(G, S, D, U, BC, KS);
+  uint64_t* bars = (uint64_t*)(smem + L.bars);  // [0,1]: h full; [2..]: Wx ring
+  __nv_bfloat16* wxs = (__nv_bfloat16*)(smem + L.wx);
+  __nv_bfloat16* hbuf = (__nv_bfloat16*)(smem + L.hbuf);
+  float* red = (float*)(smem + L.red);
+  __nv_bfloat16* stage = (__nv_bfloat16*)(smem + L.stage);
+  float* cst = (float*)(smem + L.cst);
+  float* bias_s = (float*)(smem + L.bias);
+  const uint32_t full_bar0 = smem_u32(&bars[0]);
+  const uint32_t wx_bar0 = smem_u32(&bars[2]);
+  const uint32_t hbytes = (uint32_t)nb * D * 2;
+  const uint32_t wxbytes = (uint32_t)BC * G * U * 2;
+  const size_t wx_stage_elems = (size_t)BC * G * U;
+
+  const __nv_bfloat16* Wx = (const __nv_bfloat16*)a.Wx;
+  const __nv_bfloat16* R = (const __nv_bfloat16*)a.R;
+  const __nv_bfloat16* bias = (const __nv_bfloat16*)a.bias;
+  const __nv_bfloat16* s0 = (const __nv_bfloat16*)a.s0;
+  __nv_bfloat16* states = (__nv_bfloat16*)a.states;
+  (void)Wx;
+
+  // ---- prologue ------------------------------------------------------------
+  if (tid == 0) {
+    mbar_init(full_bar0, 1);
+    mbar_init(full_bar0 + 8, 1);
+    for (int s = 0; s < FUSED_NS; ++s) mbar_init(wx_bar0 + 8 * s, 1);
+    fence_mbar_init_cluster();
+    prefetch_tensormap(&wxmap);
+  }
+  for (int e = tid; e < 2 * BC * HS; e += nthr) hbuf[e] = __float2bfloat16_rn(0.0f);
+  for (int e = tid; e < BC * U; e += nthr) stage[e] = __float2bfloat16_rn(0.0f);
+  __syncthreads();
+  for (int e = tid; e < nb * D; e += nthr) {
+    const int b = e / D, i = e - b * D;
+    float v = s0 ? __bfloat162float(s0[((size_t)(b0 + b) * N + n) * D + i]) : 0.0f;
+    hbuf[b * HS + i] = __float2bfloat16_rn(v);
+  }
+  for (int e = tid; e < S * BC * U; e += nthr) {
+    const int s = e / (BC * U), r = e - s * BC * U, b = r / U, u = r - b * U;
+    float v = 0.0f;
+    if (b < nb && s0) v = __bfloat162float(s0[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u]);
+    cst[e] = v;
+  }
+  for (int e = tid; e < G * U; e += nthr) {
+    const int g = e / U, u = e - g * U;
+    bias_s[e] = __bfloat162float(bias[((size_t)g * N + n) * D + u0 + u]);
+  }
+
+  // resident R fragments: A[m = unit j][k = input i] = R[g, n, i, j]
+  uint32_t afr[G][KT][4];
+  {
+    const int jr = u0 + mg * 16 + (lane >> 2);
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int kt = 0; kt < KT; ++kt) {
+        const int k0 = (ks * KT + kt) * 16 + 2 * (lane & 3);
+        const __nv_bfloat16* Rg = R + (size_t)(g * N + n) * D * D;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int j = jr + ((q & 1) ? 8 : 0);
+          const int k = k0 + ((q & 2) ? 8 : 0);
+          afr[g][kt][q] = pack_bf16(Rg[(size_t)k * D + j], Rg[(size_t)(k + 1) * D + j]);
+        }
+      }
+  }
+  __syncthreads();
+  cluster_sync_all();  // every CTA's barriers are initialised before any peer signals them
+
+  if (tid == 0) {
+    if (TT > 1) mbar_arrive_expect_tx(full_bar0 + 8, hbytes);  // step 1
+    if (TT > 2) mbar_arrive_expect_tx(full_bar0, hbytes);      // step 2
+    for (int s = 0; s < FUSED_NS - 1 && s < TT; ++s) {
+      mbar_arrive_expect_tx(wx_bar0 + 8 * s, wxbytes);
+      tma_load_5d(smem_u32(wxs + s * wx_stage_elems), &wxmap, wx_bar0 + 8 * s, u0, n, 0, s, b0);
+    }
+  }
+
+  bool failed = false;
+  uint32_t ph0 = 0, ph1 = 0;
+  const int nchunk = nb * (U / 8);  // 16-byte chunks of the CTA's h slice
+
+  // ---- time loop -------------------------------------------------------------
+  for (int t = 0; t < TT; ++t) {
+    const int p = t & 1;
+    if (t > 0) {
+      const uint32_t par = p ? ph1 : ph0;
+      mbar_wait_bounded(full_bar0 + 8 * p, par, a.wait_limit_ns, a.status, failed);
+      if (p) ph1 ^= 1; else ph0 ^= 1;
+      if (tid == 0 && t + 2 <= TT - 1) mbar_arrive_expect_tx(full_bar0 + 8 * p, hbytes);
+    }
+    if (tid == 0 && t + FUSED_NS - 1 < TT) {
+      const int ts = t + FUSED_NS - 1, s = ts % FUSED_NS;
+      mbar_arrive_expect_tx(wx_bar0 + 8 * s, wxbytes);
+      tma_load_5d(smem_u32(wxs + s * wx_stage_elems), &wxmap, wx_bar0 + 8 * s, u0, n, 0, ts, b0);
+    }
+
+    // rec^T = R_slice^T h_{t-1}: this warp's G m-tiles x KT k-tiles
+    float acc[G][NT][4];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[g][nt][q] = 0.0f;
+    const uint32_t hb = smem_u32(hbuf + p * BC * HS);
+#pragma unroll
+    for (int kt = 0; kt < KT; ++kt) {
+      const int k0 = (ks * KT + kt) * 16;
+      uint32_t bf[NT][2];
+      if constexpr (NT == 1) {
+        const uint32_t addr = hb + (uint32_t)(((lane & 7) * HS + k0 + ((lane >> 3) & 1) * 8) * 2);
+        ldmatrix_x2(addr, bf[0][0], bf[0][1]);
+      } else {
+#pragma unroll
+        for (int np = 0; np < NT; np += 2) {
+          const int q = lane >> 3;
+          const uint32_t addr =
+              hb + (uint32_t)((((np + (q >> 1)) * 8 + (lane & 7)) * HS + k0 + (q & 1) * 8) * 2);
+          ldmatrix_x4(addr, bf[np][0], bf[np][1], bf[np + 1][0], bf[np + 1][1]);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[g][nt], afr[g][kt], bf[nt][0], bf[nt][1]);
+    }
+    {
+      const int r = lane >> 2, bc = 2 * (lane & 3);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float* rp = red + (size_t)((mg * KS + ks) * G + g) * BC * FUSED_RED_STRIDE;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int b = nt * 8 + bc;
+          rp[b * FUSED_RED_STRIDE + r] = acc[g][nt][0];
+          rp[(b + 1) * FUSED_RED_STRIDE + r] = acc[g][nt][1];
+          rp[b * FUSED_RED_STRIDE + r + 8] = acc[g][nt][2];
+          rp[(b + 1) * FUSED_RED_STRIDE + r + 8] = acc[g][nt][3];
+        }
+      }
+    }
+    __syncthreads();
+
+    // ---- epilogue: gate assembly and cell update, one (batch row, unit) pair per thread
+    const int ws = t % FUSED_NS;
+    const __nv_bfloat16* wxt = wxs + ws * wx_stage_elems;
+    if (tid < nb * U) mbar_wait_bounded(wx_bar0 + 8 * ws, (t / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
+    for (int e = tid; e < nb * U; e += nthr) {
+      const int b = e / U, u = e - b * U;
+      const int q = u >> 4, r = u & 15;
+      float x[G], rc[G], sp[S], sn[S], pre[P];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float v = bias_s[g * U + u];
+        for (int k2 = 0; k2 < KS; ++k2)
+          v += red[((size_t)((q * KS + k2) * G + g) * BC + b) * FUSED_RED_STRIDE + r];
+        rc[g] = v;
+        x[g] = __bfloat162float(wxt[(b * G + g) * U + u]);
+      }
+#pragma unroll
+      for (int s = 0; s < S; ++s) sp[s] = cst[(s * BC + b) * U + u];
+      cell_fwd<FN, true>(x, rc, sp, sn, pre);
+      const int bg = b0 + b, j = u0 + u;
+#pragma unroll
+      for (int s = 0; s < S; ++s) {
+        cst[(s * BC + b) * U + u] = sn[s];
+        if (states) states[(((size_t)s * B + bg) * TT + t) * N * D + (size_t)n * D + j] = __float2bfloat16_rn(sn[s]);
+      }
+      stage[b * U + u] = __float2bfloat16_rn(sn[0]);
+      if (a.tape) {
+        float* tp = a.tape + (((size_t)t * B + bg) * N + n) * K * D + j;
+#pragma unroll
+        for (int k2 = 0; k2 < P; ++k2) tp[k2 * D] = pre[k2];
+#pragma unroll
+        for (int s = 0; s < S; ++s) tp[(P + s) * D] = sn[s];
+      }
+    }
+    __syncthreads();
+
+    // ---- exchange: push this CTA's slice of h_t into every CTA's next buffer
+    if (t + 1 < TT) {
+      const uint32_t dst_local = smem_u32(hbuf + (p ^ 1) * BC * HS);
+      const uint32_t bar_local = full_bar0 + 8 * (p ^ 1);
+      for (int e = tid; e < nchunk * C; e += nthr) {
+        const int dst = e / nchunk, w = e - dst * nchunk;
+        const int b = w / (U / 8), cu = w - b * (U / 8);
+        const uint4 v = *(const uint4*)(stage + b * U + cu * 8);
+        const uint32_t la = dst_local + (uint32_t)((b * HS + u0 + cu * 8) * 2);
+        st_async_16(mapa_shared(la, dst), v, mapa_shared(bar_local, dst));
+      }
+    }
+  }
+
+  // ---- epilogue of the sequence ---------------------------------------------
+  if (a.last) {
+    __nv_bfloat16* last = (__nv_bfloat16*)a.last;
+    for (int e = tid; e < nb * U; e += nthr) {
+      const int b = e / U, u = e - b * U;
+#pragma unroll
+      for (int s = 0; s < S; ++s)
+        last[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u] = __float2bfloat16_rn(cst[(s * BC + b) * U + u]);
+    }
+  }
+  __syncthreads();
+  cluster_sync_all();  // no CTA leaves while a peer may still write into its shared memory
+}
+
+// Host launcher for one cell type; the TMA descriptor covers Wx as the 5-D
+// tensor (D, N, G, T, B) with a (U, 1, G, 1, BC) box.
+template <int FN>
+cudaError_t fused_fwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream_t st) {
+  constexpr int G = FnInfo<FN>::G;
+  void (*k)(const CUtensorMap, FusedArgs) = nullptr;
+#define RNN_FUSED_PICK(NT_, KT_) \
+  if (sh.NT == NT_ && sh.KT == KT_) k = fused_fwd_kernel<FN, NT_, KT_>;
+  RNN_FUSED_PICK(1, 2) RNN_FUSED_PICK(1, 3) RNN_FUSED_PICK(1, 4)
+  RNN_FUSED_PICK(2, 2) RNN_FUSED_PICK(2, 3) RNN_FUSED_PICK(2, 4)
+#undef RNN_FUSED_PICK
+  if (!k) return cudaErrorInvalidValue;
+  CUtensorMap map;
+  const unsigned long long dims[5] = {(unsigned long long)a.D, (unsigned long long)a.N,
+                                      (unsigned long long)G, (unsigned long long)a.T,
+                                      (unsigned long long)a.B};
+  const unsigned int box[5] = {(unsigned)sh.U, 1u, (unsigned)G, 1u, (unsigned)(8 * sh.NT)};
+  cudaError_t e = encode_tensor_map_bf16(&map, a.Wx, 5, dims, box);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh.smem);
+  if (e != cudaSuccess) return e;
+  if (sh.C > 8) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  const int groups = a.N * ((a.B + 8 * sh.NT - 1) / (8 * sh.NT));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(groups * sh.C);
+  cfg.blockDim = dim3(sh.warps * 32);
+  cfg.dynamicSmemBytes = sh.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = sh.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, k, &cfg);
+  if (e != cudaSuccess) return e;
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  e = cudaLaunchKernelEx(&cfg, k, map, a);
+  note_launch();
+  return e;
+}
+
+}  // namespace rnn

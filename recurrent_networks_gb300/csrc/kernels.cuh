@@ -43,4 +43,31 @@ struct WgradArgs {
 };
 cudaError_t wgrad_run(int dtype, const WgradArgs& a, cudaStream_t st);
 
+// Arguments of the persistent cluster kernels (bf16 storage).
+struct FusedArgs {
+  int B, T, N, D, C, U, KS;
+  const void* Wx;
+  const void* R;
+  const void* bias;
+  const void* s0;
+  void* states;  // may be null (tape-only forward)
+  void* last;    // may be null
+  float* tape;   // may be null
+  const void* dstates;
+  const void* dlast;
+  void* dWx;
+  void* dr;
+  void* ds0;
+  unsigned int* status;  // device status word (bounded waits)
+  unsigned long long wait_limit_ns;
+};
+
+struct FusedShape;
+cudaError_t fused_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st);
+
+// Encodes a tiled TMA descriptor for a dense row-major bf16 tensor whose
+// dims[0] is innermost; box[] gives the tile. No swizzle, zero fill.
+cudaError_t encode_tensor_map_bf16(void* map, const void* base, int rank,
+                                   const unsigned long long* dims, const unsigned int* box);
+
 }  // namespace rnn

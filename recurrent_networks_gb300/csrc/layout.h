@@ -1,0 +1,51 @@
+// Shared-memory layouts of the persistent cluster kernels, used by the
+// kernels and by the host planner (plain C++: no CUDA dependency).
+#pragma once
+#include <stddef.h>
+
+#if defined(__CUDACC__)
+#define RNN_HD __host__ __device__
+#else
+#define RNN_HD
+#endif
+
+namespace rnn {
+
+constexpr int FUSED_NS = 4;           // Wx ring depth (steps in flight)
+constexpr int FUSED_RED_STRIDE = 20;  // floats per batch row of a partial-sum tile (16 used)
+
+// Launch shape of a persistent cluster kernel, chosen by the planner.
+struct FusedShape {
+  int C = 1;      // CTAs per cluster (one cluster per head and batch group)
+  int U = 0;      // units owned by one CTA (D / C)
+  int NT = 0;     // n-tiles of 8 batch rows (BC = 8 NT rows per cluster)
+  int KT = 0;     // k-tiles of 16 per warp
+  int KS = 0;     // warps splitting K for one 16-row group
+  int warps = 0;  // warps per CTA
+  size_t smem = 0;
+};
+
+// Forward cluster kernel: per CTA, G gates x U units, BC batch rows, K split in KS.
+struct FusedSmem {
+  size_t bars, wx, hbuf, red, stage, cst, bias, total;
+  RNN_HD static size_t take(size_t& off, size_t bytes) {
+    size_t o = off;
+    off = (off + bytes + 127) & ~(size_t)127;
+    return o;
+  }
+  RNN_HD static FusedSmem make(int G, int S, int D, int U, int BC, int KS) {
+    FusedSmem m;
+    size_t off = 0;
+    m.bars = take(off, 8 * (2 + FUSED_NS));
+    m.wx = take(off, (size_t)FUSED_NS * BC * G * U * 2);
+    m.hbuf = take(off, (size_t)2 * BC * (D + 8) * 2);
+    m.red = take(off, (size_t)(U / 16) * KS * G * BC * FUSED_RED_STRIDE * 4);
+    m.stage = take(off, (size_t)BC * U * 2);
+    m.cst = take(off, (size_t)S * BC * U * 4);
+    m.bias = take(off, (size_t)G * U * 4);
+    m.total = off;
+    return m;
+  }
+};
+
+}  // namespace rnn

@@ -1,7 +1,19 @@
 // Kernel planner (see plan.h).
+//
+// Forward cluster kernel, candidate point (C, NT, KT):
+//   divisibility   D = C * U,  U = 16 * m  (16-unit row groups per gate),
+//                  D / 16 = KS * KT  (K split over KS warps of KT k-tiles);
+//   inequalities   1 <= warps = (U / 16) * KS <= 8 (256 threads, 1 CTA/SM),
+//                  C <= 16 (non-portable cluster limit),
+//                  shared memory (FusedSmem) <= 227 KB,
+//                  registers: 4 G KT (resident R) + 4 G NT (accumulators)
+//                             + 2 NT (h fragments) + 48 (the rest) <= 255;
+//   objective      modelled step latency (cycles), smallest wins; ties go to
+//                  fewer CTAs.
 #include "plan.h"
 
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "rnn.h"
@@ -9,25 +21,123 @@
 namespace rnn {
 
 static int gates_of(int fn) { return fn == 0 ? 4 : fn == 1 ? 3 : fn == 2 ? 1 : 4; }
+static int states_of(int fn) { return fn == 0 ? 2 : fn == 1 ? 1 : fn == 2 ? 1 : 4; }
+
+static const int kClusterSizes[] = {1, 2, 3, 4, 6, 8, 12, 16};
+static const int kNT[] = {1, 2};
+static const int kKT[] = {2, 3, 4};
+
+bool fused_fwd_feasible(const PlanRequest& q, int C, int NT, int KT, const DeviceLimits& lim, Plan* out) {
+  const int G = gates_of(q.fn), S = states_of(q.fn), D = q.D;
+  if (q.dtype != RNN_BF16) return false;
+  if (C < 1 || C > lim.max_cluster || D % C) return false;
+  const int U = D / C;
+  if (U % 16) return false;
+  if (D % 16 || (D / 16) % KT) return false;
+  const int KS = (D / 16) / KT;
+  const int warps = (U / 16) * KS;
+  if (warps < 1 || warps > lim.max_warps) return false;
+  const int BC = 8 * NT;
+  const int regs = 4 * G * KT + 4 * G * NT + 2 * NT + 48;
+  if (regs > lim.regs_per_thread) return false;
+  const FusedSmem L = FusedSmem::make(G, S, D, U, BC, KS);
+  if (L.total > lim.smem_per_cta) return false;
+  const int groups = q.N * ((q.B + BC - 1) / BC);
+  const int threads = warps * 32;
+  // latency model of one step (cycles): fixed wait/barrier/DSMEM cost, the
+  // warp's dependent MMA chain, the K-split reduction, the cell update per
+  // pair, the st.async issue, and waves when the grid exceeds the SMs.
+  const int nb = q.B < BC ? q.B : BC;
+  const double pairs = (double)nb * U / threads;
+  const double mma = (double)G * KT * NT;
+  const double sends = (double)nb * (U / 8) * C / threads;
+  double cyc = 900.0 + 18.0 * mma + 6.0 * KS * G * (pairs < 1 ? 1 : pairs) +
+               140.0 * (pairs < 1 ? 1 : pairs) + 12.0 * sends + (C > 1 ? 150.0 : 0.0);
+  const int ctas = groups * C;
+  const int waves = (ctas + lim.sms - 1) / lim.sms;
+  cyc *= waves;
+  if (out) {
+    *out = Plan{};
+    out->path = RNN_PATH_FUSED;
+    out->fs.C = C;
+    out->fs.U = U;
+    out->fs.NT = NT;
+    out->fs.KT = KT;
+    out->fs.KS = KS;
+    out->fs.warps = warps;
+    out->fs.smem = L.total;
+    out->groups = groups;
+    out->regs_R = 4 * G * KT;
+    out->model_ns = cyc / 1.9;  // at ~1.9 GHz
+  }
+  return true;
+}
+
+// Optional restriction of the search (tests and tuning sweeps): the
+// environment variables RNN_PLAN_C, RNN_PLAN_NT and RNN_PLAN_KT, when set,
+// admit only candidates with that value.
+static bool env_admits(const char* name, int v) {
+  const char* s = getenv(name);
+  return !s || !*s || atoi(s) == v;
+}
+
+static int fused_fwd_plan(const PlanRequest& q, Plan* best) {
+  DeviceLimits lim;
+  int found = 0;
+  for (int C : kClusterSizes)
+    for (int NT : kNT)
+      for (int KT : kKT) {
+        Plan p;
+        if (!env_admits("RNN_PLAN_C", C) || !env_admits("RNN_PLAN_NT", NT) ||
+            !env_admits("RNN_PLAN_KT", KT))
+          continue;
+        if (!fused_fwd_feasible(q, C, NT, KT, lim, &p)) continue;
+        ++found;
+        const int ctas = p.groups * p.fs.C, bctas = best->groups * best->fs.C;
+        if (found == 1 || p.model_ns < best->model_ns - 1e-9 ||
+            (p.model_ns < best->model_ns + 1e-9 && ctas < bctas))
+          *best = p;
+      }
+  best->candidates = found;
+  return found ? RNN_OK : RNN_EUNSUPPORTED;
+}
 
 static void simt_plan(const PlanRequest& q, Plan* p) {
   *p = Plan{};
   p->path = RNN_PATH_SIMT;
-  p->Bc = q.B < 8 ? q.B : 8;
-  p->groups = q.N * ((q.B + p->Bc - 1) / p->Bc);
+  p->fs.NT = 1;
+  p->groups = q.N * ((q.B + 7) / 8);
 }
 
 int plan_select(const PlanRequest& q, Plan* out) {
   Plan p;
   switch (q.path) {
-    case RNN_PATH_AUTO:
     case RNN_PATH_SIMT:
       simt_plan(q, &p);
       *out = p;
       return RNN_OK;
+    case RNN_PATH_AUTO:
+      // the cluster kernels when a feasible point exists (bf16 forward), else the plain path
+      if (!q.bwd && fused_fwd_plan(q, &p) == RNN_OK) {
+        *out = p;
+        return RNN_OK;
+      }
+      simt_plan(q, &p);
+      *out = p;
+      return RNN_OK;
+    case RNN_PATH_FUSED:
+      if (!q.bwd && fused_fwd_plan(q, &p) == RNN_OK) {
+        *out = p;
+        return RNN_OK;
+      }
+      snprintf(p.why, sizeof(p.why),
+               "no cluster plan for fn=%d dtype=%d D=%d B=%d%s (bf16 only; D = C*U with U %% 16 == 0, "
+               "D/16 = KS*KT, <= 8 warps, smem <= 227 KB)",
+               q.fn, q.dtype, q.D, q.B, q.bwd ? " (backward)" : "");
+      *out = p;
+      return RNN_EUNSUPPORTED;
     default:
       snprintf(p.why, sizeof(p.why), "path %d not available for fn=%d D=%d", q.path, q.fn, q.D);
-      (void)gates_of;
       *out = p;
       return RNN_EUNSUPPORTED;
   }
@@ -40,10 +150,10 @@ void plan_describe(const Plan& p, int rc, char* buf, size_t len) {
   }
   const char* names[] = {"auto", "fused", "alternating", "simt"};
   snprintf(buf, len,
-           "path=%s C=%d U=%d Bc=%d NT=%d groups=%d MT=%d KT=%d ksplit=%d warps=%d regs_R=%d "
-           "smem=%zu scratch=%zu model_ns=%.0f",
-           names[p.path & 3], p.C, p.U, p.Bc, p.NT, p.groups, p.MT, p.KT, p.ksplit, p.warps,
-           p.regs_R, p.smem, p.scratch_bytes, p.model_ns);
+           "path=%s C=%d U=%d NT=%d KT=%d KS=%d warps=%d groups=%d regs_R=%d smem=%zu scratch=%zu "
+           "model_ns=%.0f candidates=%d",
+           names[p.path & 3], p.fs.C, p.fs.U, p.fs.NT, p.fs.KT, p.fs.KS, p.fs.warps, p.groups, p.regs_R,
+           p.fs.smem, p.scratch_bytes, p.model_ns, p.candidates);
 }
 
 }  // namespace rnn

@@ -1,0 +1,56 @@
+// TMA descriptor encoding and the per-cell dispatch of the cluster kernels.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kernels.cuh"
+#include "layout.h"
+
+namespace rnn {
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  }
+  return fn;
+}
+
+cudaError_t encode_tensor_map_bf16(void* map, const void* base, int rank, const unsigned long long* dims,
+                                   const unsigned int* box) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn || rank < 1 || rank > 5) return cudaErrorNotSupported;
+  cuuint64_t gdim[5], gstride[4];
+  cuuint32_t bdim[5], estr[5];
+  unsigned long long stride = 2;  // bytes
+  for (int d = 0; d < rank; ++d) {
+    gdim[d] = dims[d];
+    bdim[d] = box[d];
+    estr[d] = 1;
+    if (d > 0) gstride[d - 1] = stride;
+    stride *= dims[d];
+  }
+  CUresult r = fn((CUtensorMap*)map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, (void*)base, gdim,
+                  gstride, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int FN>
+cudaError_t fused_fwd_launch(const FusedShape&, const FusedArgs&, cudaStream_t);
+
+cudaError_t fused_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st) {
+  switch (fn) {
+    case LSTM: return fused_fwd_launch<LSTM>(sh, a, st);
+    case GRU: return fused_fwd_launch<GRU>(sh, a, st);
+    case ELMAN: return fused_fwd_launch<ELMAN>(sh, a, st);
+    case SLSTM: return fused_fwd_launch<SLSTM>(sh, a, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace rnn

@@ -89,3 +89,62 @@ def test_autograd_function_matches_abi():
     check_grad("dR", torch.float32, leaves["R"].grad, rdR)
     check_grad("db", torch.float32, leaves["b"].grad, rdb)
     check_grad("ds0", torch.float32, leaves["states0"].grad, rds0)
+
+
+# ---------------------------------------------------------------- cluster kernels
+# (fn, B, T, N, D, env restriction of the planner: cluster size C, n-tiles NT, k-tiles KT)
+FUSED_CASES = [
+    ("lstm", 3, 37, 2, 64, dict(C=1)),
+    ("lstm", 3, 37, 2, 64, dict(C=2, NT=2)),
+    ("lstm", 3, 37, 2, 64, dict(C=4, KT=4)),
+    ("lstm", 9, 21, 1, 128, dict(C=8)),
+    ("lstm", 5, 19, 1, 256, dict(C=16)),
+    ("lstm", 8, 40, 3, 256, dict(C=8, KT=4)),
+    ("gru", 9, 20, 3, 48, dict(C=3)),
+    ("gru", 16, 25, 2, 128, dict(C=4, NT=2)),
+    ("elman", 16, 33, 1, 128, dict(C=1)),
+    ("elman", 7, 18, 2, 64, dict(C=2, KT=4)),
+    ("slstm", 5, 29, 2, 96, dict(C=3, KT=3)),
+    ("slstm", 16, 23, 1, 192, dict(C=6, NT=2)),
+    ("slstm", 4, 17, 1, 192, dict(C=12)),
+]
+
+
+def _restrict(monkeypatch, restr):
+    for k in ("C", "NT", "KT"):
+        monkeypatch.delenv(f"RNN_PLAN_{k}", raising=False)
+    for k, v in restr.items():
+        monkeypatch.setenv(f"RNN_PLAN_{k}", str(v))
+
+
+@pytest.mark.parametrize("case", FUSED_CASES,
+                         ids=lambda c: "%s-B%dT%dN%dD%d-" % c[:5] + "-".join(f"{k}{v}" for k, v in c[5].items()))
+def test_fused_forward_parity(case, monkeypatch):
+    fn, B, T, N, D, restr = case
+    _restrict(monkeypatch, restr)
+    inp = _inputs(fn, (B, T, N, D), torch.bfloat16, seed=500 + B + T + D)
+    dims = _lib.make_dims(B, T, N, D, fn, torch.bfloat16, "fused")
+    rc, desc = _lib.rnn_plan_describe(dims)
+    assert rc == 0 and "path=fused" in desc and f"C={restr['C']} " in desc, desc
+    st, last, tape = run_fwd(fn, inp, "fused")
+    ref_st, ref_last = oracle_fwd(fn, inp)
+    check_states(fn, torch.bfloat16, st, ref_st)
+    check_states(fn, torch.bfloat16, last, ref_last, "last")
+    # the backward (plain path) consumes the cluster kernel's tape
+    dWx, dR, db, ds0 = run_bwd(fn, inp, st, tape, "simt")
+    rdWx, rdR, rdb, rds0 = oracle_bwd(fn, inp)
+    check_grad(f"{fn} dWx", torch.bfloat16, dWx, rdWx)
+    check_grad(f"{fn} dR", torch.bfloat16, dR, rdR)
+    check_grad(f"{fn} db", torch.bfloat16, db, rdb)
+    check_grad(f"{fn} dstates0", torch.bfloat16, ds0, rds0)
+
+
+def test_fused_matches_simt_forward_closely(monkeypatch):
+    """Same arithmetic (bf16 operands, fp32 accumulation) on both paths: the
+    states agree far more closely than either does with the fp64 oracle."""
+    _restrict(monkeypatch, dict(C=4))
+    inp = _inputs("lstm", (6, 30, 2, 128), torch.bfloat16, seed=42)
+    st_f, _, _ = run_fwd("lstm", inp, "fused", want_tape=False)
+    st_s, _, _ = run_fwd("lstm", inp, "simt", want_tape=False)
+    diff = (st_f.float() - st_s.float()).abs().max().item()
+    assert diff <= 2e-2, diff
