@@ -217,18 +217,32 @@ int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
   SimtArgs a{};
   a.B = d->B; a.T = d->T; a.N = d->N; a.D = d->D;
   a.R = R; a.s0 = states0; a.tape = (float*)tp;
-  a.dstates = dstates; a.dlast = dlast; a.dWx = dWx; a.dr = ws + w.dr; a.ds0 = dstates0;
+  // the recurrent-branch gradient equals dWx except for the GRU candidate gate:
+  // reuse dWx as the weight-gradient operand when it is there
+  void* drbuf = (d->function != RNN_GRU && dWx) ? dWx : (void*)(ws + w.dr);
+  a.dstates = dstates; a.dlast = dlast; a.dWx = dWx; a.dr = drbuf; a.ds0 = dstates0;
   rc = RNN_EUNSUPPORTED;
   prof_mark(1, 0, st);
   switch (plan.path) {
     case RNN_PATH_SIMT:
       rc = cuda_status(simt_run(d->function, d->dtype, a, true, st));
       break;
+    case RNN_PATH_FUSED: {
+      FusedArgs f{};
+      f.B = d->B; f.T = d->T; f.N = d->N; f.D = d->D;
+      f.C = plan.fs.C; f.U = plan.fs.U; f.KS = plan.fs.KS;
+      f.R = R; f.s0 = states0; f.tape = (float*)tp;
+      f.dstates = dstates; f.dlast = dlast; f.dWx = dWx; f.dr = drbuf; f.ds0 = dstates0;
+      f.status = (unsigned int*)ws;
+      f.wait_limit_ns = g_wait_limit_ns;
+      rc = cuda_status(fused_bwd_run(d->function, plan.fs, f, st));
+      break;
+    }
   }
   prof_mark(1, 1, st);
   if (rc) return rc;
   if (dR || db) {
-    WgradArgs g{d->B, d->T, d->N, d->D, z.G, states, states0, ws + w.dr, dR, db};
+    WgradArgs g{d->B, d->T, d->N, d->D, z.G, states, states0, drbuf, dR, db};
     rc = cuda_status(wgrad_run(d->dtype, g, st));
   }
   return rc;

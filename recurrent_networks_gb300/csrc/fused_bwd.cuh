@@ -1,0 +1,325 @@
+// Persistent thread-block-cluster backward scan (bf16 storage, fp32 arithmetic).
+//
+// Reverse-time counterpart of the forward cluster kernel. One cluster of C
+// CTAs runs one head and batch group from t = T-1 down to 0; CTA c owns units
+// [c*U, (c+1)*U) and carries their state gradients (fp32, shared memory).
+// Per step:
+//   1. dh_t[own units] = sum over the C CTAs of the fp32 partial products
+//      received for this step (plus dstates[:, t] and the carried terms);
+//   2. the cell derivative gives dWx[:, t] and the recurrent-branch gradient
+//      dr_t of the CTA's units (written out for the weight gradients);
+//   3. the CTA multiplies its own dr_t (bf16) with its resident slice of R,
+//        partial[i, b] = sum_{g, j in own units} R[g, n, i, j] dr_t[b, g, j],
+//      for ALL rows i (M = D, K = G*U, N = batch) on the tensor cores, and
+//   4. pushes each 16-row block of partials to the CTA owning those rows with
+//      st.async (a reduce-scatter; the owner's mbarrier counts the bytes).
+// tape[t] and dstates[:, t] stream in through a TMA ring several steps ahead.
+#pragma once
+#include <cuda.h>
+
+#include "kernels.cuh"
+#include "layout.h"
+#include "ptx.cuh"
+
+namespace rnn {
+
+template <int FN, int NT, int MT>
+__global__ void __launch_bounds__(256, 1)
+    fused_bwd_kernel(const __grid_constant__ CUtensorMap tapemap, const __grid_constant__ CUtensorMap dstmap,
+                     FusedArgs a) {
+  constexpr int G = FnInfo<FN>::G, S = FnInfo<FN>::S, P = FnInfo<FN>::P, K = P + S;
+  constexpr int BC = 8 * NT;
+  constexpr int KTM = FUSED_BWD_MAX_KTA;
+  const int C = a.C, U = a.U, D = a.D, TT = a.T, N = a.N, B = a.B;
+  const int KTA = G * U / 16;  // k-tiles of the CTA's own gradient block
+  const int KB = G * U + 8;    // row stride (elements) of the gradient operand
+  const uint32_t rank = cluster_ctarank();
+  const int grp = blockIdx.x / C;
+  const int n = grp % N;
+  const int b0 = (grp / N) * BC;
+  const int nb = min(BC, B - b0);
+  const int u0 = (int)rank * U;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  const FusedBwdSmem L = FusedBwdSmem::make(G, S, K, U, BC, C);
+  uint64_t* bars = (uint64_t*)(smem + L.bars);  // [0,1]: partials full; [2..]: ring
+  unsigned char* ring = smem + L.ring;
+  float* recv = (float*)(smem + L.recv);  // [2][C][U][BC]
+  __nv_bfloat16* drb = (__nv_bfloat16*)(smem + L.drb);  // [2][BC][KB]
+  float* ds = (float*)(smem + L.ds);    // [S][BC][U]
+  float* s0s = (float*)(smem + L.s0);   // [S][BC][U]
+  const uint32_t recv_bar0 = smem_u32(&bars[0]);
+  const uint32_t ring_bar0 = smem_u32(&bars[2]);
+  const uint32_t rbytes = (uint32_t)C * U * BC * 4;
+  const bool has_dst = a.dstates != nullptr;
+  const uint32_t stage_bytes = (uint32_t)(L.tape_bytes + (has_dst ? (size_t)S * BC * U * 2 : 0));
+
+  const __nv_bfloat16* R = (const __nv_bfloat16*)a.R;
+  const __nv_bfloat16* s0 = (const __nv_bfloat16*)a.s0;
+  const __nv_bfloat16* dlast = (const __nv_bfloat16*)a.dlast;
+  __nv_bfloat16* dWx = (__nv_bfloat16*)a.dWx;
+  __nv_bfloat16* dro = (__nv_bfloat16*)a.dr;
+  const bool write_dr = dro && (FN == GRU || (void*)dro != (void*)dWx);
+
+  // ---- prologue --------------------------------------------------------------
+  if (tid == 0) {
+    mbar_init(recv_bar0, 1);
+    mbar_init(recv_bar0 + 8, 1);
+    for (int s = 0; s < FUSED_NS; ++s) mbar_init(ring_bar0 + 8 * s, 1);
+    fence_mbar_init_cluster();
+    prefetch_tensormap(&tapemap);
+    if (has_dst) prefetch_tensormap(&dstmap);
+  }
+  for (int e = tid; e < 2 * BC * KB; e += nthr) drb[e] = __float2bfloat16_rn(0.0f);
+  for (int e = tid; e < S * BC * U; e += nthr) {
+    const int s = e / (BC * U), r = e - s * BC * U, b = r / U, u = r - b * U;
+    float v = 0.0f;
+    if (b < nb && s0) v = __bfloat162float(s0[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u]);
+    s0s[e] = v;
+    ds[e] = 0.0f;
+  }
+  // resident R fragments: A[m = row i][k = (g, j)] = R[g, n, i, u0 + j]
+  uint32_t afr[MT][KTM][4];
+  {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const int ir = (warp * MT + mt) * 16 + (lane >> 2);
+#pragma unroll
+      for (int kt = 0; kt < KTM; ++kt) {
+        if (kt < KTA) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int i = ir + ((q & 1) ? 8 : 0);
+            const int k = kt * 16 + 2 * (lane & 3) + ((q & 2) ? 8 : 0);
+            const int g = k / U, j = k - g * U;
+            afr[mt][kt][q] = *(const uint32_t*)(R + ((size_t)(g * N + n) * D + i) * D + u0 + j);
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) afr[mt][kt][q] = 0u;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  cluster_sync_all();
+
+  auto issue_stage = [&](int k) {  // processing index k <-> time step T-1-k
+    const int t = TT - 1 - k, s = k % FUSED_NS;
+    unsigned char* st = ring + (size_t)s * L.ring_stage;
+    mbar_arrive_expect_tx(ring_bar0 + 8 * s, stage_bytes);
+    tma_load_5d(smem_u32(st), &tapemap, ring_bar0 + 8 * s, u0, 0, n, b0, t);
+    if (has_dst) tma_load_5d(smem_u32(st + L.dst_off), &dstmap, ring_bar0 + 8 * s, u0, n, t, b0, 0);
+  };
+  if (tid == 0) {
+    mbar_arrive_expect_tx(recv_bar0 + 8 * ((TT - 2) & 1), rbytes);
+    if (TT >= 2) mbar_arrive_expect_tx(recv_bar0 + 8 * ((TT - 3) & 1), rbytes);
+    for (int k = 0; k < FUSED_NS - 1 && k < TT; ++k) issue_stage(k);
+  }
+
+  bool failed = false;
+  uint32_t ph[2] = {0u, 0u};
+  const int q4 = lane & 3, r8 = lane >> 2;
+
+  // ---- reverse time loop ---------------------------------------------------------
+  for (int k = 0; k < TT; ++k) {
+    const int t = TT - 1 - k;
+    const int pb = t & 1;  // gradient-operand buffer of this step
+    if (tid == 0 && k + FUSED_NS - 1 < TT) issue_stage(k + FUSED_NS - 1);
+    if (t < TT - 1) {  // partial sums for dh_t arrived
+      const int bi = t & 1;
+      mbar_wait_bounded(recv_bar0 + 8 * bi, ph[bi], a.wait_limit_ns, a.status, failed);
+      ph[bi] ^= 1u;
+      if (tid == 0 && t - 2 >= -1) mbar_arrive_expect_tx(recv_bar0 + 8 * bi, rbytes);
+    }
+    const int sc = k % FUSED_NS, sn_ = (k + 1) % FUSED_NS;
+    const float* tp = (const float*)(ring + (size_t)sc * L.ring_stage);
+    const __nv_bfloat16* dstage = (const __nv_bfloat16*)(ring + (size_t)sc * L.ring_stage + L.dst_off);
+    const float* tq = (const float*)(ring + (size_t)sn_ * L.ring_stage);
+    if (tid < nb * U) {
+      mbar_wait_bounded(ring_bar0 + 8 * sc, (k / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
+      if (t > 0) mbar_wait_bounded(ring_bar0 + 8 * sn_, ((k + 1) / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
+    }
+    const float* rv = recv + (size_t)(t & 1) * C * U * BC;
+    __nv_bfloat16* drw = drb + (size_t)pb * BC * KB;
+    for (int e = tid; e < nb * U; e += nthr) {
+      const int b = e / U, u = e - b * U;
+      float pre[P], sp[S], sn[S], dsn[S], dx[G], dr[G], dsp[S];
+#pragma unroll
+      for (int kk = 0; kk < P; ++kk) pre[kk] = tp[(b * K + kk) * U + u];
+#pragma unroll
+      for (int s = 0; s < S; ++s) {
+        sn[s] = tp[(b * K + P + s) * U + u];
+        sp[s] = t > 0 ? tq[(b * K + P + s) * U + u] : s0s[(s * BC + b) * U + u];
+        float d = ds[(s * BC + b) * U + u];
+        if (has_dst) d += __bfloat162float(dstage[(s * BC + b) * U + u]);
+        if (dlast && t == TT - 1) d += __bfloat162float(dlast[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u]);
+        dsn[s] = d;
+      }
+      if (t < TT - 1) {
+        float acc = 0.0f;
+        for (int c = 0; c < C; ++c) acc += rv[((size_t)c * U + u) * BC + b];
+        dsn[0] += acc;
+      }
+      cell_bwd<FN, true>(pre, sp, sn, dsn, dx, dr, dsp);
+      const size_t o = (((size_t)(b0 + b) * TT + t) * G) * N * D + (size_t)n * D + u0 + u;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        if (dWx) dWx[o + (size_t)g * N * D] = __float2bfloat16_rn(dx[g]);
+        if (write_dr) dro[o + (size_t)g * N * D] = __float2bfloat16_rn(dr[g]);
+        drw[b * KB + g * U + u] = __float2bfloat16_rn(dr[g]);
+      }
+#pragma unroll
+      for (int s = 0; s < S; ++s) ds[(s * BC + b) * U + u] = dsp[s];
+    }
+    __syncthreads();
+
+    // partial[i, b] = sum_k A[i][k] drb[b][k] for this warp's MT m-tiles
+    float acc[MT][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[mt][nt][q] = 0.0f;
+    const uint32_t hb = smem_u32(drw);
+#pragma unroll
+    for (int kt = 0; kt < KTM; ++kt) {
+      if (kt < KTA) {
+        const int k0 = kt * 16;
+        uint32_t bf[NT][2];
+        if constexpr (NT == 1) {
+          const uint32_t addr = hb + (uint32_t)(((lane & 7) * KB + k0 + ((lane >> 3) & 1) * 8) * 2);
+          ldmatrix_x2(addr, bf[0][0], bf[0][1]);
+        } else {
+#pragma unroll
+          for (int np = 0; np < NT; np += 2) {
+            const int q = lane >> 3;
+            const uint32_t addr =
+                hb + (uint32_t)((((np + (q >> 1)) * 8 + (lane & 7)) * KB + k0 + (q & 1) * 8) * 2);
+            ldmatrix_x4(addr, bf[np][0], bf[np][1], bf[np + 1][0], bf[np + 1][1]);
+          }
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[mt][nt], afr[mt][kt], bf[nt][0], bf[nt][1]);
+      }
+    }
+    // reduce-scatter: each lane assembles 4 consecutive batch columns of one row
+    {
+      const int bi = (t - 1) & 1;  // consumption t-1 (t = 0 feeds the final dh_{-1})
+      const uint32_t dst_base = smem_u32(recv + ((size_t)bi * C + rank) * U * BC);
+      const uint32_t bar_local = recv_bar0 + 8 * bi;
+      const bool even = (q4 & 1) == 0;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float* v = acc[mt][nt];
+          const float sa = even ? v[2] : v[0];
+          const float sb = even ? v[3] : v[1];
+          const float ra = __shfl_xor_sync(0xffffffffu, sa, 1);
+          const float rb = __shfl_xor_sync(0xffffffffu, sb, 1);
+          uint4 out;
+          int row, bcol;
+          if (even) {
+            out = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(ra), __float_as_uint(rb));
+            row = r8;
+            bcol = nt * 8 + 2 * q4;
+          } else {
+            out = make_uint4(__float_as_uint(ra), __float_as_uint(rb), __float_as_uint(v[2]), __float_as_uint(v[3]));
+            row = r8 + 8;
+            bcol = nt * 8 + 2 * q4 - 2;
+          }
+          const int i = (warp * MT + mt) * 16 + row;
+          const int owner = i / U, ul = i - owner * U;
+          const uint32_t la = dst_base + (uint32_t)((ul * BC + bcol) * 4);
+          st_async_16(mapa_shared(la, (uint32_t)owner), out, mapa_shared(bar_local, (uint32_t)owner));
+        }
+    }
+  }
+
+  // ---- dstates0: the carried gradients after step 0 ------------------------------
+  {
+    const int bi = 1;  // consumption -1
+    mbar_wait_bounded(recv_bar0 + 8 * bi, ph[bi], a.wait_limit_ns, a.status, failed);
+    const float* rv = recv + (size_t)bi * C * U * BC;
+    __nv_bfloat16* ds0 = (__nv_bfloat16*)a.ds0;
+    if (ds0)
+      for (int e = tid; e < nb * U; e += nthr) {
+        const int b = e / U, u = e - b * U;
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+          float v = ds[(s * BC + b) * U + u];
+          if (s == 0)
+            for (int c = 0; c < C; ++c) v += rv[((size_t)c * U + u) * BC + b];
+          ds0[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u] = __float2bfloat16_rn(v);
+        }
+      }
+  }
+  __syncthreads();
+  cluster_sync_all();
+}
+
+template <int FN>
+cudaError_t fused_bwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream_t st) {
+  constexpr int G = FnInfo<FN>::G, S = FnInfo<FN>::S, K = FnInfo<FN>::P + FnInfo<FN>::S;
+  void (*k)(const CUtensorMap, const CUtensorMap, FusedArgs) = nullptr;
+#define RNN_FUSED_BWD_PICK(NT_, MT_) \
+  if (sh.NT == NT_ && sh.MT == MT_) k = fused_bwd_kernel<FN, NT_, MT_>;
+  RNN_FUSED_BWD_PICK(1, 1) RNN_FUSED_BWD_PICK(1, 2) RNN_FUSED_BWD_PICK(2, 1) RNN_FUSED_BWD_PICK(2, 2)
+#undef RNN_FUSED_BWD_PICK
+  if (!k) return cudaErrorInvalidValue;
+  const unsigned BC = 8u * sh.NT;
+  CUtensorMap tmap, dmap;
+  {
+    const unsigned long long dims[5] = {(unsigned long long)a.D, (unsigned long long)K,
+                                        (unsigned long long)a.N, (unsigned long long)a.B,
+                                        (unsigned long long)a.T};
+    const unsigned int box[5] = {(unsigned)sh.U, (unsigned)K, 1u, BC, 1u};
+    cudaError_t e = encode_tensor_map(&tmap, a.tape, 4, 5, dims, box);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.dstates) {
+    const unsigned long long dims[5] = {(unsigned long long)a.D, (unsigned long long)a.N,
+                                        (unsigned long long)a.T, (unsigned long long)a.B,
+                                        (unsigned long long)S};
+    const unsigned int box[5] = {(unsigned)sh.U, 1u, 1u, BC, (unsigned)S};
+    cudaError_t e = encode_tensor_map(&dmap, a.dstates, 2, 5, dims, box);
+    if (e != cudaSuccess) return e;
+  } else {
+    dmap = tmap;  // unused
+  }
+  (void)G;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh.smem);
+  if (e != cudaSuccess) return e;
+  if (sh.C > 8) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  const int groups = a.N * ((a.B + (int)BC - 1) / (int)BC);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(groups * sh.C);
+  cfg.blockDim = dim3(sh.warps * 32);
+  cfg.dynamicSmemBytes = sh.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = sh.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, k, &cfg);
+  if (e != cudaSuccess) return e;
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  e = cudaLaunchKernelEx(&cfg, k, tmap, dmap, a);
+  note_launch();
+  return e;
+}
+
+}  // namespace rnn

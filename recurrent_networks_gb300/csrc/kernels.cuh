@@ -69,5 +69,8 @@ cudaError_t fused_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cuda
 // dims[0] is innermost; box[] gives the tile. No swizzle, zero fill.
 cudaError_t encode_tensor_map_bf16(void* map, const void* base, int rank,
                                    const unsigned long long* dims, const unsigned int* box);
+cudaError_t encode_tensor_map(void* map, const void* base, int elem_bytes, int rank,
+                              const unsigned long long* dims, const unsigned int* box);
+cudaError_t fused_bwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st);
 
 }  // namespace rnn

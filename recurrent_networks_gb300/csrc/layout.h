@@ -21,6 +21,7 @@ struct FusedShape {
   int NT = 0;     // n-tiles of 8 batch rows (BC = 8 NT rows per cluster)
   int KT = 0;     // k-tiles of 16 per warp
   int KS = 0;     // warps splitting K for one 16-row group
+  int MT = 0;     // backward: m-tiles (16 rows of dh) per warp
   int warps = 0;  // warps per CTA
   size_t smem = 0;
 };
@@ -43,6 +44,32 @@ struct FusedSmem {
     m.stage = take(off, (size_t)BC * U * 2);
     m.cst = take(off, (size_t)S * BC * U * 4);
     m.bias = take(off, (size_t)G * U * 4);
+    m.total = off;
+    return m;
+  }
+};
+
+// Backward cluster kernel: per CTA, the U units it owns; the reverse scan
+// streams tape[t] ([BC][K][U] fp32) and dstates[:, t] ([S][BC][U] bf16) through
+// a TMA ring, receives C fp32 partial sums of dh for its units per step
+// ([C][U][BC]), and feeds its own recurrent-branch gradients ([BC][G U + 8]
+// bf16) to the tensor cores.
+constexpr int FUSED_BWD_MAX_KTA = 8;  // k-tiles G*U/16 a CTA may own
+
+struct FusedBwdSmem {
+  size_t bars, ring, ring_stage, tape_bytes, dst_off, recv, drb, ds, s0, total;
+  RNN_HD static FusedBwdSmem make(int G, int S, int K, int U, int BC, int C) {
+    FusedBwdSmem m;
+    size_t off = 0;
+    m.bars = FusedSmem::take(off, 8 * (2 + FUSED_NS));
+    m.tape_bytes = (size_t)BC * K * U * 4;
+    m.dst_off = (m.tape_bytes + 127) & ~(size_t)127;
+    m.ring_stage = (m.dst_off + (size_t)S * BC * U * 2 + 127) & ~(size_t)127;
+    m.ring = FusedSmem::take(off, FUSED_NS * m.ring_stage);
+    m.recv = FusedSmem::take(off, (size_t)2 * C * U * BC * 4);
+    m.drb = FusedSmem::take(off, (size_t)2 * BC * (G * U + 8) * 2);
+    m.ds = FusedSmem::take(off, (size_t)S * BC * U * 4);
+    m.s0 = FusedSmem::take(off, (size_t)S * BC * U * 4);
     m.total = off;
     return m;
   }

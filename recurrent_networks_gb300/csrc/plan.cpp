@@ -102,6 +102,80 @@ static int fused_fwd_plan(const PlanRequest& q, Plan* best) {
   return found ? RNN_OK : RNN_EUNSUPPORTED;
 }
 
+// Backward cluster kernel, candidate point (C, NT, MT):
+//   divisibility   D = C * U, U = 16 m;  D / 16 = warps * MT (row blocks of dh);
+//   inequalities   G U / 16 <= 8 (own gradient block k-tiles), 1 <= warps <= 8,
+//                  C <= 16, shared memory (FusedBwdSmem) <= 227 KB,
+//                  registers 32 MT (resident R) + 4 MT NT + 64 <= 255.
+static const int kMT[] = {1, 2};
+
+bool fused_bwd_feasible(const PlanRequest& q, int C, int NT, int MT, const DeviceLimits& lim, Plan* out) {
+  const int G = gates_of(q.fn), S = states_of(q.fn), D = q.D;
+  const int K = (q.fn == 1 ? 4 : G) + S;
+  if (q.dtype != RNN_BF16) return false;
+  if (C < 1 || C > lim.max_cluster || D % C) return false;
+  const int U = D / C;
+  if (U % 16 || D % 16) return false;
+  const int KTA = G * U / 16;
+  if (KTA < 1 || KTA > FUSED_BWD_MAX_KTA) return false;
+  if ((D / 16) % MT) return false;
+  const int warps = (D / 16) / MT;
+  if (warps < 1 || warps > lim.max_warps) return false;
+  const int BC = 8 * NT;
+  const int regs = 32 * MT + 4 * MT * NT + 64;
+  if (regs > lim.regs_per_thread) return false;
+  const FusedBwdSmem L = FusedBwdSmem::make(G, S, K, U, BC, C);
+  if (L.total > lim.smem_per_cta) return false;
+  const int groups = q.N * ((q.B + BC - 1) / BC);
+  const int threads = warps * 32;
+  const int nb = q.B < BC ? q.B : BC;
+  double pairs = (double)nb * U / threads;
+  if (pairs < 1) pairs = 1;
+  const double mma = (double)MT * KTA * NT;
+  double cyc = 900.0 + 18.0 * mma + (160.0 + 4.0 * C) * pairs + 25.0 * MT * NT + (C > 1 ? 150.0 : 0.0);
+  const int ctas = groups * C;
+  cyc *= (ctas + lim.sms - 1) / lim.sms;
+  if (out) {
+    *out = Plan{};
+    out->path = RNN_PATH_FUSED;
+    out->fs.C = C;
+    out->fs.U = U;
+    out->fs.NT = NT;
+    out->fs.MT = MT;
+    out->fs.KT = KTA;
+    out->fs.warps = warps;
+    out->fs.smem = L.total;
+    out->groups = groups;
+    out->regs_R = 4 * MT * KTA;
+    out->model_ns = cyc / 1.9;
+  }
+  return true;
+}
+
+static int fused_bwd_plan(const PlanRequest& q, Plan* best) {
+  DeviceLimits lim;
+  int found = 0;
+  for (int C : kClusterSizes)
+    for (int NT : kNT)
+      for (int MT : kMT) {
+        Plan p;
+        if (!env_admits("RNN_PLAN_C", C) || !env_admits("RNN_PLAN_NT", NT) || !env_admits("RNN_PLAN_MT", MT))
+          continue;
+        if (!fused_bwd_feasible(q, C, NT, MT, lim, &p)) continue;
+        ++found;
+        const int ctas = p.groups * p.fs.C, bctas = best->groups * best->fs.C;
+        if (found == 1 || p.model_ns < best->model_ns - 1e-9 ||
+            (p.model_ns < best->model_ns + 1e-9 && ctas < bctas))
+          *best = p;
+      }
+  best->candidates = found;
+  return found ? RNN_OK : RNN_EUNSUPPORTED;
+}
+
+static int fused_plan(const PlanRequest& q, Plan* best) {
+  return q.bwd ? fused_bwd_plan(q, best) : fused_fwd_plan(q, best);
+}
+
 static void simt_plan(const PlanRequest& q, Plan* p) {
   *p = Plan{};
   p->path = RNN_PATH_SIMT;
@@ -117,8 +191,8 @@ int plan_select(const PlanRequest& q, Plan* out) {
       *out = p;
       return RNN_OK;
     case RNN_PATH_AUTO:
-      // the cluster kernels when a feasible point exists (bf16 forward), else the plain path
-      if (!q.bwd && fused_fwd_plan(q, &p) == RNN_OK) {
+      // the cluster kernels when a feasible point exists (bf16), else the plain path
+      if (fused_plan(q, &p) == RNN_OK) {
         *out = p;
         return RNN_OK;
       }
@@ -126,7 +200,7 @@ int plan_select(const PlanRequest& q, Plan* out) {
       *out = p;
       return RNN_OK;
     case RNN_PATH_FUSED:
-      if (!q.bwd && fused_fwd_plan(q, &p) == RNN_OK) {
+      if (fused_plan(q, &p) == RNN_OK) {
         *out = p;
         return RNN_OK;
       }

@@ -20,13 +20,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-cudaError_t encode_tensor_map_bf16(void* map, const void* base, int rank, const unsigned long long* dims,
-                                   const unsigned int* box) {
+cudaError_t encode_tensor_map(void* map, const void* base, int elem_bytes, int rank,
+                              const unsigned long long* dims, const unsigned int* box) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-  if (!fn || rank < 1 || rank > 5) return cudaErrorNotSupported;
+  if (!fn || rank < 1 || rank > 5 || (elem_bytes != 2 && elem_bytes != 4)) return cudaErrorNotSupported;
   cuuint64_t gdim[5], gstride[4];
   cuuint32_t bdim[5], estr[5];
-  unsigned long long stride = 2;  // bytes
+  unsigned long long stride = (unsigned long long)elem_bytes;  // bytes
   for (int d = 0; d < rank; ++d) {
     gdim[d] = dims[d];
     bdim[d] = box[d];
@@ -34,14 +34,33 @@ cudaError_t encode_tensor_map_bf16(void* map, const void* base, int rank, const 
     if (d > 0) gstride[d - 1] = stride;
     stride *= dims[d];
   }
-  CUresult r = fn((CUtensorMap*)map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, (void*)base, gdim,
+  const CUtensorMapDataType ty =
+      elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  CUresult r = fn((CUtensorMap*)map, ty, (cuuint32_t)rank, (void*)base, gdim,
                   gstride, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t encode_tensor_map_bf16(void* map, const void* base, int rank, const unsigned long long* dims,
+                                   const unsigned int* box) {
+  return encode_tensor_map(map, base, 2, rank, dims, box);
+}
+
 template <int FN>
 cudaError_t fused_fwd_launch(const FusedShape&, const FusedArgs&, cudaStream_t);
+template <int FN>
+cudaError_t fused_bwd_launch(const FusedShape&, const FusedArgs&, cudaStream_t);
+
+cudaError_t fused_bwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st) {
+  switch (fn) {
+    case LSTM: return fused_bwd_launch<LSTM>(sh, a, st);
+    case GRU: return fused_bwd_launch<GRU>(sh, a, st);
+    case ELMAN: return fused_bwd_launch<ELMAN>(sh, a, st);
+    case SLSTM: return fused_bwd_launch<SLSTM>(sh, a, st);
+  }
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t fused_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st) {
   switch (fn) {

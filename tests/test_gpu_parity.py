@@ -102,7 +102,7 @@ FUSED_CASES = [
     ("lstm", 8, 40, 3, 256, dict(C=8, KT=4)),
     ("gru", 9, 20, 3, 48, dict(C=3)),
     ("gru", 16, 25, 2, 128, dict(C=4, NT=2)),
-    ("elman", 16, 33, 1, 128, dict(C=1)),
+    ("elman", 16, 33, 1, 128, dict(C=2)),
     ("elman", 7, 18, 2, 64, dict(C=2, KT=4)),
     ("slstm", 5, 29, 2, 96, dict(C=3, KT=3)),
     ("slstm", 16, 23, 1, 192, dict(C=6, NT=2)),
@@ -111,7 +111,7 @@ FUSED_CASES = [
 
 
 def _restrict(monkeypatch, restr):
-    for k in ("C", "NT", "KT"):
+    for k in ("C", "NT", "KT", "MT"):
         monkeypatch.delenv(f"RNN_PLAN_{k}", raising=False)
     for k, v in restr.items():
         monkeypatch.setenv(f"RNN_PLAN_{k}", str(v))
@@ -148,3 +148,42 @@ def test_fused_matches_simt_forward_closely(monkeypatch):
     st_s, _, _ = run_fwd("lstm", inp, "simt", want_tape=False)
     diff = (st_f.float() - st_s.float()).abs().max().item()
     assert diff <= 2e-2, diff
+
+
+BWD_CASES = [
+    ("lstm", 3, 37, 2, 64, dict(C=2)),
+    ("lstm", 3, 37, 2, 64, dict(C=4, NT=2)),
+    ("lstm", 9, 21, 1, 128, dict(C=8, MT=2)),
+    ("lstm", 5, 19, 1, 256, dict(C=16)),
+    ("lstm", 8, 40, 3, 256, dict(C=8)),
+    ("gru", 9, 20, 3, 48, dict(C=3)),
+    ("gru", 16, 25, 2, 128, dict(C=4, NT=2)),
+    ("elman", 7, 18, 2, 64, dict(C=1)),
+    ("elman", 16, 33, 1, 128, dict(C=2)),
+    ("slstm", 5, 29, 2, 96, dict(C=3)),
+    ("slstm", 16, 23, 1, 192, dict(C=6, NT=2)),
+    ("slstm", 4, 17, 1, 192, dict(C=12)),
+]
+
+
+@pytest.mark.parametrize("case", BWD_CASES,
+                         ids=lambda c: "%s-B%dT%dN%dD%d-" % c[:5] + "-".join(f"{k}{v}" for k, v in c[5].items()))
+def test_fused_backward_parity(case, monkeypatch):
+    fn, B, T, N, D, restr = case
+    _restrict(monkeypatch, restr)
+    inp = _inputs(fn, (B, T, N, D), torch.bfloat16, seed=700 + B + T + D)
+    dims = _lib.make_dims(B, T, N, D, fn, torch.bfloat16, "fused")
+    rc, desc = _lib.rnn_plan_describe(dims, True)
+    assert rc == 0 and "path=fused" in desc and f"C={restr['C']} " in desc, desc
+    st, last, tape = run_fwd(fn, inp, "fused")
+    dl = torch.randn(last.shape, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16).cuda()
+    dWx, dR, db, ds0 = run_bwd(fn, inp, st, tape, "fused", dlast=dl)
+    rdWx, rdR, rdb, rds0 = oracle_bwd(fn, inp, dlast=dl)
+    check_grad(f"{fn} dWx", torch.bfloat16, dWx, rdWx)
+    check_grad(f"{fn} dR", torch.bfloat16, dR, rdR)
+    check_grad(f"{fn} db", torch.bfloat16, db, rdb)
+    check_grad(f"{fn} dstates0", torch.bfloat16, ds0, rds0)
+    # the plain path on the same tape gives nearly the same gradients
+    sdWx, _, _, sds0 = run_bwd(fn, inp, st, tape, "simt", dlast=dl)
+    d1 = (dWx.float() - sdWx.float()).abs().max().item() / max(sdWx.float().abs().max().item(), 1e-30)
+    assert d1 <= 2e-2, d1
