@@ -10,9 +10,16 @@ Tolerances (stated once, used by every parity test):
                 (bf16 keeps 8 significant bits). Gradients against the oracle
                 in its bfloat16-operand mode (the contraction operands h and
                 dr rounded to bf16, as the kernels' tensor-core operands are):
-                normwise-max relative <= 2e-2 and cosine >= 0.9995. Against the
-                plain oracle the bf16 rounding of h alone moves sLSTM gradients
-                by ~6% on short sequences, which says nothing about the kernels.
+                L2-normwise relative ||g - g*|| / ||g*|| <= 2e-2 and cosine
+                >= 0.9995 for every cell, and normwise-max relative <= 2e-2 for
+                the cells whose gradient is continuous (LSTM, GRU, Elman).
+                sLSTM is exempt from the max-norm bound: the derivative of its
+                stabiliser max(a_f + m, a_i) jumps at ties, and bf16 rounding of
+                h (plus fp32 summation order) moves near-ties to the other branch,
+                which changes single elements of dWx by O(|dm|) (~6% of the
+                maximum on B=5, T=29 cases). Against the plain oracle the bf16
+                rounding of h alone moves sLSTM gradients by ~6% even on the
+                plain path, which says nothing about the kernels.
 """
 from __future__ import annotations
 
@@ -76,6 +83,17 @@ def check_states(fn, dtype, got, ref, what="states"):
     return err_h
 
 
+def grad_errors(got, ref):
+    """(normwise-max relative, L2-normwise relative, cosine) of got vs ref."""
+    got = to_np(got) if not isinstance(got, np.ndarray) else got
+    scale = np.abs(ref).max()
+    rel = np.abs(got - ref).max() / scale if scale > 0 else float(np.abs(got).max())
+    nr = np.linalg.norm(ref)
+    l2 = np.linalg.norm(got - ref) / nr if nr > 0 else float(np.linalg.norm(got))
+    cos = float((got * ref).sum() / (np.linalg.norm(got) * nr + 1e-300)) if got.size > 1 else 1.0
+    return float(rel), float(l2), cos
+
+
 def check_grad(name, dtype, got, ref):
     tol = TOL[dtype]
     got = to_np(got)
@@ -84,10 +102,12 @@ def check_grad(name, dtype, got, ref):
     if scale == 0:
         assert np.abs(got).max() == 0, f"{name}: expected zeros"
         return 0.0
-    rel = np.abs(got - ref).max() / scale
-    assert rel <= tol["grad"], f"{name}: normwise-max relative err {rel:.3g} > {tol['grad']}"
+    rel, l2, cos = grad_errors(got, ref)
+    continuous = not name.startswith("slstm")
+    if dtype == torch.float32 or continuous:
+        assert rel <= tol["grad"], f"{name}: normwise-max relative err {rel:.3g} > {tol['grad']}"
     if tol["cos"] is not None and got.size > 1:
-        cos = float((got * ref).sum() / (np.linalg.norm(got) * np.linalg.norm(ref) + 1e-300))
+        assert l2 <= tol["grad"], f"{name}: L2-normwise relative err {l2:.3g} > {tol['grad']}"
         assert cos >= tol["cos"], f"{name}: cosine {cos:.6f} < {tol['cos']}"
     return rel
 
