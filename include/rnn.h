@@ -118,6 +118,32 @@ int rnn_bwd(const rnn_dims_t *dims, const void *Wx, const void *R, const void *b
             const void *dstates, const void *dlast, void *dWx, void *dR, void *db,
             void *dstates0, void *workspace, size_t ws_bytes, void *stream);
 
+/*
+ * Backward through time without caller workspace (no counterpart on the
+ * pages: this entry point exists for callers of this library that cannot
+ * allocate device memory -- code embedded in a host framework that owns the
+ * whole device-memory budget, or loops that must not call cudaMalloc because
+ * it can synchronise the device and stall the pipeline).
+ * Same arguments and results as rnn_bwd, minus the workspace; `tape` is
+ * required (rebuilding it would need tape-sized scratch). The scratch lives in
+ * a fixed __device__ array of RNN_BWD_NOALLOC_SCRATCH_BYTES inside the library,
+ * held by every GPU that loads it until the process exits. It holds the status
+ * word and, for GRU or when dWx is NULL, the recurrent-branch gradients
+ * (B*T*G*N*D elements of the storage type): problems whose need exceeds the
+ * array (256 bytes + those gradients) return RNN_ENOSPC before any work.
+ * The first call on a device looks the array's device address up (once per
+ * device); make that first call before any stream capture. Every call shares
+ * the array and keeps the last call's contents: calls whose work overlaps on
+ * the GPU (different streams or threads) race; calls on one stream are safe.
+ * Device-side wait time-outs of this entry point are not reported.
+ * Errors: RNN_EINVAL, RNN_EUNSUPPORTED, RNN_ENOSPC, RNN_ECUDA.
+ */
+#define RNN_BWD_NOALLOC_SCRATCH_BYTES (16u << 20)
+int rnn_bwd_noalloc(const rnn_dims_t *dims, const void *Wx, const void *R, const void *b,
+                    const void *states0, const void *states, const void *tape,
+                    const void *dstates, const void *dlast, void *dWx, void *dR, void *db,
+                    void *dstates0, void *stream);
+
 /* Synchronises `stream`, reads and clears the device status word that kernels
  * running on `workspace` recorded. Returns RNN_OK, RNN_ETIMEOUT or RNN_ECUDA. */
 int rnn_check_status(void *workspace, void *stream);

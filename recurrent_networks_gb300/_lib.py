@@ -20,7 +20,7 @@ WS_FWD, WS_BWD, WS_BWD_RECOMPUTE = 0, 1, 2
 
 EXPORTS = ["rnn_num_gates", "rnn_num_states", "rnn_tape_size", "rnn_workspace_size", "rnn_fwd",
            "rnn_bwd", "rnn_check_status", "rnn_plan_describe", "rnn_strerror", "rnn_kernel_launches",
-           "rnn_profile_events"]
+           "rnn_profile_events", "rnn_bwd_noalloc"]
 
 
 class RnnError(RuntimeError):
@@ -61,6 +61,7 @@ def load(path: str | None = None):
             lib.rnn_kernel_launches.argtypes = []
             lib.rnn_kernel_launches.restype = ctypes.c_ulonglong
             lib.rnn_profile_events.argtypes = [i, vp, vp]
+            lib.rnn_bwd_noalloc.argtypes = [dp] + [vp] * 13
             _lib = lib
     return _lib
 
@@ -148,3 +149,13 @@ def rnn_profile_events(which: int, before=None, after=None) -> int:
     b = ctypes.c_void_p(before.cuda_event) if before is not None else None
     a = ctypes.c_void_p(after.cuda_event) if after is not None else None
     return _check(load().rnn_profile_events(which, b, a), "rnn_profile_events")
+
+
+def rnn_bwd_noalloc(dims: Dims, Wx, R, b, states0, states, tape, dstates, dlast, dWx, dR, db,
+                    dstates0, stream=None) -> int:
+    """rnn_bwd without workspace: the library's fixed device scratch is used
+    instead (for callers that cannot allocate device memory)."""
+    rc = load().rnn_bwd_noalloc(ctypes.byref(dims), _p(Wx), _p(R), _p(b), _p(states0), _p(states),
+                                _p(tape), _p(dstates), _p(dlast), _p(dWx), _p(dR), _p(db), _p(dstates0),
+                                _stream(stream))
+    return _check(rc, "rnn_bwd_noalloc")
