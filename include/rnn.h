@@ -55,8 +55,10 @@ typedef enum { RNN_F32 = 0, RNN_BF16 = 1 } rnn_dtype_t;
 typedef enum {
   RNN_PATH_AUTO = 0,        /* the planner picks */
   RNN_PATH_FUSED = 1,       /* persistent thread-block-cluster kernel, R resident on chip */
-  RNN_PATH_ALTERNATING = 2, /* persistent grid kernel for R too large for one cluster */
-  RNN_PATH_SIMT = 3         /* plain per-head kernel, any size; the fp32 path */
+  RNN_PATH_ALTERNATING = 2, /* a per-step matrix product and a pointwise kernel, replayed as a CUDA graph */
+  RNN_PATH_SIMT = 3,        /* plain per-head kernel, any size; the fp32 path */
+  RNN_PATH_GRID = 4         /* persistent cooperative grid kernel for R too large for one cluster:
+                               h (forward) and dr (backward) exchanged through L2 with step counters */
 } rnn_path_t;
 
 typedef struct {

@@ -15,7 +15,7 @@ from . import build as _build
 RNN_OK, RNN_EINVAL, RNN_EUNSUPPORTED, RNN_ENOSPC, RNN_ETIMEOUT, RNN_ECUDA = range(6)
 FUNCTIONS = {"lstm": 0, "gru": 1, "elman": 2, "slstm": 3}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
-PATHS = {"auto": 0, "fused": 1, "alternating": 2, "simt": 3}
+PATHS = {"auto": 0, "fused": 1, "alternating": 2, "simt": 3, "grid": 4}
 WS_FWD, WS_BWD, WS_BWD_RECOMPUTE = 0, 1, 2
 
 EXPORTS = ["rnn_num_gates", "rnn_num_states", "rnn_tape_size", "rnn_workspace_size", "rnn_fwd",

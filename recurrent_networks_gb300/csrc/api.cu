@@ -31,7 +31,7 @@ struct Sizes {
 static bool dims_ok(const rnn_dims_t* d) {
   return d && d->B >= 1 && d->T >= 0 && d->N >= 1 && d->D >= 1 && d->function >= 0 &&
          d->function <= 3 && (d->dtype == RNN_F32 || d->dtype == RNN_BF16) && d->path >= 0 &&
-         d->path <= 3 && (size_t)d->B * d->N * d->D < ((size_t)1 << 40);
+         d->path <= 4 && (size_t)d->B * d->N * d->D < ((size_t)1 << 40);
 }
 
 static Sizes sizes_of(const rnn_dims_t* d) {
@@ -53,9 +53,10 @@ static Sizes sizes_of(const rnn_dims_t* d) {
 
 static bool aligned(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-// Workspace layout: [status 256 B][path scratch][dr buffer (bwd)][tape (bwd recompute)]
+// Workspace layout: [status 256 B][path scratch][dr buffer (bwd)][split-K partials of
+// the weight gradients (bwd)][tape (bwd recompute)]
 struct WsLayout {
-  size_t status, path, dr, tape, total;
+  size_t status, path, dr, wg, tape, total;
 };
 
 static WsLayout ws_layout(const rnn_dims_t* d, int kind, const Plan& plan) {
@@ -66,6 +67,8 @@ static WsLayout ws_layout(const rnn_dims_t* d, int kind, const Plan& plan) {
   size_t off = w.path + align256(plan.scratch_bytes);
   w.dr = off;
   if (kind != RNN_WS_FWD) off += align256(z.dr);
+  w.wg = off;
+  if (kind != RNN_WS_FWD) off += align256(wgrad_scratch_bytes(d->B, d->T, d->N, d->D, z.G, d->dtype));
   w.tape = off;
   if (kind == RNN_WS_BWD_RECOMPUTE) off += align256(z.tape);
   w.total = off;
@@ -83,7 +86,17 @@ static int choose(const rnn_dims_t* d, bool bwd, Plan* plan) {
   return plan_select(q, plan);
 }
 
-// Upper bound of every device-side wait (rnn_set_wait_limit).
+// Grid path scratch inside the workspace (after the 256-byte status word):
+// the exchange buffers [2][groups][BC][L] bf16 (L = D forward, G D backward)
+// followed by one step counter per group.
+static void grid_scratch(const rnn_dims_t* d, const Plan& plan, char* ws, bool bwd, FusedArgs* f) {
+  const size_t L = bwd ? (size_t)fn_gates(d->function) * d->D : (size_t)d->D;
+  const size_t hx = (size_t)2 * plan.groups * 8 * plan.fs.NT * L * 2;
+  f->hx = ws + 256;
+  f->counters = (unsigned int*)(ws + 256 + align256(hx));
+}
+
+// Upper bound of every device-side wait.
 static unsigned long long g_wait_limit_ns = 2000000000ull;
 
 // Runs the forward kernels (states/last/tape each optional); ws is the
@@ -110,6 +123,19 @@ static int run_forward(const rnn_dims_t* d, const Plan& plan, const void* Wx, co
       f.status = (unsigned int*)ws;
       f.wait_limit_ns = g_wait_limit_ns;
       rc = cuda_status(fused_fwd_run(d->function, plan.fs, f, st));
+      break;
+    }
+    case RNN_PATH_GRID: {
+      FusedArgs f{};
+      f.B = d->B; f.T = d->T; f.N = d->N; f.D = d->D;
+      f.C = plan.fs.C; f.U = plan.fs.U; f.KS = plan.fs.KS;
+      f.Wx = Wx; f.R = R; f.bias = b; f.s0 = s0;
+      f.states = states; f.last = last; f.tape = tape;
+      f.status = (unsigned int*)ws;
+      f.wait_limit_ns = g_wait_limit_ns;
+      grid_scratch(d, plan, ws, false, &f);
+      rc = cuda_status(cudaMemsetAsync(f.counters, 0, (size_t)plan.groups * sizeof(unsigned), st));
+      if (rc == RNN_OK) rc = cuda_status(grid_fwd_run(d->function, plan.fs, f, st));
       break;
     }
   }
@@ -238,11 +264,26 @@ int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
       rc = cuda_status(fused_bwd_run(d->function, plan.fs, f, st));
       break;
     }
+    case RNN_PATH_GRID: {
+      FusedArgs f{};
+      f.B = d->B; f.T = d->T; f.N = d->N; f.D = d->D;
+      f.C = plan.fs.C; f.U = plan.fs.U; f.KS = plan.fs.KS;
+      f.R = R; f.s0 = states0; f.tape = (float*)tp;
+      f.dstates = dstates; f.dlast = dlast; f.dWx = dWx; f.dr = drbuf; f.ds0 = dstates0;
+      f.status = (unsigned int*)ws;
+      f.wait_limit_ns = g_wait_limit_ns;
+      grid_scratch(d, plan, ws, true, &f);
+      rc = cuda_status(cudaMemsetAsync(f.counters, 0, (size_t)plan.groups * sizeof(unsigned), st));
+      if (rc == RNN_OK) rc = cuda_status(grid_bwd_run(d->function, plan.fs, f, st));
+      break;
+    }
   }
   prof_mark(1, 1, st);
   if (rc) return rc;
   if (dR || db) {
     WgradArgs g{d->B, d->T, d->N, d->D, z.G, states, states0, drbuf, dR, db};
+    g.scratch = (float*)(ws + w.wg);
+    g.scratch_bytes = w.tape - w.wg;
     rc = cuda_status(wgrad_run(d->dtype, g, st));
   }
   return rc;

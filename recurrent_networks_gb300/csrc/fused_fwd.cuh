@@ -25,14 +25,17 @@
 
 namespace rnn {
 
-template <int FN, int NT, int KT>
+// GRIDX = true is the grid variant for R too large for one cluster: C CTAs of a
+// cooperative launch share a head and batch group, and h_t goes through L2 (a
+// bf16 exchange buffer plus a per-group step counter) instead of DSMEM.
+template <int FN, int NT, int KT, bool GRIDX>
 __global__ void __launch_bounds__(256, 1)
     fused_fwd_kernel(const __grid_constant__ CUtensorMap wxmap, FusedArgs a) {
   constexpr int G = FnInfo<FN>::G, S = FnInfo<FN>::S, P = FnInfo<FN>::P, K = P + S;
   constexpr int BC = 8 * NT;
   const int C = a.C, U = a.U, D = a.D, KS = a.KS, TT = a.T, N = a.N, B = a.B;
   const int HS = D + 8;  // row stride (elements) of the h buffers
-  const uint32_t rank = cluster_ctarank();
+  const uint32_t rank = GRIDX ? (uint32_t)(blockIdx.x % C) : cluster_ctarank();
   const int grp = blockIdx.x / C;
   const int n = grp % N;
   const int b0 = (grp / N) * BC;
@@ -110,11 +113,11 @@ __global__ void __launch_bounds__(256, 1)
       }
   }
   __syncthreads();
-  cluster_sync_all();  // every CTA's barriers are initialised before any peer signals them
+  if constexpr (!GRIDX) cluster_sync_all();  // every CTA's barriers are initialised before any peer signals them
 
   if (tid == 0) {
-    if (TT > 1) mbar_arrive_expect_tx(full_bar0 + 8, hbytes);  // step 1
-    if (TT > 2) mbar_arrive_expect_tx(full_bar0, hbytes);      // step 2
+    if (!GRIDX && TT > 1) mbar_arrive_expect_tx(full_bar0 + 8, hbytes);  // step 1
+    if (!GRIDX && TT > 2) mbar_arrive_expect_tx(full_bar0, hbytes);      // step 2
     for (int s = 0; s < FUSED_NS - 1 && s < TT; ++s) {
       mbar_arrive_expect_tx(wx_bar0 + 8 * s, wxbytes);
       tma_load_5d(smem_u32(wxs + s * wx_stage_elems), &wxmap, wx_bar0 + 8 * s, u0, n, 0, s, b0);
@@ -129,10 +132,24 @@ __global__ void __launch_bounds__(256, 1)
   for (int t = 0; t < TT; ++t) {
     const int p = t & 1;
     if (t > 0) {
-      const uint32_t par = p ? ph1 : ph0;
-      mbar_wait_bounded(full_bar0 + 8 * p, par, a.wait_limit_ns, a.status, failed);
-      if (p) ph1 ^= 1; else ph0 ^= 1;
-      if (tid == 0 && t + 2 <= TT - 1) mbar_arrive_expect_tx(full_bar0 + 8 * p, hbytes);
+      if constexpr (GRIDX) {
+        // every CTA of the group published h_{t-1}; copy it from L2
+        if (tid == 0) counter_wait_bounded(a.counters + grp, (unsigned)(C * t), a.wait_limit_ns, a.status, failed);
+        __syncthreads();
+        const __nv_bfloat16* src = (const __nv_bfloat16*)a.hx + ((size_t)(p * (gridDim.x / C) + grp) * BC) * D;
+        const int rc = D / 8;
+        for (int e = tid; e < nb * rc; e += nthr) {
+          const int b = e / rc, c = e - b * rc;
+          cp_async_cg16(smem_u32(hbuf + (p * BC + b) * HS + c * 8), src + (size_t)b * D + c * 8);
+        }
+        cp_async_wait_all();
+        __syncthreads();
+      } else {
+        const uint32_t par = p ? ph1 : ph0;
+        mbar_wait_bounded(full_bar0 + 8 * p, par, a.wait_limit_ns, a.status, failed);
+        if (p) ph1 ^= 1; else ph0 ^= 1;
+        if (tid == 0 && t + 2 <= TT - 1) mbar_arrive_expect_tx(full_bar0 + 8 * p, hbytes);
+      }
     }
     if (tid == 0 && t + FUSED_NS - 1 < TT) {
       const int ts = t + FUSED_NS - 1, s = ts % FUSED_NS;
@@ -212,7 +229,13 @@ __global__ void __launch_bounds__(256, 1)
         cst[(s * BC + b) * U + u] = sn[s];
         if (states) states[(((size_t)s * B + bg) * TT + t) * N * D + (size_t)n * D + j] = __float2bfloat16_rn(sn[s]);
       }
-      stage[b * U + u] = __float2bfloat16_rn(sn[0]);
+      if constexpr (GRIDX) {
+        if (t + 1 < TT)
+          ((__nv_bfloat16*)a.hx)[((size_t)((p ^ 1) * (gridDim.x / C) + grp) * BC + b) * D + j] =
+              __float2bfloat16_rn(sn[0]);
+      } else {
+        stage[b * U + u] = __float2bfloat16_rn(sn[0]);
+      }
       if (a.tape) {
         float* tp = a.tape + (((size_t)t * B + bg) * N + n) * K * D + j;
 #pragma unroll
@@ -224,7 +247,9 @@ __global__ void __launch_bounds__(256, 1)
     __syncthreads();
 
     // ---- exchange: push this CTA's slice of h_t into every CTA's next buffer
-    if (t + 1 < TT) {
+    if (GRIDX) {
+      if (t + 1 < TT && tid == 0) counter_publish(a.counters + grp);
+    } else if (t + 1 < TT) {
       const uint32_t dst_local = smem_u32(hbuf + (p ^ 1) * BC * HS);
       const uint32_t bar_local = full_bar0 + 8 * (p ^ 1);
       for (int e = tid; e < nchunk * C; e += nthr) {
@@ -248,19 +273,24 @@ __global__ void __launch_bounds__(256, 1)
     }
   }
   __syncthreads();
-  cluster_sync_all();  // no CTA leaves while a peer may still write into its shared memory
+  if constexpr (!GRIDX) cluster_sync_all();  // no CTA leaves while a peer may still write into its shared memory
 }
 
 // Host launcher for one cell type; the TMA descriptor covers Wx as the 5-D
-// tensor (D, N, G, T, B) with a (U, 1, G, 1, BC) box.
-template <int FN>
-cudaError_t fused_fwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream_t st) {
+// tensor (D, N, G, T, B) with a (U, 1, G, 1, BC) box. GRIDX selects the
+// cooperative grid variant (no cluster; co-residency guaranteed by the launch).
+template <int FN, bool GRIDX>
+cudaError_t fwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream_t st) {
   constexpr int G = FnInfo<FN>::G;
   void (*k)(const CUtensorMap, FusedArgs) = nullptr;
 #define RNN_FUSED_PICK(NT_, KT_) \
-  if (sh.NT == NT_ && sh.KT == KT_) k = fused_fwd_kernel<FN, NT_, KT_>;
-  RNN_FUSED_PICK(1, 2) RNN_FUSED_PICK(1, 3) RNN_FUSED_PICK(1, 4)
-  RNN_FUSED_PICK(2, 2) RNN_FUSED_PICK(2, 3) RNN_FUSED_PICK(2, 4)
+  if (sh.NT == NT_ && sh.KT == KT_) k = fused_fwd_kernel<FN, NT_, KT_, GRIDX>;
+  if constexpr (GRIDX) {
+    RNN_FUSED_PICK(1, 4) RNN_FUSED_PICK(1, 8) RNN_FUSED_PICK(2, 4) RNN_FUSED_PICK(2, 8)
+  } else {
+    RNN_FUSED_PICK(1, 2) RNN_FUSED_PICK(1, 3) RNN_FUSED_PICK(1, 4)
+    RNN_FUSED_PICK(2, 2) RNN_FUSED_PICK(2, 3) RNN_FUSED_PICK(2, 4)
+  }
 #undef RNN_FUSED_PICK
   if (!k) return cudaErrorInvalidValue;
   CUtensorMap map;
@@ -272,7 +302,7 @@ cudaError_t fused_fwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStrea
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh.smem);
   if (e != cudaSuccess) return e;
-  if (sh.C > 8) {
+  if (!GRIDX && sh.C > 8) {
     e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
@@ -283,19 +313,41 @@ cudaError_t fused_fwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStrea
   cfg.dynamicSmemBytes = sh.smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = sh.C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  if (GRIDX) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    int per_sm = 0, dev = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, (int)cfg.blockDim.x, sh.smem);
+    if (e != cudaSuccess) return e;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (per_sm * sms < groups * sh.C) return cudaErrorCooperativeLaunchTooLarge;
+  } else {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = sh.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, k, &cfg);
-  if (e != cudaSuccess) return e;
-  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  if (!GRIDX) {
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, k, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+  }
   e = cudaLaunchKernelEx(&cfg, k, map, a);
   note_launch();
   return e;
+}
+
+template <int FN>
+cudaError_t fused_fwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream_t st) {
+  return fwd_launch<FN, false>(sh, a, st);
+}
+template <int FN>
+cudaError_t grid_fwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream_t st) {
+  return fwd_launch<FN, true>(sh, a, st);
 }
 
 }  // namespace rnn

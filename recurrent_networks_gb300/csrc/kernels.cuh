@@ -40,7 +40,11 @@ struct WgradArgs {
   const void* dr;
   void* dR;  // may be null
   void* db;  // may be null
+  float* scratch = nullptr;  // optional: split-K partial sums (wgrad_scratch_bytes)
+  size_t scratch_bytes = 0;
 };
+// Bytes of split-K scratch the tensor-core weight-gradient pass can use.
+size_t wgrad_scratch_bytes(int B, int T, int N, int D, int G, int dtype);
 cudaError_t wgrad_run(int dtype, const WgradArgs& a, cudaStream_t st);
 
 // Arguments of the persistent cluster kernels (bf16 storage).
@@ -60,10 +64,16 @@ struct FusedArgs {
   void* ds0;
   unsigned int* status;  // device status word (bounded waits)
   unsigned long long wait_limit_ns;
+  // grid mode (cooperative persistent kernel): h exchange buffers
+  // [2][groups][BC][D] and one step counter per group, zeroed before launch
+  void* hx = nullptr;
+  unsigned int* counters = nullptr;
 };
 
 struct FusedShape;
 cudaError_t fused_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st);
+cudaError_t grid_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st);
+cudaError_t grid_bwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st);
 
 // Encodes a tiled TMA descriptor for a dense row-major bf16 tensor whose
 // dims[0] is innermost; box[] gives the tile. No swizzle, zero fill.

@@ -75,4 +75,26 @@ struct FusedBwdSmem {
   }
 };
 
+// Backward grid kernel: the TMA ring of the cluster backward, the gathered
+// recurrent-branch gradients of the whole group ([BC][G D + 8] bf16), the
+// K-split partial sums, and the carried and initial states.
+struct GridBwdSmem {
+  size_t bars, ring, ring_stage, tape_bytes, dst_off, dbuf, red, ds, s0, total;
+  RNN_HD static GridBwdSmem make(int G, int S, int K, int D, int U, int BC, int KS) {
+    GridBwdSmem m;
+    size_t off = 0;
+    m.bars = FusedSmem::take(off, 8 * FUSED_NS);
+    m.tape_bytes = (size_t)BC * K * U * 4;
+    m.dst_off = (m.tape_bytes + 127) & ~(size_t)127;
+    m.ring_stage = (m.dst_off + (size_t)S * BC * U * 2 + 127) & ~(size_t)127;
+    m.ring = FusedSmem::take(off, FUSED_NS * m.ring_stage);
+    m.dbuf = FusedSmem::take(off, (size_t)BC * (G * D + 8) * 2);
+    m.red = FusedSmem::take(off, (size_t)(U / 16) * KS * BC * FUSED_RED_STRIDE * 4);
+    m.ds = FusedSmem::take(off, (size_t)S * BC * U * 4);
+    m.s0 = FusedSmem::take(off, (size_t)S * BC * U * 4);
+    m.total = off;
+    return m;
+  }
+};
+
 }  // namespace rnn

@@ -176,6 +176,84 @@ static int fused_plan(const PlanRequest& q, Plan* best) {
   return q.bwd ? fused_bwd_plan(q, best) : fused_fwd_plan(q, best);
 }
 
+// Grid kernels (cooperative launch, h / dr exchanged through L2), candidate
+// point (C, NT, KT):
+//   divisibility   D = C U, U = 16 m; forward D/16 = KS KT, backward
+//                  G D / 16 = KS KT; warps = (U / 16) KS;
+//   inequalities   1 <= warps <= 8, groups * C <= SMs (every CTA resident),
+//                  registers (forward 4 G KT + 4 G NT + 48, backward
+//                  4 KT + 4 NT + 64) <= 255, shared memory <= 227 KB;
+//   KT takes the instantiated values (forward 4, 8; backward 8, 16, 24, 32).
+static const int kGridC[] = {8, 16, 32, 64, 128};
+static const int kGridFwdKT[] = {4, 8};
+static const int kGridBwdKT[] = {8, 16, 24, 32};
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool grid_feasible(const PlanRequest& q, int C, int NT, int KT, const DeviceLimits& lim, Plan* out) {
+  const int G = gates_of(q.fn), S = states_of(q.fn), D = q.D;
+  const int K = (q.fn == 1 ? 4 : G) + S;
+  if (q.dtype != RNN_BF16 || D % C) return false;
+  const int U = D / C;
+  if (U % 16 || D % 16) return false;
+  const int klen = q.bwd ? G * D : D;
+  if ((klen / 16) % KT) return false;
+  const int KS = (klen / 16) / KT;
+  const int warps = (U / 16) * KS;
+  if (warps < 1 || warps > lim.max_warps) return false;
+  const int BC = 8 * NT;
+  const int groups = q.N * ((q.B + BC - 1) / BC);
+  if (groups * C > lim.sms) return false;
+  const int regs = q.bwd ? 4 * KT + 4 * NT + 64 : 4 * G * KT + 4 * G * NT + 48;
+  if (regs > lim.regs_per_thread) return false;
+  const size_t smem = q.bwd ? GridBwdSmem::make(G, S, K, D, U, BC, KS).total
+                            : FusedSmem::make(G, S, D, U, BC, KS).total;
+  if (smem > lim.smem_per_cta) return false;
+  const int nb = q.B < BC ? q.B : BC;
+  double pairs = (double)nb * U / (warps * 32);
+  if (pairs < 1) pairs = 1;
+  // step: counter round trip through L2, the gathered vector from L2
+  // (~64 B/clk/SM), the warp's MMA chain, the K-split reduction and the cell
+  const double gather = (double)nb * klen * 2 / 64.0;
+  double cyc = 2200.0 + gather + 18.0 * KT * (q.bwd ? 1 : G) * NT + 6.0 * KS * pairs + 150.0 * pairs;
+  if (out) {
+    *out = Plan{};
+    out->path = RNN_PATH_GRID;
+    out->fs.C = C;
+    out->fs.U = U;
+    out->fs.NT = NT;
+    out->fs.KT = KT;
+    out->fs.KS = KS;
+    out->fs.warps = warps;
+    out->fs.smem = smem;
+    out->groups = groups;
+    out->regs_R = q.bwd ? 4 * KT : 4 * G * KT;
+    out->scratch_bytes = align256((size_t)2 * groups * BC * klen * 2) + align256((size_t)groups * 4);
+    out->model_ns = cyc / 1.9;
+  }
+  return true;
+}
+
+static int grid_plan(const PlanRequest& q, Plan* best) {
+  DeviceLimits lim;
+  int found = 0;
+  const int* kts = q.bwd ? kGridBwdKT : kGridFwdKT;
+  const int nkt = q.bwd ? 4 : 2;
+  for (int C : kGridC)
+    for (int NT : kNT)
+      for (int x = 0; x < nkt; ++x) {
+        const int KT = kts[x];
+        Plan p;
+        if (!env_admits("RNN_PLAN_C", C) || !env_admits("RNN_PLAN_NT", NT) || !env_admits("RNN_PLAN_KT", KT))
+          continue;
+        if (!grid_feasible(q, C, NT, KT, lim, &p)) continue;
+        ++found;
+        if (found == 1 || p.model_ns < best->model_ns - 1e-9) *best = p;
+      }
+  best->candidates = found;
+  return found ? RNN_OK : RNN_EUNSUPPORTED;
+}
+
 static void simt_plan(const PlanRequest& q, Plan* p) {
   *p = Plan{};
   p->path = RNN_PATH_SIMT;
@@ -191,14 +269,26 @@ int plan_select(const PlanRequest& q, Plan* out) {
       *out = p;
       return RNN_OK;
     case RNN_PATH_AUTO:
-      // the cluster kernels when a feasible point exists (bf16), else the plain path
-      if (fused_plan(q, &p) == RNN_OK) {
+      // the cluster kernels when a feasible point exists (bf16), then the grid
+      // kernels (R too large for one cluster), else the plain path
+      if (fused_plan(q, &p) == RNN_OK || grid_plan(q, &p) == RNN_OK) {
         *out = p;
         return RNN_OK;
       }
       simt_plan(q, &p);
       *out = p;
       return RNN_OK;
+    case RNN_PATH_GRID:
+      if (grid_plan(q, &p) == RNN_OK) {
+        *out = p;
+        return RNN_OK;
+      }
+      snprintf(p.why, sizeof(p.why),
+               "no grid plan for fn=%d dtype=%d D=%d B=%d N=%d%s (bf16 only; U = D/C multiple of 16, <= 8 "
+               "warps, all CTAs resident)",
+               q.fn, q.dtype, q.D, q.B, q.N, q.bwd ? " (backward)" : "");
+      *out = p;
+      return RNN_EUNSUPPORTED;
     case RNN_PATH_FUSED:
       if (fused_plan(q, &p) == RNN_OK) {
         *out = p;
@@ -222,11 +312,11 @@ void plan_describe(const Plan& p, int rc, char* buf, size_t len) {
     snprintf(buf, len, "unsupported: %s", p.why);
     return;
   }
-  const char* names[] = {"auto", "fused", "alternating", "simt"};
+  const char* names[] = {"auto", "fused", "alternating", "simt", "grid"};
   snprintf(buf, len,
            "path=%s C=%d U=%d NT=%d KT=%d KS=%d warps=%d groups=%d regs_R=%d smem=%zu scratch=%zu "
            "model_ns=%.0f candidates=%d",
-           names[p.path & 3], p.fs.C, p.fs.U, p.fs.NT, p.fs.KT, p.fs.KS, p.fs.warps, p.groups, p.regs_R,
+           names[(p.path >= 0 && p.path <= 4) ? p.path : 0], p.fs.C, p.fs.U, p.fs.NT, p.fs.KT, p.fs.KS, p.fs.warps, p.groups, p.regs_R,
            p.fs.smem, p.scratch_bytes, p.model_ns, p.candidates);
 }
 

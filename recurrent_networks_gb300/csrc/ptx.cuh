@@ -78,6 +78,41 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// ---- grid-wide step counters (cooperative persistent kernels) -----------------
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Waits until *ctr >= target, for at most limit_ns (same failure contract as
+// mbar_wait_bounded).
+__device__ __forceinline__ bool counter_wait_bounded(const unsigned int* ctr, unsigned int target,
+                                                     uint64_t limit_ns, unsigned int* status, bool& failed) {
+  if (failed) return false;
+  if (ld_acquire_gpu(ctr) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int k = 0; k < 16; ++k)
+      if (ld_acquire_gpu(ctr) >= target) return true;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      if (status) atomicExch(status, 1u);
+      failed = true;
+      return false;
+    }
+  }
+}
+// Called by one thread after a __syncthreads(): publishes every write the CTA
+// made before the barrier and counts this CTA in.
+__device__ __forceinline__ void counter_publish(unsigned int* ctr) {
+  __threadfence();
+  atomicAdd(ctr, 1u);
+}
+__device__ __forceinline__ void cp_async_cg16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ---- cluster barrier --------------------------------------------------------
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile(

@@ -72,4 +72,29 @@ cudaError_t fused_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cuda
   return cudaErrorInvalidValue;
 }
 
+template <int FN>
+cudaError_t grid_fwd_launch(const FusedShape&, const FusedArgs&, cudaStream_t);
+template <int FN>
+cudaError_t grid_bwd_launch(const FusedShape&, const FusedArgs&, cudaStream_t);
+
+cudaError_t grid_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st) {
+  switch (fn) {
+    case LSTM: return grid_fwd_launch<LSTM>(sh, a, st);
+    case GRU: return grid_fwd_launch<GRU>(sh, a, st);
+    case ELMAN: return grid_fwd_launch<ELMAN>(sh, a, st);
+    case SLSTM: return grid_fwd_launch<SLSTM>(sh, a, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t grid_bwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st) {
+  switch (fn) {
+    case LSTM: return grid_bwd_launch<LSTM>(sh, a, st);
+    case GRU: return grid_bwd_launch<GRU>(sh, a, st);
+    case ELMAN: return grid_bwd_launch<ELMAN>(sh, a, st);
+    case SLSTM: return grid_bwd_launch<SLSTM>(sh, a, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace rnn

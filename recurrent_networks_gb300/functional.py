@@ -12,7 +12,7 @@ import torch
 from . import _lib
 
 BACKENDS = {"auto": "auto", "cuda_fused": "fused", "fused": "fused", "cuda": "alternating",
-            "alternating": "alternating", "simt": "simt"}
+            "alternating": "alternating", "simt": "simt", "grid": "grid"}
 
 
 def _dims(Wx, R, function, backend):

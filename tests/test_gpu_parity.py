@@ -187,3 +187,45 @@ def test_fused_backward_parity(case, monkeypatch):
     sdWx, _, _, sds0 = run_bwd(fn, inp, st, tape, "simt", dlast=dl)
     d1 = (dWx.float() - sdWx.float()).abs().max().item() / max(sdWx.float().abs().max().item(), 1e-30)
     assert d1 <= 2e-2, d1
+
+
+# ---------------------------------------------------------------- grid kernels
+GRID_CASES = [
+    ("lstm", 5, 23, 1, 256, dict(C=16)),
+    ("lstm", 3, 9, 1, 1024, dict(C=64)),
+    ("gru", 9, 19, 2, 128, dict(C=8)),
+    ("elman", 16, 21, 2, 256, dict(C=16, NT=2)),
+    ("slstm", 4, 17, 1, 512, dict(C=32)),
+]
+
+
+@pytest.mark.parametrize("case", GRID_CASES,
+                         ids=lambda c: "%s-B%dT%dN%dD%d-" % c[:5] + "-".join(f"{k}{v}" for k, v in c[5].items()))
+def test_grid_parity(case, monkeypatch):
+    fn, B, T, N, D, restr = case
+    _restrict(monkeypatch, restr)
+    inp = _inputs(fn, (B, T, N, D), torch.bfloat16, seed=900 + B + T + D)
+    dims = _lib.make_dims(B, T, N, D, fn, torch.bfloat16, "grid")
+    for bwd in (False, True):
+        rc, desc = _lib.rnn_plan_describe(dims, bwd)
+        assert rc == 0 and "path=grid" in desc, desc
+    st, last, tape = run_fwd(fn, inp, "grid")
+    ref_st, ref_last = oracle_fwd(fn, inp)
+    check_states(fn, torch.bfloat16, st, ref_st)
+    check_states(fn, torch.bfloat16, last, ref_last, "last")
+    dl = torch.randn(last.shape, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).cuda()
+    dWx, dR, db, ds0 = run_bwd(fn, inp, st, tape, "grid", dlast=dl)
+    rdWx, rdR, rdb, rds0 = oracle_bwd(fn, inp, dlast=dl)
+    check_grad(f"{fn} dWx", torch.bfloat16, dWx, rdWx)
+    check_grad(f"{fn} dR", torch.bfloat16, dR, rdR)
+    check_grad(f"{fn} db", torch.bfloat16, db, rdb)
+    check_grad(f"{fn} dstates0", torch.bfloat16, ds0, rds0)
+
+
+def test_grid_and_cluster_forward_agree(monkeypatch):
+    _restrict(monkeypatch, dict(C=16))
+    inp = _inputs("lstm", (8, 40, 2, 256), torch.bfloat16, seed=77)
+    st_g, _, _ = run_fwd("lstm", inp, "grid", want_tape=False)
+    st_f, _, _ = run_fwd("lstm", inp, "fused", want_tape=False)
+    diff = (st_g.float() - st_f.float()).abs().max().item()
+    assert diff <= 2e-2, diff
