@@ -168,6 +168,21 @@ unsigned long long rnn_kernel_launches(void);
  * thread-safe. Returns RNN_OK or RNN_EINVAL. */
 int rnn_profile_events(int which, void *before, void *after);
 
+/* Diagnostic phase trace of the persistent kernels (cluster and grid paths).
+ * Registers a device buffer of 8 * steps unsigned 64-bit words, or NULL to
+ * stop. Kernels launched afterwards have CTA 0, thread 0 write clock64() at
+ * eight phase points of the steps [t0, t0 + steps) of their processing order
+ * (the backward processes t = T-1 first). Forward phases: 0 step start,
+ * 1 h_{t-1} available, 2 partial products written, 3 after the CTA barrier,
+ * 4 Wx[t] staged, 5 cell update done, 6 after the CTA barrier, 7 h_t sent.
+ * Cluster backward phases: 0 step start, 1 partial dh available, 2 tape
+ * staged, 3 cell derivative done, 4 after the CTA barrier, 5 partial products
+ * computed, 6 partials sent. Grid backward phases: 0 step start, 1 step
+ * counter reached, 2 dr gathered, 3 dh reduced, 4 tape staged, 5 cell
+ * derivative done, 6 published. Process-global, not thread-safe; returns
+ * RNN_OK or RNN_EINVAL. */
+int rnn_trace(void *buf, int t0, int steps);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,7 +20,7 @@ WS_FWD, WS_BWD, WS_BWD_RECOMPUTE = 0, 1, 2
 
 EXPORTS = ["rnn_num_gates", "rnn_num_states", "rnn_tape_size", "rnn_workspace_size", "rnn_fwd",
            "rnn_bwd", "rnn_check_status", "rnn_plan_describe", "rnn_strerror", "rnn_kernel_launches",
-           "rnn_profile_events", "rnn_bwd_noalloc"]
+           "rnn_profile_events", "rnn_bwd_noalloc", "rnn_trace"]
 
 
 class RnnError(RuntimeError):
@@ -62,6 +62,7 @@ def load(path: str | None = None):
             lib.rnn_kernel_launches.restype = ctypes.c_ulonglong
             lib.rnn_profile_events.argtypes = [i, vp, vp]
             lib.rnn_bwd_noalloc.argtypes = [dp] + [vp] * 13
+            lib.rnn_trace.argtypes = [vp, i, i]
             _lib = lib
     return _lib
 
@@ -159,3 +160,9 @@ def rnn_bwd_noalloc(dims: Dims, Wx, R, b, states0, states, tape, dstates, dlast,
                                 _p(tape), _p(dstates), _p(dlast), _p(dWx), _p(dR), _p(db), _p(dstates0),
                                 _stream(stream))
     return _check(rc, "rnn_bwd_noalloc")
+
+
+def rnn_trace(buf=None, t0: int = 0, steps: int = 0) -> int:
+    """Registers a device tensor of >= 8*steps int64 for the persistent kernels'
+    phase trace (clock64 at eight points of steps [t0, t0+steps)), or None."""
+    return _check(load().rnn_trace(_p(buf), int(t0), int(steps)), "rnn_trace")

@@ -99,6 +99,15 @@ static void grid_scratch(const rnn_dims_t* d, const Plan& plan, char* ws, bool b
 // Upper bound of every device-side wait.
 static unsigned long long g_wait_limit_ns = 2000000000ull;
 
+// Phase trace of the persistent kernels (rnn_trace).
+static unsigned long long* g_trace_buf = nullptr;
+static int g_trace_t0 = 0, g_trace_steps = 0;
+static void with_trace(FusedArgs* f) {
+  f->trace = g_trace_buf;
+  f->trace_t0 = g_trace_t0;
+  f->trace_steps = g_trace_steps;
+}
+
 // Runs the forward kernels (states/last/tape each optional); ws is the
 // workspace base (status word at offset 0).
 static int run_forward(const rnn_dims_t* d, const Plan& plan, const void* Wx, const void* R,
@@ -122,6 +131,7 @@ static int run_forward(const rnn_dims_t* d, const Plan& plan, const void* Wx, co
       f.states = states; f.last = last; f.tape = tape;
       f.status = (unsigned int*)ws;
       f.wait_limit_ns = g_wait_limit_ns;
+      with_trace(&f);
       rc = cuda_status(fused_fwd_run(d->function, plan.fs, f, st));
       break;
     }
@@ -133,6 +143,7 @@ static int run_forward(const rnn_dims_t* d, const Plan& plan, const void* Wx, co
       f.states = states; f.last = last; f.tape = tape;
       f.status = (unsigned int*)ws;
       f.wait_limit_ns = g_wait_limit_ns;
+      with_trace(&f);
       grid_scratch(d, plan, ws, false, &f);
       rc = cuda_status(cudaMemsetAsync(f.counters, 0, (size_t)plan.groups * sizeof(unsigned), st));
       if (rc == RNN_OK) rc = cuda_status(grid_fwd_run(d->function, plan.fs, f, st));
@@ -261,6 +272,7 @@ int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
       f.dstates = dstates; f.dlast = dlast; f.dWx = dWx; f.dr = drbuf; f.ds0 = dstates0;
       f.status = (unsigned int*)ws;
       f.wait_limit_ns = g_wait_limit_ns;
+      with_trace(&f);
       rc = cuda_status(fused_bwd_run(d->function, plan.fs, f, st));
       break;
     }
@@ -272,6 +284,7 @@ int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
       f.dstates = dstates; f.dlast = dlast; f.dWx = dWx; f.dr = drbuf; f.ds0 = dstates0;
       f.status = (unsigned int*)ws;
       f.wait_limit_ns = g_wait_limit_ns;
+      with_trace(&f);
       grid_scratch(d, plan, ws, true, &f);
       rc = cuda_status(cudaMemsetAsync(f.counters, 0, (size_t)plan.groups * sizeof(unsigned), st));
       if (rc == RNN_OK) rc = cuda_status(grid_bwd_run(d->function, plan.fs, f, st));
@@ -319,6 +332,14 @@ int rnn_profile_events(int which, void* before, void* after) {
   if (which < 0 || which > 1) return RNN_EINVAL;
   g_prof[which][0] = (cudaEvent_t)before;
   g_prof[which][1] = (cudaEvent_t)after;
+  return RNN_OK;
+}
+
+int rnn_trace(void* buf, int t0, int steps) {
+  if (buf && (t0 < 0 || steps < 1)) return RNN_EINVAL;
+  g_trace_buf = (unsigned long long*)buf;
+  g_trace_t0 = buf ? t0 : 0;
+  g_trace_steps = buf ? steps : 0;
   return RNN_OK;
 }
 

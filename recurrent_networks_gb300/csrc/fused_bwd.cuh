@@ -123,10 +123,16 @@ __global__ void __launch_bounds__(256, 1)
   uint32_t ph[2] = {0u, 0u};
   const int q4 = lane & 3, r8 = lane >> 2;
 
+  const bool tracer = a.trace && blockIdx.x == 0 && tid == 0;
+#define RNN_TRACE(p)                                                                    \
+  if (tracer && k >= a.trace_t0 && k < a.trace_t0 + a.trace_steps)                      \
+    a.trace[(size_t)(k - a.trace_t0) * 8 + (p)] = (unsigned long long)clock64();
+
   // ---- reverse time loop ---------------------------------------------------------
   for (int k = 0; k < TT; ++k) {
     const int t = TT - 1 - k;
     const int pb = t & 1;  // gradient-operand buffer of this step
+    RNN_TRACE(0)
     if (tid == 0 && k + FUSED_NS - 1 < TT) issue_stage(k + FUSED_NS - 1);
     if (t < TT - 1) {  // partial sums for dh_t arrived
       const int bi = t & 1;
@@ -134,6 +140,7 @@ __global__ void __launch_bounds__(256, 1)
       ph[bi] ^= 1u;
       if (tid == 0 && t - 2 >= -1) mbar_arrive_expect_tx(recv_bar0 + 8 * bi, rbytes);
     }
+    RNN_TRACE(1)
     const int sc = k % FUSED_NS, sn_ = (k + 1) % FUSED_NS;
     const float* tp = (const float*)(ring + (size_t)sc * L.ring_stage);
     const __nv_bfloat16* dstage = (const __nv_bfloat16*)(ring + (size_t)sc * L.ring_stage + L.dst_off);
@@ -142,6 +149,7 @@ __global__ void __launch_bounds__(256, 1)
       mbar_wait_bounded(ring_bar0 + 8 * sc, (k / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
       if (t > 0) mbar_wait_bounded(ring_bar0 + 8 * sn_, ((k + 1) / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
     }
+    RNN_TRACE(2)
     const float* rv = recv + (size_t)(t & 1) * C * U * BC;
     __nv_bfloat16* drw = drb + (size_t)pb * BC * KB;
     for (int e = tid; e < nb * U; e += nthr) {
@@ -174,7 +182,9 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
       for (int s = 0; s < S; ++s) ds[(s * BC + b) * U + u] = dsp[s];
     }
+    RNN_TRACE(3)
     __syncthreads();
+    RNN_TRACE(4)
 
     // partial[i, b] = sum_k A[i][k] drb[b][k] for this warp's MT m-tiles
     float acc[MT][NT][4];
@@ -208,6 +218,7 @@ __global__ void __launch_bounds__(256, 1)
           for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[mt][nt], afr[mt][kt], bf[nt][0], bf[nt][1]);
       }
     }
+    RNN_TRACE(5)
     // reduce-scatter: each lane assembles 4 consecutive batch columns of one row
     {
       const int bi = (t - 1) & 1;  // consumption t-1 (t = 0 feeds the final dh_{-1})
@@ -240,7 +251,9 @@ __global__ void __launch_bounds__(256, 1)
           st_async_16(mapa_shared(la, (uint32_t)owner), out, mapa_shared(bar_local, (uint32_t)owner));
         }
     }
+    RNN_TRACE(6)
   }
+#undef RNN_TRACE
 
   // ---- dstates0: the carried gradients after step 0 ------------------------------
   {

@@ -128,9 +128,15 @@ __global__ void __launch_bounds__(256, 1)
   uint32_t ph0 = 0, ph1 = 0;
   const int nchunk = nb * (U / 8);  // 16-byte chunks of the CTA's h slice
 
+  const bool tracer = a.trace && blockIdx.x == 0 && tid == 0;
+#define RNN_TRACE(k)                                                                    \
+  if (tracer && t >= a.trace_t0 && t < a.trace_t0 + a.trace_steps)                      \
+    a.trace[(size_t)(t - a.trace_t0) * 8 + (k)] = (unsigned long long)clock64();
+
   // ---- time loop -------------------------------------------------------------
   for (int t = 0; t < TT; ++t) {
     const int p = t & 1;
+    RNN_TRACE(0)
     if (t > 0) {
       if constexpr (GRIDX) {
         // every CTA of the group published h_{t-1}; copy it from L2
@@ -151,6 +157,7 @@ __global__ void __launch_bounds__(256, 1)
         if (tid == 0 && t + 2 <= TT - 1) mbar_arrive_expect_tx(full_bar0 + 8 * p, hbytes);
       }
     }
+    RNN_TRACE(1)
     if (tid == 0 && t + FUSED_NS - 1 < TT) {
       const int ts = t + FUSED_NS - 1, s = ts % FUSED_NS;
       mbar_arrive_expect_tx(wx_bar0 + 8 * s, wxbytes);
@@ -202,12 +209,15 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
     }
+    RNN_TRACE(2)
     __syncthreads();
+    RNN_TRACE(3)
 
     // ---- epilogue: gate assembly and cell update, one (batch row, unit) pair per thread
     const int ws = t % FUSED_NS;
     const __nv_bfloat16* wxt = wxs + ws * wx_stage_elems;
     if (tid < nb * U) mbar_wait_bounded(wx_bar0 + 8 * ws, (t / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
+    RNN_TRACE(4)
     for (int e = tid; e < nb * U; e += nthr) {
       const int b = e / U, u = e - b * U;
       const int q = u >> 4, r = u & 15;
@@ -244,7 +254,9 @@ __global__ void __launch_bounds__(256, 1)
         for (int s = 0; s < S; ++s) tp[(P + s) * D] = sn[s];
       }
     }
+    RNN_TRACE(5)
     __syncthreads();
+    RNN_TRACE(6)
 
     // ---- exchange: push this CTA's slice of h_t into every CTA's next buffer
     if (GRIDX) {
@@ -260,7 +272,9 @@ __global__ void __launch_bounds__(256, 1)
         st_async_16(mapa_shared(la, dst), v, mapa_shared(bar_local, dst));
       }
     }
+    RNN_TRACE(7)
   }
+#undef RNN_TRACE
 
   // ---- epilogue of the sequence ---------------------------------------------
   if (a.last) {

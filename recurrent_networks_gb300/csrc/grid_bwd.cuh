@@ -101,12 +101,18 @@ __global__ void __launch_bounds__(256, 1)
     for (int k = 0; k < FUSED_NS - 1 && k < TT; ++k) issue_stage(k);
 
   bool failed = false;
+  const bool tracer = a.trace && blockIdx.x == 0 && tid == 0;
+#define RNN_TRACE(p)                                                                    \
+  if (tracer && kk >= a.trace_t0 && kk < a.trace_t0 + a.trace_steps)                    \
+    a.trace[(size_t)(kk - a.trace_t0) * 8 + (p)] = (unsigned long long)clock64();
   for (int kk = 0; kk <= TT; ++kk) {
     const int t = TT - 1 - kk;
     const bool have_rec = kk > 0;
+    RNN_TRACE(0)
     if (have_rec) {
       // gather dr_{t+1} of the whole group, multiply by the resident rows of R
       if (tid == 0) counter_wait_bounded(a.counters + grp, (unsigned)(C * kk), a.wait_limit_ns, a.status, failed);
+      RNN_TRACE(1)
       __syncthreads();
       const __nv_bfloat16* src = dx + ((size_t)((kk - 1) & 1) * groups + grp) * BC * KG;
       const int rc = KG / 8;
@@ -116,6 +122,7 @@ __global__ void __launch_bounds__(256, 1)
       }
       cp_async_wait_all();
       __syncthreads();
+      RNN_TRACE(2)
       float acc[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
@@ -152,6 +159,7 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
       __syncthreads();
+      RNN_TRACE(3)
     }
 
     if (kk == TT) {  // dstates0 = carried gradients after step 0
@@ -180,6 +188,7 @@ __global__ void __launch_bounds__(256, 1)
       mbar_wait_bounded(ring_bar0 + 8 * sc, (kk / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
       if (t > 0) mbar_wait_bounded(ring_bar0 + 8 * sn_, ((kk + 1) / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
     }
+    RNN_TRACE(4)
     __nv_bfloat16* dxw = dx + ((size_t)(kk & 1) * groups + grp) * BC * KG;
     for (int e = tid; e < nb * U; e += nthr) {
       const int b = e / U, u = e - b * U, q = u >> 4, r = u & 15;
@@ -208,9 +217,12 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
       for (int s = 0; s < S; ++s) ds[(s * BC + b) * U + u] = dsp[s];
     }
+    RNN_TRACE(5)
     __syncthreads();
     if (tid == 0) counter_publish(a.counters + grp);
+    RNN_TRACE(6)
   }
+#undef RNN_TRACE
 }
 
 template <int FN>

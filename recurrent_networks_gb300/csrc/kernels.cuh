@@ -68,6 +68,10 @@ struct FusedArgs {
   // [2][groups][BC][D] and one step counter per group, zeroed before launch
   void* hx = nullptr;
   unsigned int* counters = nullptr;
+  // optional phase trace (rnn_trace): CTA 0, thread 0 writes clock64() at 8
+  // phase points of steps [trace_t0, trace_t0 + trace_steps) (processing order)
+  unsigned long long* trace = nullptr;
+  int trace_t0 = 0, trace_steps = 0;
 };
 
 struct FusedShape;

@@ -16,10 +16,11 @@ Tolerances (stated once, used by every parity test):
                 sLSTM is exempt from the max-norm bound: the derivative of its
                 stabiliser max(a_f + m, a_i) jumps at ties, and bf16 rounding of
                 h (plus fp32 summation order) moves near-ties to the other branch,
-                which changes single elements of dWx by O(|dm|) (~6% of the
-                maximum on B=5, T=29 cases). Against the plain oracle the bf16
-                rounding of h alone moves sLSTM gradients by ~6% even on the
-                plain path, which says nothing about the kernels.
+                which changes single elements of dWx by O(|dm|) and, through the
+                carried dm, earlier steps too. The L2 / cosine bounds therefore
+                widen to 1.5x the oracle's own distance between its bf16-operand
+                and plain-fp64 gradients whenever that is larger: 3-5% L2 for
+                sLSTM at D = 192..512, ~0.1% for LSTM (check_grads).
 """
 from __future__ import annotations
 
@@ -110,6 +111,40 @@ def check_grad(name, dtype, got, ref):
         assert l2 <= tol["grad"], f"{name}: L2-normwise relative err {l2:.3g} > {tol['grad']}"
         assert cos >= tol["cos"], f"{name}: cosine {cos:.6f} < {tol['cos']}"
     return rel
+
+
+def check_grads(fn, inp, got, dlast=None):
+    """All four gradients (dWx, dR, db, dstates0) of the CUDA path against the
+    oracle. fp32: the TOL bounds against the plain oracle. bf16: against the
+    oracle's bfloat16-operand mode; the L2 / cosine bounds widen to 1.5x the
+    distance between the oracle's own bf16-operand and plain-fp64 gradients
+    when that is larger (the gradient's sensitivity to bf16 rounding of h: a
+    few percent for sLSTM, whose stabiliser max flips branch at near-ties,
+    ~0.1% for LSTM)."""
+    names = ("dWx", "dR", "db", "dstates0")
+    dtype = inp["Wx"].dtype
+    ref = oracle_bwd(fn, inp, dlast=dlast)
+    plain = oracle_bwd(fn, inp, dlast=dlast, round_bf16=False) if dtype == torch.bfloat16 else None
+    for k, (name, g) in enumerate(zip(names, got)):
+        if g is None:
+            continue
+        if plain is None:
+            check_grad(f"{fn} {name}", dtype, g, ref[k])
+            continue
+        tol = TOL[dtype]
+        arr = to_np(g)
+        assert np.all(np.isfinite(arr)), f"{fn} {name}: non-finite values"
+        if np.abs(ref[k]).max() == 0:
+            assert np.abs(arr).max() == 0, f"{fn} {name}: expected zeros"
+            continue
+        _, l2_s, cos_s = grad_errors(plain[k], ref[k])
+        rel, l2, cos = grad_errors(arr, ref[k])
+        l2_tol = max(tol["grad"], 1.5 * l2_s)
+        cos_tol = min(tol["cos"], 1.0 - 1.5 * (1.0 - cos_s))
+        if not fn.startswith("slstm"):
+            assert rel <= tol["grad"], f"{fn} {name}: normwise-max relative err {rel:.3g} > {tol['grad']}"
+        assert l2 <= l2_tol, f"{fn} {name}: L2-normwise relative err {l2:.3g} > {l2_tol:.3g}"
+        assert cos >= cos_tol, f"{fn} {name}: cosine {cos:.6f} < {cos_tol:.6f}"
 
 
 def is_bf16(inp):

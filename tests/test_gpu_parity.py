@@ -8,7 +8,7 @@ import torch
 from recurrent_networks_gb300 import _lib
 from recurrent_networks_gb300.synth import make_inputs
 
-from parity_util import (check_grad, check_states, oracle_bwd, oracle_fwd, run_bwd, run_fwd)
+from parity_util import (check_grad, check_grads, check_states, oracle_bwd, oracle_fwd, run_bwd, run_fwd)
 
 pytestmark = pytest.mark.gpu
 
@@ -30,11 +30,7 @@ def _full_check(fn, inp, dtype, path, backward=True, recompute=False):
     if not backward:
         return
     dWx, dR, db, ds0 = run_bwd(fn, inp, st, None if recompute else tape, path)
-    rdWx, rdR, rdb, rds0 = oracle_bwd(fn, inp)
-    check_grad(f"{fn} dWx", dtype, dWx, rdWx)
-    check_grad(f"{fn} dR", dtype, dR, rdR)
-    check_grad(f"{fn} db", dtype, db, rdb)
-    check_grad(f"{fn} dstates0", dtype, ds0, rds0)
+    check_grads(fn, inp, (dWx, dR, db, ds0))
 
 
 @pytest.mark.parametrize("fn", FNS)
@@ -132,11 +128,7 @@ def test_fused_forward_parity(case, monkeypatch):
     check_states(fn, torch.bfloat16, last, ref_last, "last")
     # the backward (plain path) consumes the cluster kernel's tape
     dWx, dR, db, ds0 = run_bwd(fn, inp, st, tape, "simt")
-    rdWx, rdR, rdb, rds0 = oracle_bwd(fn, inp)
-    check_grad(f"{fn} dWx", torch.bfloat16, dWx, rdWx)
-    check_grad(f"{fn} dR", torch.bfloat16, dR, rdR)
-    check_grad(f"{fn} db", torch.bfloat16, db, rdb)
-    check_grad(f"{fn} dstates0", torch.bfloat16, ds0, rds0)
+    check_grads(fn, inp, (dWx, dR, db, ds0))
 
 
 def test_fused_matches_simt_forward_closely(monkeypatch):
@@ -178,11 +170,7 @@ def test_fused_backward_parity(case, monkeypatch):
     st, last, tape = run_fwd(fn, inp, "fused")
     dl = torch.randn(last.shape, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16).cuda()
     dWx, dR, db, ds0 = run_bwd(fn, inp, st, tape, "fused", dlast=dl)
-    rdWx, rdR, rdb, rds0 = oracle_bwd(fn, inp, dlast=dl)
-    check_grad(f"{fn} dWx", torch.bfloat16, dWx, rdWx)
-    check_grad(f"{fn} dR", torch.bfloat16, dR, rdR)
-    check_grad(f"{fn} db", torch.bfloat16, db, rdb)
-    check_grad(f"{fn} dstates0", torch.bfloat16, ds0, rds0)
+    check_grads(fn, inp, (dWx, dR, db, ds0), dlast=dl)
     # the plain path on the same tape gives nearly the same gradients
     sdWx, _, _, sds0 = run_bwd(fn, inp, st, tape, "simt", dlast=dl)
     d1 = (dWx.float() - sdWx.float()).abs().max().item() / max(sdWx.float().abs().max().item(), 1e-30)
@@ -215,11 +203,7 @@ def test_grid_parity(case, monkeypatch):
     check_states(fn, torch.bfloat16, last, ref_last, "last")
     dl = torch.randn(last.shape, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).cuda()
     dWx, dR, db, ds0 = run_bwd(fn, inp, st, tape, "grid", dlast=dl)
-    rdWx, rdR, rdb, rds0 = oracle_bwd(fn, inp, dlast=dl)
-    check_grad(f"{fn} dWx", torch.bfloat16, dWx, rdWx)
-    check_grad(f"{fn} dR", torch.bfloat16, dR, rdR)
-    check_grad(f"{fn} db", torch.bfloat16, db, rdb)
-    check_grad(f"{fn} dstates0", torch.bfloat16, ds0, rds0)
+    check_grads(fn, inp, (dWx, dR, db, ds0), dlast=dl)
 
 
 def test_grid_and_cluster_forward_agree(monkeypatch):
