@@ -37,7 +37,7 @@ L2_BYTES = 129 * 1024 * 1024
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
@@ -69,6 +69,35 @@ def algorithmic(w, fn, esize):
                 bwd_flops=4.0 * G * D * D * units, bwd_bytes=float((2 * S + 2 * G) * D * esize * units))
 
 
+KERNEL_SOURCES = {
+    "fused_fwd_kernel": ["fused_fwd.cuh", "cells.cuh", "ptx.cuh", "layout.h", "kernels.cuh"],
+    "fused_bwd_kernel": ["fused_bwd.cuh", "cells.cuh", "ptx.cuh", "layout.h", "kernels.cuh"],
+    "grid_bwd_kernel": ["grid_bwd.cuh", "cells.cuh", "ptx.cuh", "layout.h", "kernels.cuh"],
+}
+
+
+def kernel_sources_sha(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES.get(kernel, []):
+        with open(os.path.join(ROOT, "recurrent_networks_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary (profiles/traffic.json), or None when absent or when the kernel's
+    sources changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(f"{kernel}@{workload}")
+    if not rec or rec.get("sources_sha256") != kernel_sources_sha(kernel):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -93,7 +122,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         time.sleep(0.3)
@@ -126,40 +155,50 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle
-def cpu_oracle_step(fn, inp, nthreads, sample_b):
-    """One forward + backward of the oracle over the first sample_b batch rows."""
+def cpu_oracle_step(fn, inp, nthreads, rows, steps, backward=True):
+    """One forward (+ backward) of the oracle over the first `rows` batch rows
+    and the first `steps` time steps; returns seconds."""
     from oracle import oracle
-    sub = {k: (v[:sample_b] if k == "Wx" else v) for k, v in inp.items()}
-    sub["states0"] = inp["states0"][:, :sample_b]
-    sub["dstates"] = inp["dstates"][:, :sample_b] if inp["dstates"] is not None else None
+    Wx = inp["Wx"][:rows, :steps]
+    s0 = inp["states0"][:, :rows]
     t0 = time.perf_counter()
-    oracle.fwd(fn, sub["Wx"], sub["R"], sub["b"], sub["states0"], nthreads=nthreads)
-    oracle.bwd(fn, sub["Wx"], sub["R"], sub["b"], sub["states0"], sub["dstates"], nthreads=nthreads)
+    oracle.fwd(fn, Wx, inp["R"], inp["b"], s0, nthreads=nthreads)
+    if backward:
+        dst = inp["dstates"][:, :rows, :steps]
+        oracle.bwd(fn, Wx, inp["R"], inp["b"], s0, dst, nthreads=nthreads)
     return time.perf_counter() - t0
 
 
-def oracle_sample_rows(w, fn):
-    """Batch rows timed so that one oracle step takes ~10-30 s of CPU work."""
+def oracle_sample(w, fn, cores):
+    """(batch rows, time steps) of the workload that make one oracle step about
+    20-60 s of CPU work: all rows when they fit, else a time prefix over at
+    least `cores` sequences. The metric is per (row, step), so the sample's
+    rate stands for the workload's."""
     from recurrent_networks_gb300.synth import GATES
-    G, D, T, N = GATES[fn], w["D"], w["T"], w["N"]
-    flops_per_row = 3 * 2.0 * G * D * D * T * N  # fwd + ~2x for bwd, fp64 loops
-    budget = 20e9 * 1.0  # ~1 GFLOP/s per core x 20 core-seconds
-    return max(1, min(w["B"], int(budget // flops_per_row) or 1))
+    G, D, T, N, B = GATES[fn], w["D"], w["T"], w["N"], w["B"]
+    per_row_step = (3.0 if w["backward"] else 1.0) * 2.0 * G * D * D * N  # fwd (+ bwd), fp64 loops
+    budget = 60e9
+    if per_row_step * B * T <= budget:
+        return B, T
+    rows = min(B, max(1, -(-cores // N)))
+    steps = max(8, min(T, int(budget // (per_row_step * rows))))
+    return rows, steps
 
 
 def run_reference(args, w, fn):
     from recurrent_networks_gb300.synth import workload_inputs
     cores = host_cores()
     inp = workload_inputs(args.workload, function=fn, with_grads=True)
-    rows = oracle_sample_rows(w, fn)
+    rows, steps = oracle_sample(w, fn, cores)
     times = []
     for k in range(args.warmup + args.steps):
-        dt = cpu_oracle_step(fn, inp, cores, rows)
+        dt = cpu_oracle_step(fn, inp, cores, rows, steps, w["backward"])
         if k >= args.warmup:
             times.append(dt)
     per_step = sum(times) / len(times)
-    value = rows * w["T"] / per_step
-    sample = f"{fn} fwd+bwd over {rows} of {w['B']} batch rows, all T={w['T']}, N={w['N']}, D={w['D']}, fp64"
+    value = rows * steps / per_step
+    sample = (f"{fn} {'fwd+bwd' if w['backward'] else 'fwd'} over {rows} of {w['B']} batch rows x "
+              f"{steps} of {w['T']} steps, N={w['N']}, D={w['D']}, fp64")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -295,7 +334,12 @@ def main():
         achieved = kflops / (kms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s",
                 "frac": achieved / pk["bf16"], "traffic": None}
-    roof.update({"kernel": "bwd_scan" if dom_bwd else "fwd_scan", "kernel_ms": kms,
+    plan_path = (plan_b if dom_bwd else plan_f).split()[0].split("=")[1]
+    kname = {("fused", False): "fused_fwd_kernel", ("grid", False): "fused_fwd_kernel",
+             ("fused", True): "fused_bwd_kernel", ("grid", True): "grid_bwd_kernel"}.get(
+        (plan_path, bool(dom_bwd)), f"simt_{'bwd' if dom_bwd else 'fwd'}_kernel")
+    roof["traffic"] = measured_traffic(kname, w["name"])
+    roof.update({"kernel": kname, "kernel_ms": kms,
                  "peak_source": f"{pk['source']} (MEASURED_PEAKS.json, burst)" if pk["source"] == "measured"
                  else "fallback"})
 
@@ -354,13 +398,13 @@ def main():
                          "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     # ---- the oracle on the host cores (rank 0, N=1 only), bounded sample
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and backward:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = host_cores()
-        rows = oracle_sample_rows(w, fn)
-        dt = cpu_oracle_step(fn, host, cores, rows)
-        result["cpu_baseline"] = {"value": rows * T / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                  "sample": f"{fn} fwd+bwd, {rows} of {B} batch rows, all T={T}, N={N}, "
-                                            f"D={D}, fp64, {dt:.1f} s"}
+        rows, steps = oracle_sample(w, fn, cores)
+        dt = cpu_oracle_step(fn, host, cores, rows, steps, backward)
+        result["cpu_baseline"] = {"value": rows * steps / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                  "sample": f"{fn} {'fwd+bwd' if backward else 'fwd'}, {rows} of {B} batch rows x "
+                                            f"{steps} of {T} steps, N={N}, D={D}, fp64, {dt:.1f} s"}
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:

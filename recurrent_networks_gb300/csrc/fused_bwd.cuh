@@ -120,8 +120,22 @@ __global__ void __launch_bounds__(256, 1)
   }
 
   bool failed = false;
-  uint32_t ph[2] = {0u, 0u};
+  uint32_t ph0 = 0u, ph1 = 0u;  // phase parity of the two partial-sum barriers
   const int q4 = lane & 3, r8 = lane >> 2;
+  // each lane always sends row i = (warp*MT + mt)*16 + r8 (+8 on odd lanes):
+  // its owner CTA and the cluster addresses there are fixed for the kernel
+  uint32_t send_base0[MT], send_base1[MT], send_bar0[MT], send_bar1[MT];
+  int send_row[MT];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    const int i = (warp * MT + mt) * 16 + r8 + ((q4 & 1) ? 8 : 0);
+    const int owner = i / U;
+    send_row[mt] = i - owner * U;
+    send_base0[mt] = mapa_shared(smem_u32(recv + (size_t)rank * U * BC), (uint32_t)owner);
+    send_base1[mt] = mapa_shared(smem_u32(recv + ((size_t)C + rank) * U * BC), (uint32_t)owner);
+    send_bar0[mt] = mapa_shared(recv_bar0, (uint32_t)owner);
+    send_bar1[mt] = mapa_shared(recv_bar0 + 8, (uint32_t)owner);
+  }
 
   const bool tracer = a.trace && blockIdx.x == 0 && tid == 0;
 #define RNN_TRACE(p)                                                                    \
@@ -136,8 +150,8 @@ __global__ void __launch_bounds__(256, 1)
     if (tid == 0 && k + FUSED_NS - 1 < TT) issue_stage(k + FUSED_NS - 1);
     if (t < TT - 1) {  // partial sums for dh_t arrived
       const int bi = t & 1;
-      mbar_wait_bounded(recv_bar0 + 8 * bi, ph[bi], a.wait_limit_ns, a.status, failed);
-      ph[bi] ^= 1u;
+      mbar_wait_bounded(recv_bar0 + 8 * bi, bi ? ph1 : ph0, a.wait_limit_ns, a.status, failed);
+      if (bi) ph1 ^= 1u; else ph0 ^= 1u;
       if (tid == 0 && t - 2 >= -1) mbar_arrive_expect_tx(recv_bar0 + 8 * bi, rbytes);
     }
     RNN_TRACE(1)
@@ -146,8 +160,9 @@ __global__ void __launch_bounds__(256, 1)
     const __nv_bfloat16* dstage = (const __nv_bfloat16*)(ring + (size_t)sc * L.ring_stage + L.dst_off);
     const float* tq = (const float*)(ring + (size_t)sn_ * L.ring_stage);
     if (tid < nb * U) {
-      mbar_wait_bounded(ring_bar0 + 8 * sc, (k / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
-      if (t > 0) mbar_wait_bounded(ring_bar0 + 8 * sn_, ((k + 1) / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
+      mbar_wait_bounded<false>(ring_bar0 + 8 * sc, (k / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
+      if (t > 0)
+        mbar_wait_bounded<false>(ring_bar0 + 8 * sn_, ((k + 1) / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
     }
     RNN_TRACE(2)
     const float* rv = recv + (size_t)(t & 1) * C * U * BC;
@@ -166,9 +181,13 @@ __global__ void __launch_bounds__(256, 1)
         if (dlast && t == TT - 1) d += __bfloat162float(dlast[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u]);
         dsn[s] = d;
       }
-      if (t < TT - 1) {
+      if (t < TT - 1) {  // the C partial sums, loaded together
+        float part[FUSED_MAX_C];
+#pragma unroll
+        for (int c = 0; c < FUSED_MAX_C; ++c) part[c] = c < C ? rv[((size_t)c * U + u) * BC + b] : 0.0f;
         float acc = 0.0f;
-        for (int c = 0; c < C; ++c) acc += rv[((size_t)c * U + u) * BC + b];
+#pragma unroll
+        for (int c = 0; c < FUSED_MAX_C; ++c) acc += part[c];
         dsn[0] += acc;
       }
       cell_bwd<FN, true>(pre, sp, sn, dsn, dx, dr, dsp);
@@ -222,8 +241,6 @@ __global__ void __launch_bounds__(256, 1)
     // reduce-scatter: each lane assembles 4 consecutive batch columns of one row
     {
       const int bi = (t - 1) & 1;  // consumption t-1 (t = 0 feeds the final dh_{-1})
-      const uint32_t dst_base = smem_u32(recv + ((size_t)bi * C + rank) * U * BC);
-      const uint32_t bar_local = recv_bar0 + 8 * bi;
       const bool even = (q4 & 1) == 0;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
@@ -235,20 +252,16 @@ __global__ void __launch_bounds__(256, 1)
           const float ra = __shfl_xor_sync(0xffffffffu, sa, 1);
           const float rb = __shfl_xor_sync(0xffffffffu, sb, 1);
           uint4 out;
-          int row, bcol;
+          int bcol;
           if (even) {
             out = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(ra), __float_as_uint(rb));
-            row = r8;
             bcol = nt * 8 + 2 * q4;
           } else {
             out = make_uint4(__float_as_uint(ra), __float_as_uint(rb), __float_as_uint(v[2]), __float_as_uint(v[3]));
-            row = r8 + 8;
             bcol = nt * 8 + 2 * q4 - 2;
           }
-          const int i = (warp * MT + mt) * 16 + row;
-          const int owner = i / U, ul = i - owner * U;
-          const uint32_t la = dst_base + (uint32_t)((ul * BC + bcol) * 4);
-          st_async_16(mapa_shared(la, (uint32_t)owner), out, mapa_shared(bar_local, (uint32_t)owner));
+          const uint32_t off = (uint32_t)((send_row[mt] * BC + bcol) * 4);
+          st_async_16((bi ? send_base1[mt] : send_base0[mt]) + off, out, bi ? send_bar1[mt] : send_bar0[mt]);
         }
     }
     RNN_TRACE(6)
@@ -258,7 +271,7 @@ __global__ void __launch_bounds__(256, 1)
   // ---- dstates0: the carried gradients after step 0 ------------------------------
   {
     const int bi = 1;  // consumption -1
-    mbar_wait_bounded(recv_bar0 + 8 * bi, ph[bi], a.wait_limit_ns, a.status, failed);
+    mbar_wait_bounded(recv_bar0 + 8 * bi, ph1, a.wait_limit_ns, a.status, failed);  // bi == 1
     const float* rv = recv + (size_t)bi * C * U * BC;
     __nv_bfloat16* ds0 = (__nv_bfloat16*)a.ds0;
     if (ds0)

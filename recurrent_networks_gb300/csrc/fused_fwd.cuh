@@ -127,6 +127,16 @@ __global__ void __launch_bounds__(256, 1)
   bool failed = false;
   uint32_t ph0 = 0, ph1 = 0;
   const int nchunk = nb * (U / 8);  // 16-byte chunks of the CTA's h slice
+  // cluster addresses of this thread's peer's h buffers and barriers
+  const bool fixed_peer = !GRIDX && (nthr % C) == 0;
+  uint32_t peer_h0 = 0u, peer_h1 = 0u, peer_bar0 = 0u, peer_bar1 = 0u;
+  if (fixed_peer) {
+    const uint32_t peer = (uint32_t)(tid % C);
+    peer_h0 = mapa_shared(smem_u32(hbuf), peer);
+    peer_h1 = mapa_shared(smem_u32(hbuf + BC * HS), peer);
+    peer_bar0 = mapa_shared(full_bar0, peer);
+    peer_bar1 = mapa_shared(full_bar0 + 8, peer);
+  }
 
   const bool tracer = a.trace && blockIdx.x == 0 && tid == 0;
 #define RNN_TRACE(k)                                                                    \
@@ -216,17 +226,25 @@ __global__ void __launch_bounds__(256, 1)
     // ---- epilogue: gate assembly and cell update, one (batch row, unit) pair per thread
     const int ws = t % FUSED_NS;
     const __nv_bfloat16* wxt = wxs + ws * wx_stage_elems;
-    if (tid < nb * U) mbar_wait_bounded(wx_bar0 + 8 * ws, (t / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
+    if (tid < nb * U)
+      mbar_wait_bounded<false>(wx_bar0 + 8 * ws, (t / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
     RNN_TRACE(4)
     for (int e = tid; e < nb * U; e += nthr) {
       const int b = e / U, u = e - b * U;
       const int q = u >> 4, r = u & 15;
       float x[G], rc[G], sp[S], sn[S], pre[P];
+      // all K-split partials are loaded before any is summed (independent loads)
+      float part[G][FUSED_MAX_KS];
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int k2 = 0; k2 < FUSED_MAX_KS; ++k2)
+          part[g][k2] = k2 < KS ? red[((size_t)((q * KS + k2) * G + g) * BC + b) * FUSED_RED_STRIDE + r] : 0.0f;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float v = bias_s[g * U + u];
-        for (int k2 = 0; k2 < KS; ++k2)
-          v += red[((size_t)((q * KS + k2) * G + g) * BC + b) * FUSED_RED_STRIDE + r];
+#pragma unroll
+        for (int k2 = 0; k2 < FUSED_MAX_KS; ++k2) v += part[g][k2];
         rc[g] = v;
         x[g] = __bfloat162float(wxt[(b * G + g) * U + u]);
       }
@@ -262,14 +280,18 @@ __global__ void __launch_bounds__(256, 1)
     if (GRIDX) {
       if (t + 1 < TT && tid == 0) counter_publish(a.counters + grp);
     } else if (t + 1 < TT) {
+      // chunk e goes to CTA e % C; with C | blockDim every thread keeps one peer
       const uint32_t dst_local = smem_u32(hbuf + (p ^ 1) * BC * HS);
       const uint32_t bar_local = full_bar0 + 8 * (p ^ 1);
       for (int e = tid; e < nchunk * C; e += nthr) {
-        const int dst = e / nchunk, w = e - dst * nchunk;
+        const int dst = e % C, w = e / C;
         const int b = w / (U / 8), cu = w - b * (U / 8);
         const uint4 v = *(const uint4*)(stage + b * U + cu * 8);
-        const uint32_t la = dst_local + (uint32_t)((b * HS + u0 + cu * 8) * 2);
-        st_async_16(mapa_shared(la, dst), v, mapa_shared(bar_local, dst));
+        const uint32_t off = (uint32_t)((b * HS + u0 + cu * 8) * 2);
+        if (fixed_peer)
+          st_async_16((p ? peer_h0 : peer_h1) + off, v, p ? peer_bar0 : peer_bar1);
+        else
+          st_async_16(mapa_shared(dst_local + off, dst), v, mapa_shared(bar_local, dst));
       }
     }
     RNN_TRACE(7)

@@ -185,8 +185,9 @@ __global__ void __launch_bounds__(256, 1)
     const __nv_bfloat16* dstage = (const __nv_bfloat16*)(ring + (size_t)sc * L.ring_stage + L.dst_off);
     const float* tq = (const float*)(ring + (size_t)sn_ * L.ring_stage);
     if (tid < nb * U) {
-      mbar_wait_bounded(ring_bar0 + 8 * sc, (kk / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
-      if (t > 0) mbar_wait_bounded(ring_bar0 + 8 * sn_, ((kk + 1) / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
+      mbar_wait_bounded<false>(ring_bar0 + 8 * sc, (kk / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
+      if (t > 0)
+        mbar_wait_bounded<false>(ring_bar0 + 8 * sn_, ((kk + 1) / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
     }
     RNN_TRACE(4)
     __nv_bfloat16* dxw = dx + ((size_t)(kk & 1) * groups + grp) * BC * KG;
@@ -204,8 +205,14 @@ __global__ void __launch_bounds__(256, 1)
         if (dlast && t == TT - 1) d += __bfloat162float(dlast[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u]);
         dsn[s] = d;
       }
-      if (have_rec)
-        for (int k2 = 0; k2 < KS; ++k2) dsn[0] += red[((size_t)(q * KS + k2) * BC + b) * FUSED_RED_STRIDE + r];
+      if (have_rec) {  // the K-split partials, loaded together
+        float part[FUSED_MAX_KS];
+#pragma unroll
+        for (int k2 = 0; k2 < FUSED_MAX_KS; ++k2)
+          part[k2] = k2 < KS ? red[((size_t)(q * KS + k2) * BC + b) * FUSED_RED_STRIDE + r] : 0.0f;
+#pragma unroll
+        for (int k2 = 0; k2 < FUSED_MAX_KS; ++k2) dsn[0] += part[k2];
+      }
       cell_bwd<FN, true>(pre, sp, sn, dsn, dxg, dr, dsp);
       const size_t o = (((size_t)(b0 + b) * TT + t) * G) * N * D + (size_t)n * D + u0 + u;
 #pragma unroll

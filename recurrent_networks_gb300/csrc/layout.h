@@ -13,6 +13,8 @@ namespace rnn {
 
 constexpr int FUSED_NS = 4;           // Wx ring depth (steps in flight)
 constexpr int FUSED_RED_STRIDE = 20;  // floats per batch row of a partial-sum tile (16 used)
+constexpr int FUSED_MAX_KS = 8;       // K-split warps per 16-unit group (warps <= 8)
+constexpr int FUSED_MAX_C = 16;       // CTAs per cluster
 
 // Launch shape of a persistent cluster kernel, chosen by the planner.
 struct FusedShape {

@@ -57,19 +57,35 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_try_wait_cta(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete, for at most
 // limit_ns. On time-out records STATUS_TIMEOUT in *status, sets `failed` and
 // returns false; once `failed` is set, later waits return at once so that the
 // kernel runs to its end (every CTA still reaches its final cluster barrier).
+// CLUSTER selects acquire at cluster scope (data written by peer CTAs) or at
+// CTA scope (this CTA's own TMA loads).
+template <bool CLUSTER = true>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                                   unsigned int* status, bool& failed) {
+  auto probe = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait_cta(bar, parity); };
   if (failed) return false;
-  if (mbar_try_wait_cluster(bar, parity)) return true;
+  if (probe()) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
 #pragma unroll 1
     for (int k = 0; k < 32; ++k)
-      if (mbar_try_wait_cluster(bar, parity)) return true;
+      if (probe()) return true;
     if (globaltimer_ns() - t0 > limit_ns) {
       if (status) atomicExch(status, 1u);
       failed = true;
