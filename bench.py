@@ -98,6 +98,21 @@ def measured_traffic(kernel, workload):
     return rec.get("dram_bytes_per_launch")
 
 
+def aggregate(total_ms, fwd_ms, world, units_per_rank, steps, device=None):
+    """Max over ranks of the timed totals (the slowest rank bounds the job);
+    value = the units all ranks processed / that time. Returns (ms per step,
+    value, forward-only value)."""
+    t = torch.tensor([total_ms, fwd_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    tot, fwd = float(t[0]), float(t[1])
+    ms_per_step = tot / steps
+    value = world * units_per_rank / (ms_per_step / 1e3)
+    fwd_value = world * units_per_rank / (fwd / steps / 1e3) if fwd > 0 else 0.0
+    return ms_per_step, value, fwd_value
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -303,16 +318,8 @@ def main():
     _lib.rnn_profile_events(1, None, None)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     fwd_ms = [s.elapsed_time(m) for s, m in zip(starts, mids)]
-    tot_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([tot_ms, sum(fwd_ms)], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms, fwd_tot = float(t[0]), float(t[1])
-    else:
-        fwd_tot = sum(fwd_ms)
-    ms_per_step = tot_ms / args.steps
-    value = world * B * T / (ms_per_step / 1e3)
-    fwd_value = world * B * T / (fwd_tot / args.steps / 1e3)
+    ms_per_step, value, fwd_value = aggregate(sum(step_ms), sum(fwd_ms), world, B * T, args.steps, dev)
+    fwd_tot = fwd_value and world * B * T / fwd_value * 1e3 * args.steps
 
     pk = peaks()
     alg = algorithmic(w, fn, esize)

@@ -183,6 +183,16 @@ int rnn_profile_events(int which, void *before, void *after);
  * RNN_OK or RNN_EINVAL. */
 int rnn_trace(void *buf, int t0, int steps);
 
+/* Fault injection for tests of the device-side time-out path. With step >= 0,
+ * the forward persistent kernels (cluster and grid paths) launched afterwards
+ * make CTA 0 wait, at that step, on an mbarrier that nothing signals, for at
+ * most limit_ns (1 ns .. 10 s). The wait runs out, the kernel records the
+ * time-out in the workspace status word and carries on; the step exchange
+ * itself is untouched, so results stay correct and rnn_check_status reports
+ * RNN_ETIMEOUT. step < 0 switches injection off. Process-global; returns
+ * RNN_OK or RNN_EINVAL. */
+int rnn_debug_inject_wait(int step, unsigned long long limit_ns);
+
 #ifdef __cplusplus
 }
 #endif

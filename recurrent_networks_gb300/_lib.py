@@ -20,7 +20,7 @@ WS_FWD, WS_BWD, WS_BWD_RECOMPUTE = 0, 1, 2
 
 EXPORTS = ["rnn_num_gates", "rnn_num_states", "rnn_tape_size", "rnn_workspace_size", "rnn_fwd",
            "rnn_bwd", "rnn_check_status", "rnn_plan_describe", "rnn_strerror", "rnn_kernel_launches",
-           "rnn_profile_events", "rnn_bwd_noalloc", "rnn_trace"]
+           "rnn_profile_events", "rnn_bwd_noalloc", "rnn_trace", "rnn_debug_inject_wait"]
 
 
 class RnnError(RuntimeError):
@@ -63,6 +63,7 @@ def load(path: str | None = None):
             lib.rnn_profile_events.argtypes = [i, vp, vp]
             lib.rnn_bwd_noalloc.argtypes = [dp] + [vp] * 13
             lib.rnn_trace.argtypes = [vp, i, i]
+            lib.rnn_debug_inject_wait.argtypes = [i, ctypes.c_ulonglong]
             _lib = lib
     return _lib
 
@@ -166,3 +167,9 @@ def rnn_trace(buf=None, t0: int = 0, steps: int = 0) -> int:
     """Registers a device tensor of >= 8*steps int64 for the persistent kernels'
     phase trace (clock64 at eight points of steps [t0, t0+steps)), or None."""
     return _check(load().rnn_trace(_p(buf), int(t0), int(steps)), "rnn_trace")
+
+
+def rnn_debug_inject_wait(step: int = -1, limit_ns: int = 0) -> int:
+    """Test hook: the forward persistent kernels make CTA 0 wait at `step` on a
+    barrier nothing signals, for limit_ns; step < 0 switches it off."""
+    return _check(load().rnn_debug_inject_wait(int(step), int(limit_ns)), "rnn_debug_inject_wait")

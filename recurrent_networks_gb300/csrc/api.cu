@@ -102,10 +102,16 @@ static unsigned long long g_wait_limit_ns = 2000000000ull;
 // Phase trace of the persistent kernels (rnn_trace).
 static unsigned long long* g_trace_buf = nullptr;
 static int g_trace_t0 = 0, g_trace_steps = 0;
+// Fault injection of the forward persistent kernels (rnn_debug_inject_wait).
+static int g_inject_step = -1;
+static unsigned long long g_inject_limit_ns = 0;
+
 static void with_trace(FusedArgs* f) {
   f->trace = g_trace_buf;
   f->trace_t0 = g_trace_t0;
   f->trace_steps = g_trace_steps;
+  f->inject_step = g_inject_step;
+  f->inject_limit_ns = g_inject_limit_ns;
 }
 
 // Runs the forward kernels (states/last/tape each optional); ws is the
@@ -340,6 +346,13 @@ int rnn_trace(void* buf, int t0, int steps) {
   g_trace_buf = (unsigned long long*)buf;
   g_trace_t0 = buf ? t0 : 0;
   g_trace_steps = buf ? steps : 0;
+  return RNN_OK;
+}
+
+int rnn_debug_inject_wait(int step, unsigned long long limit_ns) {
+  if (step >= 0 && (limit_ns == 0 || limit_ns > 10000000000ull)) return RNN_EINVAL;
+  g_inject_step = step < 0 ? -1 : step;
+  g_inject_limit_ns = step < 0 ? 0 : limit_ns;
   return RNN_OK;
 }
 

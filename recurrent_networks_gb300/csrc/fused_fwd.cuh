@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(256, 1)
   if (tid == 0) {
     mbar_init(full_bar0, 1);
     mbar_init(full_bar0 + 8, 1);
+    mbar_init(full_bar0 + 8 * (2 + FUSED_NS), 1);  // fault injection: nothing arrives on it
     for (int s = 0; s < FUSED_NS; ++s) mbar_init(wx_bar0 + 8 * s, 1);
     fence_mbar_init_cluster();
     prefetch_tensormap(&wxmap);
@@ -168,6 +169,12 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
     RNN_TRACE(1)
+    if (t == a.inject_step && blockIdx.x == 0) {
+      // injected fault: a wait that nothing ends runs out and records
+      // STATUS_TIMEOUT; the exchange protocol itself is left untouched
+      bool inj_failed = false;
+      mbar_wait_bounded<false>(full_bar0 + 8 * (2 + FUSED_NS), 0, a.inject_limit_ns, a.status, inj_failed);
+    }
     if (tid == 0 && t + FUSED_NS - 1 < TT) {
       const int ts = t + FUSED_NS - 1, s = ts % FUSED_NS;
       mbar_arrive_expect_tx(wx_bar0 + 8 * s, wxbytes);

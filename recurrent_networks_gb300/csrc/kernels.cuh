@@ -72,6 +72,11 @@ struct FusedArgs {
   // phase points of steps [trace_t0, trace_t0 + trace_steps) (processing order)
   unsigned long long* trace = nullptr;
   int trace_t0 = 0, trace_steps = 0;
+  // fault injection (rnn_debug_inject_wait): at this step (processing order)
+  // CTA 0 also waits on a barrier that nothing signals, for inject_limit_ns;
+  // -1 = off
+  int inject_step = -1;
+  unsigned long long inject_limit_ns = 0;
 };
 
 struct FusedShape;

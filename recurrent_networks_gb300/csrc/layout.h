@@ -39,7 +39,7 @@ struct FusedSmem {
   RNN_HD static FusedSmem make(int G, int S, int D, int U, int BC, int KS) {
     FusedSmem m;
     size_t off = 0;
-    m.bars = take(off, 8 * (2 + FUSED_NS));
+    m.bars = take(off, 8 * (3 + FUSED_NS));  // h full x2, Wx ring, one never signalled
     m.wx = take(off, (size_t)FUSED_NS * BC * G * U * 2);
     m.hbuf = take(off, (size_t)2 * BC * (D + 8) * 2);
     m.red = take(off, (size_t)(U / 16) * KS * G * BC * FUSED_RED_STRIDE * 4);
