@@ -35,25 +35,29 @@ __host__ __device__ constexpr int fn_pre(int fn) { return fn == 1 ? 4 : fn_gates
 __host__ __device__ constexpr int fn_tape(int fn) { return fn_pre(fn) + fn_states(fn); }
 
 // ---- transcendentals ------------------------------------------------------
-// FAST = true uses the PTX approximate instructions (tanh.approx.f32,
-// ex2.approx.ftz.f32); FAST = false calls CUDA's accurate tanhf / expf.
-__device__ __forceinline__ float tanh_fast(float x) {
-  float y;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
+// FAST = true builds the functions from the PTX base-2 exponential and
+// reciprocal approximations (ex2.approx.ftz.f32, rcp.approx.ftz.f32, each
+// within a few ulp of fp32):  sigmoid(x) = 1 / (1 + 2^(-x log2 e)),
+// tanh(x) = 1 - 2 / (1 + 2^(2x log2 e)); absolute error ~1e-7, so a bf16
+// rounding of h almost never lands on the other side of a tie because of it
+// (tanh.approx.f32, at ~2^-11 relative error, flipped ~1 in 4 roundings).
+// FAST = false calls CUDA's accurate tanhf / expf.
 __device__ __forceinline__ float exp2_fast(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ float rcp_fast(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 template <bool FAST> __device__ __forceinline__ float f_tanh(float x) {
-  if (FAST) return tanh_fast(x);
+  if (FAST) return fmaf(-2.0f, rcp_fast(1.0f + exp2_fast(2.8853900817779268f * x)), 1.0f);
   return tanhf(x);
 }
 template <bool FAST> __device__ __forceinline__ float f_sigmoid(float x) {
-  // sigmoid(x) = (1 + tanh(x/2)) / 2
-  if (FAST) return fmaf(0.5f, tanh_fast(0.5f * x), 0.5f);
+  if (FAST) return rcp_fast(1.0f + exp2_fast(-1.4426950408889634f * x));
   return 1.0f / (1.0f + expf(-x));
 }
 template <bool FAST> __device__ __forceinline__ float f_exp(float x) {

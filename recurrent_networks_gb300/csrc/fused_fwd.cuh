@@ -34,7 +34,8 @@ __global__ void __launch_bounds__(256, 1)
   constexpr int G = FnInfo<FN>::G, S = FnInfo<FN>::S, P = FnInfo<FN>::P, K = P + S;
   constexpr int BC = 8 * NT;
   const int C = a.C, U = a.U, D = a.D, KS = a.KS, TT = a.T, N = a.N, B = a.B;
-  const int HS = D + 8;  // row stride (elements) of the h buffers
+  const int UP = U + 8;        // row stride (elements) of one source CTA's block of h
+  const int HB = C * BC * UP;  // elements of one h buffer: [C][BC][UP]
   const uint32_t rank = GRIDX ? (uint32_t)(blockIdx.x % C) : cluster_ctarank();
   const int grp = blockIdx.x / C;
   const int n = grp % N;
@@ -52,11 +53,10 @@ __global__ void __launch_bounds__(256, 1)
   __nv_bfloat16* hbuf = (__nv_bfloat16*)(smem + L.hbuf);
   float* red = (float*)(smem + L.red);
   __nv_bfloat16* stage = (__nv_bfloat16*)(smem + L.stage);
-  float* cst = (float*)(smem + L.cst);
-  float* bias_s = (float*)(smem + L.bias);
   const uint32_t full_bar0 = smem_u32(&bars[0]);
   const uint32_t wx_bar0 = smem_u32(&bars[2]);
-  const uint32_t hbytes = (uint32_t)nb * D * 2;
+  const uint32_t slice_bytes = (uint32_t)nb * UP * 2;  // one CTA's h slice, as sent
+  const uint32_t hbytes = (uint32_t)C * slice_bytes;    // what a CTA receives per step
   const uint32_t wxbytes = (uint32_t)BC * G * U * 2;
   const size_t wx_stage_elems = (size_t)BC * G * U;
 
@@ -76,23 +76,28 @@ __global__ void __launch_bounds__(256, 1)
     fence_mbar_init_cluster();
     prefetch_tensormap(&wxmap);
   }
-  for (int e = tid; e < 2 * BC * HS; e += nthr) hbuf[e] = __float2bfloat16_rn(0.0f);
-  for (int e = tid; e < BC * U; e += nthr) stage[e] = __float2bfloat16_rn(0.0f);
+  for (int e = tid; e < 2 * HB; e += nthr) hbuf[e] = __float2bfloat16_rn(0.0f);
+  for (int e = tid; e < 2 * BC * UP; e += nthr) stage[e] = __float2bfloat16_rn(0.0f);
   __syncthreads();
   for (int e = tid; e < nb * D; e += nthr) {
-    const int b = e / D, i = e - b * D;
+    const int b = e / D, i = e - b * D, src = i / U;
     float v = s0 ? __bfloat162float(s0[((size_t)(b0 + b) * N + n) * D + i]) : 0.0f;
-    hbuf[b * HS + i] = __float2bfloat16_rn(v);
+    hbuf[(src * BC + b) * UP + i - src * U] = __float2bfloat16_rn(v);
   }
-  for (int e = tid; e < S * BC * U; e += nthr) {
-    const int s = e / (BC * U), r = e - s * BC * U, b = r / U, u = r - b * U;
-    float v = 0.0f;
-    if (b < nb && s0) v = __bfloat162float(s0[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u]);
-    cst[e] = v;
-  }
-  for (int e = tid; e < G * U; e += nthr) {
-    const int g = e / U, u = e - g * U;
-    bias_s[e] = __bfloat162float(bias[((size_t)g * N + n) * D + u0 + u]);
+  // Each thread owns the (batch row, unit) pairs e = tid + k * blockDim
+  // (k < FUSED_PPT) for the whole sequence: their carried states (fp32) and
+  // biases live in registers.
+  float csr[FUSED_PPT][S], bsr[FUSED_PPT][G];
+#pragma unroll
+  for (int k = 0; k < FUSED_PPT; ++k) {
+    const int e = tid + k * nthr, b = e / U, u = e - b * U;
+    const bool own = e < nb * U;
+#pragma unroll
+    for (int s = 0; s < S; ++s)
+      csr[k][s] = (own && s0) ? __bfloat162float(s0[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u]) : 0.0f;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      bsr[k][g] = own ? __bfloat162float(bias[((size_t)g * N + n) * D + u0 + u]) : 0.0f;
   }
 
   // resident R fragments: A[m = unit j][k = input i] = R[g, n, i, j]
@@ -127,14 +132,13 @@ __global__ void __launch_bounds__(256, 1)
 
   bool failed = false;
   uint32_t ph0 = 0, ph1 = 0;
-  const int nchunk = nb * (U / 8);  // 16-byte chunks of the CTA's h slice
-  // cluster addresses of this thread's peer's h buffers and barriers
-  const bool fixed_peer = !GRIDX && (nthr % C) == 0;
+  // thread c < C sends this CTA's slice to CTA c with one bulk copy per step:
+  // cluster addresses of this CTA's block in c's two h buffers and c's barriers
   uint32_t peer_h0 = 0u, peer_h1 = 0u, peer_bar0 = 0u, peer_bar1 = 0u;
-  if (fixed_peer) {
-    const uint32_t peer = (uint32_t)(tid % C);
-    peer_h0 = mapa_shared(smem_u32(hbuf), peer);
-    peer_h1 = mapa_shared(smem_u32(hbuf + BC * HS), peer);
+  if (!GRIDX && tid < C) {
+    const uint32_t peer = (uint32_t)tid;
+    peer_h0 = mapa_shared(smem_u32(hbuf + (size_t)rank * BC * UP), peer);
+    peer_h1 = mapa_shared(smem_u32(hbuf + HB + (size_t)rank * BC * UP), peer);
     peer_bar0 = mapa_shared(full_bar0, peer);
     peer_bar1 = mapa_shared(full_bar0 + 8, peer);
   }
@@ -156,8 +160,8 @@ __global__ void __launch_bounds__(256, 1)
         const __nv_bfloat16* src = (const __nv_bfloat16*)a.hx + ((size_t)(p * (gridDim.x / C) + grp) * BC) * D;
         const int rc = D / 8;
         for (int e = tid; e < nb * rc; e += nthr) {
-          const int b = e / rc, c = e - b * rc;
-          cp_async_cg16(smem_u32(hbuf + (p * BC + b) * HS + c * 8), src + (size_t)b * D + c * 8);
+          const int b = e / rc, i = (e - b * rc) * 8, sblk = i / U;
+          cp_async_cg16(smem_u32(hbuf + p * HB + (sblk * BC + b) * UP + i - sblk * U), src + (size_t)b * D + i);
         }
         cp_async_wait_all();
         __syncthreads();
@@ -189,20 +193,21 @@ __global__ void __launch_bounds__(256, 1)
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[g][nt][q] = 0.0f;
-    const uint32_t hb = smem_u32(hbuf + p * BC * HS);
+    const uint32_t hb = smem_u32(hbuf + p * HB);
 #pragma unroll
     for (int kt = 0; kt < KT; ++kt) {
       const int k0 = (ks * KT + kt) * 16;
+      const int sblk = k0 / U;  // the source CTA whose block holds inputs k0 .. k0+15
+      const uint32_t blk = hb + (uint32_t)((sblk * BC * UP + k0 - sblk * U) * 2);
       uint32_t bf[NT][2];
       if constexpr (NT == 1) {
-        const uint32_t addr = hb + (uint32_t)(((lane & 7) * HS + k0 + ((lane >> 3) & 1) * 8) * 2);
+        const uint32_t addr = blk + (uint32_t)(((lane & 7) * UP + ((lane >> 3) & 1) * 8) * 2);
         ldmatrix_x2(addr, bf[0][0], bf[0][1]);
       } else {
 #pragma unroll
         for (int np = 0; np < NT; np += 2) {
           const int q = lane >> 3;
-          const uint32_t addr =
-              hb + (uint32_t)((((np + (q >> 1)) * 8 + (lane & 7)) * HS + k0 + (q & 1) * 8) * 2);
+          const uint32_t addr = blk + (uint32_t)((((np + (q >> 1)) * 8 + (lane & 7)) * UP + (q & 1) * 8) * 2);
           ldmatrix_x4(addr, bf[np][0], bf[np][1], bf[np + 1][0], bf[np + 1][1]);
         }
       }
@@ -236,10 +241,13 @@ __global__ void __launch_bounds__(256, 1)
     if (tid < nb * U)
       mbar_wait_bounded<false>(wx_bar0 + 8 * ws, (t / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
     RNN_TRACE(4)
-    for (int e = tid; e < nb * U; e += nthr) {
+#pragma unroll
+    for (int kp = 0; kp < FUSED_PPT; ++kp) {
+      const int e = tid + kp * nthr;
+      if (e >= nb * U) break;
       const int b = e / U, u = e - b * U;
       const int q = u >> 4, r = u & 15;
-      float x[G], rc[G], sp[S], sn[S], pre[P];
+      float x[G], rc[G], sn[S], pre[P];
       // all K-split partials are loaded before any is summed (independent loads)
       float part[G][FUSED_MAX_KS];
 #pragma unroll
@@ -249,19 +257,17 @@ __global__ void __launch_bounds__(256, 1)
           part[g][k2] = k2 < KS ? red[((size_t)((q * KS + k2) * G + g) * BC + b) * FUSED_RED_STRIDE + r] : 0.0f;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float v = bias_s[g * U + u];
+        float v = bsr[kp][g];
 #pragma unroll
         for (int k2 = 0; k2 < FUSED_MAX_KS; ++k2) v += part[g][k2];
         rc[g] = v;
         x[g] = __bfloat162float(wxt[(b * G + g) * U + u]);
       }
-#pragma unroll
-      for (int s = 0; s < S; ++s) sp[s] = cst[(s * BC + b) * U + u];
-      cell_fwd<FN, true>(x, rc, sp, sn, pre);
+      cell_fwd<FN, true>(x, rc, csr[kp], sn, pre);
       const int bg = b0 + b, j = u0 + u;
 #pragma unroll
       for (int s = 0; s < S; ++s) {
-        cst[(s * BC + b) * U + u] = sn[s];
+        csr[kp][s] = sn[s];
         if (states) states[(((size_t)s * B + bg) * TT + t) * N * D + (size_t)n * D + j] = __float2bfloat16_rn(sn[s]);
       }
       if constexpr (GRIDX) {
@@ -269,7 +275,7 @@ __global__ void __launch_bounds__(256, 1)
           ((__nv_bfloat16*)a.hx)[((size_t)((p ^ 1) * (gridDim.x / C) + grp) * BC + b) * D + j] =
               __float2bfloat16_rn(sn[0]);
       } else {
-        stage[b * U + u] = __float2bfloat16_rn(sn[0]);
+        stage[(p * BC + b) * UP + u] = __float2bfloat16_rn(sn[0]);
       }
       if (a.tape) {
         float* tp = a.tape + (((size_t)t * B + bg) * N + n) * K * D + j;
@@ -280,26 +286,19 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
     RNN_TRACE(5)
+    if constexpr (!GRIDX) fence_proxy_async_smem();  // the staged slice is read by bulk copies
     __syncthreads();
     RNN_TRACE(6)
 
-    // ---- exchange: push this CTA's slice of h_t into every CTA's next buffer
+    // ---- exchange: push this CTA's slice of h_t into every CTA's next buffer.
+    // The staged slice stage[p] is not rewritten before step t + 2, whose wait
+    // needs every peer's h_{t+1}, which in turn needed this step's copies to
+    // have landed (so their reads of stage[p] are over).
     if (GRIDX) {
       if (t + 1 < TT && tid == 0) counter_publish(a.counters + grp);
-    } else if (t + 1 < TT) {
-      // chunk e goes to CTA e % C; with C | blockDim every thread keeps one peer
-      const uint32_t dst_local = smem_u32(hbuf + (p ^ 1) * BC * HS);
-      const uint32_t bar_local = full_bar0 + 8 * (p ^ 1);
-      for (int e = tid; e < nchunk * C; e += nthr) {
-        const int dst = e % C, w = e / C;
-        const int b = w / (U / 8), cu = w - b * (U / 8);
-        const uint4 v = *(const uint4*)(stage + b * U + cu * 8);
-        const uint32_t off = (uint32_t)((b * HS + u0 + cu * 8) * 2);
-        if (fixed_peer)
-          st_async_16((p ? peer_h0 : peer_h1) + off, v, p ? peer_bar0 : peer_bar1);
-        else
-          st_async_16(mapa_shared(dst_local + off, dst), v, mapa_shared(bar_local, dst));
-      }
+    } else if (t + 1 < TT && tid < C) {
+      bulk_copy_to_peer(p ? peer_h0 : peer_h1, smem_u32(stage + p * BC * UP), slice_bytes,
+                        p ? peer_bar0 : peer_bar1);
     }
     RNN_TRACE(7)
   }
@@ -308,11 +307,14 @@ __global__ void __launch_bounds__(256, 1)
   // ---- epilogue of the sequence ---------------------------------------------
   if (a.last) {
     __nv_bfloat16* last = (__nv_bfloat16*)a.last;
-    for (int e = tid; e < nb * U; e += nthr) {
+#pragma unroll
+    for (int kp = 0; kp < FUSED_PPT; ++kp) {
+      const int e = tid + kp * nthr;
+      if (e >= nb * U) break;
       const int b = e / U, u = e - b * U;
 #pragma unroll
       for (int s = 0; s < S; ++s)
-        last[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u] = __float2bfloat16_rn(cst[(s * BC + b) * U + u]);
+        last[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u] = __float2bfloat16_rn(csr[kp][s]);
     }
   }
   __syncthreads();

@@ -15,6 +15,7 @@ constexpr int FUSED_NS = 4;           // Wx ring depth (steps in flight)
 constexpr int FUSED_RED_STRIDE = 20;  // floats per batch row of a partial-sum tile (16 used)
 constexpr int FUSED_MAX_KS = 8;       // K-split warps per 16-unit group (warps <= 8)
 constexpr int FUSED_MAX_C = 16;       // CTAs per cluster
+constexpr int FUSED_PPT = 2;          // (batch row, unit) pairs a thread carries in registers
 
 // Launch shape of a persistent cluster kernel, chosen by the planner.
 struct FusedShape {
@@ -39,13 +40,17 @@ struct FusedSmem {
   RNN_HD static FusedSmem make(int G, int S, int D, int U, int BC, int KS) {
     FusedSmem m;
     size_t off = 0;
+    // h_{t-1} is kept per source CTA: hbuf[2][C][BC][U + 8] (bf16, rows padded
+    // by 16 bytes so that ldmatrix rows fall on distinct banks); the CTA's own
+    // slice of h_t is staged in the same row format, double-buffered.
+    const int C = D / U, UP = U + 8;
     m.bars = take(off, 8 * (3 + FUSED_NS));  // h full x2, Wx ring, one never signalled
     m.wx = take(off, (size_t)FUSED_NS * BC * G * U * 2);
-    m.hbuf = take(off, (size_t)2 * BC * (D + 8) * 2);
+    m.hbuf = take(off, (size_t)2 * C * BC * UP * 2);
     m.red = take(off, (size_t)(U / 16) * KS * G * BC * FUSED_RED_STRIDE * 4);
-    m.stage = take(off, (size_t)BC * U * 2);
-    m.cst = take(off, (size_t)S * BC * U * 4);
-    m.bias = take(off, (size_t)G * U * 4);
+    m.stage = take(off, (size_t)2 * BC * UP * 2);
+    m.cst = m.bias = off;  // carried states and biases are held in registers
+    (void)S;
     m.total = off;
     return m;
   }

@@ -38,6 +38,7 @@ bool fused_fwd_feasible(const PlanRequest& q, int C, int NT, int KT, const Devic
   const int warps = (U / 16) * KS;
   if (warps < 1 || warps > lim.max_warps) return false;
   const int BC = 8 * NT;
+  if ((q.B < BC ? q.B : BC) * U > FUSED_PPT * warps * 32) return false;  // pairs held in registers
   const int regs = 4 * G * KT + 4 * G * NT + 2 * NT + 48;
   if (regs > lim.regs_per_thread) return false;
   const FusedSmem L = FusedSmem::make(G, S, D, U, BC, KS);
@@ -204,6 +205,7 @@ bool grid_feasible(const PlanRequest& q, int C, int NT, int KT, const DeviceLimi
   const int BC = 8 * NT;
   const int groups = q.N * ((q.B + BC - 1) / BC);
   if (groups * C > lim.sms) return false;
+  if (!q.bwd && (q.B < BC ? q.B : BC) * U > FUSED_PPT * warps * 32) return false;  // pairs in registers
   const int regs = q.bwd ? 4 * KT + 4 * NT + 64 : 4 * G * KT + 4 * G * NT + 48;
   if (regs > lim.regs_per_thread) return false;
   const size_t smem = q.bwd ? GridBwdSmem::make(G, S, K, D, U, BC, KS).total

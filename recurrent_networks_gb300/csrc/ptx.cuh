@@ -148,6 +148,21 @@ __device__ __forceinline__ void st_async_16(uint32_t raddr, uint4 v, uint32_t rb
       : "memory");
 }
 
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a
+// shared::cluster address, completing `bytes` transactions on the mbarrier at
+// shared::cluster address `rbar` in the destination CTA.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t rdst, uint32_t src, uint32_t bytes, uint32_t rbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(rdst),
+      "r"(src), "r"(bytes), "r"(rbar)
+      : "memory");
+}
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (bulk copy / TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---- TMA ----------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int c0, int c1, int c2, int c3, int c4) {
