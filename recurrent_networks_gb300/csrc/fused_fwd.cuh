@@ -100,9 +100,11 @@ __global__ void __launch_bounds__(256, 1)
       bsr[k][g] = own ? __bfloat162float(bias[((size_t)g * N + n) * D + u0 + u]) : 0.0f;
   }
 
-  // resident R fragments: A[m = unit j][k = input i] = R[g, n, i, j]
+  // resident R fragments: A[m = unit j][k = input i] = R[g, n, i, j]. Warps
+  // past the (U/16) * KS that the product needs only join the cell update.
+  const bool mma_warp = warp < (U / 16) * KS;
   uint32_t afr[G][KT][4];
-  {
+  if (mma_warp) {
     const int jr = u0 + mg * 16 + (lane >> 2);
 #pragma unroll
     for (int g = 0; g < G; ++g)
@@ -186,6 +188,7 @@ __global__ void __launch_bounds__(256, 1)
     }
 
     // rec^T = R_slice^T h_{t-1}: this warp's G m-tiles x KT k-tiles
+    if (mma_warp) {
     float acc[G][NT][4];
 #pragma unroll
     for (int g = 0; g < G; ++g)
@@ -231,6 +234,7 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
     }
+    }  // mma_warp
     RNN_TRACE(2)
     __syncthreads();
     RNN_TRACE(3)

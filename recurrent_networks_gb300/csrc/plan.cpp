@@ -27,6 +27,15 @@ static const int kClusterSizes[] = {1, 2, 3, 4, 6, 8, 12, 16};
 static const int kNT[] = {1, 2};
 static const int kKT[] = {2, 3, 4};
 
+// Warps of a forward kernel: the (U/16) * KS that the product needs, or more
+// when the cell update needs them (each thread carries at most FUSED_PPT
+// (batch row, unit) pairs in registers).
+static int fwd_warps(int U, int KS, int nb) {
+  const int mma = (U / 16) * KS;
+  const int cell = (nb * U + FUSED_PPT * 32 - 1) / (FUSED_PPT * 32);
+  return mma > cell ? mma : cell;
+}
+
 bool fused_fwd_feasible(const PlanRequest& q, int C, int NT, int KT, const DeviceLimits& lim, Plan* out) {
   const int G = gates_of(q.fn), S = states_of(q.fn), D = q.D;
   if (q.dtype != RNN_BF16) return false;
@@ -35,10 +44,9 @@ bool fused_fwd_feasible(const PlanRequest& q, int C, int NT, int KT, const Devic
   if (U % 16) return false;
   if (D % 16 || (D / 16) % KT) return false;
   const int KS = (D / 16) / KT;
-  const int warps = (U / 16) * KS;
-  if (warps < 1 || warps > lim.max_warps) return false;
   const int BC = 8 * NT;
-  if ((q.B < BC ? q.B : BC) * U > FUSED_PPT * warps * 32) return false;  // pairs held in registers
+  const int warps = fwd_warps(U, KS, q.B < BC ? q.B : BC);
+  if (warps < 1 || warps > lim.max_warps) return false;
   const int regs = 4 * G * KT + 4 * G * NT + 2 * NT + 48;
   if (regs > lim.regs_per_thread) return false;
   const FusedSmem L = FusedSmem::make(G, S, D, U, BC, KS);
@@ -200,12 +208,11 @@ bool grid_feasible(const PlanRequest& q, int C, int NT, int KT, const DeviceLimi
   const int klen = q.bwd ? G * D : D;
   if ((klen / 16) % KT) return false;
   const int KS = (klen / 16) / KT;
-  const int warps = (U / 16) * KS;
-  if (warps < 1 || warps > lim.max_warps) return false;
   const int BC = 8 * NT;
+  const int warps = q.bwd ? (U / 16) * KS : fwd_warps(U, KS, q.B < BC ? q.B : BC);
+  if (warps < 1 || warps > lim.max_warps) return false;
   const int groups = q.N * ((q.B + BC - 1) / BC);
   if (groups * C > lim.sms) return false;
-  if (!q.bwd && (q.B < BC ? q.B : BC) * U > FUSED_PPT * warps * 32) return false;  // pairs in registers
   const int regs = q.bwd ? 4 * KT + 4 * NT + 64 : 4 * G * KT + 4 * G * NT + 48;
   if (regs > lim.regs_per_thread) return false;
   const size_t smem = q.bwd ? GridBwdSmem::make(G, S, K, D, U, BC, KS).total

@@ -17,6 +17,17 @@ DTYPES = [torch.float32, torch.bfloat16]
 SMALL = [(3, 37, 2, 48), (1, 5, 1, 16), (9, 20, 3, 64)]
 
 
+def assert_states_close(a, b, tol=2e-2):
+    """Two bf16 paths with the same arithmetic: h within tol, the other states
+    within tol relative to max(1, |x|) (one bf16 ulp of a c of 8 is 0.03)."""
+    a, b = a.float(), b.float()
+    dh = (a[0] - b[0]).abs().max().item()
+    assert dh <= tol, dh
+    if a.shape[0] > 1:
+        rel = ((a[1:] - b[1:]).abs() / b[1:].abs().clamp_min(1.0)).max().item()
+        assert rel <= tol, rel
+
+
 def _inputs(fn, shape, dtype, seed):
     B, T, N, D = shape
     return make_inputs(fn, B, T, N, D, dtype, seed=seed, device="cuda")
@@ -138,8 +149,7 @@ def test_fused_matches_simt_forward_closely(monkeypatch):
     inp = _inputs("lstm", (6, 30, 2, 128), torch.bfloat16, seed=42)
     st_f, _, _ = run_fwd("lstm", inp, "fused", want_tape=False)
     st_s, _, _ = run_fwd("lstm", inp, "simt", want_tape=False)
-    diff = (st_f.float() - st_s.float()).abs().max().item()
-    assert diff <= 2e-2, diff
+    assert_states_close(st_f, st_s)
 
 
 BWD_CASES = [
@@ -211,5 +221,4 @@ def test_grid_and_cluster_forward_agree(monkeypatch):
     inp = _inputs("lstm", (8, 40, 2, 256), torch.bfloat16, seed=77)
     st_g, _, _ = run_fwd("lstm", inp, "grid", want_tape=False)
     st_f, _, _ = run_fwd("lstm", inp, "fused", want_tape=False)
-    diff = (st_g.float() - st_f.float()).abs().max().item()
-    assert diff <= 2e-2, diff
+    assert_states_close(st_g, st_f)
