@@ -28,7 +28,7 @@ namespace rnn {
 // GRIDX = true is the grid variant for R too large for one cluster: C CTAs of a
 // cooperative launch share a head and batch group, and h_t goes through L2 (a
 // bf16 exchange buffer plus a per-group step counter) instead of DSMEM.
-template <int FN, int NT, int KT, bool GRIDX>
+template <int FN, int NT, int KT, bool ALLG, bool GRIDX>
 __global__ void __launch_bounds__(256, 1)
     fused_fwd_kernel(const __grid_constant__ CUtensorMap wxmap, FusedArgs a) {
   constexpr int G = FnInfo<FN>::G, S = FnInfo<FN>::S, P = FnInfo<FN>::P, K = P + S;
@@ -44,7 +44,13 @@ __global__ void __launch_bounds__(256, 1)
   const int u0 = (int)rank * U;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int mg = warp / KS, ks = warp - mg * KS;
+  // warp -> (16-unit group mg, gate group gq of GW gates, K slice ks): GW
+  // 16 x (8 NT) tiles over KT k-tiles; the KS partial tiles are summed in the
+  // cell update
+  constexpr int GW = ALLG ? G : 1, GQ = G / GW;
+  constexpr int CH = GW == 1 ? 2 : 1;  // accumulator chains per tile
+  const int mg = warp / (GQ * KS), wrem = warp - mg * (GQ * KS);
+  const int gq = wrem / KS, ks = wrem - gq * KS;
 
   extern __shared__ __align__(128) unsigned char smem[];
   const FusedSmem L = FusedSmem::make(G, S, D, U, BC, KS);
@@ -102,23 +108,24 @@ __global__ void __launch_bounds__(256, 1)
 
   // resident R fragments: A[m = unit j][k = input i] = R[g, n, i, j]. Warps
   // past the (U/16) * KS that the product needs only join the cell update.
-  const bool mma_warp = warp < (U / 16) * KS;
-  uint32_t afr[G][KT][4];
+  const bool mma_warp = warp < (U / 16) * GQ * KS;
+  uint32_t afr[GW][KT][4];
   if (mma_warp) {
     const int jr = u0 + mg * 16 + (lane >> 2);
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+    for (int gi = 0; gi < GW; ++gi) {
+      const __nv_bfloat16* Rg = R + (size_t)((gq * GW + gi) * N + n) * D * D;
 #pragma unroll
       for (int kt = 0; kt < KT; ++kt) {
         const int k0 = (ks * KT + kt) * 16 + 2 * (lane & 3);
-        const __nv_bfloat16* Rg = R + (size_t)(g * N + n) * D * D;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int j = jr + ((q & 1) ? 8 : 0);
           const int k = k0 + ((q & 2) ? 8 : 0);
-          afr[g][kt][q] = pack_bf16(Rg[(size_t)k * D + j], Rg[(size_t)(k + 1) * D + j]);
+          afr[gi][kt][q] = pack_bf16(Rg[(size_t)k * D + j], Rg[(size_t)(k + 1) * D + j]);
         }
       }
+    }
   }
   __syncthreads();
   if constexpr (!GRIDX) cluster_sync_all();  // every CTA's barriers are initialised before any peer signals them
@@ -187,15 +194,18 @@ __global__ void __launch_bounds__(256, 1)
       tma_load_5d(smem_u32(wxs + s * wx_stage_elems), &wxmap, wx_bar0 + 8 * s, u0, n, 0, ts, b0);
     }
 
-    // rec^T = R_slice^T h_{t-1}: this warp's G m-tiles x KT k-tiles
+    // rec^T = R_slice^T h_{t-1}: this warp's gate tile over KT k-tiles, in
+    // two accumulator chains (even / odd k-tiles) to halve the MMA latency
     if (mma_warp) {
-    float acc[G][NT][4];
+    float acc[GW][CH][NT][4];
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+    for (int gi = 0; gi < GW; ++gi)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+      for (int c2 = 0; c2 < CH; ++c2)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[g][nt][q] = 0.0f;
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[gi][c2][nt][q] = 0.0f;
     const uint32_t hb = smem_u32(hbuf + p * HB);
 #pragma unroll
     for (int kt = 0; kt < KT; ++kt) {
@@ -215,22 +225,26 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
 #pragma unroll
-      for (int g = 0; g < G; ++g)
+      for (int gi = 0; gi < GW; ++gi)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[g][nt], afr[g][kt], bf[nt][0], bf[nt][1]);
+        for (int nt = 0; nt < NT; ++nt)
+          mma_bf16_16816(acc[gi][kt % CH][nt], afr[gi][kt], bf[nt][0], bf[nt][1]);
     }
     {
       const int r = lane >> 2, bc = 2 * (lane & 3);
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float* rp = red + (size_t)((mg * KS + ks) * G + g) * BC * FUSED_RED_STRIDE;
+      for (int gi = 0; gi < GW; ++gi) {
+        float* rp = red + (size_t)((mg * KS + ks) * G + gq * GW + gi) * BC * FUSED_RED_STRIDE;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
+          float v[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) v[q] = CH == 2 ? acc[gi][0][nt][q] + acc[gi][CH - 1][nt][q] : acc[gi][0][nt][q];
           const int b = nt * 8 + bc;
-          rp[b * FUSED_RED_STRIDE + r] = acc[g][nt][0];
-          rp[(b + 1) * FUSED_RED_STRIDE + r] = acc[g][nt][1];
-          rp[b * FUSED_RED_STRIDE + r + 8] = acc[g][nt][2];
-          rp[(b + 1) * FUSED_RED_STRIDE + r + 8] = acc[g][nt][3];
+          rp[b * FUSED_RED_STRIDE + r] = v[0];
+          rp[(b + 1) * FUSED_RED_STRIDE + r] = v[1];
+          rp[b * FUSED_RED_STRIDE + r + 8] = v[2];
+          rp[(b + 1) * FUSED_RED_STRIDE + r + 8] = v[3];
         }
       }
     }
@@ -332,13 +346,18 @@ template <int FN, bool GRIDX>
 cudaError_t fwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream_t st) {
   constexpr int G = FnInfo<FN>::G;
   void (*k)(const CUtensorMap, FusedArgs) = nullptr;
-#define RNN_FUSED_PICK(NT_, KT_) \
-  if (sh.NT == NT_ && sh.KT == KT_) k = fused_fwd_kernel<FN, NT_, KT_, GRIDX>;
+#define RNN_FUSED_PICK(NT_, KT_, AG_) \
+  if (sh.NT == NT_ && sh.KT == KT_ && sh.allg == AG_) k = fused_fwd_kernel<FN, NT_, KT_, AG_, GRIDX>;
   if constexpr (GRIDX) {
-    RNN_FUSED_PICK(1, 4) RNN_FUSED_PICK(1, 8) RNN_FUSED_PICK(2, 4) RNN_FUSED_PICK(2, 8)
+    RNN_FUSED_PICK(1, 8, false) RNN_FUSED_PICK(1, 16, false) RNN_FUSED_PICK(1, 32, false)
+    RNN_FUSED_PICK(2, 8, false) RNN_FUSED_PICK(2, 16, false) RNN_FUSED_PICK(2, 32, false)
   } else {
-    RNN_FUSED_PICK(1, 2) RNN_FUSED_PICK(1, 3) RNN_FUSED_PICK(1, 4)
-    RNN_FUSED_PICK(2, 2) RNN_FUSED_PICK(2, 3) RNN_FUSED_PICK(2, 4)
+    // one gate per warp (long K per warp, few partial sums) ...
+    RNN_FUSED_PICK(1, 4, false) RNN_FUSED_PICK(1, 6, false) RNN_FUSED_PICK(1, 8, false)
+    RNN_FUSED_PICK(1, 12, false) RNN_FUSED_PICK(1, 16, false)
+    // ... or all G gates per warp (wide slices, short K per warp)
+    RNN_FUSED_PICK(1, 2, true) RNN_FUSED_PICK(1, 3, true) RNN_FUSED_PICK(1, 4, true)
+    RNN_FUSED_PICK(2, 2, true) RNN_FUSED_PICK(2, 3, true) RNN_FUSED_PICK(2, 4, true)
   }
 #undef RNN_FUSED_PICK
   if (!k) return cudaErrorInvalidValue;

@@ -25,6 +25,7 @@ struct FusedShape {
   int KT = 0;     // k-tiles of 16 per warp
   int KS = 0;     // warps splitting K for one 16-row group
   int MT = 0;     // backward: m-tiles (16 rows of dh) per warp
+  bool allg = false;  // forward: a warp holds all G gate tiles (else one gate)
   int warps = 0;  // warps per CTA
   size_t smem = 0;
 };

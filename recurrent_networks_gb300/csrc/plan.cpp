@@ -1,15 +1,7 @@
-// Kernel planner (see plan.h).
-//
-// Forward cluster kernel, candidate point (C, NT, KT):
-//   divisibility   D = C * U,  U = 16 * m  (16-unit row groups per gate),
-//                  D / 16 = KS * KT  (K split over KS warps of KT k-tiles);
-//   inequalities   1 <= warps = (U / 16) * KS <= 8 (256 threads, 1 CTA/SM),
-//                  C <= 16 (non-portable cluster limit),
-//                  shared memory (FusedSmem) <= 227 KB,
-//                  registers: 4 G KT (resident R) + 4 G NT (accumulators)
-//                             + 2 NT (h fragments) + 48 (the rest) <= 255;
-//   objective      modelled step latency (cycles), smallest wins; ties go to
-//                  fewer CTAs.
+// Kernel planner (see plan.h): for every kernel family, enumerate the
+// instantiated tile parameters, keep the points that satisfy the divisibility,
+// warp, register, shared-memory and cluster constraints, and pick the one with
+// the smallest modelled step latency (ties go to fewer CTAs).
 #include "plan.h"
 
 #include <stdio.h>
@@ -25,18 +17,27 @@ static int states_of(int fn) { return fn == 0 ? 2 : fn == 1 ? 1 : fn == 2 ? 1 : 
 
 static const int kClusterSizes[] = {1, 2, 3, 4, 6, 8, 12, 16};
 static const int kNT[] = {1, 2};
-static const int kKT[] = {2, 3, 4};
+// instantiated k-tiles per warp of the forward cluster kernel: a warp holds
+// all G gate tiles over a short K (allg) or one gate tile over a long K
+static const int kKTAllG[] = {2, 3, 4};
+static const int kKTOneG[] = {4, 6, 8, 12, 16};
 
-// Warps of a forward kernel: the (U/16) * KS that the product needs, or more
-// when the cell update needs them (each thread carries at most FUSED_PPT
-// (batch row, unit) pairs in registers).
-static int fwd_warps(int U, int KS, int nb) {
-  const int mma = (U / 16) * KS;
+// Warps of a forward kernel: the (U/16) * (G/GW) * KS that the product needs,
+// or more when the cell update needs them (each thread carries at most
+// FUSED_PPT (batch row, unit) pairs in registers).
+static int fwd_warps(int U, int GQ, int KS, int nb) {
+  const int mma = (U / 16) * GQ * KS;
   const int cell = (nb * U + FUSED_PPT * 32 - 1) / (FUSED_PPT * 32);
   return mma > cell ? mma : cell;
 }
 
-bool fused_fwd_feasible(const PlanRequest& q, int C, int NT, int KT, const DeviceLimits& lim, Plan* out) {
+// Forward cluster kernel, candidate point (C, NT, KT, allg):
+//   divisibility   D = C U, U = 16 m;  D / 16 = KS KT;
+//   inequalities   1 <= warps <= 8, C <= 16, shared memory <= 227 KB,
+//                  registers 4 GW KT (R) + 4 GW CH NT (accumulators) + 80 <= 255,
+//                  with GW = G (allg) or 1, CH = 2 chains when GW = 1.
+bool fused_fwd_feasible(const PlanRequest& q, int C, int NT, int KT, bool allg, const DeviceLimits& lim,
+                        Plan* out) {
   const int G = gates_of(q.fn), S = states_of(q.fn), D = q.D;
   if (q.dtype != RNN_BF16) return false;
   if (C < 1 || C > lim.max_cluster || D % C) return false;
@@ -44,27 +45,28 @@ bool fused_fwd_feasible(const PlanRequest& q, int C, int NT, int KT, const Devic
   if (U % 16) return false;
   if (D % 16 || (D / 16) % KT) return false;
   const int KS = (D / 16) / KT;
+  if (KS > FUSED_MAX_KS) return false;
+  const int GW = allg ? G : 1, GQ = G / GW, CH = GW == 1 ? 2 : 1;
   const int BC = 8 * NT;
-  const int warps = fwd_warps(U, KS, q.B < BC ? q.B : BC);
+  const int nb = q.B < BC ? q.B : BC;
+  const int warps = fwd_warps(U, GQ, KS, nb);
   if (warps < 1 || warps > lim.max_warps) return false;
-  const int regs = 4 * G * KT + 4 * G * NT + 2 * NT + 48;
+  const int regs = 4 * GW * KT + 4 * GW * CH * NT + 80;
   if (regs > lim.regs_per_thread) return false;
   const FusedSmem L = FusedSmem::make(G, S, D, U, BC, KS);
   if (L.total > lim.smem_per_cta) return false;
   const int groups = q.N * ((q.B + BC - 1) / BC);
   const int threads = warps * 32;
-  // latency model of one step (cycles): fixed wait/barrier/DSMEM cost, the
-  // warp's dependent MMA chain, the K-split reduction, the cell update per
-  // pair, the st.async issue, and waves when the grid exceeds the SMs.
-  const int nb = q.B < BC ? q.B : BC;
-  const double pairs = (double)nb * U / threads;
-  const double mma = (double)G * KT * NT;
-  const double sends = (double)nb * (U / 8) * C / threads;
-  double cyc = 900.0 + 18.0 * mma + 6.0 * KS * G * (pairs < 1 ? 1 : pairs) +
-               140.0 * (pairs < 1 ? 1 : pairs) + 12.0 * sends + (C > 1 ? 150.0 : 0.0);
+  // latency model of one step (cycles), calibrated on the phase trace: the
+  // exchange round trip, the warp's MMA issue and dependent chain, the
+  // shared-memory loads of the K-split partial sums (G KS per pair), the cell
+  // update, and waves when the grid exceeds the SMs.
+  double pairs = (double)nb * U / threads;
+  if (pairs < 1) pairs = 1;
+  double cyc = 900.0 + 10.0 * GW * KT * NT + 28.0 * KT / CH + 14.0 * G * KS * pairs + 250.0 * pairs +
+               (C > 1 ? 600.0 : 0.0);
   const int ctas = groups * C;
-  const int waves = (ctas + lim.sms - 1) / lim.sms;
-  cyc *= waves;
+  cyc *= (ctas + lim.sms - 1) / lim.sms;
   if (out) {
     *out = Plan{};
     out->path = RNN_PATH_FUSED;
@@ -73,10 +75,11 @@ bool fused_fwd_feasible(const PlanRequest& q, int C, int NT, int KT, const Devic
     out->fs.NT = NT;
     out->fs.KT = KT;
     out->fs.KS = KS;
+    out->fs.allg = allg;
     out->fs.warps = warps;
     out->fs.smem = L.total;
     out->groups = groups;
-    out->regs_R = 4 * G * KT;
+    out->regs_R = 4 * GW * KT;
     out->model_ns = cyc / 1.9;  // at ~1.9 GHz
   }
   return true;
@@ -94,18 +97,24 @@ static int fused_fwd_plan(const PlanRequest& q, Plan* best) {
   DeviceLimits lim;
   int found = 0;
   for (int C : kClusterSizes)
-    for (int NT : kNT)
-      for (int KT : kKT) {
-        Plan p;
-        if (!env_admits("RNN_PLAN_C", C) || !env_admits("RNN_PLAN_NT", NT) ||
-            !env_admits("RNN_PLAN_KT", KT))
-          continue;
-        if (!fused_fwd_feasible(q, C, NT, KT, lim, &p)) continue;
-        ++found;
-        const int ctas = p.groups * p.fs.C, bctas = best->groups * best->fs.C;
-        if (found == 1 || p.model_ns < best->model_ns - 1e-9 ||
-            (p.model_ns < best->model_ns + 1e-9 && ctas < bctas))
-          *best = p;
+    for (int ag = 0; ag < 2; ++ag)
+      for (int NT : kNT) {
+        if (!ag && NT != 1) continue;  // one-gate kernels are built for one n-tile
+        const int* kts = ag ? kKTAllG : kKTOneG;
+        const int nkt = ag ? 3 : 5;
+        for (int x = 0; x < nkt; ++x) {
+          const int KT = kts[x];
+          Plan p;
+          if (!env_admits("RNN_PLAN_C", C) || !env_admits("RNN_PLAN_NT", NT) ||
+              !env_admits("RNN_PLAN_KT", KT) || !env_admits("RNN_PLAN_ALLG", ag))
+            continue;
+          if (!fused_fwd_feasible(q, C, NT, KT, ag != 0, lim, &p)) continue;
+          ++found;
+          const int ctas = p.groups * p.fs.C, bctas = best->groups * best->fs.C;
+          if (found == 1 || p.model_ns < best->model_ns - 1e-9 ||
+              (p.model_ns < best->model_ns + 1e-9 && ctas < bctas))
+            *best = p;
+        }
       }
   best->candidates = found;
   return found ? RNN_OK : RNN_EUNSUPPORTED;
@@ -194,7 +203,7 @@ static int fused_plan(const PlanRequest& q, Plan* best) {
 //                  4 KT + 4 NT + 64) <= 255, shared memory <= 227 KB;
 //   KT takes the instantiated values (forward 4, 8; backward 8, 16, 24, 32).
 static const int kGridC[] = {8, 16, 32, 64, 128};
-static const int kGridFwdKT[] = {4, 8};
+static const int kGridFwdKT[] = {8, 16, 32};
 static const int kGridBwdKT[] = {8, 16, 24, 32};
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -209,11 +218,12 @@ bool grid_feasible(const PlanRequest& q, int C, int NT, int KT, const DeviceLimi
   if ((klen / 16) % KT) return false;
   const int KS = (klen / 16) / KT;
   const int BC = 8 * NT;
-  const int warps = q.bwd ? (U / 16) * KS : fwd_warps(U, KS, q.B < BC ? q.B : BC);
+  // forward: one gate tile per warp (G tiles per 16-unit group)
+  const int warps = q.bwd ? (U / 16) * KS : fwd_warps(U, G, KS, q.B < BC ? q.B : BC);
   if (warps < 1 || warps > lim.max_warps) return false;
   const int groups = q.N * ((q.B + BC - 1) / BC);
   if (groups * C > lim.sms) return false;
-  const int regs = q.bwd ? 4 * KT + 4 * NT + 64 : 4 * G * KT + 4 * G * NT + 48;
+  const int regs = q.bwd ? 4 * KT + 4 * NT + 64 : 4 * KT + 8 * NT + 80;
   if (regs > lim.regs_per_thread) return false;
   const size_t smem = q.bwd ? GridBwdSmem::make(G, S, K, D, U, BC, KS).total
                             : FusedSmem::make(G, S, D, U, BC, KS).total;
@@ -224,7 +234,7 @@ bool grid_feasible(const PlanRequest& q, int C, int NT, int KT, const DeviceLimi
   // step: counter round trip through L2, the gathered vector from L2
   // (~64 B/clk/SM), the warp's MMA chain, the K-split reduction and the cell
   const double gather = (double)nb * klen * 2 / 64.0;
-  double cyc = 2200.0 + gather + 18.0 * KT * (q.bwd ? 1 : G) * NT + 6.0 * KS * pairs + 150.0 * pairs;
+  double cyc = 2200.0 + gather + 18.0 * KT * NT + 6.0 * KS * (q.bwd ? 1 : G) * pairs + 150.0 * pairs;
   if (out) {
     *out = Plan{};
     out->path = RNN_PATH_GRID;
@@ -236,7 +246,7 @@ bool grid_feasible(const PlanRequest& q, int C, int NT, int KT, const DeviceLimi
     out->fs.warps = warps;
     out->fs.smem = smem;
     out->groups = groups;
-    out->regs_R = q.bwd ? 4 * KT : 4 * G * KT;
+    out->regs_R = 4 * KT;
     out->scratch_bytes = align256((size_t)2 * groups * BC * klen * 2) + align256((size_t)groups * 4);
     out->model_ns = cyc / 1.9;
   }
@@ -247,7 +257,7 @@ static int grid_plan(const PlanRequest& q, Plan* best) {
   DeviceLimits lim;
   int found = 0;
   const int* kts = q.bwd ? kGridBwdKT : kGridFwdKT;
-  const int nkt = q.bwd ? 4 : 2;
+  const int nkt = q.bwd ? 4 : 3;
   for (int C : kGridC)
     for (int NT : kNT)
       for (int x = 0; x < nkt; ++x) {

@@ -36,7 +36,8 @@ struct Plan {
 
 // The constraint check for one candidate point of the forward cluster kernel
 // (exposed for tests): returns true and fills *out when every constraint holds.
-bool fused_fwd_feasible(const PlanRequest& q, int C, int NT, int KT, const DeviceLimits& lim, Plan* out);
+bool fused_fwd_feasible(const PlanRequest& q, int C, int NT, int KT, bool allg, const DeviceLimits& lim,
+                        Plan* out);
 
 int plan_select(const PlanRequest& q, Plan* out);  // RNN_OK or RNN_EUNSUPPORTED
 void plan_describe(const Plan& p, int rc, char* buf, size_t len);
