@@ -48,7 +48,6 @@ __global__ void __launch_bounds__(256, 1)
   unsigned char* ring = smem + L.ring;
   float* recv = (float*)(smem + L.recv);  // [2][C][U][BC]
   __nv_bfloat16* drb = (__nv_bfloat16*)(smem + L.drb);  // [2][BC][KB]
-  float* ds = (float*)(smem + L.ds);    // [S][BC][U]
   float* s0s = (float*)(smem + L.s0);   // [S][BC][U]
   const uint32_t recv_bar0 = smem_u32(&bars[0]);
   const uint32_t ring_bar0 = smem_u32(&bars[2]);
@@ -78,8 +77,14 @@ __global__ void __launch_bounds__(256, 1)
     float v = 0.0f;
     if (b < nb && s0) v = __bfloat162float(s0[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u]);
     s0s[e] = v;
-    ds[e] = 0.0f;
   }
+  // carried state gradients of this thread's (batch row, unit) pairs
+  // e = tid + k * blockDim (k < FUSED_PPT), in registers for the whole scan
+  float dsr[FUSED_PPT][S];
+#pragma unroll
+  for (int k = 0; k < FUSED_PPT; ++k)
+#pragma unroll
+    for (int s = 0; s < S; ++s) dsr[k][s] = 0.0f;
   // resident R fragments: A[m = row i][k = (g, j)] = R[g, n, i, u0 + j]
   uint32_t afr[MT][KTM][4];
   {
@@ -167,7 +172,10 @@ __global__ void __launch_bounds__(256, 1)
     RNN_TRACE(2)
     const float* rv = recv + (size_t)(t & 1) * C * U * BC;
     __nv_bfloat16* drw = drb + (size_t)pb * BC * KB;
-    for (int e = tid; e < nb * U; e += nthr) {
+#pragma unroll
+    for (int kp = 0; kp < FUSED_PPT; ++kp) {
+      const int e = tid + kp * nthr;
+      if (e >= nb * U) break;
       const int b = e / U, u = e - b * U;
       float pre[P], sp[S], sn[S], dsn[S], dx[G], dr[G], dsp[S];
 #pragma unroll
@@ -176,7 +184,7 @@ __global__ void __launch_bounds__(256, 1)
       for (int s = 0; s < S; ++s) {
         sn[s] = tp[(b * K + P + s) * U + u];
         sp[s] = t > 0 ? tq[(b * K + P + s) * U + u] : s0s[(s * BC + b) * U + u];
-        float d = ds[(s * BC + b) * U + u];
+        float d = dsr[kp][s];
         if (has_dst) d += __bfloat162float(dstage[(s * BC + b) * U + u]);
         if (dlast && t == TT - 1) d += __bfloat162float(dlast[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u]);
         dsn[s] = d;
@@ -199,7 +207,7 @@ __global__ void __launch_bounds__(256, 1)
         drw[b * KB + g * U + u] = __float2bfloat16_rn(dr[g]);
       }
 #pragma unroll
-      for (int s = 0; s < S; ++s) ds[(s * BC + b) * U + u] = dsp[s];
+      for (int s = 0; s < S; ++s) dsr[kp][s] = dsp[s];
     }
     RNN_TRACE(3)
     __syncthreads();
@@ -274,17 +282,21 @@ __global__ void __launch_bounds__(256, 1)
     mbar_wait_bounded(recv_bar0 + 8 * bi, ph1, a.wait_limit_ns, a.status, failed);  // bi == 1
     const float* rv = recv + (size_t)bi * C * U * BC;
     __nv_bfloat16* ds0 = (__nv_bfloat16*)a.ds0;
-    if (ds0)
-      for (int e = tid; e < nb * U; e += nthr) {
+    if (ds0) {
+#pragma unroll
+      for (int kp = 0; kp < FUSED_PPT; ++kp) {
+        const int e = tid + kp * nthr;
+        if (e >= nb * U) break;
         const int b = e / U, u = e - b * U;
 #pragma unroll
         for (int s = 0; s < S; ++s) {
-          float v = ds[(s * BC + b) * U + u];
+          float v = dsr[kp][s];
           if (s == 0)
             for (int c = 0; c < C; ++c) v += rv[((size_t)c * U + u) * BC + b];
           ds0[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u] = __float2bfloat16_rn(v);
         }
       }
+    }
   }
   __syncthreads();
   cluster_sync_all();

@@ -76,7 +76,7 @@ struct FusedBwdSmem {
     m.ring = FusedSmem::take(off, FUSED_NS * m.ring_stage);
     m.recv = FusedSmem::take(off, (size_t)2 * C * U * BC * 4);
     m.drb = FusedSmem::take(off, (size_t)2 * BC * (G * U + 8) * 2);
-    m.ds = FusedSmem::take(off, (size_t)S * BC * U * 4);
+    m.ds = off;  // the carried gradients are held in registers
     m.s0 = FusedSmem::take(off, (size_t)S * BC * U * 4);
     m.total = off;
     return m;

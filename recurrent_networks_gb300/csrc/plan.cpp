@@ -140,6 +140,7 @@ bool fused_bwd_feasible(const PlanRequest& q, int C, int NT, int MT, const Devic
   const int warps = (D / 16) / MT;
   if (warps < 1 || warps > lim.max_warps) return false;
   const int BC = 8 * NT;
+  if ((q.B < BC ? q.B : BC) * U > FUSED_PPT * warps * 32) return false;  // carried pairs in registers
   const int regs = 32 * MT + 4 * MT * NT + 64;
   if (regs > lim.regs_per_thread) return false;
   const FusedBwdSmem L = FusedBwdSmem::make(G, S, K, U, BC, C);
