@@ -11,11 +11,12 @@
 //    M = G*U, N = batch, K = D, split over warps along M (16-unit groups) and K;
 //  - h_{t-1} (bf16, all D units) sits in shared memory; after the pointwise
 //    update every CTA pushes its U-slice of h_t into every peer's buffer with
-//    st.async, whose mbarrier transaction count is the step's only
-//    synchronisation (no cluster-wide barrier inside the time loop);
+//    one bulk copy (shared::cta -> shared::cluster) per peer, whose mbarrier
+//    transaction count is the step's only synchronisation (no cluster-wide
+//    barrier inside the time loop);
 //  - Wx[:, t] for the CTA's slice streams in through a TMA ring NS steps ahead;
 //  - the cell update runs in the epilogue with c, n, m carried in fp32 in
-//    shared memory; states and the backward's tape are written straight out.
+//    registers; states and the backward's tape are written straight out.
 #pragma once
 #include <cuda.h>
 
@@ -48,7 +49,8 @@ __global__ void __launch_bounds__(256, 1)
   // 16 x (8 NT) tiles over KT k-tiles; the KS partial tiles are summed in the
   // cell update
   constexpr int GW = ALLG ? G : 1, GQ = G / GW;
-  constexpr int CH = GW == 1 ? 2 : 1;  // accumulator chains per tile
+  // accumulator chains per tile (four where the registers allow)
+  constexpr int CH = GW == 1 ? ((KT >= 4 && KT * NT <= 32) ? 4 : (KT >= 2 ? 2 : 1)) : 1;
   const int mg = warp / (GQ * KS), wrem = warp - mg * (GQ * KS);
   const int gq = wrem / KS, ks = wrem - gq * KS;
 
@@ -141,16 +143,10 @@ __global__ void __launch_bounds__(256, 1)
 
   bool failed = false;
   uint32_t ph0 = 0, ph1 = 0;
-  // thread c < C sends this CTA's slice to CTA c with one bulk copy per step:
-  // cluster addresses of this CTA's block in c's two h buffers and c's barriers
-  uint32_t peer_h0 = 0u, peer_h1 = 0u, peer_bar0 = 0u, peer_bar1 = 0u;
-  if (!GRIDX && tid < C) {
-    const uint32_t peer = (uint32_t)tid;
-    peer_h0 = mapa_shared(smem_u32(hbuf + (size_t)rank * BC * UP), peer);
-    peer_h1 = mapa_shared(smem_u32(hbuf + HB + (size_t)rank * BC * UP), peer);
-    peer_bar0 = mapa_shared(full_bar0, peer);
-    peer_bar1 = mapa_shared(full_bar0 + 8, peer);
-  }
+  // lane 0 of warp w sends this CTA's slice to the peers rank + w, rank + w +
+  // warps, ... (mod C), one bulk copy each: the copies of a step are issued by
+  // all warps side by side rather than one after another by a single warp
+  const int nwarps = nthr >> 5;
 
   const bool tracer = a.trace && blockIdx.x == 0 && tid == 0;
 #define RNN_TRACE(k)                                                                    \
@@ -182,6 +178,11 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
     RNN_TRACE(1)
+    const int ws = t % FUSED_NS;
+    // Wx[:, t] (loaded NS - 1 steps ahead): one thread observes the TMA
+    // completion; the barrier after the product orders it for every thread
+    if (tid == nthr - 1)
+      mbar_wait_bounded<false>(wx_bar0 + 8 * ws, (t / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
     if (t == a.inject_step && blockIdx.x == 0) {
       // injected fault: a wait that nothing ends runs out and records
       // STATUS_TIMEOUT; the exchange protocol itself is left untouched
@@ -195,7 +196,8 @@ __global__ void __launch_bounds__(256, 1)
     }
 
     // rec^T = R_slice^T h_{t-1}: this warp's gate tile over KT k-tiles, in
-    // two accumulator chains (even / odd k-tiles) to halve the MMA latency
+    // CH accumulator chains (k-tile kt feeds chain kt % CH) to shorten the
+    // dependent MMA sequence
     if (mma_warp) {
     float acc[GW][CH][NT][4];
 #pragma unroll
@@ -239,7 +241,14 @@ __global__ void __launch_bounds__(256, 1)
         for (int nt = 0; nt < NT; ++nt) {
           float v[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) v[q] = CH == 2 ? acc[gi][0][nt][q] + acc[gi][CH - 1][nt][q] : acc[gi][0][nt][q];
+          for (int q = 0; q < 4; ++q) {
+            if constexpr (CH == 4)
+              v[q] = (acc[gi][0][nt][q] + acc[gi][1][nt][q]) + (acc[gi][2][nt][q] + acc[gi][3][nt][q]);
+            else if constexpr (CH == 2)
+              v[q] = acc[gi][0][nt][q] + acc[gi][1][nt][q];
+            else
+              v[q] = acc[gi][0][nt][q];
+          }
           const int b = nt * 8 + bc;
           rp[b * FUSED_RED_STRIDE + r] = v[0];
           rp[(b + 1) * FUSED_RED_STRIDE + r] = v[1];
@@ -254,11 +263,9 @@ __global__ void __launch_bounds__(256, 1)
     RNN_TRACE(3)
 
     // ---- epilogue: gate assembly and cell update, one (batch row, unit) pair per thread
-    const int ws = t % FUSED_NS;
     const __nv_bfloat16* wxt = wxs + ws * wx_stage_elems;
-    if (tid < nb * U)
-      mbar_wait_bounded<false>(wx_bar0 + 8 * ws, (t / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
     RNN_TRACE(4)
+    float prk[FUSED_PPT][P];  // pre-activations kept for the tape, written after the exchange
 #pragma unroll
     for (int kp = 0; kp < FUSED_PPT; ++kp) {
       const int e = tid + kp * nthr;
@@ -282,25 +289,17 @@ __global__ void __launch_bounds__(256, 1)
         x[g] = __bfloat162float(wxt[(b * G + g) * U + u]);
       }
       cell_fwd<FN, true>(x, rc, csr[kp], sn, pre);
-      const int bg = b0 + b, j = u0 + u;
+      const int j = u0 + u;
 #pragma unroll
-      for (int s = 0; s < S; ++s) {
-        csr[kp][s] = sn[s];
-        if (states) states[(((size_t)s * B + bg) * TT + t) * N * D + (size_t)n * D + j] = __float2bfloat16_rn(sn[s]);
-      }
+      for (int s = 0; s < S; ++s) csr[kp][s] = sn[s];
+#pragma unroll
+      for (int k2 = 0; k2 < P; ++k2) prk[kp][k2] = pre[k2];
       if constexpr (GRIDX) {
         if (t + 1 < TT)
           ((__nv_bfloat16*)a.hx)[((size_t)((p ^ 1) * (gridDim.x / C) + grp) * BC + b) * D + j] =
               __float2bfloat16_rn(sn[0]);
       } else {
         stage[(p * BC + b) * UP + u] = __float2bfloat16_rn(sn[0]);
-      }
-      if (a.tape) {
-        float* tp = a.tape + (((size_t)t * B + bg) * N + n) * K * D + j;
-#pragma unroll
-        for (int k2 = 0; k2 < P; ++k2) tp[k2 * D] = pre[k2];
-#pragma unroll
-        for (int s = 0; s < S; ++s) tp[(P + s) * D] = sn[s];
       }
     }
     RNN_TRACE(5)
@@ -314,11 +313,36 @@ __global__ void __launch_bounds__(256, 1)
     // have landed (so their reads of stage[p] are over).
     if (GRIDX) {
       if (t + 1 < TT && tid == 0) counter_publish(a.counters + grp);
-    } else if (t + 1 < TT && tid < C) {
-      bulk_copy_to_peer(p ? peer_h0 : peer_h1, smem_u32(stage + p * BC * UP), slice_bytes,
-                        p ? peer_bar0 : peer_bar1);
+    } else if (t + 1 < TT && lane == 0) {
+      const uint32_t dst = smem_u32(hbuf + (p ^ 1) * HB + (size_t)rank * BC * UP);
+      const uint32_t bar = full_bar0 + 8 * (p ^ 1);
+      const uint32_t src = smem_u32(stage + p * BC * UP);
+      for (int c = warp; c < C; c += nwarps) {
+        int peer = (int)rank + c;
+        if (peer >= C) peer -= C;
+        bulk_copy_to_peer(mapa_shared(dst, (uint32_t)peer), src, slice_bytes, mapa_shared(bar, (uint32_t)peer));
+      }
     }
     RNN_TRACE(7)
+    // states and tape of this step, off the exchange's critical path
+#pragma unroll
+    for (int kp = 0; kp < FUSED_PPT; ++kp) {
+      const int e = tid + kp * nthr;
+      if (e >= nb * U) break;
+      const int b = e / U, u = e - b * U, bg = b0 + b, j = u0 + u;
+      if (states) {
+#pragma unroll
+        for (int s = 0; s < S; ++s)
+          states[(((size_t)s * B + bg) * TT + t) * N * D + (size_t)n * D + j] = __float2bfloat16_rn(csr[kp][s]);
+      }
+      if (a.tape) {
+        float* tp = a.tape + (((size_t)t * B + bg) * N + n) * K * D + j;
+#pragma unroll
+        for (int k2 = 0; k2 < P; ++k2) tp[k2 * D] = prk[kp][k2];
+#pragma unroll
+        for (int s = 0; s < S; ++s) tp[(P + s) * D] = csr[kp][s];
+      }
+    }
   }
 #undef RNN_TRACE
 

@@ -71,24 +71,34 @@ __global__ void __launch_bounds__(256) wgrad_simt_kernel(WgradArgs a) {
   }
 }
 
-// db: block = 32 units x 8 k-slices, reduced through shared memory.
+// db: block = 32 units x 32 k-slices (strided rows, several loads in flight
+// per thread), reduced through shared memory in a fixed order.
+constexpr int BG_KS = 32;
 template <typename T>
-__global__ void __launch_bounds__(256) bgrad_kernel(WgradArgs a) {
-  __shared__ float part[8][33];
+__global__ void __launch_bounds__(32 * BG_KS) bgrad_kernel(WgradArgs a) {
+  __shared__ float part[BG_KS][33];
   const int lane = threadIdx.x % 32, ks = threadIdx.x / 32;
   const int j = blockIdx.x * 32 + lane;
   const int gn = blockIdx.y, g = gn / a.N, n = gn - g * a.N;
   const int K = a.B * a.T, D = a.D;
   const T* dr = (const T*)a.dr;
-  float s = 0.0f;
-  if (j < D)
-    for (int k = ks; k < K; k += 8) s += ldf(dr + ((size_t)k * a.G + g) * a.N * D + (size_t)n * D + j);
-  part[ks][lane] = s;
+  float s0 = 0.0f, s1 = 0.0f;
+  if (j < D) {
+    const size_t stride = (size_t)a.G * a.N * D;
+    const T* p = dr + (size_t)g * a.N * D + (size_t)n * D + j;
+    int k = ks;
+    for (; k + BG_KS < K; k += 2 * BG_KS) {
+      s0 += ldf(p + (size_t)k * stride);
+      s1 += ldf(p + (size_t)(k + BG_KS) * stride);
+    }
+    if (k < K) s0 += ldf(p + (size_t)k * stride);
+  }
+  part[ks][lane] = s0 + s1;
   __syncthreads();
   if (ks == 0 && j < D) {
     float tot = 0.0f;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) tot += part[q][lane];
+#pragma unroll 8
+    for (int q = 0; q < BG_KS; ++q) tot += part[q][lane];
     stf((T*)a.db + ((size_t)g * a.N + n) * D + j, tot);
   }
 }
@@ -103,7 +113,7 @@ static cudaError_t wgrad_launch(const WgradArgs& a, cudaStream_t st) {
   }
   if (a.db) {
     dim3 grid((a.D + 31) / 32, GN);
-    bgrad_kernel<T><<<grid, 256, 0, st>>>(a);
+    bgrad_kernel<T><<<grid, 32 * BG_KS, 0, st>>>(a);
     note_launch();
   }
   return cudaGetLastError();
@@ -306,7 +316,7 @@ cudaError_t wgrad_run(int dtype, const WgradArgs& a, cudaStream_t st) {
   }
   if (a.db) {
     dim3 g2((a.D + 31) / 32, a.G * a.N);
-    bgrad_kernel<__nv_bfloat16><<<g2, 256, 0, st>>>(a);
+    bgrad_kernel<__nv_bfloat16><<<g2, 32 * BG_KS, 0, st>>>(a);
     note_launch();
   }
   return cudaGetLastError();

@@ -112,7 +112,7 @@ FUSED_CASES = [
     ("elman", 16, 33, 1, 128, dict(C=2)),
     ("elman", 7, 18, 2, 64, dict(C=2, KT=4)),
     ("slstm", 5, 29, 2, 96, dict(C=3, KT=3)),
-    ("slstm", 16, 23, 1, 192, dict(C=6, NT=2)),
+    ("slstm", 16, 23, 1, 192, dict(C=12, NT=2)),
     ("slstm", 4, 17, 1, 192, dict(C=12)),
 ]
 
@@ -160,10 +160,10 @@ BWD_CASES = [
     ("lstm", 8, 40, 3, 256, dict(C=8)),
     ("gru", 9, 20, 3, 48, dict(C=3)),
     ("gru", 16, 25, 2, 128, dict(C=4, NT=2)),
-    ("elman", 7, 18, 2, 64, dict(C=1)),
+    ("elman", 7, 18, 2, 64, dict(C=2)),
     ("elman", 16, 33, 1, 128, dict(C=2)),
     ("slstm", 5, 29, 2, 96, dict(C=3)),
-    ("slstm", 16, 23, 1, 192, dict(C=6, NT=2)),
+    ("slstm", 16, 23, 1, 192, dict(C=12, NT=2)),
     ("slstm", 4, 17, 1, 192, dict(C=12)),
 ]
 
