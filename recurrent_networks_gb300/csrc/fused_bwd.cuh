@@ -46,12 +46,18 @@ __global__ void __launch_bounds__(256, 1)
   const FusedBwdSmem L = FusedBwdSmem::make(G, S, K, U, BC, C);
   uint64_t* bars = (uint64_t*)(smem + L.bars);  // [0,1]: partials full; [2..]: ring
   unsigned char* ring = smem + L.ring;
-  float* recv = (float*)(smem + L.recv);  // [2][C][U][BC]
+  // [2][C][U][BC]; within a unit's row the 16-byte groups of batch columns are
+  // XOR-swizzled by the unit (column b is stored at b ^ 4 swz(u)), so that
+  // readers of one batch column across 16 consecutive units meet at most
+  // two-way bank conflicts while each sender's pair of lanes still fills
+  // whole aligned 32-byte sectors
+  float* recv = (float*)(smem + L.recv);
+  auto swz = [](int u) { return NT == 1 ? ((u >> 2) & 1) : ((u >> 1) & 3); };
   __nv_bfloat16* drb = (__nv_bfloat16*)(smem + L.drb);  // [2][BC][KB]
   float* s0s = (float*)(smem + L.s0);   // [S][BC][U]
   const uint32_t recv_bar0 = smem_u32(&bars[0]);
   const uint32_t ring_bar0 = smem_u32(&bars[2]);
-  const uint32_t rbytes = (uint32_t)C * U * BC * 4;
+  const uint32_t rbytes = (uint32_t)C * U * BC * 4;  // payload bytes (padding not sent)
   const bool has_dst = a.dstates != nullptr;
   const uint32_t stage_bytes = (uint32_t)(L.tape_bytes + (has_dst ? (size_t)S * BC * U * 2 : 0));
 
@@ -121,7 +127,7 @@ __global__ void __launch_bounds__(256, 1)
   if (tid == 0) {
     mbar_arrive_expect_tx(recv_bar0 + 8 * ((TT - 2) & 1), rbytes);
     if (TT >= 2) mbar_arrive_expect_tx(recv_bar0 + 8 * ((TT - 3) & 1), rbytes);
-    for (int k = 0; k < FUSED_NS - 1 && k < TT; ++k) issue_stage(k);
+    for (int k = 0; k < FUSED_NS && k < TT; ++k) issue_stage(k);
   }
 
   bool failed = false;
@@ -152,7 +158,6 @@ __global__ void __launch_bounds__(256, 1)
     const int t = TT - 1 - k;
     const int pb = t & 1;  // gradient-operand buffer of this step
     RNN_TRACE(0)
-    if (tid == 0 && k + FUSED_NS - 1 < TT) issue_stage(k + FUSED_NS - 1);
     if (t < TT - 1) {  // partial sums for dh_t arrived
       const int bi = t & 1;
       mbar_wait_bounded(recv_bar0 + 8 * bi, bi ? ph1 : ph0, a.wait_limit_ns, a.status, failed);
@@ -164,7 +169,7 @@ __global__ void __launch_bounds__(256, 1)
     const float* tp = (const float*)(ring + (size_t)sc * L.ring_stage);
     const __nv_bfloat16* dstage = (const __nv_bfloat16*)(ring + (size_t)sc * L.ring_stage + L.dst_off);
     const float* tq = (const float*)(ring + (size_t)sn_ * L.ring_stage);
-    if (tid < nb * U) {
+    if (k == 0 && tid < nb * U) {  // later steps: waited for one step ahead, below
       mbar_wait_bounded<false>(ring_bar0 + 8 * sc, (k / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
       if (t > 0)
         mbar_wait_bounded<false>(ring_bar0 + 8 * sn_, ((k + 1) / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
@@ -191,8 +196,9 @@ __global__ void __launch_bounds__(256, 1)
       }
       if (t < TT - 1) {  // the C partial sums, loaded together
         float part[FUSED_MAX_C];
+        const int bs = b ^ (4 * swz(u));
 #pragma unroll
-        for (int c = 0; c < FUSED_MAX_C; ++c) part[c] = c < C ? rv[((size_t)c * U + u) * BC + b] : 0.0f;
+        for (int c = 0; c < FUSED_MAX_C; ++c) part[c] = c < C ? rv[((size_t)c * U + u) * BC + bs] : 0.0f;
         float acc = 0.0f;
 #pragma unroll
         for (int c = 0; c < FUSED_MAX_C; ++c) acc += part[c];
@@ -208,6 +214,16 @@ __global__ void __launch_bounds__(256, 1)
       }
 #pragma unroll
       for (int s = 0; s < S; ++s) dsr[kp][s] = dsp[s];
+    }
+    // one thread observes the TMA completion of the two stages the next step
+    // reads (loaded NS - 2 or more steps ago); the barrier below orders them
+    // for every thread
+    if (tid == nthr - 1 && k + 1 < TT) {
+      mbar_wait_bounded<false>(ring_bar0 + 8 * ((k + 1) % FUSED_NS), ((k + 1) / FUSED_NS) & 1, a.wait_limit_ns,
+                               a.status, failed);
+      if (k + 2 < TT)
+        mbar_wait_bounded<false>(ring_bar0 + 8 * ((k + 2) % FUSED_NS), ((k + 2) / FUSED_NS) & 1, a.wait_limit_ns,
+                                 a.status, failed);
     }
     RNN_TRACE(3)
     __syncthreads();
@@ -268,11 +284,14 @@ __global__ void __launch_bounds__(256, 1)
             out = make_uint4(__float_as_uint(ra), __float_as_uint(rb), __float_as_uint(v[2]), __float_as_uint(v[3]));
             bcol = nt * 8 + 2 * q4 - 2;
           }
-          const uint32_t off = (uint32_t)((send_row[mt] * BC + bcol) * 4);
+          const uint32_t off = (uint32_t)((send_row[mt] * BC + (bcol ^ (4 * swz(send_row[mt])))) * 4);
           st_async_16((bi ? send_base1[mt] : send_base0[mt]) + off, out, bi ? send_bar1[mt] : send_bar0[mt]);
         }
     }
     RNN_TRACE(6)
+    // tape and upstream gradients of step k + NS into the ring slot this
+    // step's derivative has finished reading
+    if (tid == nthr - 32 && k + FUSED_NS < TT) issue_stage(k + FUSED_NS);
   }
 #undef RNN_TRACE
 
@@ -292,7 +311,7 @@ __global__ void __launch_bounds__(256, 1)
         for (int s = 0; s < S; ++s) {
           float v = dsr[kp][s];
           if (s == 0)
-            for (int c = 0; c < C; ++c) v += rv[((size_t)c * U + u) * BC + b];
+            for (int c = 0; c < C; ++c) v += rv[((size_t)c * U + u) * BC + (b ^ (4 * swz(u)))];
           ds0[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u] = __float2bfloat16_rn(v);
         }
       }

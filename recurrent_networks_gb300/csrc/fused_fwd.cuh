@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(256, 1)
   if (tid == 0) {
     if (!GRIDX && TT > 1) mbar_arrive_expect_tx(full_bar0 + 8, hbytes);  // step 1
     if (!GRIDX && TT > 2) mbar_arrive_expect_tx(full_bar0, hbytes);      // step 2
-    for (int s = 0; s < FUSED_NS - 1 && s < TT; ++s) {
+    for (int s = 0; s < FUSED_NS && s < TT; ++s) {
       mbar_arrive_expect_tx(wx_bar0 + 8 * s, wxbytes);
       tma_load_5d(smem_u32(wxs + s * wx_stage_elems), &wxmap, wx_bar0 + 8 * s, u0, n, 0, s, b0);
     }
@@ -188,11 +188,6 @@ __global__ void __launch_bounds__(256, 1)
       // STATUS_TIMEOUT; the exchange protocol itself is left untouched
       bool inj_failed = false;
       mbar_wait_bounded<false>(full_bar0 + 8 * (2 + FUSED_NS), 0, a.inject_limit_ns, a.status, inj_failed);
-    }
-    if (tid == 0 && t + FUSED_NS - 1 < TT) {
-      const int ts = t + FUSED_NS - 1, s = ts % FUSED_NS;
-      mbar_arrive_expect_tx(wx_bar0 + 8 * s, wxbytes);
-      tma_load_5d(smem_u32(wxs + s * wx_stage_elems), &wxmap, wx_bar0 + 8 * s, u0, n, 0, ts, b0);
     }
 
     // rec^T = R_slice^T h_{t-1}: this warp's gate tile over KT k-tiles, in
@@ -324,6 +319,12 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
     RNN_TRACE(7)
+    // Wx[:, t + NS] into the ring slot this step's update has finished reading
+    if (tid == nthr - 32 && t + FUSED_NS < TT) {
+      const int ts = t + FUSED_NS;
+      mbar_arrive_expect_tx(wx_bar0 + 8 * ws, wxbytes);
+      tma_load_5d(smem_u32(wxs + ws * wx_stage_elems), &wxmap, wx_bar0 + 8 * ws, u0, n, 0, ts, b0);
+    }
     // states and tape of this step, off the exchange's critical path
 #pragma unroll
     for (int kp = 0; kp < FUSED_PPT; ++kp) {
