@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--function", default=None, help="override the workload's cell (workload 3: gru|elman)")
-    ap.add_argument("--path", default="auto", choices=["auto", "fused", "alternating", "simt"])
+    ap.add_argument("--path", default="auto", choices=["auto", "fused", "alternating", "simt", "grid"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()

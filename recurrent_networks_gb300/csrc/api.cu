@@ -96,6 +96,15 @@ static void grid_scratch(const rnn_dims_t* d, const Plan& plan, char* ws, bool b
   f->counters = (unsigned int*)(ws + 256 + align256(hx));
 }
 
+// Alternating path scratch inside the workspace: the bf16 ping-pong buffer,
+// then the fp32 carried values.
+static void alt_scratch(const rnn_dims_t* d, char* ws, bool bwd, AltArgs* a) {
+  const size_t per = (size_t)d->B * d->N * d->D;
+  const size_t x = bwd ? 2 * per * fn_gates(d->function) * 2 : 2 * per * 2;
+  a->xbuf = ws + 256;
+  a->cst = (float*)(ws + 256 + align256(x));
+}
+
 // Upper bound of every device-side wait.
 static unsigned long long g_wait_limit_ns = 2000000000ull;
 
@@ -153,6 +162,15 @@ static int run_forward(const rnn_dims_t* d, const Plan& plan, const void* Wx, co
       grid_scratch(d, plan, ws, false, &f);
       rc = cuda_status(cudaMemsetAsync(f.counters, 0, (size_t)plan.groups * sizeof(unsigned), st));
       if (rc == RNN_OK) rc = cuda_status(grid_fwd_run(d->function, plan.fs, f, st));
+      break;
+    }
+    case RNN_PATH_ALTERNATING: {
+      AltArgs g{};
+      g.B = d->B; g.T = d->T; g.N = d->N; g.D = d->D;
+      g.Wx = Wx; g.R = R; g.bias = b; g.s0 = s0;
+      g.states = states; g.last = last; g.tape = tape;
+      alt_scratch(d, ws, false, &g);
+      rc = cuda_status(alt_fwd_run(d->function, g, st));
       break;
     }
   }
@@ -294,6 +312,15 @@ int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
       grid_scratch(d, plan, ws, true, &f);
       rc = cuda_status(cudaMemsetAsync(f.counters, 0, (size_t)plan.groups * sizeof(unsigned), st));
       if (rc == RNN_OK) rc = cuda_status(grid_bwd_run(d->function, plan.fs, f, st));
+      break;
+    }
+    case RNN_PATH_ALTERNATING: {
+      AltArgs g{};
+      g.B = d->B; g.T = d->T; g.N = d->N; g.D = d->D;
+      g.R = R; g.s0 = states0; g.tape = (float*)tp;
+      g.dstates = dstates; g.dlast = dlast; g.dWx = dWx; g.dr = drbuf; g.ds0 = dstates0;
+      alt_scratch(d, ws, true, &g);
+      rc = cuda_status(alt_bwd_run(d->function, g, st));
       break;
     }
   }

@@ -79,6 +79,27 @@ struct FusedArgs {
   unsigned long long inject_limit_ns = 0;
 };
 
+// Arguments of the alternating path (one launch per step, replayed as a graph).
+struct AltArgs {
+  int B, T, N, D;
+  const void* Wx;
+  const void* R;
+  const void* bias;
+  const void* s0;
+  void* states;  // may be null
+  void* last;    // may be null
+  float* tape;   // fwd: may be null; bwd: in
+  const void* dstates;
+  const void* dlast;
+  void* dWx;
+  void* dr;
+  void* ds0;
+  void* xbuf;  // fwd: h ping-pong [2][B][N][D]; bwd: dr ping-pong [2][B][G][N][D] (bf16)
+  float* cst;  // fwd: carried states; bwd: carried state gradients [S][B][N][D] (fp32)
+};
+cudaError_t alt_fwd_run(int fn, const AltArgs& a, cudaStream_t st);
+cudaError_t alt_bwd_run(int fn, const AltArgs& a, cudaStream_t st);
+
 struct FusedShape;
 cudaError_t fused_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st);
 cudaError_t grid_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st);

@@ -274,6 +274,21 @@ static int grid_plan(const PlanRequest& q, Plan* best) {
   return found ? RNN_OK : RNN_EUNSUPPORTED;
 }
 
+// Alternating path: one kernel per step streams R from L2 / HBM; feasible for
+// bf16 whenever the unit tiles (16 units; 64 for Elman) divide D. The model is
+// the step's R bytes at an L2 rate of ~10 TB/s plus ~2 us of launch spacing.
+static int alt_plan(const PlanRequest& q, Plan* p) {
+  *p = Plan{};
+  if (q.dtype != RNN_BF16 || !alt_supported(q.fn, q.D)) return RNN_EUNSUPPORTED;
+  p->path = RNN_PATH_ALTERNATING;
+  p->fs.NT = q.B <= 16 ? 1 : 2;
+  p->groups = q.N * ((q.B + 16 * p->fs.NT - 1) / (16 * p->fs.NT));
+  p->scratch_bytes = alt_scratch_bytes(q.fn, q.B, q.N, q.D, q.bwd);
+  p->model_ns = 2000.0 + (double)gates_of(q.fn) * q.N * q.D * q.D * 2 / 1.0e4;
+  p->candidates = 1;
+  return RNN_OK;
+}
+
 static void simt_plan(const PlanRequest& q, Plan* p) {
   *p = Plan{};
   p->path = RNN_PATH_SIMT;
@@ -290,8 +305,9 @@ int plan_select(const PlanRequest& q, Plan* out) {
       return RNN_OK;
     case RNN_PATH_AUTO:
       // the cluster kernels when a feasible point exists (bf16), then the grid
-      // kernels (R too large for one cluster), else the plain path
-      if (fused_plan(q, &p) == RNN_OK || grid_plan(q, &p) == RNN_OK) {
+      // kernels (R too large for one cluster), then the alternating path (R
+      // streamed every step), else the plain path
+      if (fused_plan(q, &p) == RNN_OK || grid_plan(q, &p) == RNN_OK || alt_plan(q, &p) == RNN_OK) {
         *out = p;
         return RNN_OK;
       }
@@ -307,6 +323,17 @@ int plan_select(const PlanRequest& q, Plan* out) {
                "no grid plan for fn=%d dtype=%d D=%d B=%d N=%d%s (bf16 only; U = D/C multiple of 16, <= 8 "
                "warps, all CTAs resident)",
                q.fn, q.dtype, q.D, q.B, q.N, q.bwd ? " (backward)" : "");
+      *out = p;
+      return RNN_EUNSUPPORTED;
+    case RNN_PATH_ALTERNATING:
+      if (alt_plan(q, &p) == RNN_OK) {
+        *out = p;
+        return RNN_OK;
+      }
+      snprintf(p.why, sizeof(p.why),
+               "no alternating plan for fn=%d dtype=%d D=%d (bf16 only; D a multiple of the 16-unit tile, "
+               "64 for elman)",
+               q.fn, q.dtype, q.D);
       *out = p;
       return RNN_EUNSUPPORTED;
     case RNN_PATH_FUSED:

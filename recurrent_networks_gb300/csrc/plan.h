@@ -39,6 +39,11 @@ struct Plan {
 bool fused_fwd_feasible(const PlanRequest& q, int C, int NT, int KT, bool allg, const DeviceLimits& lim,
                         Plan* out);
 
+// Alternating path (csrc/alt.cu): whether the unit tiles divide D, and the
+// workspace its ping-pong and carried-state buffers take.
+int alt_supported(int fn, int D);
+size_t alt_scratch_bytes(int fn, int B, int N, int D, bool bwd);
+
 int plan_select(const PlanRequest& q, Plan* out);  // RNN_OK or RNN_EUNSUPPORTED
 void plan_describe(const Plan& p, int rc, char* buf, size_t len);
 

@@ -222,3 +222,74 @@ def test_grid_and_cluster_forward_agree(monkeypatch):
     st_g, _, _ = run_fwd("lstm", inp, "grid", want_tape=False)
     st_f, _, _ = run_fwd("lstm", inp, "fused", want_tape=False)
     assert_states_close(st_g, st_f)
+
+
+# ---------------------------------------------------------- alternating path
+ALT_CASES = [
+    ("lstm", 5, 13, 2, 64),
+    ("gru", 9, 11, 1, 48),
+    ("elman", 16, 9, 2, 128),
+    ("slstm", 20, 7, 1, 64),     # two m-tiles per batch tile
+    ("lstm", 3, 6, 1, 1024),
+    ("gru", 33, 4, 1, 256),      # two batch tiles, ragged
+]
+
+
+@pytest.mark.parametrize("case", ALT_CASES, ids=lambda c: "%s-B%dT%dN%dD%d" % c)
+def test_alternating_parity(case):
+    fn, B, T, N, D = case
+    inp = _inputs(fn, (B, T, N, D), torch.bfloat16, seed=1300 + B + T + D)
+    dims = _lib.make_dims(B, T, N, D, fn, torch.bfloat16, "alternating")
+    for bwd in (False, True):
+        rc, desc = _lib.rnn_plan_describe(dims, bwd)
+        assert rc == 0 and "path=alternating" in desc, desc
+    st, last, tape = run_fwd(fn, inp, "alternating")
+    ref_st, ref_last = oracle_fwd(fn, inp)
+    check_states(fn, torch.bfloat16, st, ref_st)
+    check_states(fn, torch.bfloat16, last, ref_last, "last")
+    dl = torch.randn(last.shape, generator=torch.Generator().manual_seed(6)).to(torch.bfloat16).cuda()
+    dWx, dR, db, ds0 = run_bwd(fn, inp, st, tape, "alternating", dlast=dl)
+    check_grads(fn, inp, (dWx, dR, db, ds0), dlast=dl)
+    # the tape is shared by every path: the plain backward on it agrees
+    sdWx, _, _, _ = run_bwd(fn, inp, st, tape, "simt", dlast=dl)
+    d1 = (dWx.float() - sdWx.float()).abs().max().item() / max(sdWx.float().abs().max().item(), 1e-30)
+    assert d1 <= 2e-2, d1
+
+
+def test_alternating_replays_its_graph():
+    """Calls with the same buffers replay the captured graph: identical results
+    for identical inputs, and new values written into the input buffers are
+    picked up (the graph holds pointers, not data)."""
+    fn, B, T, N, D = "lstm", 4, 10, 1, 128
+    inp = _inputs(fn, (B, T, N, D), torch.bfloat16, seed=1401)
+    S = _lib.rnn_num_states(fn)
+    dims = _lib.make_dims(B, T, N, D, fn, torch.bfloat16, "alternating")
+    states = torch.empty((S, B, T, N, D), dtype=torch.bfloat16, device="cuda")
+    last = torch.empty((S, B, 1, N, D), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(_lib.rnn_workspace_size(dims, _lib.WS_FWD), dtype=torch.uint8, device="cuda")
+    before = _lib.rnn_kernel_launches()
+    outs = []
+    for k in range(3):
+        if k == 2:
+            inp["Wx"].mul_(0.5)
+        _lib.rnn_fwd(dims, inp["Wx"], inp["R"], inp["b"], inp["states0"], states, last, None, ws)
+        _lib.rnn_check_status(ws)
+        outs.append(states.clone())
+    assert _lib.rnn_kernel_launches() - before == 3 * (T + 1)
+    assert torch.equal(outs[0], outs[1])
+    ref_st, _ = oracle_fwd(fn, inp)
+    check_states(fn, torch.bfloat16, outs[2], ref_st)
+
+
+def test_auto_takes_alternating_when_r_does_not_fit():
+    fn, B, T, N, D = "lstm", 17, 5, 1, 2048
+    dims = _lib.make_dims(B, T, N, D, fn, torch.bfloat16, "auto")
+    for bwd in (False, True):
+        rc, desc = _lib.rnn_plan_describe(dims, bwd)
+        assert rc == 0 and "path=alternating" in desc, desc
+    inp = _inputs(fn, (B, T, N, D), torch.bfloat16, seed=1402)
+    st, last, tape = run_fwd(fn, inp, "auto")
+    ref_st, _ = oracle_fwd(fn, inp)
+    check_states(fn, torch.bfloat16, st, ref_st)
+    dWx, dR, db, ds0 = run_bwd(fn, inp, st, tape, "auto")
+    check_grads(fn, inp, (dWx, dR, db, ds0))
