@@ -343,7 +343,8 @@ def main():
                 "frac": achieved / pk["bf16"], "traffic": None}
     plan_path = (plan_b if dom_bwd else plan_f).split()[0].split("=")[1]
     kname = {("fused", False): "fused_fwd_kernel", ("grid", False): "fused_fwd_kernel",
-             ("fused", True): "fused_bwd_kernel", ("grid", True): "grid_bwd_kernel"}.get(
+             ("fused", True): "fused_bwd_kernel", ("grid", True): "grid_bwd_kernel",
+             ("alternating", False): "alt_fwd_step", ("alternating", True): "alt_bwd_step"}.get(
         (plan_path, bool(dom_bwd)), f"simt_{'bwd' if dom_bwd else 'fwd'}_kernel")
     roof["traffic"] = measured_traffic(kname, w["name"])
     roof.update({"kernel": kname, "kernel_ms": kms,

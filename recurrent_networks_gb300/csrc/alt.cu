@@ -41,6 +41,12 @@ template <int N_>
 __device__ __forceinline__ void cpa_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N_) : "memory");
 }
+// Programmatic dependent launch: let the next step's grid start while this one
+// runs (it only prefetches R before its own dependency wait), and wait for the
+// previous step's grid (complete, memory visible) before touching its outputs.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
@@ -68,27 +74,33 @@ struct AltStage {
 };
 
 // ---- forward step -----------------------------------------------------------
+// 8 warps split the D/16 k-chunks (unevenly when they do not divide); after
+// the product the partial sums meet in shared memory and the 256 threads take
+// PPT (batch row, unit) pairs each through the cell.
+constexpr int ALT_WARPS = 8, ALT_THREADS = 32 * ALT_WARPS;
+
 template <int FN, int MT>
-__global__ void __launch_bounds__(256) alt_fwd_step(AltArgs a, int t) {
+__global__ void __launch_bounds__(ALT_THREADS) alt_fwd_step(AltArgs a, int t) {
   constexpr int G = FnInfo<FN>::G, S = FnInfo<FN>::S, P = FnInfo<FN>::P, K = P + S;
   constexpr int UT = AltFwdTile<FN>::UT, NC = AltFwdTile<FN>::NC, NNT = NC / 8;
-  constexpr int BM = 16 * MT;
+  constexpr int BM = 16 * MT, PPT = BM * UT / ALT_THREADS;
   using Stg = AltStage<NC, ALT_BK, MT>;  // B chunk [16 k][NC cols]
   constexpr int RSTR = NC + 8;            // fp32 row stride of the K-split partials
   const int D = a.D, N = a.N, B = a.B, T = a.T;
-  const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u0 = blockIdx.x * UT, n = blockIdx.y, b0 = blockIdx.z * BM;
   const int nb = min(BM, B - b0);
-  const int KW = D / nw, nchunk = KW / ALT_BK, kbeg = warp * KW;
+  const int nchunk_all = D / ALT_BK;
+  const int cbeg = warp * nchunk_all / ALT_WARPS, nchunk = (warp + 1) * nchunk_all / ALT_WARPS - cbeg;
 
   extern __shared__ __align__(128) unsigned char alt_smem[];
   __nv_bfloat16* wbase = (__nv_bfloat16*)alt_smem + (size_t)warp * ALT_NSTG * Stg::ELEMS;
   const __nv_bfloat16* R = (const __nv_bfloat16*)a.R;
   const __nv_bfloat16* hin = (const __nv_bfloat16*)a.xbuf + (size_t)(t & 1) * B * N * D;
 
-  auto load_chunk = [&](int c) {
+  auto load_r = [&](int c) {
     __nv_bfloat16* st = wbase + (c % ALT_NSTG) * Stg::ELEMS;
-    const int k0 = kbeg + c * ALT_BK;
+    const int k0 = (cbeg + c) * ALT_BK;
     // B: rows k0..k0+15 of R[g, n, :, u0 .. u0 + UT), UT/8 pieces of 16 bytes per gate
     constexpr int PPR = G * (UT / 8);  // pieces per row
     for (int e = lane; e < ALT_BK * PPR; e += 32) {
@@ -96,8 +108,11 @@ __global__ void __launch_bounds__(256) alt_fwd_step(AltArgs a, int t) {
       const __nv_bfloat16* src = R + ((size_t)(g * N + n) * D + k0 + r) * D + u0 + p8 * 8;
       cpa16(smem_u32(st + r * Stg::BSTR + g * UT + p8 * 8), src, true);
     }
+  };
+  auto load_h = [&](int c) {
+    __nv_bfloat16* as = wbase + (c % ALT_NSTG) * Stg::ELEMS + Stg::B_ELEMS;
+    const int k0 = (cbeg + c) * ALT_BK;
     // A: h_{t-1}[b0 + b, n, k0 .. k0 + 15], two pieces per row, zero rows past nb
-    __nv_bfloat16* as = st + Stg::B_ELEMS;
     for (int e = lane; e < BM * 2; e += 32) {
       const int r = e >> 1, p8 = e & 1;
       const bool ok = r < nb;
@@ -114,15 +129,41 @@ __global__ void __launch_bounds__(256) alt_fwd_step(AltArgs a, int t) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) acc[m][j][q] = 0.0f;
 
+  // Nothing before the dependency wait depends on the previous step: R of the
+  // first stages, and this step's Wx and bias for the thread's pairs, are in
+  // flight while the previous step finishes. cp.async groups: R0 .. R(NS-2),
+  // then h0 .. h(NS-2), then one group per later chunk; waiting for all but
+  // the newest NS - 2 groups at chunk c always covers chunk c's R and h.
 #pragma unroll
   for (int c = 0; c < ALT_NSTG - 1; ++c) {
-    if (c < nchunk) load_chunk(c);
+    if (c < nchunk) load_r(c);
+    cpa_commit();
+  }
+  const __nv_bfloat16* Wx = (const __nv_bfloat16*)a.Wx;
+  const __nv_bfloat16* bias = (const __nv_bfloat16*)a.bias;
+  float xk[PPT][G], bk[PPT][G];
+#pragma unroll
+  for (int k = 0; k < PPT; ++k) {
+    const int e = threadIdx.x + k * ALT_THREADS, b = e / UT, u = e - b * UT, j = u0 + u;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      xk[k][g] = b < nb ? __bfloat162float(Wx[((((size_t)(b0 + b) * T + t) * G + g) * N + n) * D + j]) : 0.0f;
+      bk[k][g] = __bfloat162float(bias[((size_t)g * N + n) * D + j]);
+    }
+  }
+  pdl_wait();
+#pragma unroll
+  for (int c = 0; c < ALT_NSTG - 1; ++c) {
+    if (c < nchunk) load_h(c);
     cpa_commit();
   }
   for (int c = 0; c < nchunk; ++c) {
     cpa_wait<ALT_NSTG - 2>();
     __syncwarp();
-    if (c + ALT_NSTG - 1 < nchunk) load_chunk(c + ALT_NSTG - 1);
+    if (c + ALT_NSTG - 1 < nchunk) {
+      load_r(c + ALT_NSTG - 1);
+      load_h(c + ALT_NSTG - 1);
+    }
     cpa_commit();
     const __nv_bfloat16* st = wbase + (c % ALT_NSTG) * Stg::ELEMS;
     const __nv_bfloat16* as = st + Stg::B_ELEMS;
@@ -144,8 +185,10 @@ __global__ void __launch_bounds__(256) alt_fwd_step(AltArgs a, int t) {
     }
   }
   cpa_wait<0>();
+  // the next step may now start its own prefetch
+  pdl_launch_dependents();
   __syncthreads();  // every warp is done with its pipeline: the region becomes the partial sums
-  float* red = (float*)alt_smem;  // [nw][BM][RSTR]
+  float* red = (float*)alt_smem;  // [ALT_WARPS][BM][RSTR]
   {
     float* rw = red + (size_t)warp * BM * RSTR;
 #pragma unroll
@@ -161,24 +204,24 @@ __global__ void __launch_bounds__(256) alt_fwd_step(AltArgs a, int t) {
   }
   __syncthreads();
 
-  const __nv_bfloat16* Wx = (const __nv_bfloat16*)a.Wx;
-  const __nv_bfloat16* bias = (const __nv_bfloat16*)a.bias;
   __nv_bfloat16* states = (__nv_bfloat16*)a.states;
   __nv_bfloat16* last = (__nv_bfloat16*)a.last;
   __nv_bfloat16* hout = (__nv_bfloat16*)a.xbuf + (size_t)((t + 1) & 1) * B * N * D;
-  for (int e = threadIdx.x; e < nb * UT; e += blockDim.x) {
-    const int b = e / UT, u = e - b * UT, bg = b0 + b, j = u0 + u;
-    float x[G], rc[G], sp[S], sn[S], pre[P];
+#pragma unroll
+  for (int k = 0; k < PPT; ++k) {
+    const int e = threadIdx.x + k * ALT_THREADS, b = e / UT, u = e - b * UT, bg = b0 + b, j = u0 + u;
+    if (b >= nb) break;
+    float rc[G], sp[S], sn[S], pre[P];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      float v = __bfloat162float(bias[((size_t)g * N + n) * D + j]);
-      for (int w = 0; w < nw; ++w) v += red[((size_t)w * BM + b) * RSTR + g * UT + u];
+      float v = bk[k][g];
+#pragma unroll
+      for (int w = 0; w < ALT_WARPS; ++w) v += red[((size_t)w * BM + b) * RSTR + g * UT + u];
       rc[g] = v;
-      x[g] = __bfloat162float(Wx[((((size_t)bg * T + t) * G + g) * N + n) * D + j]);
     }
 #pragma unroll
     for (int s = 0; s < S; ++s) sp[s] = a.cst[(((size_t)s * B + bg) * N + n) * D + j];
-    cell_fwd<FN, true>(x, rc, sp, sn, pre);
+    cell_fwd<FN, true>(xk[k], rc, sp, sn, pre);
 #pragma unroll
     for (int s = 0; s < S; ++s) {
       a.cst[(((size_t)s * B + bg) * N + n) * D + j] = sn[s];
@@ -215,18 +258,19 @@ __global__ void alt_fwd_init(AltArgs a) {
 
 // ---- backward step ------------------------------------------------------------
 template <int FN, int MT>
-__global__ void __launch_bounds__(256) alt_bwd_step(AltArgs a, int t) {
+__global__ void __launch_bounds__(ALT_THREADS) alt_bwd_step(AltArgs a, int t) {
   constexpr int G = FnInfo<FN>::G, S = FnInfo<FN>::S, P = FnInfo<FN>::P, K = P + S;
   constexpr int UB = ALT_UB, NNT = UB / 8;
-  constexpr int BM = 16 * MT;
+  constexpr int BM = 16 * MT, PPT = BM * UB / ALT_THREADS;
   // B chunk stored [UB cols (units i)][16 k]: each column's k values contiguous
   using Stg = AltStage<ALT_BK, UB, MT>;
   constexpr int RSTR = UB + 4;
   const int D = a.D, N = a.N, B = a.B, T = a.T;
-  const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i0 = blockIdx.x * UB, n = blockIdx.y, b0 = blockIdx.z * BM;
   const int nb = min(BM, B - b0);
-  const int KW = G * D / nw, nchunk = KW / ALT_BK, kbeg = warp * KW;
+  const int nchunk_all = G * D / ALT_BK;
+  const int cbeg = warp * nchunk_all / ALT_WARPS, nchunk = (warp + 1) * nchunk_all / ALT_WARPS - cbeg;
   const bool have_rec = t < T - 1;  // dr_{t+1} exists
 
   extern __shared__ __align__(128) unsigned char alt_smem[];
@@ -235,15 +279,17 @@ __global__ void __launch_bounds__(256) alt_bwd_step(AltArgs a, int t) {
   const size_t drsz = (size_t)B * G * N * D;
   const __nv_bfloat16* drin = (const __nv_bfloat16*)a.xbuf + (size_t)((t + 1) & 1) * drsz;
 
-  auto load_chunk = [&](int c) {
+  auto load_r = [&](int c) {
     __nv_bfloat16* st = wbase + (c % ALT_NSTG) * Stg::ELEMS;
-    const int k0 = kbeg + c * ALT_BK, g = k0 / D, j0 = k0 - g * D;
+    const int k0 = (cbeg + c) * ALT_BK, g = k0 / D, j0 = k0 - g * D;
     // B: R[g, n, i0 + i, j0 .. j0 + 15] for the UB units i, two pieces each
-    {
-      const int i = lane >> 1, p8 = lane & 1;  // UB * 2 = 32 pieces
-      const __nv_bfloat16* src = R + ((size_t)(g * N + n) * D + i0 + i) * D + j0 + p8 * 8;
-      cpa16(smem_u32(st + i * Stg::BSTR + p8 * 8), src, true);
-    }
+    const int i = lane >> 1, p8 = lane & 1;  // UB * 2 = 32 pieces
+    const __nv_bfloat16* src = R + ((size_t)(g * N + n) * D + i0 + i) * D + j0 + p8 * 8;
+    cpa16(smem_u32(st + i * Stg::BSTR + p8 * 8), src, true);
+  };
+  auto load_dr = [&](int c) {
+    __nv_bfloat16* st = wbase + (c % ALT_NSTG) * Stg::ELEMS;
+    const int k0 = (cbeg + c) * ALT_BK, g = k0 / D, j0 = k0 - g * D;
     // A: dr_{t+1}[b0 + b, g, n, j0 .. j0 + 15]
     __nv_bfloat16* as = st + Stg::B_ELEMS;
     for (int e = lane; e < BM * 2; e += 32) {
@@ -261,16 +307,55 @@ __global__ void __launch_bounds__(256) alt_bwd_step(AltArgs a, int t) {
     for (int j = 0; j < NNT; ++j)
 #pragma unroll
       for (int q = 0; q < 4; ++q) acc[m][j][q] = 0.0f;
+  if (have_rec) {  // R first, the previous step's dr after the dependency wait
+#pragma unroll
+    for (int c = 0; c < ALT_NSTG - 1; ++c) {
+      if (c < nchunk) load_r(c);
+      cpa_commit();
+    }
+  }
+  // the tape and the upstream gradients of this step come from earlier work:
+  // loaded before the dependency wait too
+  const __nv_bfloat16* s0 = (const __nv_bfloat16*)a.s0;
+  const __nv_bfloat16* dstates = (const __nv_bfloat16*)a.dstates;
+  const __nv_bfloat16* dlast = (const __nv_bfloat16*)a.dlast;
+  float prek[PPT][P], snk[PPT][S], spk[PPT][S], upk[PPT][S];
+  if (t >= 0) {
+#pragma unroll
+    for (int k = 0; k < PPT; ++k) {
+      const int e = threadIdx.x + k * ALT_THREADS, b = e / UB, u = e - b * UB, j = i0 + u;
+      const int bg = b0 + (b < nb ? b : 0);
+      const float* tp = a.tape + (((size_t)t * B + bg) * N + n) * K * D + j;
+#pragma unroll
+      for (int k2 = 0; k2 < P; ++k2) prek[k][k2] = tp[k2 * D];
+#pragma unroll
+      for (int s = 0; s < S; ++s) {
+        snk[k][s] = tp[(P + s) * D];
+        if (t > 0)
+          spk[k][s] = a.tape[(((size_t)(t - 1) * B + bg) * N + n) * K * D + (size_t)(P + s) * D + j];
+        else
+          spk[k][s] = s0 ? __bfloat162float(s0[(((size_t)s * B + bg) * N + n) * D + j]) : 0.0f;
+        float d = 0.0f;
+        if (dstates) d += __bfloat162float(dstates[(((size_t)s * B + bg) * T + t) * N * D + (size_t)n * D + j]);
+        if (dlast && t == T - 1) d += __bfloat162float(dlast[(((size_t)s * B + bg) * N + n) * D + j]);
+        upk[k][s] = d;
+      }
+    }
+  }
+  pdl_wait();
   if (have_rec) {
 #pragma unroll
     for (int c = 0; c < ALT_NSTG - 1; ++c) {
-      if (c < nchunk) load_chunk(c);
+      if (c < nchunk) load_dr(c);
       cpa_commit();
     }
     for (int c = 0; c < nchunk; ++c) {
       cpa_wait<ALT_NSTG - 2>();
       __syncwarp();
-      if (c + ALT_NSTG - 1 < nchunk) load_chunk(c + ALT_NSTG - 1);
+      if (c + ALT_NSTG - 1 < nchunk) {
+        load_r(c + ALT_NSTG - 1);
+        load_dr(c + ALT_NSTG - 1);
+      }
       cpa_commit();
       const __nv_bfloat16* st = wbase + (c % ALT_NSTG) * Stg::ELEMS;
       const __nv_bfloat16* as = st + Stg::B_ELEMS;
@@ -291,8 +376,9 @@ __global__ void __launch_bounds__(256) alt_bwd_step(AltArgs a, int t) {
     }
     cpa_wait<0>();
   }
+  pdl_launch_dependents();
   __syncthreads();
-  float* red = (float*)alt_smem;  // [nw][BM][RSTR]
+  float* red = (float*)alt_smem;  // [ALT_WARPS][BM][RSTR]
   {
     float* rw = red + (size_t)warp * BM * RSTR;
 #pragma unroll
@@ -308,17 +394,17 @@ __global__ void __launch_bounds__(256) alt_bwd_step(AltArgs a, int t) {
   }
   __syncthreads();
 
-  const __nv_bfloat16* s0 = (const __nv_bfloat16*)a.s0;
-  const __nv_bfloat16* dstates = (const __nv_bfloat16*)a.dstates;
-  const __nv_bfloat16* dlast = (const __nv_bfloat16*)a.dlast;
   __nv_bfloat16* dWx = (__nv_bfloat16*)a.dWx;
   __nv_bfloat16* dro = (__nv_bfloat16*)a.dr;
   const bool write_dr = dro && (FN == GRU || (void*)dro != (void*)dWx);
   __nv_bfloat16* drout = (__nv_bfloat16*)a.xbuf + (size_t)(t & 1) * drsz;
-  for (int e = threadIdx.x; e < nb * UB; e += blockDim.x) {
-    const int b = e / UB, u = e - b * UB, bg = b0 + b, j = i0 + u;
+#pragma unroll
+  for (int k = 0; k < PPT; ++k) {
+    const int e = threadIdx.x + k * ALT_THREADS, b = e / UB, u = e - b * UB, bg = b0 + b, j = i0 + u;
+    if (b >= nb) break;
     float dh = 0.0f;
-    for (int w = 0; w < nw; ++w) dh += red[((size_t)w * BM + b) * RSTR + u];
+#pragma unroll
+    for (int w = 0; w < ALT_WARPS; ++w) dh += red[((size_t)w * BM + b) * RSTR + u];
     if (t < 0) {  // dstates0: carried gradients plus the product of dr_0
       __nv_bfloat16* ds0 = (__nv_bfloat16*)a.ds0;
 #pragma unroll
@@ -329,24 +415,14 @@ __global__ void __launch_bounds__(256) alt_bwd_step(AltArgs a, int t) {
       }
       continue;
     }
-    float pre[P], sp[S], sn[S], dsn[S], dx[G], dr[G], dsp[S];
-    const float* tp = a.tape + (((size_t)t * B + bg) * N + n) * K * D + j;
-#pragma unroll
-    for (int k2 = 0; k2 < P; ++k2) pre[k2] = tp[k2 * D];
+    float dsn[S], dx[G], dr[G], dsp[S];
 #pragma unroll
     for (int s = 0; s < S; ++s) {
-      sn[s] = tp[(P + s) * D];
-      if (t > 0)
-        sp[s] = a.tape[(((size_t)(t - 1) * B + bg) * N + n) * K * D + (size_t)(P + s) * D + j];
-      else
-        sp[s] = s0 ? __bfloat162float(s0[(((size_t)s * B + bg) * N + n) * D + j]) : 0.0f;
-      float d = a.cst[(((size_t)s * B + bg) * N + n) * D + j];
-      if (dstates) d += __bfloat162float(dstates[(((size_t)s * B + bg) * T + t) * N * D + (size_t)n * D + j]);
-      if (dlast && t == T - 1) d += __bfloat162float(dlast[(((size_t)s * B + bg) * N + n) * D + j]);
+      float d = a.cst[(((size_t)s * B + bg) * N + n) * D + j] + upk[k][s];
       if (s == 0) d += dh;
       dsn[s] = d;
     }
-    cell_bwd<FN, true>(pre, sp, sn, dsn, dx, dr, dsp);
+    cell_bwd<FN, true>(prek[k], spk[k], snk[k], dsn, dx, dr, dsp);
     const size_t o = (((size_t)bg * T + t) * G) * N * D + (size_t)n * D + j;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -364,24 +440,17 @@ __global__ void alt_zero(float* p, size_t n) {
     p[e] = 0.0f;
 }
 
-// K-split warps: the largest of 8, 4, 2, 1 that divides the k-chunks.
-int alt_warps(int kchunks) {
-  for (int w = 8; w > 1; w >>= 1)
-    if (kchunks % w == 0) return w;
-  return 1;
-}
-
 template <int FN, int MT>
-size_t alt_fwd_smem(int warps) {
+size_t alt_fwd_smem() {
   constexpr int NC = AltFwdTile<FN>::NC;
-  const size_t pipe = (size_t)warps * ALT_NSTG * AltStage<NC, ALT_BK, MT>::ELEMS * 2;
-  const size_t red = (size_t)warps * 16 * MT * (NC + 8) * 4;
+  const size_t pipe = (size_t)ALT_WARPS * ALT_NSTG * AltStage<NC, ALT_BK, MT>::ELEMS * 2;
+  const size_t red = (size_t)ALT_WARPS * 16 * MT * (NC + 8) * 4;
   return pipe > red ? pipe : red;
 }
 template <int FN, int MT>
-size_t alt_bwd_smem(int warps) {
-  const size_t pipe = (size_t)warps * ALT_NSTG * AltStage<ALT_BK, ALT_UB, MT>::ELEMS * 2;
-  const size_t red = (size_t)warps * 16 * MT * (ALT_UB + 4) * 4;
+size_t alt_bwd_smem() {
+  const size_t pipe = (size_t)ALT_WARPS * ALT_NSTG * AltStage<ALT_BK, ALT_UB, MT>::ELEMS * 2;
+  const size_t red = (size_t)ALT_WARPS * 16 * MT * (ALT_UB + 4) * 4;
   return pipe > red ? pipe : red;
 }
 
@@ -411,33 +480,50 @@ GraphKey key_of(int fn, bool bwd, const AltArgs& a) {
   return k;
 }
 
+// Launch with programmatic stream serialisation: the kernel may begin while
+// its predecessor in the stream still runs; it orders itself with
+// griddepcontrol.wait.
+template <typename... Args>
+cudaError_t launch_pdl(void (*k)(Args...), dim3 grid, int threads, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
 template <int FN, int MT>
 cudaError_t enqueue_fwd(const AltArgs& a, cudaStream_t st) {
   constexpr int UT = AltFwdTile<FN>::UT;
-  const int warps = alt_warps(a.D / ALT_BK);
-  const size_t smem = alt_fwd_smem<FN, MT>(warps);
+  const size_t smem = alt_fwd_smem<FN, MT>();
   cudaError_t e = cudaFuncSetAttribute(alt_fwd_step<FN, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const size_t per = (size_t)a.B * a.N * a.D;
   alt_fwd_init<FN><<<(unsigned)((per + 255) / 256 < 1184 ? (per + 255) / 256 : 1184), 256, 0, st>>>(a);
   const dim3 grid(a.D / UT, a.N, (a.B + 16 * MT - 1) / (16 * MT));
-  for (int t = 0; t < a.T; ++t) alt_fwd_step<FN, MT><<<grid, warps * 32, smem, st>>>(a, t);
-  return cudaGetLastError();
+  for (int t = 0; t < a.T && e == cudaSuccess; ++t) e = launch_pdl(alt_fwd_step<FN, MT>, grid, ALT_THREADS, smem, st, a, t);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int FN, int MT>
 cudaError_t enqueue_bwd(const AltArgs& a, cudaStream_t st) {
-  constexpr int G = FnInfo<FN>::G, S = FnInfo<FN>::S;
-  const int warps = alt_warps(G * a.D / ALT_BK);
-  const size_t smem = alt_bwd_smem<FN, MT>(warps);
+  constexpr int S = FnInfo<FN>::S;
+  const size_t smem = alt_bwd_smem<FN, MT>();
   cudaError_t e = cudaFuncSetAttribute(alt_bwd_step<FN, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const size_t n = (size_t)S * a.B * a.N * a.D;
   alt_zero<<<(unsigned)((n + 255) / 256 < 1184 ? (n + 255) / 256 : 1184), 256, 0, st>>>(a.cst, n);
   const dim3 grid(a.D / ALT_UB, a.N, (a.B + 16 * MT - 1) / (16 * MT));
-  for (int t = a.T - 1; t >= 0; --t) alt_bwd_step<FN, MT><<<grid, warps * 32, smem, st>>>(a, t);
-  if (a.ds0) alt_bwd_step<FN, MT><<<grid, warps * 32, smem, st>>>(a, -1);
-  return cudaGetLastError();
+  for (int t = a.T - 1; t >= 0 && e == cudaSuccess; --t)
+    e = launch_pdl(alt_bwd_step<FN, MT>, grid, ALT_THREADS, smem, st, a, t);
+  if (a.ds0 && e == cudaSuccess) e = launch_pdl(alt_bwd_step<FN, MT>, grid, ALT_THREADS, smem, st, a, -1);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int FN>
