@@ -330,6 +330,8 @@ int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
     WgradArgs g{d->B, d->T, d->N, d->D, z.G, states, states0, drbuf, dR, db};
     g.scratch = (float*)(ws + w.wg);
     g.scratch_bytes = w.tape - w.wg;
+    g.status = (unsigned int*)ws;
+    g.wait_limit_ns = g_wait_limit_ns;
     rc = cuda_status(wgrad_run(d->dtype, g, st));
   }
   return rc;

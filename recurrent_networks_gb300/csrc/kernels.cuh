@@ -42,6 +42,8 @@ struct WgradArgs {
   void* db;  // may be null
   float* scratch = nullptr;  // optional: split-K partial sums (wgrad_scratch_bytes)
   size_t scratch_bytes = 0;
+  unsigned int* status = nullptr;  // device status word for the bounded waits (may be null)
+  unsigned long long wait_limit_ns = 2000000000ull;
 };
 // Bytes of split-K scratch the tensor-core weight-gradient pass can use.
 size_t wgrad_scratch_bytes(int B, int T, int N, int D, int G, int dtype);
@@ -111,6 +113,13 @@ cudaError_t encode_tensor_map_bf16(void* map, const void* base, int rank,
                                    const unsigned long long* dims, const unsigned int* box);
 cudaError_t encode_tensor_map(void* map, const void* base, int elem_bytes, int rank,
                               const unsigned long long* dims, const unsigned int* box);
+// bf16, 128-byte swizzle (box[0] * 2 <= 128): the layout the tcgen05 operands read
+cudaError_t encode_tensor_map_sw128(void* map, const void* base, int rank, const unsigned long long* dims,
+                                    const unsigned int* box);
+// dR on the 5th-generation tensor cores (bf16, D % 8 == 0); the caller adds db.
+bool wgrad_umma_supported(const WgradArgs& a);
+int wgrad_umma_splits(int B, int T, int N, int D, int G);
+cudaError_t wgrad_umma_run(const WgradArgs& a, int splits, cudaStream_t st);
 cudaError_t fused_bwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st);
 
 }  // namespace rnn

@@ -290,12 +290,39 @@ static int wgrad_splits(int B, int T, int N, int D, int G) {
 
 size_t wgrad_scratch_bytes(int B, int T, int N, int D, int G, int dtype) {
   if (dtype != 1 || D % 8) return 0;
-  const int s = wgrad_splits(B, T, N, D, G);
+  int s = wgrad_splits(B, T, N, D, G);
+  const int su = wgrad_umma_splits(B, T, N, D, G);
+  if (su > s) s = su;
   return s > 1 ? (size_t)s * G * N * D * D * sizeof(float) : 0;
+}
+
+// db after the tensor-core dR: the column sums of dr.
+static cudaError_t bgrad_launch(const WgradArgs& a, cudaStream_t st) {
+  if (a.db) {
+    dim3 g2((a.D + 31) / 32, a.G * a.N);
+    bgrad_kernel<__nv_bfloat16><<<g2, 32 * BG_KS, 0, st>>>(a);
+    note_launch();
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t wgrad_run(int dtype, const WgradArgs& a, cudaStream_t st) {
   if (dtype != 1 || a.D % 8 || !a.dR) return dtype == 1 ? wgrad_launch<__nv_bfloat16>(a, st) : wgrad_launch<float>(a, st);
+  if (wgrad_umma_supported(a)) {  // tcgen05 GEMM, accumulator in tensor memory
+    int su = wgrad_umma_splits(a.B, a.T, a.N, a.D, a.G);
+    const size_t need = (size_t)su * a.G * a.N * a.D * a.D * sizeof(float);
+    if (su > 1 && (!a.scratch || a.scratch_bytes < need)) su = 1;
+    const cudaError_t e = wgrad_umma_run(a, su, st);
+    if (e == cudaSuccess) {
+      if (su > 1) {
+        wgrad_reduce_kernel<<<2 * 152, 256, 0, st>>>(a, su);
+        note_launch();
+      }
+      return bgrad_launch(a, st);
+    }
+    if (e != cudaErrorInvalidValue && e != cudaErrorNotSupported) return e;
+    (void)cudaGetLastError();  // the operands do not fit the TMA boxes: the mma.sync GEMM below
+  }
   int splits = wgrad_splits(a.B, a.T, a.N, a.D, a.G);
   const size_t need = (size_t)splits * a.G * a.N * a.D * a.D * sizeof(float);
   if (splits > 1 && (!a.scratch || a.scratch_bytes < need)) splits = 1;

@@ -293,3 +293,17 @@ def test_auto_takes_alternating_when_r_does_not_fit():
     check_states(fn, torch.bfloat16, st, ref_st)
     dWx, dR, db, ds0 = run_bwd(fn, inp, st, tape, "auto")
     check_grads(fn, inp, (dWx, dR, db, ds0))
+
+
+# ------------------------------------------------- weight gradients (tcgen05)
+@pytest.mark.parametrize("case", [("lstm", 3, 200, 2, 192), ("gru", 70, 9, 1, 64), ("slstm", 2, 130, 1, 320)],
+                         ids=lambda c: "%s-B%dT%dN%dD%d" % c)
+def test_weight_gradient_tiles(case):
+    """dR and db through the tensor-memory GEMM: ragged 128-unit tiles (D = 192,
+    320), runs of steps that end inside a 64-step tile (T = 200, 130, 9), a batch
+    wider than one 64-row initial-state tile (B = 70), split-K partial sums."""
+    fn, B, T, N, D = case
+    inp = _inputs(fn, (B, T, N, D), torch.bfloat16, seed=1500 + B + T + D)
+    st, last, tape = run_fwd(fn, inp, "simt")
+    dWx, dR, db, ds0 = run_bwd(fn, inp, st, tape, "simt")
+    check_grads(fn, inp, (dWx, dR, db, ds0))
