@@ -45,7 +45,34 @@ def parse():
     ap.add_argument("--path", default="auto", choices=["auto", "fused", "alternating", "simt", "grid"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--trace", action="store_true",
+                    help="print the per-phase cycle medians of the persistent scan kernels (rnn_trace) "
+                         "instead of the bench line")
     return ap.parse_args()
+
+
+def phase_trace(step_fn, backward, T):
+    """Median clock64 cycles between the phase points of the persistent
+    kernels (CTA 0, thread 0), over up to 200 steps after the first 10."""
+    from recurrent_networks_gb300 import _lib
+    steps = max(1, min(200, T - 20))
+    buf = torch.zeros(8 * steps, dtype=torch.int64, device="cuda")
+    out = {}
+    for which in (("fwd", "bwd") if backward else ("fwd",)):
+        buf.zero_()
+        _lib.rnn_trace(buf, 10, steps)
+        step_fn(which)
+        torch.cuda.synchronize()
+        _lib.rnn_trace(None)
+        tr = buf.view(steps, 8).cpu().tolist()
+        phases = {}
+        for p in range(1, 8):
+            d = [r[p] - r[p - 1] for r in tr if r[p] and r[p - 1]]
+            if d:
+                phases[f"{p - 1}->{p}"] = statistics.median(d)
+        per = [tr[i + 1][0] - tr[i][0] for i in range(steps - 1) if tr[i + 1][0] and tr[i][0]]
+        out[which] = {"step_cycles": statistics.median(per) if per else None, "phase_cycles": phases}
+    return out
 
 
 def peaks():
@@ -285,6 +312,20 @@ def main():
     _lib.rnn_check_status(ws)
     torch.cuda.synchronize()
 
+    if args.trace:
+        def one(which):
+            if which == "fwd":
+                _lib.rnn_fwd(dims, inp["Wx"], inp["R"], inp["b"], inp["states0"], states, last, tape, ws)
+            else:
+                _lib.rnn_bwd(dims, inp["Wx"], inp["R"], inp["b"], inp["states0"], states, tape, inp["dstates"],
+                             None, dWx, dR, db, ds0, ws)
+        res = {"trace": phase_trace(one, backward, T), "workload": w["name"], "plan_fwd": plan_f,
+               "plan_bwd": plan_b}
+        _lib.rnn_check_status(ws)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return
+
     # timed region: per-step events; L2 flushed before every step, outside the event window
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -368,6 +409,23 @@ def main():
               "step_latency_ns": {"fwd": f_ms * 1e6 / T, "bwd": (b_ms * 1e6 / T) if backward else None},
               "roofline": roof, "gpu_launches": launches}
     result["clocks"] = clk.summary()
+
+    # ---- latency floor of the cluster exchange (outside the timed region): the
+    # forward's per-step h exchange alone, for the plan's cluster size and slice
+    if plan_f.startswith("path=fused"):
+        pf = dict(kv.split("=") for kv in plan_f.split()[1:] if "=" in kv)
+        C, U, NT = int(pf["C"]), int(pf["U"]), int(pf["NT"])
+        slice_bytes = min(B, 8 * NT) * (U + 8) * 2
+        fl = torch.zeros(2, dtype=torch.int64, device=dev)
+        _lib.rnn_exchange_floor(C, slice_bytes, 2000, fl)
+        torch.cuda.synchronize()
+        cyc, st_fl = (int(x) for x in fl.cpu().tolist())
+        mhz = result["clocks"].get("sm_mhz") or 2070.0
+        fl_ns = cyc / mhz * 1e3
+        result["latency_floor"] = {
+            "what": f"h exchange alone: cluster of {C}, {slice_bytes} B bulk copy to each peer per step",
+            "cycles_per_step": cyc, "ns_per_step": fl_ns, "status": st_fl,
+            "fwd_step_over_floor": (f_ms * 1e6 / T) / fl_ns if fl_ns > 0 else None}
 
     # ---- e2e through the C ABI with host buffers (pinned), copies inside the window
     if not args.no_e2e:

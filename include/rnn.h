@@ -193,6 +193,19 @@ int rnn_trace(void *buf, int t0, int steps);
  * RNN_OK or RNN_EINVAL. */
 int rnn_debug_inject_wait(int step, unsigned long long limit_ns);
 
+/* Latency floor of the cluster exchange (a measurement aid). Runs a kernel
+ * whose steps hold only the h exchange of the forward cluster kernel: every
+ * CTA of one cluster of C CTAs (1 .. 16) stages a slice of slice_bytes
+ * (16 .. 4096, a multiple of 16), sends it to every CTA of the cluster with
+ * one bulk copy per peer (lane 0 of each of the 8 warps issuing every 8th
+ * copy), and waits on an mbarrier transaction count (bounded, 2 s) for the C
+ * slices of the step, for `steps` (2 .. 1e6) steps. Writes to out[0] the
+ * clock64 cycles per step seen by CTA 0 and to out[1] the status (0 = ok,
+ * 1 = a wait ran out); `out` is a device buffer of two unsigned 64-bit words
+ * owned by the caller. Asynchronous on `stream`. Returns RNN_OK, RNN_EINVAL
+ * or RNN_ECUDA. */
+int rnn_exchange_floor(int C, int slice_bytes, int steps, void *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

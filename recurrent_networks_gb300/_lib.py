@@ -64,6 +64,7 @@ def load(path: str | None = None):
             lib.rnn_bwd_noalloc.argtypes = [dp] + [vp] * 13
             lib.rnn_trace.argtypes = [vp, i, i]
             lib.rnn_debug_inject_wait.argtypes = [i, ctypes.c_ulonglong]
+            lib.rnn_exchange_floor.argtypes = [i, i, i, vp, vp]
             _lib = lib
     return _lib
 
@@ -173,3 +174,11 @@ def rnn_debug_inject_wait(step: int = -1, limit_ns: int = 0) -> int:
     """Test hook: the forward persistent kernels make CTA 0 wait at `step` on a
     barrier nothing signals, for limit_ns; step < 0 switches it off."""
     return _check(load().rnn_debug_inject_wait(int(step), int(limit_ns)), "rnn_debug_inject_wait")
+
+
+def rnn_exchange_floor(C: int, slice_bytes: int, steps: int, out, stream=None) -> int:
+    """Runs the exchange-only kernel (one cluster of C CTAs, bulk copies of
+    slice_bytes to every peer per step) for `steps` steps; `out` is a device
+    tensor of >= 2 int64: cycles per step of CTA 0, then the status."""
+    return _check(load().rnn_exchange_floor(int(C), int(slice_bytes), int(steps), _p(out), _stream(stream)),
+                  "rnn_exchange_floor")

@@ -1,0 +1,107 @@
+// Latency floor of the cluster h exchange: the steps of the forward cluster
+// kernel with the product and the cell update taken out. Each step: wait for
+// the C slices of the previous step (mbarrier transaction count, bounded),
+// order the staged slice for the async proxy, a CTA barrier, then one bulk
+// copy per peer (shared::cta -> shared::cluster) into the peer's next buffer,
+// issued by lane 0 of the warps in the same rotation as the forward kernel.
+#include <stdio.h>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+#include "rnn.h"
+
+namespace rnn {
+
+namespace {
+
+__global__ void __launch_bounds__(256, 1) exchange_floor_kernel(int slice_bytes, int steps, unsigned long long* out) {
+  extern __shared__ __align__(128) unsigned char fl_smem[];
+  const int C = (int)gridDim.x;  // the grid is one cluster
+  uint64_t* bars = (uint64_t*)fl_smem;
+  unsigned char* hbuf = fl_smem + 128;                          // [2][C][slice]
+  unsigned char* stage = hbuf + (size_t)2 * C * slice_bytes;    // [2][slice]
+  const uint32_t rank = cluster_ctarank();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+  const uint32_t bar0 = smem_u32(&bars[0]);
+  unsigned int* status = (unsigned int*)(out + 1);
+  const unsigned long long limit = 2000000000ull;
+  if (tid == 0) {
+    mbar_init(bar0, 1);
+    mbar_init(bar0 + 8, 1);
+    fence_mbar_init_cluster();
+  }
+  for (int e = tid; e < 2 * slice_bytes; e += blockDim.x) stage[e] = (unsigned char)e;
+  __syncthreads();
+  cluster_sync_all();
+  const uint32_t hbytes = (uint32_t)C * slice_bytes;
+  if (tid == 0) {
+    if (steps > 1) mbar_arrive_expect_tx(bar0 + 8, hbytes);
+    if (steps > 2) mbar_arrive_expect_tx(bar0, hbytes);
+  }
+  bool failed = false;
+  uint32_t ph0 = 0, ph1 = 0;
+  const long long t0 = clock64();
+  for (int t = 0; t < steps; ++t) {
+    const int p = t & 1;
+    if (t > 0) {
+      mbar_wait_bounded(bar0 + 8 * p, p ? ph1 : ph0, limit, status, failed);
+      if (p) ph1 ^= 1u; else ph0 ^= 1u;
+      if (tid == 0 && t + 2 <= steps - 1) mbar_arrive_expect_tx(bar0 + 8 * p, hbytes);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (t + 1 < steps && lane == 0) {
+      const uint32_t dst = smem_u32(hbuf + (size_t)(p ^ 1) * C * slice_bytes + (size_t)rank * slice_bytes);
+      const uint32_t bar = bar0 + 8 * (p ^ 1);
+      const uint32_t src = smem_u32(stage + (size_t)p * slice_bytes);
+      for (int c = warp; c < C; c += nwarps) {
+        int peer = (int)rank + c;
+        if (peer >= C) peer -= C;
+        bulk_copy_to_peer(mapa_shared(dst, (uint32_t)peer), src, (uint32_t)slice_bytes,
+                          mapa_shared(bar, (uint32_t)peer));
+      }
+    }
+  }
+  const long long t1 = clock64();
+  __syncthreads();
+  cluster_sync_all();  // no CTA leaves while a peer may still write into its shared memory
+  if (rank == 0 && tid == 0) out[0] = (unsigned long long)((t1 - t0) / steps);
+}
+
+}  // namespace
+
+}  // namespace rnn
+
+using namespace rnn;
+
+extern "C" int rnn_exchange_floor(int C, int slice_bytes, int steps, void* out, void* stream) {
+  if (C < 1 || C > 16 || slice_bytes < 16 || slice_bytes > 4096 || slice_bytes % 16 || steps < 2 ||
+      steps > 1000000 || !out || ((uintptr_t)out & 7u))
+    return RNN_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t smem = 128 + (size_t)2 * C * slice_bytes + (size_t)2 * slice_bytes;
+  cudaError_t e = cudaMemsetAsync(out, 0, 16, st);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(exchange_floor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess && C > 8) e = cudaFuncSetAttribute(exchange_floor_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, exchange_floor_kernel, slice_bytes, steps, (unsigned long long*)out);
+    note_launch();
+  }
+  if (e != cudaSuccess) {
+    fprintf(stderr, "librnn_gb300: CUDA error: %s\n", cudaGetErrorString(e));
+    return RNN_ECUDA;
+  }
+  return RNN_OK;
+}

@@ -50,3 +50,20 @@ def test_injected_wait_times_out_and_is_reported(path, shape):
 def test_injection_arguments_validated():
     assert _lib.load().rnn_debug_inject_wait(3, 0) == _lib.RNN_EINVAL
     assert _lib.load().rnn_debug_inject_wait(-1, 0) == _lib.RNN_OK
+
+
+def test_exchange_floor_runs_and_reports():
+    """The exchange-only kernel completes with status 0 and a cycles-per-step
+    figure that grows with the number of peers (more bulk copies per step)."""
+    out = torch.zeros(2, dtype=torch.int64, device="cuda")
+    cyc = {}
+    for C in (2, 16):
+        _lib.rnn_exchange_floor(C, 384, 500, out)
+        torch.cuda.synchronize()
+        v = out.cpu().tolist()
+        assert v[1] == 0, v
+        assert 100 < v[0] < 1_000_000, v
+        cyc[C] = v[0]
+    assert cyc[16] > cyc[2], cyc
+    with pytest.raises(_lib.RnnError):
+        _lib.rnn_exchange_floor(17, 384, 500, out)
