@@ -69,18 +69,26 @@ def to_np(t):
     return t.detach().float().cpu().double().numpy()
 
 
-def check_states(fn, dtype, got, ref, what="states"):
+def check_states(fn, dtype, got, ref, what="states", calib=None):
+    """h against the stated bound; the other states (c, n, m) against theirs.
+    calib: the oracle's states in its bfloat16-operand mode for the same
+    inputs. Over long sequences the rounding of h to bf16 alone moves the
+    integrating states (sLSTM c, n, m over 2048 steps: ~10% of max(1, |x|));
+    the bound on those states then widens to 1.5x the oracle's own distance
+    between its bf16-operand and plain-fp64 states, as for the gradients."""
     tol = TOL[dtype]
     got = to_np(got)
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     err_h = np.abs(got[0] - ref[0]).max() if got[0].size else 0.0
     assert err_h <= tol["h"], f"{fn} {what} h: max abs err {err_h:.3g} > {tol['h']}"
     for s in range(1, got.shape[0]):
-        e = np.abs(got[s] - ref[s])
-        if tol["states_rel"]:
-            e = e / np.maximum(1.0, np.abs(ref[s]))
+        den = np.maximum(1.0, np.abs(ref[s])) if tol["states_rel"] else 1.0
+        e = np.abs(got[s] - ref[s]) / den
         m = e.max() if e.size else 0.0
-        assert m <= tol["states"], f"{fn} {what} state {s}: err {m:.3g} > {tol['states']}"
+        bound = tol["states"]
+        if calib is not None and e.size:
+            bound = max(bound, 1.5 * float((np.abs(calib[s] - ref[s]) / den).max()))
+        assert m <= bound, f"{fn} {what} state {s}: err {m:.3g} > {bound:.3g}"
     return err_h
 
 
