@@ -193,6 +193,31 @@ int rnn_trace(void *buf, int t0, int steps);
  * RNN_OK or RNN_EINVAL. */
 int rnn_debug_inject_wait(int step, unsigned long long limit_ns);
 
+/*
+ * Input projection ahead of the scan (developnotes "deep learning operators",
+ * section 5.3 LSTM, MyLSTM.forward, computes each gate's input branch as
+ * x_t W_ih^T + b_ih; the FlashRNN announcement's flashrnn() takes that product
+ * as its input Wx). For BT = B*T rows, on the tensor cores:
+ *     Wx[m, c] = sum_i x[m, i] * W_x[c, i] + bias[c]
+ *   x    [BT][I]   layer input (row m = b*T + t)                        (in)
+ *   W_x  [C][I]    weights in the weight_ih layout: C = G*N*D rows in the
+ *                  order of Wx's (g, n, d) axes                          (in)
+ *   bias [C]       or NULL                                              (in)
+ *   Wx   [BT][C]   = the scan's Wx [B,T,G,N,D]                           (out)
+ * All bf16 device pointers, 16-byte aligned; I and C multiples of 8 and at
+ * least 64; BT >= 1. workspace: rnn_input_proj_workspace_size() bytes (its
+ * first 256 bytes hold the status word that rnn_check_status reads).
+ * Errors: RNN_EINVAL, RNN_ENOSPC, RNN_ECUDA.
+ */
+size_t rnn_input_proj_workspace_size(int BT, int I, int C); /* 0 for invalid sizes */
+int rnn_input_proj_fwd(int BT, int I, int C, const void *x, const void *W, const void *bias, void *Wx,
+                       void *workspace, size_t ws_bytes, void *stream);
+/* Backward of rnn_input_proj_fwd given dWx [BT][C]: dx [BT][I] = dWx W_x,
+ * dW [C][I] = dWx^T x, dbias [C] = column sums of dWx; each output may be
+ * NULL when not wanted. Same conventions and errors as the forward. */
+int rnn_input_proj_bwd(int BT, int I, int C, const void *x, const void *W, const void *dWx, void *dx, void *dW,
+                       void *dbias, void *workspace, size_t ws_bytes, void *stream);
+
 /* Latency floor of the cluster exchange (a measurement aid). Runs a kernel
  * whose steps hold only the h exchange of the forward cluster kernel: every
  * CTA of one cluster of C CTAs (1 .. 16) stages a slice of slice_bytes

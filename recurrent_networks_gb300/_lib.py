@@ -65,6 +65,10 @@ def load(path: str | None = None):
             lib.rnn_trace.argtypes = [vp, i, i]
             lib.rnn_debug_inject_wait.argtypes = [i, ctypes.c_ulonglong]
             lib.rnn_exchange_floor.argtypes = [i, i, i, vp, vp]
+            lib.rnn_input_proj_workspace_size.argtypes = [i, i, i]
+            lib.rnn_input_proj_workspace_size.restype = sz
+            lib.rnn_input_proj_fwd.argtypes = [i, i, i] + [vp] * 5 + [sz, vp]
+            lib.rnn_input_proj_bwd.argtypes = [i, i, i] + [vp] * 7 + [sz, vp]
             _lib = lib
     return _lib
 
@@ -182,3 +186,21 @@ def rnn_exchange_floor(C: int, slice_bytes: int, steps: int, out, stream=None) -
     tensor of >= 2 int64: cycles per step of CTA 0, then the status."""
     return _check(load().rnn_exchange_floor(int(C), int(slice_bytes), int(steps), _p(out), _stream(stream)),
                   "rnn_exchange_floor")
+
+
+def rnn_input_proj_workspace_size(BT: int, I: int, C: int) -> int:
+    return int(load().rnn_input_proj_workspace_size(int(BT), int(I), int(C)))
+
+
+def rnn_input_proj_fwd(BT: int, I: int, C: int, x, W, bias, Wx, workspace, stream=None) -> int:
+    """Wx[BT][C] = x[BT][I] W_x[C][I]^T (+ bias[C]) on the tensor cores (bf16)."""
+    rc = load().rnn_input_proj_fwd(int(BT), int(I), int(C), _p(x), _p(W), _p(bias), _p(Wx), _p(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream))
+    return _check(rc, "rnn_input_proj_fwd")
+
+
+def rnn_input_proj_bwd(BT: int, I: int, C: int, x, W, dWx, dx, dW, dbias, workspace, stream=None) -> int:
+    """dx = dWx W_x, dW = dWx^T x, dbias = column sums of dWx (each may be None)."""
+    rc = load().rnn_input_proj_bwd(int(BT), int(I), int(C), _p(x), _p(W), _p(dWx), _p(dx), _p(dW), _p(dbias),
+                                   _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    return _check(rc, "rnn_input_proj_bwd")

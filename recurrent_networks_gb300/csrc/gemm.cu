@@ -1,0 +1,338 @@
+// Input projection of the scan on the 5th-generation tensor cores.
+//
+// developnotes "deep learning operators", section 5.3 LSTM (MyLSTM.forward)
+// computes the input branch of every gate as x_t W_ih^T + b_ih before adding
+// the recurrent branch; the FlashRNN announcement's flashrnn() takes that
+// product, Wx, as its input. These kernels compute it for a whole sequence at
+// once, with W_x in the weight_ih layout [C][I] (C = G N D output columns in
+// the order of Wx's last three axes):
+//   forward   Wx[m, c]  = sum_i x[m, i] W_x[c, i] (+ bias[c])   m = (b, t), K = I
+//   backward  dx[m, i]  = sum_c dWx[m, c] W_x[c, i]              K = C
+//             dW_x[c, i] = sum_m dWx[m, c] x[m, i]               K = B T (split-K)
+//             dbias[c]  = sum_m dWx[m, c]
+// One generic GEMM, D[M][N] = sum_k A(m, k) B(k, n), with either operand stored
+// K-major (k contiguous: rows of 64 k per 128-byte TMA box) or MN-major (m / n
+// contiguous: boxes of 64 m / n by 64 k), both 128-byte swizzled, in the
+// canonical layouts tcgen05 reads; 128 x 128 tiles, a 4-stage TMA / mbarrier
+// ring, the fp32 accumulator in tensor memory. The roles are those of the
+// weight-gradient kernel: thread 0 loads, thread 32 issues the MMAs, four warps
+// drain the accumulator.
+#include <stdio.h>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+#include "rnn.h"
+
+namespace rnn {
+
+namespace {
+
+constexpr int GM_TILE = 128, GM_BK = 64, GM_STAGES = 4;
+constexpr int GM_HALF = 64 * 128;                 // a 64 x 64 bf16 box
+constexpr int GM_OPERAND = 2 * GM_HALF;           // one operand's k-chunk of a tile
+constexpr int GM_STAGE = 2 * GM_OPERAND;
+constexpr int GM_SMEM = GM_STAGES * GM_STAGE + 1024 + 256;
+
+// K-major (128-byte swizzle): 8-row groups 1 KB apart, a 16-element k step is
+// 32 bytes further along the 128-byte row. MN-major: the two 64-wide halves of
+// the tile 8 KB apart, 8-row k groups 1 KB apart, a 16-row k step is 2 KB.
+__device__ __forceinline__ uint64_t gm_desc(uint32_t base, bool kmajor, int k16) {
+  const uint32_t addr = base + (uint32_t)(kmajor ? k16 * 32 : k16 * 2048);
+  const uint32_t lbo = kmajor ? 16u : (uint32_t)GM_HALF;
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+
+struct GemmArgs {
+  int M, N, K;
+  int splits, kps;          // k-chunks of 64 per split
+  __nv_bfloat16* C;         // [M][N] bf16 (splits == 1)
+  float* partial;           // [splits][M][N] fp32 (splits > 1)
+  const __nv_bfloat16* bias;  // [N] or null (splits == 1 only)
+  unsigned int* status;
+  unsigned long long wait_limit_ns;
+};
+
+template <bool AK, bool BK>
+__global__ void __launch_bounds__(128, 1)
+    gemm_umma_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap, GemmArgs a) {
+  extern __shared__ unsigned char gm_raw[];
+  unsigned char* sm = (unsigned char*)(((uintptr_t)gm_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(sm + GM_STAGES * GM_STAGE);
+  uint32_t* tslot = (uint32_t*)(bars + 2 * GM_STAGES + 1);
+  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[GM_STAGES]), accb = smem_u32(&bars[2 * GM_STAGES]);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n0 = blockIdx.x * GM_TILE, m0 = blockIdx.y * GM_TILE, split = blockIdx.z;
+  const int nchunk = (a.K + GM_BK - 1) / GM_BK;
+  const int c0 = split * a.kps, nq = min(nchunk, c0 + a.kps) - c0;
+
+  if (tid == 0) {
+    for (int s = 0; s < GM_STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(accb, 1);
+    fence_mbar_init_cluster();
+    prefetch_tensormap(&amap);
+    prefetch_tensormap(&bmap);
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" ::"r"(smem_u32(tslot)) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tslot;
+  bool failed = false;
+  int nissued = 0;
+
+  if (tid == 0) {  // ---- TMA producer
+    for (int it = 0; it < nq; ++it) {
+      const int s = it % GM_STAGES;
+      if (it >= GM_STAGES &&
+          !mbar_wait_bounded<false>(empty0 + 8 * s, ((it / GM_STAGES) - 1) & 1, a.wait_limit_ns, a.status, failed))
+        break;
+      nissued = it + 1;
+      const uint32_t fb = full0 + 8 * s;
+      unsigned char* As = sm + (size_t)s * GM_STAGE;
+      unsigned char* Bs = As + GM_OPERAND;
+      const int k0 = (c0 + it) * GM_BK;
+      mbar_arrive_expect_tx(fb, GM_STAGE);
+      if constexpr (AK) {  // rows m0 .. m0+127, k0 .. k0+63
+        tma_load_5d(smem_u32(As), &amap, fb, k0, m0, 0, 0, 0);
+      } else {             // two 64-wide m halves, k rows k0 .. k0+63
+        tma_load_5d(smem_u32(As), &amap, fb, m0, k0, 0, 0, 0);
+        tma_load_5d(smem_u32(As + GM_HALF), &amap, fb, m0 + 64, k0, 0, 0, 0);
+      }
+      if constexpr (BK) {
+        tma_load_5d(smem_u32(Bs), &bmap, fb, k0, n0, 0, 0, 0);
+      } else {
+        tma_load_5d(smem_u32(Bs), &bmap, fb, n0, k0, 0, 0, 0);
+        tma_load_5d(smem_u32(Bs + GM_HALF), &bmap, fb, n0 + 64, k0, 0, 0, 0);
+      }
+    }
+  } else if (tid == 32) {  // ---- MMA issuer
+    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((AK ? 0u : 1u) << 15) | ((BK ? 0u : 1u) << 16) |
+                           ((uint32_t)(GM_TILE >> 3) << 17) | ((uint32_t)(GM_TILE >> 4) << 24);
+    for (int it = 0; it < nq; ++it) {
+      const int s = it % GM_STAGES;
+      mbar_wait_bounded<false>(full0 + 8 * s, (it / GM_STAGES) & 1, a.wait_limit_ns, a.status, failed);
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t As = smem_u32(sm + (size_t)s * GM_STAGE), Bs = As + GM_OPERAND;
+      if (!failed) {
+#pragma unroll
+        for (int k = 0; k < GM_BK / 16; ++k) {
+          const uint64_t ad = gm_desc(As, AK, k), bd = gm_desc(Bs, BK, k);
+          const uint32_t acc = (it | k) ? 1u : 0u;
+          asm volatile(
+              "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+              " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem),
+              "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
+              : "memory");
+        }
+      }
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(empty0 + 8 * s)
+                   : "memory");
+    }
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(accb) : "memory");
+  }
+
+  mbar_wait_bounded<false>(accb, 0, a.wait_limit_ns, a.status, failed);
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const int m = m0 + warp * 32 + lane;  // TMEM lane = tile row
+  for (int cc = 0; cc < GM_TILE; cc += 32) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)cc));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    if (m >= a.M || failed) continue;
+    const int n = n0 + cc;
+    if (a.splits == 1) {
+      __nv_bfloat16* out = a.C + (size_t)m * a.N + n;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        if (n + c < a.N) {
+          float v = __uint_as_float(r[c]);
+          if (a.bias) v += __bfloat162float(a.bias[n + c]);
+          out[c] = __float2bfloat16_rn(v);
+        }
+      }
+    } else {
+      float* out = a.partial + ((size_t)split * a.M + m) * a.N + n;
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (n + c < a.N) out[c] = __uint_as_float(r[c]);
+    }
+  }
+  if (tid == 0 && failed) {
+    for (int it = nissued - GM_STAGES > 0 ? nissued - GM_STAGES : 0; it < nissued; ++it) {
+      bool f2 = false;
+      mbar_wait_bounded<false>(full0 + 8 * (it % GM_STAGES), (it / GM_STAGES) & 1, a.wait_limit_ns, nullptr, f2);
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(tmem) : "memory");
+}
+
+// Sum of the split-K partials in a fixed order, rounded to bf16.
+__global__ void gemm_reduce_kernel(const float* partial, __nv_bfloat16* C, size_t MN, int splits) {
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < MN; e += (size_t)gridDim.x * blockDim.x) {
+    float s = 0.0f;
+    for (int k = 0; k < splits; ++k) s += partial[(size_t)k * MN + e];
+    C[e] = __float2bfloat16_rn(s);
+  }
+}
+
+// Column sums of a [rows][cols] bf16 matrix (dbias = sum over m of dWx[m, c]).
+__global__ void colsum_kernel(const __nv_bfloat16* X, __nv_bfloat16* out, int rows, int cols) {
+  __shared__ float part[32][33];
+  const int c = blockIdx.x * 32 + (threadIdx.x & 31), ks = threadIdx.x >> 5;
+  float s = 0.0f;
+  if (c < cols)
+    for (int r = ks; r < rows; r += 32) s += __bfloat162float(X[(size_t)r * cols + c]);
+  part[ks][threadIdx.x & 31] = s;
+  __syncthreads();
+  if (ks == 0 && c < cols) {
+    float tot = 0.0f;
+    for (int q = 0; q < 32; ++q) tot += part[q][threadIdx.x & 31];
+    out[c] = __float2bfloat16_rn(tot);
+  }
+}
+
+// D[M][N] = A(m, k) B(k, n); a_kmajor: A stored [M][K] (else [K][M]); b_kmajor:
+// B stored [N][K] (else [K][N]).
+cudaError_t gemm_run(bool a_kmajor, bool b_kmajor, int M, int N, int K, const void* A, const void* B,
+                     const void* bias, void* C, float* scratch, size_t scratch_bytes, unsigned int* status,
+                     cudaStream_t st) {
+  CUtensorMap am, bm;
+  cudaError_t e;
+  {
+    const unsigned long long dims_k[5] = {(unsigned long long)K, (unsigned long long)M, 1, 1, 1};
+    const unsigned long long dims_m[5] = {(unsigned long long)M, (unsigned long long)K, 1, 1, 1};
+    const unsigned int box_k[5] = {64, 128, 1, 1, 1}, box_m[5] = {64, 64, 1, 1, 1};
+    e = encode_tensor_map_sw128(&am, A, 5, a_kmajor ? dims_k : dims_m, a_kmajor ? box_k : box_m);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const unsigned long long dims_k[5] = {(unsigned long long)K, (unsigned long long)N, 1, 1, 1};
+    const unsigned long long dims_n[5] = {(unsigned long long)N, (unsigned long long)K, 1, 1, 1};
+    const unsigned int box_k[5] = {64, 128, 1, 1, 1}, box_n[5] = {64, 64, 1, 1, 1};
+    e = encode_tensor_map_sw128(&bm, B, 5, b_kmajor ? dims_k : dims_n, b_kmajor ? box_k : box_n);
+    if (e != cudaSuccess) return e;
+  }
+  const int tiles = ((M + GM_TILE - 1) / GM_TILE) * ((N + GM_TILE - 1) / GM_TILE);
+  const int nchunk = (K + GM_BK - 1) / GM_BK;
+  int splits = (152 + tiles - 1) / tiles;
+  if (splits > nchunk / 2) splits = nchunk / 2;
+  if (splits > 32) splits = 32;
+  if (splits < 1) splits = 1;
+  if (splits > 1 && (bias || !scratch || scratch_bytes < (size_t)splits * M * N * sizeof(float))) splits = 1;
+  GemmArgs g{};
+  g.M = M; g.N = N; g.K = K;
+  g.kps = (nchunk + splits - 1) / splits;
+  g.splits = (nchunk + g.kps - 1) / g.kps;
+  g.C = (__nv_bfloat16*)C;
+  g.partial = scratch;
+  g.bias = (const __nv_bfloat16*)bias;
+  g.status = status;
+  g.wait_limit_ns = 2000000000ull;
+  void (*k)(const CUtensorMap, const CUtensorMap, GemmArgs) =
+      a_kmajor ? (b_kmajor ? gemm_umma_kernel<true, true> : gemm_umma_kernel<true, false>)
+               : (b_kmajor ? gemm_umma_kernel<false, true> : gemm_umma_kernel<false, false>);
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((N + GM_TILE - 1) / GM_TILE, (M + GM_TILE - 1) / GM_TILE, g.splits);
+  k<<<grid, 128, GM_SMEM, st>>>(am, bm, g);
+  note_launch();
+  if (g.splits > 1) {
+    gemm_reduce_kernel<<<2 * 152, 256, 0, st>>>(scratch, (__nv_bfloat16*)C, (size_t)M * N, g.splits);
+    note_launch();
+  }
+  return cudaGetLastError();
+}
+
+int proj_splits_bound(int M, int N, int K) {
+  const int tiles = ((M + GM_TILE - 1) / GM_TILE) * ((N + GM_TILE - 1) / GM_TILE);
+  const int nchunk = (K + GM_BK - 1) / GM_BK;
+  int splits = (152 + tiles - 1) / tiles;
+  if (splits > nchunk / 2) splits = nchunk / 2;
+  if (splits > 32) splits = 32;
+  return splits < 1 ? 1 : splits;
+}
+
+bool proj_dims_ok(int BT, int I, int C) {
+  // TMA: 16-byte row strides (I, C multiples of 8); boxes of 64 along I and C
+  return BT >= 1 && I >= 64 && C >= 64 && I % 8 == 0 && C % 8 == 0;
+}
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return RNN_OK;
+  fprintf(stderr, "librnn_gb300: CUDA error: %s\n", cudaGetErrorString(e));
+  return RNN_ECUDA;
+}
+
+bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace
+
+}  // namespace rnn
+
+using namespace rnn;
+
+extern "C" {
+
+size_t rnn_input_proj_workspace_size(int BT, int I, int C) {
+  if (!proj_dims_ok(BT, I, C)) return 0;
+  const int s = proj_splits_bound(C, I, BT);  // dW_x: M = C, N = I, K = B T
+  return 256 + (s > 1 ? (size_t)s * C * I * sizeof(float) : 0);
+}
+
+int rnn_input_proj_fwd(int BT, int I, int C, const void* x, const void* W, const void* bias, void* Wx,
+                       void* workspace, size_t ws_bytes, void* stream) {
+  if (!proj_dims_ok(BT, I, C) || !x || !W || !Wx || !workspace) return RNN_EINVAL;
+  if (!al16(x) || !al16(W) || !al16(Wx) || !al16(workspace) || (bias && !al16(bias))) return RNN_EINVAL;
+  if (ws_bytes < rnn_input_proj_workspace_size(BT, I, C)) return RNN_ENOSPC;
+  cudaStream_t st = (cudaStream_t)stream;
+  int rc = cuda_status(cudaMemsetAsync(workspace, 0, 256, st));
+  if (rc) return rc;
+  // Wx[m, c] = x[m, :] . W_x[c, :]: A = x [BT][I] (K-major), B = W_x [C][I] (K-major)
+  return cuda_status(gemm_run(true, true, BT, C, I, x, W, bias, Wx, nullptr, 0, (unsigned int*)workspace, st));
+}
+
+int rnn_input_proj_bwd(int BT, int I, int C, const void* x, const void* W, const void* dWx, void* dx, void* dW,
+                       void* dbias, void* workspace, size_t ws_bytes, void* stream) {
+  if (!proj_dims_ok(BT, I, C) || !x || !W || !dWx || !workspace) return RNN_EINVAL;
+  const void* ptrs[] = {x, W, dWx, dx, dW, dbias, workspace};
+  for (const void* p : ptrs)
+    if (p && !al16(p)) return RNN_EINVAL;
+  if (ws_bytes < rnn_input_proj_workspace_size(BT, I, C)) return RNN_ENOSPC;
+  cudaStream_t st = (cudaStream_t)stream;
+  int rc = cuda_status(cudaMemsetAsync(workspace, 0, 256, st));
+  if (rc) return rc;
+  unsigned int* status = (unsigned int*)workspace;
+  if (dx) {  // dx[m, i] = dWx[m, :] . W_x[:, i]: A = dWx [BT][C] (K-major), B = W_x [C][I] (MN-major)
+    rc = cuda_status(gemm_run(true, false, BT, I, C, dWx, W, nullptr, dx, nullptr, 0, status, st));
+    if (rc) return rc;
+  }
+  if (dW) {  // dW_x[c, i] = sum_m dWx[m, c] x[m, i]: A = dWx (MN-major), B = x [BT][I] (MN-major)
+    float* scratch = (float*)((char*)workspace + 256);
+    rc = cuda_status(gemm_run(false, false, C, I, BT, dWx, x, nullptr, dW, scratch, ws_bytes - 256, status, st));
+    if (rc) return rc;
+  }
+  if (dbias) {
+    colsum_kernel<<<(C + 31) / 32, 1024, 0, st>>>((const __nv_bfloat16*)dWx, (__nv_bfloat16*)dbias, BT, C);
+    note_launch();
+    rc = cuda_status(cudaGetLastError());
+  }
+  return rc;
+}
+
+}  // extern "C"

@@ -335,3 +335,47 @@ def test_bf16_operand_mode_against_torch_autograd(fn):
     np.testing.assert_allclose(ds0[0, :, 0, 0], h0.grad.numpy(), rtol=1e-10, atol=1e-12)
     if fn == "lstm":
         np.testing.assert_allclose(ds0[1, :, 0, 0], c0.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+# ------------------------------------------------------- input projection oracle
+def test_projection_matches_torch_linear_and_autograd():
+    """The projection oracle against torch.nn.functional.linear in float64 and
+    its autograd gradients (a library routine, not a retyped formula)."""
+    from oracle import projection
+    g = torch.Generator().manual_seed(11)
+    x = torch.randn(37, 24, generator=g, dtype=torch.float64, requires_grad=True)
+    W = torch.randn(40, 24, generator=g, dtype=torch.float64, requires_grad=True)
+    bias = torch.randn(40, generator=g, dtype=torch.float64, requires_grad=True)
+    dy = torch.randn(37, 40, generator=g, dtype=torch.float64)
+    y = torch.nn.functional.linear(x, W, bias)
+    y.backward(dy)
+    np.testing.assert_allclose(projection.fwd(x, W, bias), y.detach().numpy(), rtol=1e-12, atol=1e-12)
+    dx, dW, db = projection.bwd(x, W, dy)
+    np.testing.assert_allclose(dx, x.grad.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dW, W.grad.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(db, bias.grad.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_projection_then_scan_is_torch_lstm_with_input_weights():
+    """Projection followed by the scan oracle equals torch.nn.LSTM with
+    input_size = I: weight_ih = W_x, bias_ih = projection bias, weight_hh =
+    the stacked R[g]^T blocks, bias_hh = b (one head)."""
+    from oracle import oracle, projection
+    B, T, I, D = 3, 7, 5, 4
+    g = torch.Generator().manual_seed(12)
+    x = torch.randn(B, T, I, generator=g, dtype=torch.float64)
+    W = torch.randn(4 * D, I, generator=g, dtype=torch.float64)
+    bias_x = torch.randn(4 * D, generator=g, dtype=torch.float64)
+    R = torch.randn(4, 1, D, D, generator=g, dtype=torch.float64) / 2
+    b = torch.randn(4, 1, D, generator=g, dtype=torch.float64)
+    s0 = torch.randn(2, B, 1, 1, D, generator=g, dtype=torch.float64)
+    Wx = projection.fwd(x.reshape(B * T, I), W, bias_x).reshape(B, T, 4, 1, D)
+    st, _ = oracle.fwd("lstm", Wx, R.numpy(), b.numpy(), s0.numpy())
+    lstm = torch.nn.LSTM(I, D, batch_first=True).double()
+    with torch.no_grad():
+        lstm.weight_ih_l0.copy_(W)
+        lstm.bias_ih_l0.copy_(bias_x)
+        lstm.weight_hh_l0.copy_(torch.cat([R[k, 0].t() for k in range(4)], dim=0))
+        lstm.bias_hh_l0.copy_(b[:, 0].reshape(-1))
+        out, _ = lstm(x, (s0[0, :, 0, 0][None], s0[1, :, 0, 0][None]))
+    np.testing.assert_allclose(st[0, :, :, 0, :], out.numpy(), rtol=1e-10, atol=1e-12)
