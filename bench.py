@@ -45,10 +45,63 @@ def parse():
     ap.add_argument("--path", default="auto", choices=["auto", "fused", "alternating", "simt", "grid"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--input-proj", action="store_true",
+                    help="time the tensor-core input projection (Wx = x W_x^T, I = N*D, and its backward) "
+                         "on the workload's B*T rows instead of the scan")
     ap.add_argument("--trace", action="store_true",
                     help="print the per-phase cycle medians of the persistent scan kernels (rnn_trace) "
                          "instead of the bench line")
     return ap.parse_args()
+
+
+def proj_bench(args, w, fn, dev, _lib):
+    """The input projection of one layer of the workload: x [B*T, I = N*D] ->
+    Wx [B*T, G*N*D], and its backward (dx, dW_x, dbias), timed with CUDA
+    events, the L2 flushed before every step outside the event window."""
+    B, T, N, D = w["B"], w["T"], w["N"], w["D"]
+    G = {"lstm": 4, "gru": 3, "elman": 1, "slstm": 4}[fn]
+    BT, I, C = B * T, N * D, G * N * D
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn(BT, I, generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn(C, I, generator=g) / I ** 0.5).to(torch.bfloat16).to(dev)
+    bias = torch.randn(C, generator=g).to(torch.bfloat16).to(dev)
+    dWx = torch.randn(BT, C, generator=g).to(torch.bfloat16).to(dev)
+    Wx, dx, dW, db = (torch.empty(s, dtype=torch.bfloat16, device=dev) for s in ((BT, C), (BT, I), (C, I), (C,)))
+    ws = torch.empty(_lib.rnn_input_proj_workspace_size(BT, I, C), dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    fwd = lambda: _lib.rnn_input_proj_fwd(BT, I, C, x, W, bias, Wx, ws)
+    bwd = lambda: _lib.rnn_input_proj_bwd(BT, I, C, x, W, dWx, dx, dW, db, ws)
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    tf, tb = [], []
+    for _ in range(args.steps):
+        flush.zero_()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        fwd()
+        e[1].record()
+        bwd()
+        e[2].record()
+        torch.cuda.synchronize()
+        tf.append(e[0].elapsed_time(e[1]))
+        tb.append(e[1].elapsed_time(e[2]))
+    _lib.rnn_check_status(ws)
+    pk = peaks()
+    f_fl, b_fl = 2.0 * BT * I * C, 4.0 * BT * I * C
+    f_ms, b_ms = statistics.median(tf), statistics.median(tb)
+    ach = (f_fl + b_fl) / ((f_ms + b_ms) / 1e3) / 1e12
+    return {"metric": "input projection TFLOP/s (forward + backward)", "value": ach, "unit": "TFLOP/s",
+            "higher_is_better": True, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w["name"], "rows": BT, "I": I, "C": C,
+                       "l2": "flushed (256 MiB write) before every step, outside the event window"},
+            "fwd": {"ms": f_ms, "tflops": f_fl / (f_ms / 1e3) / 1e12},
+            "bwd": {"ms": b_ms, "tflops": b_fl / (b_ms / 1e3) / 1e12},
+            "roofline": {"bound": "tensor", "achieved": ach, "peak": pk["bf16"], "unit": "TFLOP/s",
+                         "frac": ach / pk["bf16"], "traffic": None,
+                         "peak_source": f"{pk['source']} (MEASURED_PEAKS.json, burst)"}}
 
 
 def phase_trace(step_fn, backward, T):
@@ -274,6 +327,10 @@ def main():
     from recurrent_networks_gb300 import _lib
     from recurrent_networks_gb300.synth import workload_inputs
     _lib.load()
+    if args.input_proj:
+        if rank == 0:
+            print(json.dumps(proj_bench(args, w, fn, dev, _lib)), flush=True)
+        return
     dtype = w["dtype"]
     esize = 2 if dtype == torch.bfloat16 else 4
     B, T, N, D = w["B"], w["T"], w["N"], w["D"]

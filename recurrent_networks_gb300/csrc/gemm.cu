@@ -156,19 +156,47 @@ __global__ void __launch_bounds__(128, 1)
     const int n = n0 + cc;
     if (a.splits == 1) {
       __nv_bfloat16* out = a.C + (size_t)m * a.N + n;
+      if (n + 32 <= a.N) {  // 16-byte stores (N is a multiple of 8)
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        if (n + c < a.N) {
-          float v = __uint_as_float(r[c]);
-          if (a.bias) v += __bfloat162float(a.bias[n + c]);
-          out[c] = __float2bfloat16_rn(v);
+        for (int v = 0; v < 4; ++v) {
+          float f[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(r[8 * v + q]);
+          if (a.bias) {
+            const uint4 bb = *(const uint4*)(a.bias + n + 8 * v);
+            const __nv_bfloat16* bh = (const __nv_bfloat16*)&bb;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) f[q] += __bfloat162float(bh[q]);
+          }
+          uint4 w;
+          w.x = pack_bf16(__float2bfloat16_rn(f[0]), __float2bfloat16_rn(f[1]));
+          w.y = pack_bf16(__float2bfloat16_rn(f[2]), __float2bfloat16_rn(f[3]));
+          w.z = pack_bf16(__float2bfloat16_rn(f[4]), __float2bfloat16_rn(f[5]));
+          w.w = pack_bf16(__float2bfloat16_rn(f[6]), __float2bfloat16_rn(f[7]));
+          *(uint4*)(out + 8 * v) = w;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          if (n + c < a.N) {
+            float v = __uint_as_float(r[c]);
+            if (a.bias) v += __bfloat162float(a.bias[n + c]);
+            out[c] = __float2bfloat16_rn(v);
+          }
         }
       }
     } else {
       float* out = a.partial + ((size_t)split * a.M + m) * a.N + n;
+      if (n + 32 <= a.N) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        if (n + c < a.N) out[c] = __uint_as_float(r[c]);
+        for (int v = 0; v < 8; ++v)
+          *(float4*)(out + 4 * v) = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                                __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (n + c < a.N) out[c] = __uint_as_float(r[c]);
+      }
     }
   }
   if (tid == 0 && failed) {
