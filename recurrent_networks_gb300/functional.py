@@ -73,3 +73,62 @@ def flashrnn(Wx, R, b, states=None, function: str = "lstm", backend: str = "auto
     if not Wx.is_cuda:
         raise RuntimeError("flashrnn runs on CUDA tensors only (there is no CPU path)")
     return _ScanFn.apply(Wx, R, b, states, function, backend)
+
+
+class _ProjFn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, W, bias):
+        BT, I = x.shape
+        C = W.shape[0]
+        x, W = x.contiguous(), W.contiguous()
+        bias = bias.contiguous() if bias is not None else None
+        Wx = torch.empty((BT, C), dtype=x.dtype, device=x.device)
+        ws = torch.empty(_lib.rnn_input_proj_workspace_size(BT, I, C), dtype=torch.uint8, device=x.device)
+        _lib.rnn_input_proj_fwd(BT, I, C, x, W, bias, Wx, ws)
+        ctx.has_bias = bias is not None
+        ctx.save_for_backward(x, W)
+        return Wx
+
+    @staticmethod
+    def backward(ctx, dWx):
+        x, W = ctx.saved_tensors
+        BT, I = x.shape
+        C = W.shape[0]
+        dWx = dWx.contiguous()
+        dx = torch.empty_like(x) if ctx.needs_input_grad[0] else None
+        dW = torch.empty_like(W) if ctx.needs_input_grad[1] else None
+        db = torch.empty((C,), dtype=x.dtype, device=x.device) if (ctx.has_bias and ctx.needs_input_grad[2]) else None
+        ws = torch.empty(_lib.rnn_input_proj_workspace_size(BT, I, C), dtype=torch.uint8, device=x.device)
+        _lib.rnn_input_proj_bwd(BT, I, C, x, W, dWx, dx, dW, db, ws)
+        return dx, dW, db
+
+
+def input_projection(x, W, bias=None):
+    """Wx = x W^T (+ bias) on the tensor cores: x [..., I], W [C, I] (the
+    weight_ih layout), bias [C] or None; returns [..., C]. bf16, CUDA only."""
+    if not x.is_cuda:
+        raise RuntimeError("input_projection runs on CUDA tensors only (there is no CPU path)")
+    lead = x.shape[:-1]
+    y = _ProjFn.apply(x.reshape(-1, x.shape[-1]), W, bias)
+    return y.reshape(*lead, W.shape[0])
+
+
+def flashrnn_stack(x, layers, function: str = "lstm", backend: str = "auto"):
+    """Stacked layers: layer l projects its input (x for l = 0, the previous
+    layer's h, [B, T, N*D], otherwise) with W_x [G*N*D, I_l] (+ bias_x) and
+    runs the head-wise scan with R, b and initial states (or zeros).
+    layers: sequence of dicts with keys W_x, bias_x (optional), R, b, states
+    (optional). Returns (h of the last layer [B, T, N*D], [(states, last) of
+    every layer]). Differentiable end to end (autograd chains the kernels'
+    backward passes)."""
+    B, T = x.shape[0], x.shape[1]
+    h = x
+    outs = []
+    for layer in layers:
+        R = layer["R"]
+        G, N, D = R.shape[0], R.shape[1], R.shape[2]
+        Wx = input_projection(h, layer["W_x"], layer.get("bias_x")).reshape(B, T, G, N, D)
+        states, last = flashrnn(Wx, R, layer["b"], layer.get("states"), function, backend)
+        outs.append((states, last))
+        h = states[0].reshape(B, T, N * D)
+    return h, outs

@@ -379,3 +379,50 @@ def test_projection_then_scan_is_torch_lstm_with_input_weights():
         lstm.bias_hh_l0.copy_(b[:, 0].reshape(-1))
         out, _ = lstm(x, (s0[0, :, 0, 0][None], s0[1, :, 0, 0][None]))
     np.testing.assert_allclose(st[0, :, :, 0, :], out.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_stack_oracle_matches_two_layer_torch_lstm():
+    """The chained oracle (projection then scan, per layer, and its backward
+    through both layers) against torch.nn.LSTM(num_layers=2) in float64:
+    outputs and every gradient by autograd."""
+    from oracle import stack
+    B, T, I, D = 2, 6, 5, 4
+    g = torch.Generator().manual_seed(21)
+    x = torch.randn(B, T, I, generator=g, dtype=torch.float64, requires_grad=True)
+    layers, torch_w = [], []
+    for l in range(2):
+        Il = I if l == 0 else D
+        W = torch.randn(4 * D, Il, generator=g, dtype=torch.float64)
+        bx = torch.randn(4 * D, generator=g, dtype=torch.float64)
+        R = torch.randn(4, 1, D, D, generator=g, dtype=torch.float64) / 2
+        b = torch.randn(4, 1, D, generator=g, dtype=torch.float64)
+        s0 = torch.randn(2, B, 1, 1, D, generator=g, dtype=torch.float64)
+        layers.append(dict(W_x=W.numpy(), bias_x=bx.numpy(), R=R.numpy(), b=b.numpy(), states=s0.numpy()))
+        torch_w.append((W, bx, R, b, s0))
+    lstm = torch.nn.LSTM(I, D, num_layers=2, batch_first=True).double()
+    with torch.no_grad():
+        for l, (W, bx, R, b, s0) in enumerate(torch_w):
+            getattr(lstm, f"weight_ih_l{l}").copy_(W)
+            getattr(lstm, f"bias_ih_l{l}").copy_(bx)
+            getattr(lstm, f"weight_hh_l{l}").copy_(torch.cat([R[k, 0].t() for k in range(4)], dim=0))
+            getattr(lstm, f"bias_hh_l{l}").copy_(b[:, 0].reshape(-1))
+    h0 = torch.stack([w[4][0, :, 0, 0] for w in torch_w]).clone().requires_grad_(True)
+    c0 = torch.stack([w[4][1, :, 0, 0] for w in torch_w]).clone().requires_grad_(True)
+    out, _ = lstm(x, (h0, c0))
+    dh = torch.randn(B, T, D, generator=g, dtype=torch.float64)
+    out.backward(dh)
+    h, _, _ = stack.fwd("lstm", x.detach().numpy(), layers)
+    np.testing.assert_allclose(h, out.detach().numpy(), rtol=1e-10, atol=1e-12)
+    dx, grads = stack.bwd("lstm", x.detach().numpy(), layers, dh.numpy())
+    np.testing.assert_allclose(dx, x.grad.numpy(), rtol=1e-9, atol=1e-11)
+    for l in range(2):
+        gw = grads[l]
+        np.testing.assert_allclose(gw["W_x"], getattr(lstm, f"weight_ih_l{l}").grad.numpy(), rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(gw["bias_x"], getattr(lstm, f"bias_ih_l{l}").grad.numpy(), rtol=1e-9, atol=1e-11)
+        whh = getattr(lstm, f"weight_hh_l{l}").grad.numpy()  # rows (g, j), columns i  = dR[g][i][j]^T
+        dR_t = np.concatenate([gw["R"][k, 0].T for k in range(4)], axis=0)
+        np.testing.assert_allclose(dR_t, whh, rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(gw["b"][:, 0].reshape(-1), getattr(lstm, f"bias_hh_l{l}").grad.numpy(),
+                                   rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(gw["states"][0, :, 0, 0], h0.grad[l].numpy(), rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(gw["states"][1, :, 0, 0], c0.grad[l].numpy(), rtol=1e-9, atol=1e-11)
