@@ -48,9 +48,11 @@ extern "C" {
 #define RNN_ECUDA 5       /* a CUDA runtime call or launch failed */
 
 /* ---- enumerations ---------------------------------------------------------- */
-typedef enum { RNN_LSTM = 0, RNN_GRU = 1, RNN_ELMAN = 2, RNN_SLSTM = 3 } rnn_function_t;
+typedef enum { RNN_LSTM = 0, RNN_GRU = 1, RNN_ELMAN = 2, RNN_SLSTM = 3, RNN_SLSTM_LOGSIG = 4 } rnn_function_t;
 /* (G, S) = (4, 2) LSTM, (3, 1) GRU, (1, 1) Elman, (4, 4) sLSTM.
- * State order: LSTM h,c; GRU h; Elman h; sLSTM h,c,n,m. */
+ * State order: LSTM h,c; GRU h; Elman h; sLSTM h,c,n,m.
+ * RNN_SLSTM: exponential forget gate, log f = a_f. RNN_SLSTM_LOGSIG: sigmoid
+ * forget gate, log f = log sigmoid(a_f); otherwise identical. */
 typedef enum { RNN_F32 = 0, RNN_BF16 = 1 } rnn_dtype_t;
 typedef enum {
   RNN_PATH_AUTO = 0,        /* the planner picks */

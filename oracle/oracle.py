@@ -24,9 +24,9 @@ _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-FUNCTIONS = {"lstm": 0, "gru": 1, "elman": 2, "slstm": 3}
-GATES = {"lstm": 4, "gru": 3, "elman": 1, "slstm": 4}
-STATES = {"lstm": 2, "gru": 1, "elman": 1, "slstm": 4}
+FUNCTIONS = {"lstm": 0, "gru": 1, "elman": 2, "slstm": 3, "slstm_logsig": 4}
+GATES = {"lstm": 4, "gru": 3, "elman": 1, "slstm": 4, "slstm_logsig": 4}
+STATES = {"lstm": 2, "gru": 1, "elman": 1, "slstm": 4, "slstm_logsig": 4}
 
 
 def build(force: bool = False) -> str:

@@ -22,6 +22,8 @@
  *    m' = max(a_f + m, a_i), i' = exp(a_i - m'), f' = exp(a_f + m - m'),
  *    c' = f' c + i' tanh(a_z), n' = f' n + i', h' = sigmoid(a_o) c'/n'.
  *    At a tie of the max the derivative goes to the a_f + m branch.
+ *  - The sigmoid-forget sLSTM (function 4) is the other reading of that gate:
+ *    log f = log sigmoid(a_f) in place of a_f in every formula above.
  *
  * The backward is back-propagation through time written by hand: the exact
  * derivative of the forward formulas above, step by step in reverse.
@@ -43,6 +45,7 @@ int oracle_num_gates(int fn) {
     case ORACLE_GRU: return 3;
     case ORACLE_ELMAN: return 1;
     case ORACLE_SLSTM: return 4;
+    case ORACLE_SLSTM_LOGSIG: return 4;
   }
   return -1;
 }
@@ -53,11 +56,14 @@ int oracle_num_states(int fn) {
     case ORACLE_GRU: return 1;
     case ORACLE_ELMAN: return 1;
     case ORACLE_SLSTM: return 4;
+    case ORACLE_SLSTM_LOGSIG: return 4;
   }
   return -1;
 }
 
 static double sigmoid(double v) { return 1.0 / (1.0 + exp(-v)); }
+/* log sigmoid(v) = -log(1 + exp(-v)), written so that neither branch overflows */
+static double log_sigmoid(double v) { return (v < 0.0 ? v : 0.0) - log1p(exp(-fabs(v))); }
 
 /* ---- one cell, one unit --------------------------------------------------
  * x[g]   : the input pre-activation Wx[b,t,g,n,j]
@@ -83,13 +89,14 @@ static void cell_fwd(int fn, const double *x, const double *rec,
     sn[0] = (1.0 - z) * nn + z * sp[0];
   } else if (fn == ORACLE_ELMAN) {
     sn[0] = tanh(x[0] + rec[0]);
-  } else { /* ORACLE_SLSTM */
+  } else { /* ORACLE_SLSTM, ORACLE_SLSTM_LOGSIG */
     double ai = x[0] + rec[0], af = x[1] + rec[1];
     double az = x[2] + rec[2], ao = x[3] + rec[3];
     double mp = sp[3];
-    double m = (af + mp >= ai) ? af + mp : ai;
+    double lf = (fn == ORACLE_SLSTM_LOGSIG) ? log_sigmoid(af) : af; /* log f */
+    double m = (lf + mp >= ai) ? lf + mp : ai;
     double ig = exp(ai - m);
-    double fg = exp(af + mp - m);
+    double fg = exp(lf + mp - m);
     double c = fg * sp[1] + ig * tanh(az);
     double n = fg * sp[2] + ig;
     sn[1] = c;
@@ -144,13 +151,14 @@ static void cell_bwd(int fn, const double *x, const double *rec,
     double h = sn[0];
     dx[0] = dsn[0] * (1.0 - h * h);
     drec[0] = dx[0];
-  } else { /* ORACLE_SLSTM */
+  } else { /* ORACLE_SLSTM, ORACLE_SLSTM_LOGSIG */
     double ai = x[0] + rec[0], af = x[1] + rec[1];
     double az = x[2] + rec[2], ao = x[3] + rec[3];
     double cp = sp[1], np = sp[2], mp = sp[3];
     double c = sn[1], n = sn[2], m = sn[3];
+    double lf = (fn == ORACLE_SLSTM_LOGSIG) ? log_sigmoid(af) : af; /* log f */
     double ig = exp(ai - m);
-    double fg = exp(af + mp - m);
+    double fg = exp(lf + mp - m);
     double zt = tanh(az);
     double o = sigmoid(ao);
     double dh = dsn[0];
@@ -163,17 +171,18 @@ static void cell_bwd(int fn, const double *x, const double *rec,
     double dig = dc * zt + dn;
     double dzt = dc * ig;
     double dai = dig * ig;
-    double daf = dfg * fg;
+    double dlf = dfg * fg; /* gradient reaching log f */
     double dmp = dfg * fg;
     dm -= dig * ig + dfg * fg;
-    if (af + mp >= ai) { /* tie goes to the forget branch */
-      daf += dm;
+    if (lf + mp >= ai) { /* tie goes to the forget branch */
+      dlf += dm;
       dmp += dm;
     } else {
       dai += dm;
     }
     dx[0] = dai;
-    dx[1] = daf;
+    /* d log sigmoid(a) / da = sigmoid(-a) */
+    dx[1] = (fn == ORACLE_SLSTM_LOGSIG) ? dlf * sigmoid(-af) : dlf;
     dx[2] = dzt * (1.0 - zt * zt);
     dx[3] = d_o * o * (1.0 - o);
     for (s = 0; s < 4; ++s) drec[s] = dx[s];
@@ -421,7 +430,7 @@ static int run(problem_t *p, int backward, int nthreads) {
 static int setup(problem_t *p, int fn, int B, int T, int N, int D, int flags) {
   memset(p, 0, sizeof(*p));
   p->flags = flags;
-  if (fn < 0 || fn > 3 || B < 0 || T < 0 || N < 0 || D < 0) return -1;
+  if (fn < 0 || fn > 4 || B < 0 || T < 0 || N < 0 || D < 0) return -1;
   p->fn = fn;
   p->B = B;
   p->T = T;

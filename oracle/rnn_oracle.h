@@ -35,7 +35,7 @@
 extern "C" {
 #endif
 
-enum { ORACLE_LSTM = 0, ORACLE_GRU = 1, ORACLE_ELMAN = 2, ORACLE_SLSTM = 3 };
+enum { ORACLE_LSTM = 0, ORACLE_GRU = 1, ORACLE_ELMAN = 2, ORACLE_SLSTM = 3, ORACLE_SLSTM_LOGSIG = 4 };
 
 /* flags: ORACLE_ROUND_BF16 = the bfloat16 storage mode, in which the operands
  * of every recurrent contraction (h_{t-1} in h.R, the recurrent-branch

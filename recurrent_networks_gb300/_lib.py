@@ -13,7 +13,7 @@ import torch
 from . import build as _build
 
 RNN_OK, RNN_EINVAL, RNN_EUNSUPPORTED, RNN_ENOSPC, RNN_ETIMEOUT, RNN_ECUDA = range(6)
-FUNCTIONS = {"lstm": 0, "gru": 1, "elman": 2, "slstm": 3}
+FUNCTIONS = {"lstm": 0, "gru": 1, "elman": 2, "slstm": 3, "slstm_logsig": 4}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 PATHS = {"auto": 0, "fused": 1, "alternating": 2, "simt": 3, "grid": 4}
 WS_FWD, WS_BWD, WS_BWD_RECOMPUTE = 0, 1, 2

@@ -538,6 +538,7 @@ cudaError_t enqueue_any(int fn, const AltArgs& a, bool bwd, cudaStream_t st) {
     case GRU: return enqueue<GRU>(a, bwd, st);
     case ELMAN: return enqueue<ELMAN>(a, bwd, st);
     case SLSTM: return enqueue<SLSTM>(a, bwd, st);
+    case SLSTM_LS: return enqueue<SLSTM_LS>(a, bwd, st);
   }
   return cudaErrorInvalidValue;
 }

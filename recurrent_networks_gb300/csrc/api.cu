@@ -30,7 +30,7 @@ struct Sizes {
 
 static bool dims_ok(const rnn_dims_t* d) {
   return d && d->B >= 1 && d->T >= 0 && d->N >= 1 && d->D >= 1 && d->function >= 0 &&
-         d->function <= 3 && (d->dtype == RNN_F32 || d->dtype == RNN_BF16) && d->path >= 0 &&
+         d->function <= 4 && (d->dtype == RNN_F32 || d->dtype == RNN_BF16) && d->path >= 0 &&
          d->path <= 4 && (size_t)d->B * d->N * d->D < ((size_t)1 << 40);
 }
 
@@ -184,8 +184,8 @@ using namespace rnn;
 
 extern "C" {
 
-int rnn_num_gates(int function) { return function >= 0 && function <= 3 ? fn_gates(function) : -1; }
-int rnn_num_states(int function) { return function >= 0 && function <= 3 ? fn_states(function) : -1; }
+int rnn_num_gates(int function) { return function >= 0 && function <= 4 ? fn_gates(function) : -1; }
+int rnn_num_states(int function) { return function >= 0 && function <= 4 ? fn_states(function) : -1; }
 
 size_t rnn_tape_size(const rnn_dims_t* d) {
   if (!dims_ok(d)) return 0;

@@ -7,26 +7,28 @@
 // sLSTM (i,f,z,o; states h,c,n,m; exponential gates with stabiliser m, log f =
 // a_f; the max's derivative goes to the forget branch on a tie) are the
 // readings the FlashRNN announcement's function list (lstm, gru, elman,
-// slstm) leaves to us.
+// slstm) leaves to us. SLSTM_LS is the other reading of the sLSTM forget
+// gate, a sigmoid: log f = log sigmoid(a_f), the rest unchanged.
 //
 // Tape record of one (t, b, n, unit), fp32, K = G + S (+1 for GRU) values:
 //   LSTM  a_i a_f a_g a_o | h c
 //   GRU   a_r a_z x_n q   | h        (q = rec_n, the recurrent branch of n)
 //   Elman a               | h
-//   sLSTM a_i a_f a_z a_o | h c n m
+//   sLSTM a_i a_f a_z a_o | h c n m   (also the sigmoid-forget sLSTM, SLSTM_LS)
 #pragma once
 #include <cuda_bf16.h>
 #include <stdint.h>
 
 namespace rnn {
 
-enum { LSTM = 0, GRU = 1, ELMAN = 2, SLSTM = 3 };
+enum { LSTM = 0, GRU = 1, ELMAN = 2, SLSTM = 3, SLSTM_LS = 4 };
 
 template <int FN> struct FnInfo;
 template <> struct FnInfo<LSTM> { static constexpr int G = 4, S = 2, P = 4; };
 template <> struct FnInfo<GRU> { static constexpr int G = 3, S = 1, P = 4; };
 template <> struct FnInfo<ELMAN> { static constexpr int G = 1, S = 1, P = 1; };
 template <> struct FnInfo<SLSTM> { static constexpr int G = 4, S = 4, P = 4; };
+template <> struct FnInfo<SLSTM_LS> { static constexpr int G = 4, S = 4, P = 4; };
 // P = number of "pre" values on the tape; tape width K = P + S.
 
 __host__ __device__ constexpr int fn_gates(int fn) { return fn == 0 ? 4 : fn == 1 ? 3 : fn == 2 ? 1 : 4; }
@@ -64,6 +66,13 @@ template <bool FAST> __device__ __forceinline__ float f_exp(float x) {
   if (FAST) return exp2_fast(x * 1.4426950408889634f);
   return expf(x);
 }
+// log sigmoid(x) = min(x, 0) - log(1 + exp(-|x|)), in a form that neither
+// overflows nor cancels; FAST uses the exp / log intrinsics (absolute error
+// ~1e-7, far below the bf16 rounding of the states it feeds).
+template <bool FAST> __device__ __forceinline__ float f_logsigmoid(float x) {
+  if (FAST) return fminf(x, 0.0f) - __logf(1.0f + __expf(-fabsf(x)));
+  return fminf(x, 0.0f) - log1pf(expf(-fabsf(x)));
+}
 
 // ---- forward --------------------------------------------------------------
 // x[g]: Wx pre-activation; r[g]: recurrent branch (h.R + b); sp: previous
@@ -89,10 +98,11 @@ __device__ __forceinline__ void cell_fwd(const float* x, const float* r, const f
     float a = x[0] + r[0];
     sn[0] = f_tanh<FAST>(a);
     pre[0] = a;
-  } else {  // SLSTM
+  } else {  // SLSTM (log f = a_f) and SLSTM_LS (log f = log sigmoid(a_f))
     float ai = x[0] + r[0], af = x[1] + r[1], az = x[2] + r[2], ao = x[3] + r[3];
     float mp = sp[3];
-    float fm = af + mp;
+    const float lf = FN == SLSTM_LS ? f_logsigmoid<FAST>(af) : af;
+    float fm = lf + mp;
     float m = fm >= ai ? fm : ai;
     float ig = f_exp<FAST>(ai - m), fg = f_exp<FAST>(fm - m);
     float c = fmaf(fg, sp[1], ig * f_tanh<FAST>(az));
@@ -141,11 +151,12 @@ __device__ __forceinline__ void cell_bwd(const float* pre, const float* sp, cons
     dx[0] = dsn[0] * (1.0f - h * h);
     dr[0] = dx[0];
     dsp[0] = 0.0f;
-  } else {  // SLSTM
+  } else {  // SLSTM and SLSTM_LS (gradients through log f, then d log f / d a_f)
     float ai = pre[0], af = pre[1], az = pre[2], ao = pre[3];
     float cp = sp[1], np = sp[2], mp = sp[3];
     float c = sn[1], n = sn[2], m = sn[3];
-    float ig = f_exp<FAST>(ai - m), fg = f_exp<FAST>(af + mp - m);
+    const float lf = FN == SLSTM_LS ? f_logsigmoid<FAST>(af) : af;
+    float ig = f_exp<FAST>(ai - m), fg = f_exp<FAST>(lf + mp - m);
     float zt = f_tanh<FAST>(az), o = f_sigmoid<FAST>(ao);
     float dh = dsn[0];
     float rn = 1.0f / n;
@@ -156,10 +167,11 @@ __device__ __forceinline__ void cell_bwd(const float* pre, const float* sp, cons
     float dfg = fmaf(dc, cp, dn * np);
     float dig = fmaf(dc, zt, dn);
     float dai = dig * ig;
-    float daf = dfg * fg;
-    float dmp = daf;
-    float dm = dsn[3] - dai - daf;
-    if (af + mp >= ai) { daf += dm; dmp += dm; } else { dai += dm; }
+    float dlf = dfg * fg;
+    float dmp = dlf;
+    float dm = dsn[3] - dai - dlf;
+    if (lf + mp >= ai) { dlf += dm; dmp += dm; } else { dai += dm; }
+    const float daf = FN == SLSTM_LS ? dlf * f_sigmoid<FAST>(-af) : dlf;
     dx[0] = dai; dx[1] = daf;
     dx[2] = dc * ig * (1.0f - zt * zt);
     dx[3] = dh * y * o * (1.0f - o);

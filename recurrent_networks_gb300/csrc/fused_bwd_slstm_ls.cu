@@ -1,0 +1,6 @@
+// Instantiation of the backward cluster kernels for one cell type.
+#include "fused_bwd.cuh"
+
+namespace rnn {
+template cudaError_t fused_bwd_launch<SLSTM_LS>(const FusedShape&, const FusedArgs&, cudaStream_t);
+}  // namespace rnn

@@ -1,0 +1,6 @@
+// Instantiation of the grid backward kernels for one cell type.
+#include "grid_bwd.cuh"
+
+namespace rnn {
+template cudaError_t grid_bwd_launch<SLSTM_LS>(const FusedShape&, const FusedArgs&, cudaStream_t);
+}  // namespace rnn

@@ -240,6 +240,7 @@ cudaError_t simt_run(int fn, int dtype, const SimtArgs& a, bool bwd, cudaStream_
     RNN_SIMT_CASE(GRU)
     RNN_SIMT_CASE(ELMAN)
     RNN_SIMT_CASE(SLSTM)
+    RNN_SIMT_CASE(SLSTM_LS)
   }
 #undef RNN_SIMT_CASE
   return cudaErrorInvalidValue;

@@ -78,6 +78,7 @@ cudaError_t fused_bwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cuda
     case GRU: return fused_bwd_launch<GRU>(sh, a, st);
     case ELMAN: return fused_bwd_launch<ELMAN>(sh, a, st);
     case SLSTM: return fused_bwd_launch<SLSTM>(sh, a, st);
+    case SLSTM_LS: return fused_bwd_launch<SLSTM_LS>(sh, a, st);
   }
   return cudaErrorInvalidValue;
 }
@@ -88,6 +89,7 @@ cudaError_t fused_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cuda
     case GRU: return fused_fwd_launch<GRU>(sh, a, st);
     case ELMAN: return fused_fwd_launch<ELMAN>(sh, a, st);
     case SLSTM: return fused_fwd_launch<SLSTM>(sh, a, st);
+    case SLSTM_LS: return fused_fwd_launch<SLSTM_LS>(sh, a, st);
   }
   return cudaErrorInvalidValue;
 }
@@ -103,6 +105,7 @@ cudaError_t grid_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaS
     case GRU: return grid_fwd_launch<GRU>(sh, a, st);
     case ELMAN: return grid_fwd_launch<ELMAN>(sh, a, st);
     case SLSTM: return grid_fwd_launch<SLSTM>(sh, a, st);
+    case SLSTM_LS: return grid_fwd_launch<SLSTM_LS>(sh, a, st);
   }
   return cudaErrorInvalidValue;
 }
@@ -113,6 +116,7 @@ cudaError_t grid_bwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaS
     case GRU: return grid_bwd_launch<GRU>(sh, a, st);
     case ELMAN: return grid_bwd_launch<ELMAN>(sh, a, st);
     case SLSTM: return grid_bwd_launch<SLSTM>(sh, a, st);
+    case SLSTM_LS: return grid_bwd_launch<SLSTM_LS>(sh, a, st);
   }
   return cudaErrorInvalidValue;
 }

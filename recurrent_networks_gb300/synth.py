@@ -14,8 +14,8 @@ import math
 
 import torch
 
-GATES = {"lstm": 4, "gru": 3, "elman": 1, "slstm": 4}
-STATES = {"lstm": 2, "gru": 1, "elman": 1, "slstm": 4}
+GATES = {"lstm": 4, "gru": 3, "elman": 1, "slstm": 4, "slstm_logsig": 4}
+STATES = {"lstm": 2, "gru": 1, "elman": 1, "slstm": 4, "slstm_logsig": 4}
 
 # The five measured workloads. Seeds are 1000 + index.
 WORKLOADS = {
@@ -41,7 +41,7 @@ def make_inputs(function: str, B: int, T: int, N: int, D: int, dtype=torch.bfloa
     R = torch.randn((G, N, D, D), generator=g) / math.sqrt(D)
     b = torch.randn((G, N, D), generator=g)
     s0 = torch.randn((S, B, 1, N, D), generator=g)
-    if function == "slstm":
+    if function.startswith("slstm"):
         s0[2] = 1.0
         s0[3] = 0.0
     dst = torch.randn((S, B, T, N, D), generator=g) if with_grads else None

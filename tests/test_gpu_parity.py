@@ -12,7 +12,7 @@ from parity_util import (check_grad, check_grads, check_states, oracle_bwd, orac
 
 pytestmark = pytest.mark.gpu
 
-FNS = ["lstm", "gru", "elman", "slstm"]
+FNS = ["lstm", "gru", "elman", "slstm", "slstm_logsig"]
 DTYPES = [torch.float32, torch.bfloat16]
 SMALL = [(3, 37, 2, 48), (1, 5, 1, 16), (9, 20, 3, 64)]
 
@@ -114,6 +114,7 @@ FUSED_CASES = [
     ("slstm", 5, 29, 2, 96, dict(C=3, KT=3)),
     ("slstm", 16, 23, 1, 192, dict(C=12, NT=2)),
     ("slstm", 4, 17, 1, 192, dict(C=12)),
+    ("slstm_logsig", 6, 31, 2, 128, dict(C=8)),
 ]
 
 
@@ -165,6 +166,7 @@ BWD_CASES = [
     ("slstm", 5, 29, 2, 96, dict(C=3)),
     ("slstm", 16, 23, 1, 192, dict(C=12, NT=2)),
     ("slstm", 4, 17, 1, 192, dict(C=12)),
+    ("slstm_logsig", 6, 31, 2, 128, dict(C=8)),
 ]
 
 
@@ -194,6 +196,7 @@ GRID_CASES = [
     ("gru", 9, 19, 2, 128, dict(C=8)),
     ("elman", 16, 21, 2, 256, dict(C=16, NT=2)),
     ("slstm", 4, 17, 1, 512, dict(C=32)),
+    ("slstm_logsig", 5, 13, 1, 512, dict(C=32)),
 ]
 
 
@@ -232,6 +235,7 @@ ALT_CASES = [
     ("slstm", 20, 7, 1, 64),     # two m-tiles per batch tile
     ("lstm", 3, 6, 1, 1024),
     ("gru", 33, 4, 1, 256),      # two batch tiles, ragged
+    ("slstm_logsig", 7, 9, 2, 64),
 ]
 
 

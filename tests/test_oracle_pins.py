@@ -19,7 +19,7 @@ import torch
 from oracle import oracle
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_steps.json")
-FNS = ["lstm", "gru", "elman", "slstm"]
+FNS = ["lstm", "gru", "elman", "slstm", "slstm_logsig"]
 
 
 def rand_problem(fn, B, T, N, D, seed, rscale=1.0):
@@ -29,7 +29,7 @@ def rand_problem(fn, B, T, N, D, seed, rscale=1.0):
     R = rng.normal(size=(G, N, D, D)) * rscale / math.sqrt(D)
     b = rng.normal(size=(G, N, D))
     s0 = rng.normal(size=(S, B, 1, N, D))
-    if fn == "slstm":
+    if fn.startswith("slstm"):
         s0[2] = np.abs(s0[2]) + 0.5  # normaliser must be positive
         s0[3] = rng.normal(size=s0[3].shape) * 0.5
     return Wx, R, b, s0
@@ -148,39 +148,48 @@ def _preacts(Wx, R, b, h_prev):
     return Wx + np.einsum("btni,gnij->btgnj", h_prev, R) + b[None, None]
 
 
-def test_slstm_unstabilised_closed_form():
-    """Stabilised states times exp(m) equal the plain exponential-gating
-    recurrence c~ = e^{a_f} c~ + e^{a_i} tanh(a_z), n~ likewise; h = sig(a_o) c~/n~."""
+def _forget(fn, af):
+    """The forget gate f (not its log): e^{a_f} for slstm, sigmoid(a_f) for
+    slstm_logsig, written directly rather than through the log."""
+    return np.exp(af) if fn == "slstm" else 1.0 / (1.0 + np.exp(-af))
+
+
+@pytest.mark.parametrize("fn", ["slstm", "slstm_logsig"])
+def test_slstm_unstabilised_closed_form(fn):
+    """Stabilised states times exp(m) equal the plain recurrence
+    c~ = f c~ + e^{a_i} tanh(a_z), n~ = f n~ + e^{a_i}; h = sig(a_o) c~/n~,
+    with f = e^{a_f} (slstm) or sigmoid(a_f) (slstm_logsig)."""
     B, T, N, D = 2, 12, 2, 3
-    Wx, R, b, s0 = rand_problem("slstm", B, T, N, D, seed=21)
-    st, _ = oracle.fwd("slstm", Wx, R, b, s0)
+    Wx, R, b, s0 = rand_problem(fn, B, T, N, D, seed=21)
+    st, _ = oracle.fwd(fn, Wx, R, b, s0)
     h_prev = np.concatenate([s0[0], st[0, :, :-1]], axis=1)
     a = _preacts(Wx, R, b, h_prev)
     ct = s0[1, :, 0] * np.exp(s0[3, :, 0])
     nt = s0[2, :, 0] * np.exp(s0[3, :, 0])
     for t in range(T):
         ai, af, az, ao = (a[:, t, g] for g in range(4))
-        ct = np.exp(af) * ct + np.exp(ai) * np.tanh(az)
-        nt = np.exp(af) * nt + np.exp(ai)
+        ct = _forget(fn, af) * ct + np.exp(ai) * np.tanh(az)
+        nt = _forget(fn, af) * nt + np.exp(ai)
         h = ct / nt / (1 + np.exp(-ao))
         np.testing.assert_allclose(st[0, :, t], h, rtol=1e-11, atol=1e-13)
         np.testing.assert_allclose(st[1, :, t] * np.exp(st[3, :, t]), ct, rtol=1e-11, atol=1e-13)
         np.testing.assert_allclose(st[2, :, t] * np.exp(st[3, :, t]), nt, rtol=1e-11, atol=1e-13)
 
 
-def test_slstm_stabiliser_invariants():
+@pytest.mark.parametrize("fn", ["slstm", "slstm_logsig"])
+def test_slstm_stabiliser_invariants(fn):
     B, T, N, D = 3, 40, 2, 4
-    Wx, R, b, s0 = rand_problem("slstm", B, T, N, D, seed=8, rscale=2.0)
+    Wx, R, b, s0 = rand_problem(fn, B, T, N, D, seed=8, rscale=2.0)
     Wx *= 3.0  # large gate values: the unstabilised form would overflow soon
     s0[2] = 1.0
     s0[3] = 0.0
-    st, _ = oracle.fwd("slstm", Wx, R, b, s0)
+    st, _ = oracle.fwd(fn, Wx, R, b, s0)
     assert np.all(np.isfinite(st))
     h_prev = np.concatenate([s0[0], st[0, :, :-1]], axis=1)
     m_prev = np.concatenate([s0[3], st[3, :, :-1]], axis=1)
     a = _preacts(Wx, R, b, h_prev)
     ig = np.exp(a[:, :, 0] - st[3])
-    fg = np.exp(a[:, :, 1] + m_prev - st[3])
+    fg = _forget(fn, a[:, :, 1]) * np.exp(m_prev - st[3])
     # a is recomputed here in another summation order: allow rounding only
     assert np.all(ig <= 1.0 + 1e-12) and np.all(fg <= 1.0 + 1e-12)
     np.testing.assert_allclose(np.maximum(ig, fg), 1.0, rtol=0, atol=1e-12)
@@ -190,16 +199,17 @@ def test_slstm_stabiliser_invariants():
     assert np.all(np.abs(st[1] / st[2]) <= bound + 1e-12)
 
 
-def test_slstm_shift_invariance():
+@pytest.mark.parametrize("fn", ["slstm", "slstm_logsig"])
+def test_slstm_shift_invariance(fn):
     B, T, N, D = 2, 10, 1, 3
-    Wx, R, b, s0 = rand_problem("slstm", B, T, N, D, seed=13)
-    st, _ = oracle.fwd("slstm", Wx, R, b, s0)
+    Wx, R, b, s0 = rand_problem(fn, B, T, N, D, seed=13)
+    st, _ = oracle.fwd(fn, Wx, R, b, s0)
     k = 0.7
     s1 = s0.copy()
     s1[3] += k
     s1[1] *= math.exp(-k)
     s1[2] *= math.exp(-k)
-    st2, _ = oracle.fwd("slstm", Wx, R, b, s1)
+    st2, _ = oracle.fwd(fn, Wx, R, b, s1)
     np.testing.assert_allclose(st2[0], st[0], rtol=1e-12, atol=1e-13)
 
 
