@@ -502,7 +502,7 @@ template <int FN, int MT>
 cudaError_t enqueue_fwd(const AltArgs& a, cudaStream_t st) {
   constexpr int UT = AltFwdTile<FN>::UT;
   const size_t smem = alt_fwd_smem<FN, MT>();
-  cudaError_t e = cudaFuncSetAttribute(alt_fwd_step<FN, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_smem_attr((const void*)alt_fwd_step<FN, MT>, smem);
   if (e != cudaSuccess) return e;
   const size_t per = (size_t)a.B * a.N * a.D;
   alt_fwd_init<FN><<<(unsigned)((per + 255) / 256 < 1184 ? (per + 255) / 256 : 1184), 256, 0, st>>>(a);
@@ -515,7 +515,7 @@ template <int FN, int MT>
 cudaError_t enqueue_bwd(const AltArgs& a, cudaStream_t st) {
   constexpr int S = FnInfo<FN>::S;
   const size_t smem = alt_bwd_smem<FN, MT>();
-  cudaError_t e = cudaFuncSetAttribute(alt_bwd_step<FN, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_smem_attr((const void*)alt_bwd_step<FN, MT>, smem);
   if (e != cudaSuccess) return e;
   const size_t n = (size_t)S * a.B * a.N * a.D;
   alt_zero<<<(unsigned)((n + 255) / 256 < 1184 ? (n + 255) / 256 : 1184), 256, 0, st>>>(a.cst, n);

@@ -5,6 +5,8 @@
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
+#include <vector>
 
 #include "kernels.cuh"
 #include "plan.h"
@@ -14,6 +16,48 @@ namespace rnn {
 
 static std::atomic<unsigned long long> g_launches{0};
 void note_launch(int count) { g_launches.fetch_add((unsigned long long)count); }
+
+namespace {
+struct AttrEntry {
+  const void* func;
+  int dev;
+  size_t smem;
+  bool nonportable;
+};
+std::mutex g_attr_mu;
+std::vector<AttrEntry> g_attrs;
+
+AttrEntry* attr_entry(const void* func, int dev) {
+  for (auto& e : g_attrs)
+    if (e.func == func && e.dev == dev) return &e;
+  g_attrs.push_back(AttrEntry{func, dev, 0, false});
+  return &g_attrs.back();
+}
+}  // namespace
+
+cudaError_t set_smem_attr(const void* func, size_t smem) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  AttrEntry* a = attr_entry(func, dev);
+  if (smem <= a->smem) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess) a->smem = smem;
+  return e;
+}
+
+cudaError_t set_nonportable_cluster(const void* func) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  AttrEntry* a = attr_entry(func, dev);
+  if (a->nonportable) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) a->nonportable = true;
+  return e;
+}
 
 // Optional events recorded around the scan kernel (rnn_profile_events).
 static cudaEvent_t g_prof[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};

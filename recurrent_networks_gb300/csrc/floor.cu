@@ -81,8 +81,8 @@ extern "C" int rnn_exchange_floor(int C, int slice_bytes, int steps, void* out, 
   cudaStream_t st = (cudaStream_t)stream;
   const size_t smem = 128 + (size_t)2 * C * slice_bytes + (size_t)2 * slice_bytes;
   cudaError_t e = cudaMemsetAsync(out, 0, 16, st);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(exchange_floor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e == cudaSuccess && C > 8) e = cudaFuncSetAttribute(exchange_floor_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) e = set_smem_attr((const void*)exchange_floor_kernel, (size_t)smem);
+  if (e == cudaSuccess && C > 8) e = set_nonportable_cluster((const void*)exchange_floor_kernel);
   if (e == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C);

@@ -351,10 +351,10 @@ cudaError_t fused_bwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStrea
     dmap = tmap;  // unused
   }
   (void)G;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh.smem);
+  cudaError_t e = set_smem_attr((const void*)k, (size_t)sh.smem);
   if (e != cudaSuccess) return e;
   if (sh.C > 8) {
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = set_nonportable_cluster((const void*)k);
     if (e != cudaSuccess) return e;
   }
   const int groups = a.N * ((a.B + (int)BC - 1) / (int)BC);

@@ -393,10 +393,10 @@ cudaError_t fwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream_t st
   const unsigned int box[5] = {(unsigned)sh.U, 1u, (unsigned)G, 1u, (unsigned)(8 * sh.NT)};
   cudaError_t e = encode_tensor_map_bf16(&map, a.Wx, 5, dims, box);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh.smem);
+  e = set_smem_attr((const void*)k, (size_t)sh.smem);
   if (e != cudaSuccess) return e;
   if (!GRIDX && sh.C > 8) {
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = set_nonportable_cluster((const void*)k);
     if (e != cudaSuccess) return e;
   }
   const int groups = a.N * ((a.B + 8 * sh.NT - 1) / (8 * sh.NT));

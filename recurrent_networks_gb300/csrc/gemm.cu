@@ -275,7 +275,7 @@ cudaError_t gemm_run(bool a_kmajor, bool b_kmajor, int M, int N, int K, const vo
   void (*k)(const CUtensorMap, const CUtensorMap, GemmArgs) =
       a_kmajor ? (b_kmajor ? gemm_umma_kernel<true, true> : gemm_umma_kernel<true, false>)
                : (b_kmajor ? gemm_umma_kernel<false, true> : gemm_umma_kernel<false, false>);
-  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM);
+  e = set_smem_attr((const void*)k, (size_t)GM_SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((N + GM_TILE - 1) / GM_TILE, (M + GM_TILE - 1) / GM_TILE, g.splits);
   k<<<grid, 128, GM_SMEM, st>>>(am, bm, g);

@@ -260,7 +260,7 @@ cudaError_t grid_bwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream
   } else {
     dmap = tmap;
   }
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh.smem);
+  cudaError_t e = set_smem_attr((const void*)k, (size_t)sh.smem);
   if (e != cudaSuccess) return e;
   const int groups = a.N * ((a.B + (int)BC - 1) / (int)BC);
   int per_sm = 0, dev = 0, sms = 0;

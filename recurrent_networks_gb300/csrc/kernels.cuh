@@ -11,9 +11,17 @@ namespace rnn {
 // Counts kernel launches for rnn_kernel_launches(); every launcher calls it.
 void note_launch(int count = 1);
 
+// cudaFuncSetAttribute, called once per (device, kernel) for the largest
+// dynamic shared memory requested so far (and once for the non-portable
+// cluster size): the runtime call costs microseconds of host time that a
+// small problem's launch would otherwise pay on every call.
+cudaError_t set_smem_attr(const void* func, size_t smem);
+cudaError_t set_nonportable_cluster(const void* func);
+
 // Arguments of the plain per-head kernels (and of the weight-gradient pass).
 struct SimtArgs {
   int B, T, N, D, BB;
+  int r_smem = 0;  // 1: the head's R (fp32) is staged in shared memory (transposed for the backward)
   const void* Wx;
   const void* R;
   const void* bias;

@@ -14,6 +14,17 @@ namespace rnn {
 
 constexpr int SIMT_BBM = 8;  // max batch rows per CTA
 
+// Every step runs in phases separated by CTA barriers, each spread over all
+// threads:
+//   forward   A: rec[g][bb][j] = b[g, j] + sum_i h[bb][i] R[g, n, i, j]   (one (g, bb, j) per thread)
+//             B: cell update of (bb, j)                                   (one pair per thread)
+//   backward  A: cell derivative of (bb, j) -> dr[g][bb][j]
+//             B: part[g][bb][i] = sum_j dr[g][bb][j] R[g, n, i, j]       (one (g, bb, i) per thread)
+//             C: dS[0][bb][i] += sum_g part[g][bb][i]   (folded into the next step's phase A)
+// R (fp32) sits in shared memory when it fits (transposed for the backward,
+// so that consecutive threads read consecutive addresses); otherwise it is
+// read through L1 / L2. Each dot product keeps four independent partial sums.
+
 template <int FN, typename T>
 __global__ void __launch_bounds__(256) simt_fwd_kernel(SimtArgs a) {
   constexpr int G = FnInfo<FN>::G, S = FnInfo<FN>::S, P = FnInfo<FN>::P, K = P + S;
@@ -27,78 +38,104 @@ __global__ void __launch_bounds__(256) simt_fwd_kernel(SimtArgs a) {
   T* states = (T*)a.states;
   T* last = (T*)a.last;
   extern __shared__ float smem[];
-  float* cur = smem;                       // [S][BS][D]  carried states (thread-owned units)
-  float* hop = smem + S * BS * D;          // [2][BS][D]  h as the contraction operand
-
-  for (int j = threadIdx.x; j < D; j += blockDim.x)
-    for (int bb = 0; bb < BB; ++bb)
-      for (int s = 0; s < S; ++s) {
-        float v = s0 ? ldf(s0 + ((size_t)(s * B + b0 + bb) * N + n) * D + j) : 0.0f;
-        cur[(s * BS + bb) * D + j] = v;
-        if (s == 0) hop[bb * D + j] = v;
-      }
+  float* cur = smem;                       // [S][BS][D]  carried states
+  float* hop = cur + S * BS * D;           // [2][BS][D]  h as the contraction operand
+  float* rec = hop + 2 * BS * D;           // [G][BS][D]  recurrent branch of the step
+  float* Rs = rec + G * BS * D;            // [G][D][D]   R[g, n] in fp32 when it fits (r_smem)
+  if (a.r_smem)
+    for (int e = threadIdx.x; e < G * D * D; e += blockDim.x) {
+      const int g = e / (D * D), r = e - g * D * D;
+      Rs[e] = ldf(R + (size_t)(g * N + n) * D * D + r);
+    }
+  for (int e = threadIdx.x; e < BB * D; e += blockDim.x) {
+    const int bb = e / D, j = e - bb * D;
+    for (int s = 0; s < S; ++s) {
+      const float v = s0 ? ldf(s0 + ((size_t)(s * B + b0 + bb) * N + n) * D + j) : 0.0f;
+      cur[(s * BS + bb) * D + j] = v;
+      if (s == 0) hop[bb * D + j] = v;
+    }
+  }
   __syncthreads();
+
+  // Wx of the thread's first pair is loaded one step ahead (its latency hides
+  // behind the next step's dot products)
+  float xnext[G];
+  const int e0 = threadIdx.x;
+  if (e0 < BB * D && TT > 0) {
+    const int bb = e0 / D, j = e0 - bb * D;
+#pragma unroll
+    for (int g = 0; g < G; ++g) xnext[g] = ldf(Wx + (((size_t)(b0 + bb) * TT + 0) * G + g) * N * D + (size_t)n * D + j);
+  }
 
   for (int t = 0; t < TT; ++t) {
     const float* hin = hop + (t & 1) * BS * D;
     float* hout = hop + ((t + 1) & 1) * BS * D;
-    for (int j = threadIdx.x; j < D; j += blockDim.x) {
-      float acc[G][SIMT_BBM];
+    // phase A: the G * BB * D dot products of the step
+    for (int e = threadIdx.x; e < G * BB * D; e += blockDim.x) {
+      const int g = e / (BB * D), r = e - g * BB * D, bb = r / D, j = r - bb * D;
+      const float* hv = hin + bb * D;
+      float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
+      int i = 0;
+      if (a.r_smem) {
+        const float* rc = Rs + (size_t)g * D * D + j;
+        for (; i + 4 <= D; i += 4) {
+          p0 = fmaf(hv[i], rc[(size_t)i * D], p0);
+          p1 = fmaf(hv[i + 1], rc[(size_t)(i + 1) * D], p1);
+          p2 = fmaf(hv[i + 2], rc[(size_t)(i + 2) * D], p2);
+          p3 = fmaf(hv[i + 3], rc[(size_t)(i + 3) * D], p3);
+        }
+        for (; i < D; ++i) p0 = fmaf(hv[i], rc[(size_t)i * D], p0);
+      } else {
+        const T* rc = R + (size_t)(g * N + n) * D * D + j;
+        for (; i + 4 <= D; i += 4) {
+          p0 = fmaf(hv[i], ldf(rc + (size_t)i * D), p0);
+          p1 = fmaf(hv[i + 1], ldf(rc + (size_t)(i + 1) * D), p1);
+          p2 = fmaf(hv[i + 2], ldf(rc + (size_t)(i + 2) * D), p2);
+          p3 = fmaf(hv[i + 3], ldf(rc + (size_t)(i + 3) * D), p3);
+        }
+        for (; i < D; ++i) p0 = fmaf(hv[i], ldf(rc + (size_t)i * D), p0);
+      }
+      rec[(g * BS + bb) * D + j] = ldf(bias + (size_t)(g * N + n) * D + j) + ((p0 + p1) + (p2 + p3));
+    }
+    __syncthreads();
+    // phase B: the cell update of every (batch row, unit) pair
+    for (int e = threadIdx.x; e < BB * D; e += blockDim.x) {
+      const int bb = e / D, j = e - bb * D, b = b0 + bb;
+      float x[G], r[G], sp[S], sn[S], pre[P];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float bv = ldf(bias + (size_t)(g * N + n) * D + j);
-#pragma unroll
-        for (int bb = 0; bb < SIMT_BBM; ++bb) acc[g][bb] = bv;
+        x[g] = e == e0 ? xnext[g] : ldf(Wx + (((size_t)b * TT + t) * G + g) * N * D + (size_t)n * D + j);
+        r[g] = rec[(g * BS + bb) * D + j];
       }
-      for (int i = 0; i < D; ++i) {
-        float rv[G];
+      if (e == e0 && t + 1 < TT) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) rv[g] = ldf(R + ((size_t)(g * N + n) * D + i) * D + j);
-#pragma unroll
-        for (int bb = 0; bb < SIMT_BBM; ++bb) {
-          if (bb < BB) {
-            float hv = hin[bb * D + i];
-#pragma unroll
-            for (int g = 0; g < G; ++g) acc[g][bb] = fmaf(hv, rv[g], acc[g][bb]);
-          }
-        }
+        for (int g = 0; g < G; ++g) xnext[g] = ldf(Wx + (((size_t)b * TT + t + 1) * G + g) * N * D + (size_t)n * D + j);
       }
 #pragma unroll
-      for (int bb = 0; bb < SIMT_BBM; ++bb) {
-        if (bb < BB) {
-          const int b = b0 + bb;
-          float x[G], r[G], sp[S], sn[S], pre[P];
+      for (int s = 0; s < S; ++s) sp[s] = cur[(s * BS + bb) * D + j];
+      cell_fwd<FN, FAST>(x, r, sp, sn, pre);
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            x[g] = ldf(Wx + (((size_t)b * TT + t) * G + g) * N * D + (size_t)n * D + j);
-            r[g] = acc[g][bb];
-          }
+      for (int s = 0; s < S; ++s) {
+        cur[(s * BS + bb) * D + j] = sn[s];
+        if (states) stf(states + (((size_t)s * B + b) * TT + t) * N * D + (size_t)n * D + j, sn[s]);
+      }
+      hout[bb * D + j] = roundas((const T*)nullptr, sn[0]);
+      if (a.tape) {
+        float* tp = a.tape + (((size_t)t * B + b) * N + n) * K * D + j;
 #pragma unroll
-          for (int s = 0; s < S; ++s) sp[s] = cur[(s * BS + bb) * D + j];
-          cell_fwd<FN, FAST>(x, r, sp, sn, pre);
+        for (int k = 0; k < P; ++k) tp[k * D] = pre[k];
 #pragma unroll
-          for (int s = 0; s < S; ++s) {
-            cur[(s * BS + bb) * D + j] = sn[s];
-            if (states) stf(states + (((size_t)s * B + b) * TT + t) * N * D + (size_t)n * D + j, sn[s]);
-          }
-          hout[bb * D + j] = roundas((const T*)nullptr, sn[0]);
-          if (a.tape) {
-            float* tp = a.tape + (((size_t)t * B + b) * N + n) * K * D + j;
-#pragma unroll
-            for (int k = 0; k < P; ++k) tp[k * D] = pre[k];
-#pragma unroll
-            for (int s = 0; s < S; ++s) tp[(P + s) * D] = sn[s];
-          }
-        }
+        for (int s = 0; s < S; ++s) tp[(P + s) * D] = sn[s];
       }
     }
     __syncthreads();
   }
   if (last)
-    for (int j = threadIdx.x; j < D; j += blockDim.x)
-      for (int bb = 0; bb < BB; ++bb)
-        for (int s = 0; s < S; ++s)
-          stf(last + ((size_t)(s * B + b0 + bb) * N + n) * D + j, cur[(s * BS + bb) * D + j]);
+    for (int e = threadIdx.x; e < BB * D; e += blockDim.x) {
+      const int bb = e / D, j = e - bb * D;
+      for (int s = 0; s < S; ++s)
+        stf(last + ((size_t)(s * B + b0 + bb) * N + n) * D + j, cur[(s * BS + bb) * D + j]);
+    }
 }
 
 template <int FN, typename T>
@@ -115,93 +152,137 @@ __global__ void __launch_bounds__(256) simt_bwd_kernel(SimtArgs a) {
   T* dr_out = (T*)a.dr;
   T* ds0 = (T*)a.ds0;
   extern __shared__ float smem[];
-  float* dS = smem;                       // [S][BS][D] carried deltas (thread-owned units)
-  float* drs = smem + S * BS * D;         // [2][G][BS][D] recurrent-branch grads of the step
+  float* dS = smem;                        // [S][BS][D]  carried deltas
+  float* drs = dS + S * BS * D;            // [G][BS][D]  recurrent-branch grads of the step (operand)
+  float* part = drs + G * BS * D;          // [G][BS][D]  per-gate partial dh_{t-1}
+  float* RTs = part + G * BS * D;          // [G][D j][D i] R[g, n]^T in fp32 when it fits (r_smem)
+  if (a.r_smem)
+    for (int e = threadIdx.x; e < G * D * D; e += blockDim.x) {
+      const int g = e / (D * D), r = e - g * D * D, i = r / D, j = r - i * D;
+      RTs[((size_t)g * D + j) * D + i] = ldf(R + (size_t)(g * N + n) * D * D + r);
+    }
+  for (int e = threadIdx.x; e < BB * D; e += blockDim.x) {
+    const int bb = e / D, j = e - bb * D;
+    for (int s = 0; s < S; ++s) {
+      float v = 0.0f;
+      if (TT == 0 && dlast) v = ldf(dlast + ((size_t)(s * B + b0 + bb) * N + n) * D + j);
+      dS[(s * BS + bb) * D + j] = v;
+    }
+    for (int g = 0; g < G; ++g) part[(g * BS + bb) * D + j] = 0.0f;
+  }
+  __syncthreads();
 
-  for (int j = threadIdx.x; j < D; j += blockDim.x)
-    for (int bb = 0; bb < BB; ++bb)
-      for (int s = 0; s < S; ++s) {
-        float v = 0.0f;
-        if (TT == 0 && dlast) v = ldf(dlast + ((size_t)(s * B + b0 + bb) * N + n) * D + j);
-        dS[(s * BS + bb) * D + j] = v;
-      }
+  // the step's tape record, previous states and upstream gradients of the
+  // thread's first pair are loaded one step ahead
+  const int e0 = threadIdx.x;
+  float npre[P], nsn[S], nsp[S], nup[S];
+  auto fetch = [&](int tt, int e, float* pre, float* sn, float* sp, float* up) {
+    const int bb = e / D, j = e - bb * D, b = b0 + bb;
+    const float* tp = a.tape + (((size_t)tt * B + b) * N + n) * K * D + j;
+#pragma unroll
+    for (int k = 0; k < P; ++k) pre[k] = tp[k * D];
+#pragma unroll
+    for (int s = 0; s < S; ++s) sn[s] = tp[(P + s) * D];
+    if (tt > 0) {
+      const float* tq = a.tape + (((size_t)(tt - 1) * B + b) * N + n) * K * D + j;
+#pragma unroll
+      for (int s = 0; s < S; ++s) sp[s] = tq[(P + s) * D];
+    } else {
+#pragma unroll
+      for (int s = 0; s < S; ++s) sp[s] = s0 ? ldf(s0 + ((size_t)(s * B + b) * N + n) * D + j) : 0.0f;
+    }
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+      float d = 0.0f;
+      if (dstates) d += ldf(dstates + (((size_t)s * B + b) * TT + tt) * N * D + (size_t)n * D + j);
+      if (dlast && tt == TT - 1) d += ldf(dlast + ((size_t)(s * B + b) * N + n) * D + j);
+      up[s] = d;
+    }
+  };
+  if (e0 < BB * D && TT > 0) fetch(TT - 1, e0, npre, nsn, nsp, nup);
 
   for (int t = TT - 1; t >= 0; --t) {
-    float* drw = drs + (t & 1) * G * BS * D;
-    for (int j = threadIdx.x; j < D; j += blockDim.x) {
+    // phase A: cell derivative of every pair; dh_t gathers the G partials of
+    // the later step first
+    for (int e = threadIdx.x; e < BB * D; e += blockDim.x) {
+      const int bb = e / D, j = e - bb * D, b = b0 + bb;
+      float hsum = 0.0f;
 #pragma unroll
-      for (int bb = 0; bb < SIMT_BBM; ++bb) {
-        if (bb < BB) {
-          const int b = b0 + bb;
-          float pre[P], sp[S], sn[S], dsn[S], dx[G], dr[G], dsp[S];
-          const float* tp = a.tape + (((size_t)t * B + b) * N + n) * K * D + j;
+      for (int g = 0; g < G; ++g) hsum += part[(g * BS + bb) * D + j];
+      float pre[P], sp[S], sn[S], up[S], dsn[S], dx[G], dr[G], dsp[S];
+      if (e == e0) {
 #pragma unroll
-          for (int k = 0; k < P; ++k) pre[k] = tp[k * D];
+        for (int k = 0; k < P; ++k) pre[k] = npre[k];
 #pragma unroll
-          for (int s = 0; s < S; ++s) sn[s] = tp[(P + s) * D];
-          if (t > 0) {
-            const float* tq = a.tape + (((size_t)(t - 1) * B + b) * N + n) * K * D + j;
-#pragma unroll
-            for (int s = 0; s < S; ++s) sp[s] = tq[(P + s) * D];
-          } else {
-#pragma unroll
-            for (int s = 0; s < S; ++s)
-              sp[s] = s0 ? ldf(s0 + ((size_t)(s * B + b) * N + n) * D + j) : 0.0f;
-          }
-#pragma unroll
-          for (int s = 0; s < S; ++s) {
-            float d = dS[(s * BS + bb) * D + j];
-            if (dstates) d += ldf(dstates + (((size_t)s * B + b) * TT + t) * N * D + (size_t)n * D + j);
-            if (dlast && t == TT - 1) d += ldf(dlast + ((size_t)(s * B + b) * N + n) * D + j);
-            dsn[s] = d;
-          }
-          cell_bwd<FN, FAST>(pre, sp, sn, dsn, dx, dr, dsp);
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            size_t o = (((size_t)b * TT + t) * G + g) * N * D + (size_t)n * D + j;
-            if (dWx) stf(dWx + o, dx[g]);
-            stf(dr_out + o, dr[g]);
-            drw[(g * BS + bb) * D + j] = roundas((const T*)nullptr, dr[g]);
-          }
-#pragma unroll
-          for (int s = 0; s < S; ++s) dS[(s * BS + bb) * D + j] = dsp[s];
-        }
+        for (int s = 0; s < S; ++s) { sn[s] = nsn[s]; sp[s] = nsp[s]; up[s] = nup[s]; }
+        if (t > 0) fetch(t - 1, e0, npre, nsn, nsp, nup);
+      } else {
+        fetch(t, e, pre, sn, sp, up);
       }
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < D; i += blockDim.x) {
-      float acc[SIMT_BBM];
 #pragma unroll
-      for (int bb = 0; bb < SIMT_BBM; ++bb) acc[bb] = 0.0f;
+      for (int s = 0; s < S; ++s) {
+        float d = dS[(s * BS + bb) * D + j] + up[s];
+        if (s == 0) d += hsum;
+        dsn[s] = d;
+      }
+      cell_bwd<FN, FAST>(pre, sp, sn, dsn, dx, dr, dsp);
+#pragma unroll
       for (int g = 0; g < G; ++g) {
-        const T* row = R + ((size_t)(g * N + n) * D + i) * D;
-        for (int j = 0; j < D; ++j) {
-          float rv = ldf(row + j);
-#pragma unroll
-          for (int bb = 0; bb < SIMT_BBM; ++bb)
-            if (bb < BB) acc[bb] = fmaf(drw[(g * BS + bb) * D + j], rv, acc[bb]);
-        }
+        const size_t o = (((size_t)b * TT + t) * G + g) * N * D + (size_t)n * D + j;
+        if (dWx) stf(dWx + o, dx[g]);
+        stf(dr_out + o, dr[g]);
+        drs[(g * BS + bb) * D + j] = roundas((const T*)nullptr, dr[g]);
       }
 #pragma unroll
-      for (int bb = 0; bb < SIMT_BBM; ++bb)
-        if (bb < BB) dS[bb * D + i] += acc[bb];
+      for (int s = 0; s < S; ++s) dS[(s * BS + bb) * D + j] = dsp[s];
     }
-  }
-  if (ds0) {
     __syncthreads();
-    for (int j = threadIdx.x; j < D; j += blockDim.x)
-      for (int bb = 0; bb < BB; ++bb)
-        for (int s = 0; s < S; ++s)
-          stf(ds0 + ((size_t)(s * B + b0 + bb) * N + n) * D + j, dS[(s * BS + bb) * D + j]);
+    // phase B: part[g][bb][i] = sum_j dr[g][bb][j] R[g, n, i, j]
+    for (int e = threadIdx.x; e < G * BB * D; e += blockDim.x) {
+      const int g = e / (BB * D), r = e - g * BB * D, bb = r / D, i = r - bb * D;
+      const float* dv = drs + (g * BS + bb) * D;
+      float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
+      int j = 0;
+      if (a.r_smem) {
+        const float* rc = RTs + (size_t)g * D * D + i;
+        for (; j + 4 <= D; j += 4) {
+          p0 = fmaf(dv[j], rc[(size_t)j * D], p0);
+          p1 = fmaf(dv[j + 1], rc[(size_t)(j + 1) * D], p1);
+          p2 = fmaf(dv[j + 2], rc[(size_t)(j + 2) * D], p2);
+          p3 = fmaf(dv[j + 3], rc[(size_t)(j + 3) * D], p3);
+        }
+        for (; j < D; ++j) p0 = fmaf(dv[j], rc[(size_t)j * D], p0);
+      } else {
+        const T* row = R + ((size_t)(g * N + n) * D + i) * D;
+        for (; j + 4 <= D; j += 4) {
+          p0 = fmaf(dv[j], ldf(row + j), p0);
+          p1 = fmaf(dv[j + 1], ldf(row + j + 1), p1);
+          p2 = fmaf(dv[j + 2], ldf(row + j + 2), p2);
+          p3 = fmaf(dv[j + 3], ldf(row + j + 3), p3);
+        }
+        for (; j < D; ++j) p0 = fmaf(dv[j], ldf(row + j), p0);
+      }
+      part[(g * BS + bb) * D + i] = (p0 + p1) + (p2 + p3);
+    }
+    __syncthreads();
   }
+  if (ds0)
+    for (int e = threadIdx.x; e < BB * D; e += blockDim.x) {
+      const int bb = e / D, j = e - bb * D;
+      float hsum = 0.0f;
+#pragma unroll
+      for (int g = 0; g < G; ++g) hsum += part[(g * BS + bb) * D + j];
+      for (int s = 0; s < S; ++s)
+        stf(ds0 + ((size_t)(s * B + b0 + bb) * N + n) * D + j, dS[(s * BS + bb) * D + j] + (s == 0 ? hsum : 0.0f));
+    }
 }
 
 // ---- host launchers ----------------------------------------------------------
 
 static int simt_bb(int fn, int B, int D, bool bwd, size_t* smem_out) {
   const int S = fn_states(fn), G = fn_gates(fn);
-  // shared floats per batch row: fwd S*D + 2*D ; bwd S*D + 2*G*D
-  size_t per = (bwd ? (size_t)(S + 2 * G) * D : (size_t)(S + 2) * D) * sizeof(float);
+  // shared floats per batch row: fwd (S + 2 + G) D ; bwd (S + 2 G) D
+  size_t per = (bwd ? (size_t)(S + 2 * G) * D : (size_t)(S + 2 + G) * D) * sizeof(float);
   int bb = B < SIMT_BBM ? B : SIMT_BBM;
   while (bb > 0 && per * bb > 200 * 1024) --bb;
   *smem_out = per * (bb > 0 ? bb : 1);
@@ -215,11 +296,17 @@ static cudaError_t launch_simt(const SimtArgs& a0, bool bwd, cudaStream_t st) {
   int BB = simt_bb(FN, a.B, a.D, bwd, &smem);
   if (BB <= 0) return cudaErrorInvalidValue;
   a.BB = BB;
+  // the head's R in shared memory (fp32) when it fits beside the state buffers
+  const size_t rbytes = (size_t)FnInfo<FN>::G * a.D * a.D * sizeof(float);
+  a.r_smem = smem + rbytes <= 200 * 1024 ? 1 : 0;
+  if (a.r_smem) smem += rbytes;
   dim3 grid(a.N, (a.B + BB - 1) / BB);
   void (*k)(SimtArgs) = bwd ? simt_bwd_kernel<FN, T> : simt_fwd_kernel<FN, T>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_smem_attr((const void*)k, (size_t)smem);
   if (e != cudaSuccess) return e;
-  int threads = a.D >= 256 ? 256 : ((a.D + 31) / 32) * 32;
+  // one (gate, row, unit) dot product per thread in the wide phase
+  const int work = FnInfo<FN>::G * BB * a.D;
+  int threads = work >= 256 ? 256 : ((work + 31) / 32) * 32;
   k<<<grid, threads, smem, st>>>(a);
   note_launch();
   return cudaGetLastError();

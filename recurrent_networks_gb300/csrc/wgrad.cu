@@ -333,7 +333,7 @@ cudaError_t wgrad_run(int dtype, const WgradArgs& a, cudaStream_t st) {
   if (splits < 1) splits = 1;
   dim3 grid((a.D + WM_BN - 1) / WM_BN, (a.D + WM_BM - 1) / WM_BM, a.G * a.N * splits);
   const int smem = 2 * WM_STAGES * WM_BK * WM_LD * (int)sizeof(__nv_bfloat16);
-  cudaError_t e = cudaFuncSetAttribute(wgrad_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_smem_attr((const void*)wgrad_mma_kernel, (size_t)smem);
   if (e != cudaSuccess) return e;
   wgrad_mma_kernel<<<grid, 256, smem, st>>>(a, splits, kchunk);
   note_launch();

@@ -240,7 +240,7 @@ cudaError_t wgrad_umma_run(const WgradArgs& a, int splits, cudaStream_t st) {
     e = encode_tensor_map_sw128(&bs0, a.dr, 5, dims, box_b);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = cudaFuncSetAttribute(wgrad_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, UM_SMEM);
+  cudaError_t e = set_smem_attr((const void*)wgrad_umma_kernel, (size_t)UM_SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((a.D + UM_TILE - 1) / UM_TILE, (a.D + UM_TILE - 1) / UM_TILE, a.G * a.N * splits);
   wgrad_umma_kernel<<<grid, 128, UM_SMEM, st>>>(amain, as0, bmain, bs0, a, splits, kps, tpb, s0_tiles);
