@@ -27,11 +27,15 @@ namespace rnn {
 
 namespace {
 
+// tiles: 128 rows of M by BN (128 or 256) columns of N, k-chunks of 64
 constexpr int GM_TILE = 128, GM_BK = 64, GM_STAGES = 4;
 constexpr int GM_HALF = 64 * 128;                 // a 64 x 64 bf16 box
-constexpr int GM_OPERAND = 2 * GM_HALF;           // one operand's k-chunk of a tile
-constexpr int GM_STAGE = 2 * GM_OPERAND;
-constexpr int GM_SMEM = GM_STAGES * GM_STAGE + 1024 + 256;
+constexpr int GM_OPERAND = 2 * GM_HALF;           // the A operand's k-chunk of a tile
+template <int BN> struct GmTile {
+  static constexpr int B_BYTES = BN / 64 * GM_HALF;    // the B operand's k-chunk
+  static constexpr int STAGE = GM_OPERAND + B_BYTES;
+  static constexpr int SMEM = GM_STAGES * STAGE + 1024 + 256;
+};
 
 // K-major (128-byte swizzle): 8-row groups 1 KB apart, a 16-element k step is
 // 32 bytes further along the 128-byte row. MN-major: the two 64-wide halves of
@@ -53,16 +57,17 @@ struct GemmArgs {
   unsigned long long wait_limit_ns;
 };
 
-template <bool AK, bool BK>
+template <bool AK, bool BK, int BN>
 __global__ void __launch_bounds__(128, 1)
     gemm_umma_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap, GemmArgs a) {
+  constexpr int GM_STAGE = GmTile<BN>::STAGE;
   extern __shared__ unsigned char gm_raw[];
   unsigned char* sm = (unsigned char*)(((uintptr_t)gm_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + GM_STAGES * GM_STAGE);
   uint32_t* tslot = (uint32_t*)(bars + 2 * GM_STAGES + 1);
   const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[GM_STAGES]), accb = smem_u32(&bars[2 * GM_STAGES]);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n0 = blockIdx.x * GM_TILE, m0 = blockIdx.y * GM_TILE, split = blockIdx.z;
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * GM_TILE, split = blockIdx.z;
   const int nchunk = (a.K + GM_BK - 1) / GM_BK;
   const int c0 = split * a.kps, nq = min(nchunk, c0 + a.kps) - c0;
 
@@ -77,7 +82,8 @@ __global__ void __launch_bounds__(128, 1)
     prefetch_tensormap(&bmap);
   }
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" ::"r"(smem_u32(tslot)) : "memory");
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)), "n"(BN)
+                 : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -105,16 +111,16 @@ __global__ void __launch_bounds__(128, 1)
         tma_load_5d(smem_u32(As), &amap, fb, m0, k0, 0, 0, 0);
         tma_load_5d(smem_u32(As + GM_HALF), &amap, fb, m0 + 64, k0, 0, 0, 0);
       }
-      if constexpr (BK) {
+      if constexpr (BK) {  // BN rows n0 .. n0+BN-1, k0 .. k0+63
         tma_load_5d(smem_u32(Bs), &bmap, fb, k0, n0, 0, 0, 0);
-      } else {
-        tma_load_5d(smem_u32(Bs), &bmap, fb, n0, k0, 0, 0, 0);
-        tma_load_5d(smem_u32(Bs + GM_HALF), &bmap, fb, n0 + 64, k0, 0, 0, 0);
+      } else {             // BN/64 column groups of 64, k rows k0 .. k0+63
+#pragma unroll
+        for (int h = 0; h < BN / 64; ++h) tma_load_5d(smem_u32(Bs + h * GM_HALF), &bmap, fb, n0 + 64 * h, k0, 0, 0, 0);
       }
     }
   } else if (tid == 32) {  // ---- MMA issuer
     const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((AK ? 0u : 1u) << 15) | ((BK ? 0u : 1u) << 16) |
-                           ((uint32_t)(GM_TILE >> 3) << 17) | ((uint32_t)(GM_TILE >> 4) << 24);
+                           ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(GM_TILE >> 4) << 24);
     for (int it = 0; it < nq; ++it) {
       const int s = it % GM_STAGES;
       mbar_wait_bounded<false>(full0 + 8 * s, (it / GM_STAGES) & 1, a.wait_limit_ns, a.status, failed);
@@ -141,7 +147,7 @@ __global__ void __launch_bounds__(128, 1)
   mbar_wait_bounded<false>(accb, 0, a.wait_limit_ns, a.status, failed);
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const int m = m0 + warp * 32 + lane;  // TMEM lane = tile row
-  for (int cc = 0; cc < GM_TILE; cc += 32) {
+  for (int cc = 0; cc < BN; cc += 32) {
     uint32_t r[32];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -207,7 +213,7 @@ __global__ void __launch_bounds__(128, 1)
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(tmem) : "memory");
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(BN) : "memory");
 }
 
 // Sum of the split-K partials in a fixed order, rounded to bf16.
@@ -249,14 +255,16 @@ cudaError_t gemm_run(bool a_kmajor, bool b_kmajor, int M, int N, int K, const vo
     e = encode_tensor_map_sw128(&am, A, 5, a_kmajor ? dims_k : dims_m, a_kmajor ? box_k : box_m);
     if (e != cudaSuccess) return e;
   }
+  // 256-wide N tiles when N allows: twice the MMA work per byte loaded
+  const int BN = N >= 256 ? 256 : 128;
   {
     const unsigned long long dims_k[5] = {(unsigned long long)K, (unsigned long long)N, 1, 1, 1};
     const unsigned long long dims_n[5] = {(unsigned long long)N, (unsigned long long)K, 1, 1, 1};
-    const unsigned int box_k[5] = {64, 128, 1, 1, 1}, box_n[5] = {64, 64, 1, 1, 1};
+    const unsigned int box_k[5] = {64, (unsigned)BN, 1, 1, 1}, box_n[5] = {64, 64, 1, 1, 1};
     e = encode_tensor_map_sw128(&bm, B, 5, b_kmajor ? dims_k : dims_n, b_kmajor ? box_k : box_n);
     if (e != cudaSuccess) return e;
   }
-  const int tiles = ((M + GM_TILE - 1) / GM_TILE) * ((N + GM_TILE - 1) / GM_TILE);
+  const int tiles = ((M + GM_TILE - 1) / GM_TILE) * ((N + BN - 1) / BN);
   const int nchunk = (K + GM_BK - 1) / GM_BK;
   int splits = (152 + tiles - 1) / tiles;
   if (splits > nchunk / 2) splits = nchunk / 2;
@@ -272,13 +280,18 @@ cudaError_t gemm_run(bool a_kmajor, bool b_kmajor, int M, int N, int K, const vo
   g.bias = (const __nv_bfloat16*)bias;
   g.status = status;
   g.wait_limit_ns = 2000000000ull;
-  void (*k)(const CUtensorMap, const CUtensorMap, GemmArgs) =
-      a_kmajor ? (b_kmajor ? gemm_umma_kernel<true, true> : gemm_umma_kernel<true, false>)
-               : (b_kmajor ? gemm_umma_kernel<false, true> : gemm_umma_kernel<false, false>);
-  e = set_smem_attr((const void*)k, (size_t)GM_SMEM);
+  void (*k)(const CUtensorMap, const CUtensorMap, GemmArgs);
+  if (BN == 256)
+    k = a_kmajor ? (b_kmajor ? gemm_umma_kernel<true, true, 256> : gemm_umma_kernel<true, false, 256>)
+                 : (b_kmajor ? gemm_umma_kernel<false, true, 256> : gemm_umma_kernel<false, false, 256>);
+  else
+    k = a_kmajor ? (b_kmajor ? gemm_umma_kernel<true, true, 128> : gemm_umma_kernel<true, false, 128>)
+                 : (b_kmajor ? gemm_umma_kernel<false, true, 128> : gemm_umma_kernel<false, false, 128>);
+  const int smem = BN == 256 ? GmTile<256>::SMEM : GmTile<128>::SMEM;
+  e = set_smem_attr((const void*)k, (size_t)smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((N + GM_TILE - 1) / GM_TILE, (M + GM_TILE - 1) / GM_TILE, g.splits);
-  k<<<grid, 128, GM_SMEM, st>>>(am, bm, g);
+  const dim3 grid((N + BN - 1) / BN, (M + GM_TILE - 1) / GM_TILE, g.splits);
+  k<<<grid, 128, smem, st>>>(am, bm, g);
   note_launch();
   if (g.splits > 1) {
     gemm_reduce_kernel<<<2 * 152, 256, 0, st>>>(scratch, (__nv_bfloat16*)C, (size_t)M * N, g.splits);
@@ -288,7 +301,8 @@ cudaError_t gemm_run(bool a_kmajor, bool b_kmajor, int M, int N, int K, const vo
 }
 
 int proj_splits_bound(int M, int N, int K) {
-  const int tiles = ((M + GM_TILE - 1) / GM_TILE) * ((N + GM_TILE - 1) / GM_TILE);
+  const int BN = N >= 256 ? 256 : 128;  // the tile width gemm_run picks
+  const int tiles = ((M + GM_TILE - 1) / GM_TILE) * ((N + BN - 1) / BN);
   const int nchunk = (K + GM_BK - 1) / GM_BK;
   int splits = (152 + tiles - 1) / tiles;
   if (splits > nchunk / 2) splits = nchunk / 2;
