@@ -121,8 +121,9 @@ __device__ __forceinline__ bool counter_wait_bounded(const unsigned int* ctr, un
 // Called by one thread after a __syncthreads(): publishes every write the CTA
 // made before the barrier and counts this CTA in.
 __device__ __forceinline__ void counter_publish(unsigned int* ctr) {
-  __threadfence();
-  atomicAdd(ctr, 1u);
+  // a release at gpu scope is cumulative: it covers the writes this thread
+  // observed through the barrier as well as its own
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
 }
 __device__ __forceinline__ void cp_async_cg16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
