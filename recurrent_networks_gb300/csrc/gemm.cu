@@ -13,10 +13,12 @@
 // One generic GEMM, D[M][N] = sum_k A(m, k) B(k, n), with either operand stored
 // K-major (k contiguous: rows of 64 k per 128-byte TMA box) or MN-major (m / n
 // contiguous: boxes of 64 m / n by 64 k), both 128-byte swizzled, in the
-// canonical layouts tcgen05 reads; 128 x 128 tiles, a 4-stage TMA / mbarrier
-// ring, the fp32 accumulator in tensor memory. The roles are those of the
-// weight-gradient kernel: thread 0 loads, thread 32 issues the MMAs, four warps
-// drain the accumulator.
+// canonical layouts tcgen05 reads; 128 x BN tiles (BN = 128 or 256), the fp32
+// accumulator in tensor memory. The kernel is persistent: one CTA per SM walks
+// the tiles (and split-K slices), with warp-specialised roles. Warp 0 feeds a
+// TMA / mbarrier ring that runs ahead across tile boundaries, warp 1 issues the
+// MMAs, and warps 2-5 drain the accumulator. Tensor memory holds two
+// accumulators, so one tile's epilogue overlaps the next tile's MMAs.
 #include <stdio.h>
 
 #include "kernels.cuh"
@@ -28,13 +30,15 @@ namespace rnn {
 namespace {
 
 // tiles: 128 rows of M by BN (128 or 256) columns of N, k-chunks of 64
-constexpr int GM_TILE = 128, GM_BK = 64, GM_STAGES = 4;
+constexpr int GM_TILE = 128, GM_BK = 64;
 constexpr int GM_HALF = 64 * 128;                 // a 64 x 64 bf16 box
 constexpr int GM_OPERAND = 2 * GM_HALF;           // the A operand's k-chunk of a tile
+constexpr int GM_THREADS = 192;                   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 template <int BN> struct GmTile {
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
   static constexpr int B_BYTES = BN / 64 * GM_HALF;    // the B operand's k-chunk
   static constexpr int STAGE = GM_OPERAND + B_BYTES;
-  static constexpr int SMEM = GM_STAGES * STAGE + 1024 + 256;
+  static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
 };
 
 // K-major (128-byte swizzle): 8-row groups 1 KB apart, a 16-element k step is
@@ -58,31 +62,48 @@ struct GemmArgs {
 };
 
 template <bool AK, bool BK, int BN>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(GM_THREADS, 1)
     gemm_umma_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap, GemmArgs a) {
-  constexpr int GM_STAGE = GmTile<BN>::STAGE;
+  constexpr int NS = GmTile<BN>::STAGES, STAGE = GmTile<BN>::STAGE;
   extern __shared__ unsigned char gm_raw[];
   unsigned char* sm = (unsigned char*)(((uintptr_t)gm_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t* bars = (uint64_t*)(sm + GM_STAGES * GM_STAGE);
-  uint32_t* tslot = (uint32_t*)(bars + 2 * GM_STAGES + 1);
-  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[GM_STAGES]), accb = smem_u32(&bars[2 * GM_STAGES]);
+  // full[NS], empty[NS], accumulator full[2], accumulator empty[2], final
+  uint64_t* bars = (uint64_t*)(sm + NS * STAGE);
+  uint32_t* tslot = (uint32_t*)(bars + 2 * NS + 5);
+  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[NS]);
+  const uint32_t accf0 = smem_u32(&bars[2 * NS]), acce0 = accf0 + 16, finb = accf0 + 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * GM_TILE, split = blockIdx.z;
+  const int mtiles = (a.M + GM_TILE - 1) / GM_TILE, ntiles = (a.N + BN - 1) / BN;
+  const int units = mtiles * ntiles * a.splits;
   const int nchunk = (a.K + GM_BK - 1) / GM_BK;
-  const int c0 = split * a.kps, nq = min(nchunk, c0 + a.kps) - c0;
+  // unit u: split-K slice u / (mtiles ntiles), then m-tile, then n-tile
+  // fastest, so the CTAs working side by side share A tiles through L2
+  auto decode = [&](int u, int& m0, int& n0, int& c0, int& nq, int& split) {
+    split = u / (mtiles * ntiles);
+    const int r = u - split * mtiles * ntiles, mt = r / ntiles;
+    m0 = mt * GM_TILE;
+    n0 = (r - mt * ntiles) * BN;
+    c0 = split * a.kps;
+    nq = min(nchunk, c0 + a.kps) - c0;
+  };
 
   if (tid == 0) {
-    for (int s = 0; s < GM_STAGES; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
-    mbar_init(accb, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf0 + 8 * b, 1);
+      mbar_init(acce0 + 8 * b, 4);  // one arrival per epilogue warp
+    }
+    mbar_init(finb, 1);
     fence_mbar_init_cluster();
     prefetch_tensormap(&amap);
     prefetch_tensormap(&bmap);
   }
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)), "n"(BN)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                 "n"(2 * BN)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -91,129 +112,169 @@ __global__ void __launch_bounds__(128, 1)
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tslot;
   bool failed = false;
-  int nissued = 0;
 
-  if (tid == 0) {  // ---- TMA producer
-    for (int it = 0; it < nq; ++it) {
-      const int s = it % GM_STAGES;
-      if (it >= GM_STAGES &&
-          !mbar_wait_bounded<false>(empty0 + 8 * s, ((it / GM_STAGES) - 1) & 1, a.wait_limit_ns, a.status, failed))
-        break;
-      nissued = it + 1;
-      const uint32_t fb = full0 + 8 * s;
-      unsigned char* As = sm + (size_t)s * GM_STAGE;
-      unsigned char* Bs = As + GM_OPERAND;
-      const int k0 = (c0 + it) * GM_BK;
-      mbar_arrive_expect_tx(fb, GM_STAGE);
-      if constexpr (AK) {  // rows m0 .. m0+127, k0 .. k0+63
-        tma_load_5d(smem_u32(As), &amap, fb, k0, m0, 0, 0, 0);
-      } else {             // two 64-wide m halves, k rows k0 .. k0+63
-        tma_load_5d(smem_u32(As), &amap, fb, m0, k0, 0, 0, 0);
-        tma_load_5d(smem_u32(As + GM_HALF), &amap, fb, m0 + 64, k0, 0, 0, 0);
-      }
-      if constexpr (BK) {  // BN rows n0 .. n0+BN-1, k0 .. k0+63
-        tma_load_5d(smem_u32(Bs), &bmap, fb, k0, n0, 0, 0, 0);
-      } else {             // BN/64 column groups of 64, k rows k0 .. k0+63
-#pragma unroll
-        for (int h = 0; h < BN / 64; ++h) tma_load_5d(smem_u32(Bs + h * GM_HALF), &bmap, fb, n0 + 64 * h, k0, 0, 0, 0);
-      }
-    }
-  } else if (tid == 32) {  // ---- MMA issuer
-    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((AK ? 0u : 1u) << 15) | ((BK ? 0u : 1u) << 16) |
-                           ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(GM_TILE >> 4) << 24);
-    for (int it = 0; it < nq; ++it) {
-      const int s = it % GM_STAGES;
-      mbar_wait_bounded<false>(full0 + 8 * s, (it / GM_STAGES) & 1, a.wait_limit_ns, a.status, failed);
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t As = smem_u32(sm + (size_t)s * GM_STAGE), Bs = As + GM_OPERAND;
-      if (!failed) {
-#pragma unroll
-        for (int k = 0; k < GM_BK / 16; ++k) {
-          const uint64_t ad = gm_desc(As, AK, k), bd = gm_desc(Bs, BK, k);
-          const uint32_t acc = (it | k) ? 1u : 0u;
-          asm volatile(
-              "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-              " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem),
-              "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
-              : "memory");
-        }
-      }
-      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(empty0 + 8 * s)
-                   : "memory");
-    }
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(accb) : "memory");
-  }
-
-  mbar_wait_bounded<false>(accb, 0, a.wait_limit_ns, a.status, failed);
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  const int m = m0 + warp * 32 + lane;  // TMEM lane = tile row
-  for (int cc = 0; cc < BN; cc += 32) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)cc));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    if (m >= a.M || failed) continue;
-    const int n = n0 + cc;
-    if (a.splits == 1) {
-      __nv_bfloat16* out = a.C + (size_t)m * a.N + n;
-      if (n + 32 <= a.N) {  // 16-byte stores (N is a multiple of 8)
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          float f[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(r[8 * v + q]);
-          if (a.bias) {
-            const uint4 bb = *(const uint4*)(a.bias + n + 8 * v);
-            const __nv_bfloat16* bh = (const __nv_bfloat16*)&bb;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) f[q] += __bfloat162float(bh[q]);
+  if (warp == 0) {
+    if (lane == 0) {  // ---- TMA producer
+      int it = 0, issued = 0;
+      for (int u = blockIdx.x; u < units && !failed; u += gridDim.x) {
+        int m0, n0, c0, nq, split;
+        decode(u, m0, n0, c0, nq, split);
+        for (int q = 0; q < nq; ++q, ++it) {
+          const int s = it % NS;
+          if (it >= NS &&
+              !mbar_wait_bounded<false>(empty0 + 8 * s, ((it / NS) - 1) & 1, a.wait_limit_ns, a.status, failed))
+            break;
+          const uint32_t fb = full0 + 8 * s;
+          unsigned char* As = sm + (size_t)s * STAGE;
+          unsigned char* Bs = As + GM_OPERAND;
+          const int k0 = (c0 + q) * GM_BK;
+          mbar_arrive_expect_tx(fb, STAGE);
+          if constexpr (AK) {  // rows m0 .. m0+127, k0 .. k0+63
+            tma_load_5d(smem_u32(As), &amap, fb, k0, m0, 0, 0, 0);
+          } else {             // two 64-wide m halves, k rows k0 .. k0+63
+            tma_load_5d(smem_u32(As), &amap, fb, m0, k0, 0, 0, 0);
+            tma_load_5d(smem_u32(As + GM_HALF), &amap, fb, m0 + 64, k0, 0, 0, 0);
           }
-          uint4 w;
-          w.x = pack_bf16(__float2bfloat16_rn(f[0]), __float2bfloat16_rn(f[1]));
-          w.y = pack_bf16(__float2bfloat16_rn(f[2]), __float2bfloat16_rn(f[3]));
-          w.z = pack_bf16(__float2bfloat16_rn(f[4]), __float2bfloat16_rn(f[5]));
-          w.w = pack_bf16(__float2bfloat16_rn(f[6]), __float2bfloat16_rn(f[7]));
-          *(uint4*)(out + 8 * v) = w;
-        }
-      } else {
+          if constexpr (BK) {  // BN rows n0 .. n0+BN-1, k0 .. k0+63
+            tma_load_5d(smem_u32(Bs), &bmap, fb, k0, n0, 0, 0, 0);
+          } else {             // BN/64 column groups of 64, k rows k0 .. k0+63
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          if (n + c < a.N) {
-            float v = __uint_as_float(r[c]);
-            if (a.bias) v += __bfloat162float(a.bias[n + c]);
-            out[c] = __float2bfloat16_rn(v);
+            for (int h = 0; h < BN / 64; ++h)
+              tma_load_5d(smem_u32(Bs + h * GM_HALF), &bmap, fb, n0 + 64 * h, k0, 0, 0, 0);
           }
+          issued = it + 1;
         }
       }
-    } else {
-      float* out = a.partial + ((size_t)split * a.M + m) * a.N + n;
-      if (n + 32 <= a.N) {
-#pragma unroll
-        for (int v = 0; v < 8; ++v)
-          *(float4*)(out + 4 * v) = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                                __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-      } else {
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (n + c < a.N) out[c] = __uint_as_float(r[c]);
+      if (failed) {  // let the copies in flight land before the CTA exits
+        for (int i = issued - NS > 0 ? issued - NS : 0; i < issued; ++i) {
+          bool f2 = false;
+          mbar_wait_bounded<false>(full0 + 8 * (i % NS), (i / NS) & 1, a.wait_limit_ns, nullptr, f2);
+        }
       }
     }
-  }
-  if (tid == 0 && failed) {
-    for (int it = nissued - GM_STAGES > 0 ? nissued - GM_STAGES : 0; it < nissued; ++it) {
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---- MMA issuer
+      const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((AK ? 0u : 1u) << 15) | ((BK ? 0u : 1u) << 16) |
+                             ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(GM_TILE >> 4) << 24);
+      int it = 0, tc = 0;
+      for (int u = blockIdx.x; u < units && !failed; u += gridDim.x, ++tc) {
+        int m0, n0, c0, nq, split;
+        decode(u, m0, n0, c0, nq, split);
+        const int b = tc & 1;
+        // the epilogue of tile tc - 2 has drained accumulator b
+        if (tc >= 2) mbar_wait_bounded<false>(acce0 + 8 * b, ((tc >> 1) - 1) & 1, a.wait_limit_ns, a.status, failed);
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t dacc = tmem + (uint32_t)(b * BN);
+        for (int q = 0; q < nq; ++q, ++it) {
+          const int s = it % NS;
+          mbar_wait_bounded<false>(full0 + 8 * s, (it / NS) & 1, a.wait_limit_ns, a.status, failed);
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t As = smem_u32(sm + (size_t)s * STAGE), Bs = As + GM_OPERAND;
+          if (!failed) {
+#pragma unroll
+            for (int k = 0; k < GM_BK / 16; ++k) {
+              const uint64_t ad = gm_desc(As, AK, k), bd = gm_desc(Bs, BK, k);
+              const uint32_t acc = (q | k) ? 1u : 0u;
+              asm volatile(
+                  "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                  " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(dacc),
+                  "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
+                  : "memory");
+            }
+          }
+          asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                           empty0 + 8 * s)
+                       : "memory");
+        }
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(accf0 + 8 * b)
+                     : "memory");
+      }
+      // every MMA this thread issued has completed once this arrives
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(finb) : "memory");
       bool f2 = false;
-      mbar_wait_bounded<false>(full0 + 8 * (it % GM_STAGES), (it / GM_STAGES) & 1, a.wait_limit_ns, nullptr, f2);
+      mbar_wait_bounded<false>(finb, 0, a.wait_limit_ns, nullptr, f2);
+    }
+  } else {  // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 = tile rows
+    const int ew = warp & 3;
+    int tc = 0;
+    for (int u = blockIdx.x; u < units && !failed; u += gridDim.x, ++tc) {
+      int m0, n0, c0, nq, split;
+      decode(u, m0, n0, c0, nq, split);
+      const int b = tc & 1;
+      mbar_wait_bounded<false>(accf0 + 8 * b, (tc >> 1) & 1, a.wait_limit_ns, a.status, failed);
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int m = m0 + ew * 32 + lane;
+      for (int cc = 0; cc < BN; cc += 32) {
+        uint32_t r[32];
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+              "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+              "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+              "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+            : "r"(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(b * BN + cc)));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (m >= a.M || n0 + cc >= a.N || failed) continue;
+        const int n = n0 + cc;
+        if (a.splits == 1) {
+          __nv_bfloat16* out = a.C + (size_t)m * a.N + n;
+          if (n + 32 <= a.N) {  // 16-byte stores (N is a multiple of 8)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float f[8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(r[8 * v + q]);
+              if (a.bias) {
+                const uint4 bb = *(const uint4*)(a.bias + n + 8 * v);
+                const __nv_bfloat16* bh = (const __nv_bfloat16*)&bb;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) f[q] += __bfloat162float(bh[q]);
+              }
+              uint4 w;
+              w.x = pack_bf16(__float2bfloat16_rn(f[0]), __float2bfloat16_rn(f[1]));
+              w.y = pack_bf16(__float2bfloat16_rn(f[2]), __float2bfloat16_rn(f[3]));
+              w.z = pack_bf16(__float2bfloat16_rn(f[4]), __float2bfloat16_rn(f[5]));
+              w.w = pack_bf16(__float2bfloat16_rn(f[6]), __float2bfloat16_rn(f[7]));
+              *(uint4*)(out + 8 * v) = w;
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              if (n + c < a.N) {
+                float v = __uint_as_float(r[c]);
+                if (a.bias) v += __bfloat162float(a.bias[n + c]);
+                out[c] = __float2bfloat16_rn(v);
+              }
+            }
+          }
+        } else {
+          float* out = a.partial + ((size_t)split * a.M + m) * a.N + n;
+          if (n + 32 <= a.N) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              *(float4*)(out + 4 * v) = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                                    __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (n + c < a.N) out[c] = __uint_as_float(r[c]);
+          }
+        }
+      }
+      // accumulator b is free for tile tc + 2
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce0 + 8 * b);
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(BN) : "memory");
+  if (warp == 0) {
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(2 * BN) : "memory");
+  }
 }
 
 // Sum of the split-K partials in a fixed order, rounded to bf16.
@@ -239,6 +300,16 @@ __global__ void colsum_kernel(const __nv_bfloat16* X, __nv_bfloat16* out, int ro
     for (int q = 0; q < 32; ++q) tot += part[q][threadIdx.x & 31];
     out[c] = __float2bfloat16_rn(tot);
   }
+}
+
+int num_sms() {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
+  }
+  return sms;
 }
 
 // D[M][N] = A(m, k) B(k, n); a_kmajor: A stored [M][K] (else [K][M]); b_kmajor:
@@ -290,8 +361,11 @@ cudaError_t gemm_run(bool a_kmajor, bool b_kmajor, int M, int N, int K, const vo
   const int smem = BN == 256 ? GmTile<256>::SMEM : GmTile<128>::SMEM;
   e = set_smem_attr((const void*)k, (size_t)smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((N + BN - 1) / BN, (M + GM_TILE - 1) / GM_TILE, g.splits);
-  k<<<grid, 128, smem, st>>>(am, bm, g);
+  // persistent: one CTA per SM (the shared-memory ring and the two
+  // accumulators take the whole SM), never more CTAs than work units
+  const int units = tiles * g.splits;
+  const int ctas = units < num_sms() ? units : num_sms();
+  k<<<ctas, GM_THREADS, smem, st>>>(am, bm, g);
   note_launch();
   if (g.splits > 1) {
     gemm_reduce_kernel<<<2 * 152, 256, 0, st>>>(scratch, (__nv_bfloat16*)C, (size_t)M * N, g.splits);
