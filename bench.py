@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--input-proj", action="store_true",
                     help="time the tensor-core input projection (Wx = x W_x^T, I = N*D, and its backward) "
                          "on the workload's B*T rows instead of the scan")
+    ap.add_argument("--proj-shape", default=None, metavar="ROWS,I,C",
+                    help="with --input-proj: time this projection shape instead of the workload's")
     ap.add_argument("--trace", action="store_true",
                     help="print the per-phase cycle medians of the persistent scan kernels (rnn_trace) "
                          "instead of the bench line")
@@ -61,6 +63,8 @@ def proj_bench(args, w, fn, dev, _lib):
     B, T, N, D = w["B"], w["T"], w["N"], w["D"]
     G = {"lstm": 4, "gru": 3, "elman": 1, "slstm": 4}[fn]
     BT, I, C = B * T, N * D, G * N * D
+    if args.proj_shape:
+        BT, I, C = (int(v) for v in args.proj_shape.split(","))
     g = torch.Generator().manual_seed(7)
     x = torch.randn(BT, I, generator=g).to(torch.bfloat16).to(dev)
     W = (torch.randn(C, I, generator=g) / I ** 0.5).to(torch.bfloat16).to(dev)
@@ -95,7 +99,8 @@ def proj_bench(args, w, fn, dev, _lib):
     return {"metric": "input projection TFLOP/s (forward + backward)", "value": ach, "unit": "TFLOP/s",
             "higher_is_better": True, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": w["name"], "rows": BT, "I": I, "C": C,
+            "config": {"workload": w["name"] if not args.proj_shape else "projection %dx%dx%d" % (BT, I, C),
+                       "rows": BT, "I": I, "C": C,
                        "l2": "flushed (256 MiB write) before every step, outside the event window"},
             "fwd": {"ms": f_ms, "tflops": f_fl / (f_ms / 1e3) / 1e12},
             "bwd": {"ms": b_ms, "tflops": b_fl / (b_ms / 1e3) / 1e12},

@@ -288,17 +288,100 @@ static int wgrad_splits(int B, int T, int N, int D, int G) {
   return splits < 1 ? 1 : splits;
 }
 
+// ---- db for bf16 dr: two passes over 16-byte loads ------------------------------
+// dr is [K = B T rows][Cn = G N D columns]. Pass 1: block (x, y) sums rows
+// [y rpc, (y+1) rpc) of 256 columns (8 per thread, 8 row lanes, four rows in
+// flight per lane) into partial[y][Cn] (fp32). Pass 2 adds the partials of
+// each column in chunk order. Both orders are fixed, so db is deterministic.
+constexpr int BGV_MAX_CHUNKS = 64;
+static int bgrad_chunks(int K, int Cn) {
+  const int colblocks = (Cn + 255) / 256;
+  int c = (4 * 152 + colblocks - 1) / colblocks;  // about four blocks per SM
+  if (c > BGV_MAX_CHUNKS) c = BGV_MAX_CHUNKS;
+  if (c > (K + 31) / 32) c = (K + 31) / 32;      // at least 32 rows per chunk
+  return c < 1 ? 1 : c;
+}
+
+__global__ void __launch_bounds__(256) bgrad_partial_kernel(const __nv_bfloat16* dr, float* partial, int K, int Cn,
+                                                            int rpc) {
+  __shared__ float red[8][256];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int c0 = blockIdx.x * 256 + tx * 8;
+  const int r0 = blockIdx.y * rpc, r1 = min(K, r0 + rpc);
+  float acc[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+  auto add = [&](const uint4& v) {
+    const __nv_bfloat16* h = (const __nv_bfloat16*)&v;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] += __bfloat162float(h[q]);
+  };
+  if (c0 < Cn) {  // Cn is a multiple of 8: the 8 columns are all inside
+    const __nv_bfloat16* p = dr + c0;
+    int r = r0 + ty;
+    for (; r + 24 < r1; r += 32) {
+      const uint4 v0 = *(const uint4*)(p + (size_t)r * Cn), v1 = *(const uint4*)(p + (size_t)(r + 8) * Cn);
+      const uint4 v2 = *(const uint4*)(p + (size_t)(r + 16) * Cn), v3 = *(const uint4*)(p + (size_t)(r + 24) * Cn);
+      add(v0);
+      add(v1);
+      add(v2);
+      add(v3);
+    }
+    for (; r < r1; r += 8) add(*(const uint4*)(p + (size_t)r * Cn));
+  }
+#pragma unroll
+  for (int q = 0; q < 8; ++q) red[ty][tx * 8 + q] = acc[q];
+  __syncthreads();
+  if (ty == 0 && c0 < Cn) {
+    float t[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float v = 0.0f;
+#pragma unroll
+      for (int y = 0; y < 8; ++y) v += red[y][tx * 8 + q];
+      t[q] = v;
+    }
+    float* out = partial + (size_t)blockIdx.y * Cn + c0;
+    *(float4*)out = make_float4(t[0], t[1], t[2], t[3]);
+    *(float4*)(out + 4) = make_float4(t[4], t[5], t[6], t[7]);
+  }
+}
+
+__global__ void bgrad_final_kernel(const float* partial, __nv_bfloat16* db, int Cn, int chunks) {
+  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < Cn; c += gridDim.x * blockDim.x) {
+    float v = 0.0f;
+    for (int k = 0; k < chunks; ++k) v += partial[(size_t)k * Cn + c];
+    db[c] = __float2bfloat16_rn(v);
+  }
+}
+
 size_t wgrad_scratch_bytes(int B, int T, int N, int D, int G, int dtype) {
   if (dtype != 1 || D % 8) return 0;
   int s = wgrad_splits(B, T, N, D, G);
   const int su = wgrad_umma_splits(B, T, N, D, G);
   if (su > s) s = su;
-  return s > 1 ? (size_t)s * G * N * D * D * sizeof(float) : 0;
+  const size_t dR_part = s > 1 ? (size_t)s * G * N * D * D * sizeof(float) : 0;
+  // the db partials reuse the region after the dR partials have been reduced
+  const size_t db_part = (size_t)bgrad_chunks(B * T, G * N * D) * G * N * D * sizeof(float);
+  return dR_part > db_part ? dR_part : db_part;
 }
 
-// db after the tensor-core dR: the column sums of dr.
+// db after the tensor-core dR: the column sums of dr (two passes when the
+// scratch and alignment allow, else one block per 32 columns).
 static cudaError_t bgrad_launch(const WgradArgs& a, cudaStream_t st) {
-  if (a.db) {
+  if (!a.db) return cudaSuccess;
+  const int K = a.B * a.T, Cn = a.G * a.N * a.D;
+  const int chunks = bgrad_chunks(K, Cn);
+  if (Cn % 8 == 0 && ((uintptr_t)a.dr & 15) == 0 && a.scratch &&
+      a.scratch_bytes >= (size_t)chunks * Cn * sizeof(float)) {
+    const int rpc = (K + chunks - 1) / chunks;
+    const int used = (K + rpc - 1) / rpc;  // chunks that hold rows
+    bgrad_partial_kernel<<<dim3((Cn + 255) / 256, used), 256, 0, st>>>((const __nv_bfloat16*)a.dr, a.scratch, K, Cn,
+                                                                       rpc);
+    note_launch();
+    bgrad_final_kernel<<<(Cn + 255) / 256, 256, 0, st>>>(a.scratch, (__nv_bfloat16*)a.db, Cn, used);
+    note_launch();
+  } else {
     dim3 g2((a.D + 31) / 32, a.G * a.N);
     bgrad_kernel<__nv_bfloat16><<<g2, 32 * BG_KS, 0, st>>>(a);
     note_launch();
@@ -341,12 +424,7 @@ cudaError_t wgrad_run(int dtype, const WgradArgs& a, cudaStream_t st) {
     wgrad_reduce_kernel<<<2 * 152, 256, 0, st>>>(a, splits);
     note_launch();
   }
-  if (a.db) {
-    dim3 g2((a.D + 31) / 32, a.G * a.N);
-    bgrad_kernel<__nv_bfloat16><<<g2, 32 * BG_KS, 0, st>>>(a);
-    note_launch();
-  }
-  return cudaGetLastError();
+  return bgrad_launch(a, st);
 }
 
 }  // namespace rnn
