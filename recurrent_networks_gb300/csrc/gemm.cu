@@ -38,7 +38,9 @@ template <int BN> struct GmTile {
   static constexpr int STAGES = BN == 256 ? 4 : 6;
   static constexpr int B_BYTES = BN / 64 * GM_HALF;    // the B operand's k-chunk
   static constexpr int STAGE = GM_OPERAND + B_BYTES;
-  static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+  // + alignment slack, barriers (256 B), each epilogue warp's copy of the
+  // tile's bias row (fp32)
+  static constexpr int SMEM = STAGES * STAGE + 1024 + 256 + 4 * BN * 4;
 };
 
 // K-major (128-byte swizzle): 8-row groups 1 KB apart, a 16-element k step is
@@ -70,6 +72,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
   // full[NS], empty[NS], accumulator full[2], accumulator empty[2], final
   uint64_t* bars = (uint64_t*)(sm + NS * STAGE);
   uint32_t* tslot = (uint32_t*)(bars + 2 * NS + 5);
+  float* bias_sm = (float*)(sm + NS * STAGE + 256);  // [4][BN]: the epilogue warps' bias rows
   const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[NS]);
   const uint32_t accf0 = smem_u32(&bars[2 * NS]), acce0 = accf0 + 16, finb = accf0 + 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -196,12 +199,19 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     }
   } else {  // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 = tile rows
     const int ew = warp & 3;
+    float* bsm = bias_sm + ew * BN;
     int tc = 0;
     for (int u = blockIdx.x; u < units && !failed; u += gridDim.x, ++tc) {
       int m0, n0, c0, nq, split;
       decode(u, m0, n0, c0, nq, split);
       const int b = tc & 1;
+      if (a.bias) {  // the tile's BN bias values, once per warp rather than per row
+        __syncwarp();  // the previous tile's reads are done
+        for (int c = lane; c < BN; c += 32) bsm[c] = n0 + c < a.N ? __bfloat162float(a.bias[n0 + c]) : 0.0f;
+        __syncwarp();
+      }
       mbar_wait_bounded<false>(accf0 + 8 * b, (tc >> 1) & 1, a.wait_limit_ns, a.status, failed);
+      failed = __any_sync(0xffffffffu, failed);  // the warp leaves the loop together
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int m = m0 + ew * 32 + lane;
       for (int cc = 0; cc < BN; cc += 32) {
@@ -227,10 +237,9 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
 #pragma unroll
               for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(r[8 * v + q]);
               if (a.bias) {
-                const uint4 bb = *(const uint4*)(a.bias + n + 8 * v);
-                const __nv_bfloat16* bh = (const __nv_bfloat16*)&bb;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) f[q] += __bfloat162float(bh[q]);
+                const float4 b0 = *(const float4*)(bsm + cc + 8 * v), b1 = *(const float4*)(bsm + cc + 8 * v + 4);
+                f[0] += b0.x; f[1] += b0.y; f[2] += b0.z; f[3] += b0.w;
+                f[4] += b1.x; f[5] += b1.y; f[6] += b1.z; f[7] += b1.w;
               }
               uint4 w;
               w.x = pack_bf16(__float2bfloat16_rn(f[0]), __float2bfloat16_rn(f[1]));
@@ -244,7 +253,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
             for (int c = 0; c < 32; ++c) {
               if (n + c < a.N) {
                 float v = __uint_as_float(r[c]);
-                if (a.bias) v += __bfloat162float(a.bias[n + c]);
+                if (a.bias) v += bsm[cc + c];
                 out[c] = __float2bfloat16_rn(v);
               }
             }
