@@ -19,7 +19,10 @@
 // TMA / mbarrier ring that runs ahead across tile boundaries, warp 1 issues the
 // MMAs, and warps 2-5 drain the accumulator. Tensor memory holds two
 // accumulators, so one tile's epilogue overlaps the next tile's MMAs.
+#include <math.h>
 #include <stdio.h>
+
+#include <cmath>
 
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -321,6 +324,37 @@ int num_sms() {
   return sms;
 }
 
+// Tile width and split-K count of one GEMM, from a small cost model of the
+// persistent kernel on 152 SMs: the time is the number of waves of work units
+// times one unit's MMA cycles (128 x BN x 64 per k-chunk at about 2300 MACs
+// per cycle and SM; a 128-wide tile at 85% of a 256-wide one's rate), plus,
+// with split-K, the fp32 partials written and read back (8 bytes per output
+// and split at about 2900 bytes per cycle).
+struct Tiling {
+  int BN, splits, kps;
+};
+Tiling choose_tiling(int M, int N, int K, bool split_ok) {
+  const int sms = 152, nchunk = (K + GM_BK - 1) / GM_BK;
+  Tiling best{N >= 256 ? 256 : 128, 1, nchunk};
+  double best_cost = 1e300;
+  for (int BN = 256; BN >= 128; BN -= 128) {
+    if (BN == 256 && N < 256) continue;
+    const double tiles = (double)((M + GM_TILE - 1) / GM_TILE) * ((N + BN - 1) / BN);
+    const int smax = split_ok ? (nchunk / 2 < 32 ? nchunk / 2 : 32) : 1;
+    for (int sp = 1; sp <= (smax < 1 ? 1 : smax); ++sp) {
+      const int kps = (nchunk + sp - 1) / sp, se = (nchunk + kps - 1) / kps;
+      const double waves = std::ceil(tiles * se / sms);
+      double cost = waves * GM_TILE * BN * kps * GM_BK / (2300.0 * (BN == 256 ? 1.0 : 0.85));
+      if (se > 1) cost += 8.0 * se * M * N / 2900.0;
+      if (cost < best_cost * 0.999) {
+        best_cost = cost;
+        best = Tiling{BN, se, kps};
+      }
+    }
+  }
+  return best;
+}
+
 // D[M][N] = A(m, k) B(k, n); a_kmajor: A stored [M][K] (else [K][M]); b_kmajor:
 // B stored [N][K] (else [K][N]).
 cudaError_t gemm_run(bool a_kmajor, bool b_kmajor, int M, int N, int K, const void* A, const void* B,
@@ -335,8 +369,9 @@ cudaError_t gemm_run(bool a_kmajor, bool b_kmajor, int M, int N, int K, const vo
     e = encode_tensor_map_sw128(&am, A, 5, a_kmajor ? dims_k : dims_m, a_kmajor ? box_k : box_m);
     if (e != cudaSuccess) return e;
   }
-  // 256-wide N tiles when N allows: twice the MMA work per byte loaded
-  const int BN = N >= 256 ? 256 : 128;
+  Tiling tl = choose_tiling(M, N, K, !bias && scratch);
+  if (tl.splits > 1 && scratch_bytes < (size_t)tl.splits * M * N * sizeof(float)) tl = choose_tiling(M, N, K, false);
+  const int BN = tl.BN;
   {
     const unsigned long long dims_k[5] = {(unsigned long long)K, (unsigned long long)N, 1, 1, 1};
     const unsigned long long dims_n[5] = {(unsigned long long)N, (unsigned long long)K, 1, 1, 1};
@@ -345,16 +380,10 @@ cudaError_t gemm_run(bool a_kmajor, bool b_kmajor, int M, int N, int K, const vo
     if (e != cudaSuccess) return e;
   }
   const int tiles = ((M + GM_TILE - 1) / GM_TILE) * ((N + BN - 1) / BN);
-  const int nchunk = (K + GM_BK - 1) / GM_BK;
-  int splits = (152 + tiles - 1) / tiles;
-  if (splits > nchunk / 2) splits = nchunk / 2;
-  if (splits > 32) splits = 32;
-  if (splits < 1) splits = 1;
-  if (splits > 1 && (bias || !scratch || scratch_bytes < (size_t)splits * M * N * sizeof(float))) splits = 1;
   GemmArgs g{};
   g.M = M; g.N = N; g.K = K;
-  g.kps = (nchunk + splits - 1) / splits;
-  g.splits = (nchunk + g.kps - 1) / g.kps;
+  g.kps = tl.kps;
+  g.splits = tl.splits;
   g.C = (__nv_bfloat16*)C;
   g.partial = scratch;
   g.bias = (const __nv_bfloat16*)bias;
@@ -383,15 +412,7 @@ cudaError_t gemm_run(bool a_kmajor, bool b_kmajor, int M, int N, int K, const vo
   return cudaGetLastError();
 }
 
-int proj_splits_bound(int M, int N, int K) {
-  const int BN = N >= 256 ? 256 : 128;  // the tile width gemm_run picks
-  const int tiles = ((M + GM_TILE - 1) / GM_TILE) * ((N + BN - 1) / BN);
-  const int nchunk = (K + GM_BK - 1) / GM_BK;
-  int splits = (152 + tiles - 1) / tiles;
-  if (splits > nchunk / 2) splits = nchunk / 2;
-  if (splits > 32) splits = 32;
-  return splits < 1 ? 1 : splits;
-}
+int proj_splits_bound(int M, int N, int K) { return choose_tiling(M, N, K, true).splits; }
 
 bool proj_dims_ok(int BT, int I, int C) {
   // TMA: 16-byte row strides (I, C multiples of 8); boxes of 64 along I and C
