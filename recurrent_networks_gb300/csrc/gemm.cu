@@ -37,13 +37,14 @@ constexpr int GM_TILE = 128, GM_BK = 64;
 constexpr int GM_HALF = 64 * 128;                 // a 64 x 64 bf16 box
 constexpr int GM_OPERAND = 2 * GM_HALF;           // the A operand's k-chunk of a tile
 constexpr int GM_THREADS = 192;                   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int GM_STAGING = 2 * 2048;              // per epilogue warp: two 32-row x 64-byte store boxes
 template <int BN> struct GmTile {
   static constexpr int STAGES = BN == 256 ? 4 : 6;
   static constexpr int B_BYTES = BN / 64 * GM_HALF;    // the B operand's k-chunk
   static constexpr int STAGE = GM_OPERAND + B_BYTES;
-  // + alignment slack, barriers (256 B), each epilogue warp's copy of the
-  // tile's bias row (fp32)
-  static constexpr int SMEM = STAGES * STAGE + 1024 + 256 + 4 * BN * 4;
+  // + alignment slack, each epilogue warp's two 2 KB store staging buffers,
+  // barriers (256 B), each epilogue warp's copy of the tile's bias row (fp32)
+  static constexpr int SMEM = STAGES * STAGE + 1024 + 4 * GM_STAGING + 256 + 4 * BN * 4;
 };
 
 // K-major (128-byte swizzle): 8-row groups 1 KB apart, a 16-element k step is
@@ -55,6 +56,19 @@ __device__ __forceinline__ uint64_t gm_desc(uint32_t base, bool kmajor, int k16)
   return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
          (1ull << 46) | (2ull << 61);
 }
+
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (lane = row)
+__device__ __forceinline__ void tmem_ld32(uint32_t* r, uint32_t taddr) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 struct GemmArgs {
   int M, N, K;
@@ -68,14 +82,16 @@ struct GemmArgs {
 
 template <bool AK, bool BK, int BN>
 __global__ void __launch_bounds__(GM_THREADS, 1)
-    gemm_umma_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap, GemmArgs a) {
+    gemm_umma_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
+                     const __grid_constant__ CUtensorMap cmap, GemmArgs a) {
   constexpr int NS = GmTile<BN>::STAGES, STAGE = GmTile<BN>::STAGE;
   extern __shared__ unsigned char gm_raw[];
   unsigned char* sm = (unsigned char*)(((uintptr_t)gm_raw + 1023) & ~(uintptr_t)1023);
   // full[NS], empty[NS], accumulator full[2], accumulator empty[2], final
-  uint64_t* bars = (uint64_t*)(sm + NS * STAGE);
+  unsigned char* staging = sm + NS * STAGE;  // [4][2][2 KB], 1 KB aligned (64-byte swizzle)
+  uint64_t* bars = (uint64_t*)(staging + 4 * GM_STAGING);
   uint32_t* tslot = (uint32_t*)(bars + 2 * NS + 5);
-  float* bias_sm = (float*)(sm + NS * STAGE + 256);  // [4][BN]: the epilogue warps' bias rows
+  float* bias_sm = (float*)(staging + 4 * GM_STAGING + 256);  // [4][BN]: the epilogue warps' bias rows
   const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[NS]);
   const uint32_t accf0 = smem_u32(&bars[2 * NS]), acce0 = accf0 + 16, finb = accf0 + 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -203,37 +219,61 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
   } else {  // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 = tile rows
     const int ew = warp & 3;
     float* bsm = bias_sm + ew * BN;
-    int tc = 0;
+    unsigned char* stg = staging + ew * GM_STAGING;
+    int sbuf = 0, tc = 0;
+    // each warp keeps the tile's BN bias values in shared memory (read by
+    // every row) and the next tile's in registers (loaded one tile ahead)
+    float bv[BN / 32];
+    auto load_bias = [&](int nb0) {
+#pragma unroll
+      for (int q = 0; q < BN / 32; ++q) {
+        const int c = nb0 + lane + 32 * q;
+        bv[q] = c < a.N ? __bfloat162float(__ldg(a.bias + c)) : 0.0f;
+      }
+    };
+    if (a.bias && (int)blockIdx.x < units) {
+      int m1, n1, c1, q1, s1;
+      decode(blockIdx.x, m1, n1, c1, q1, s1);
+      load_bias(n1);
+    }
     for (int u = blockIdx.x; u < units && !failed; u += gridDim.x, ++tc) {
       int m0, n0, c0, nq, split;
       decode(u, m0, n0, c0, nq, split);
       const int b = tc & 1;
-      if (a.bias) {  // the tile's BN bias values, once per warp rather than per row
-        __syncwarp();  // the previous tile's reads are done
-        for (int c = lane; c < BN; c += 32) bsm[c] = n0 + c < a.N ? __bfloat162float(a.bias[n0 + c]) : 0.0f;
-        __syncwarp();
-      }
       mbar_wait_bounded<false>(accf0 + 8 * b, (tc >> 1) & 1, a.wait_limit_ns, a.status, failed);
       failed = __any_sync(0xffffffffu, failed);  // the warp leaves the loop together
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int m = m0 + ew * 32 + lane;
-      for (int cc = 0; cc < BN; cc += 32) {
-        uint32_t r[32];
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-              "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-              "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-              "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-            : "r"(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(b * BN + cc)));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (m >= a.M || n0 + cc >= a.N || failed) continue;
-        const int n = n0 + cc;
-        if (a.splits == 1) {
-          __nv_bfloat16* out = a.C + (size_t)m * a.N + n;
-          if (n + 32 <= a.N) {  // 16-byte stores (N is a multiple of 8)
+      if (a.bias) {
+        __syncwarp();  // the previous tile's reads of bsm are done
+#pragma unroll
+        for (int q = 0; q < BN / 32; ++q) bsm[lane + 32 * q] = bv[q];
+        __syncwarp();
+        // the next tile's bias, in flight while this tile drains
+        const int un = u + gridDim.x;
+        if (un < units) {
+          int m1, n1, c1, q1, s1;
+          decode(un, m1, n1, c1, q1, s1);
+          load_bias(n1);
+        }
+      }
+      // Each 32-column chunk of the warp's 32 rows goes out through shared
+      // memory as TMA stores (one 32 x 32 bf16 box, or two 32 x 16 fp32 boxes
+      // of split-K partials) from alternating staging buffers; TMA clips the
+      // boxes at the matrix edges.
+      // The TMEM read of the next 32-column chunk is in flight while this one
+      // is converted and stored.
+      const uint32_t trow = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(b * BN);
+      auto emit = [&](const uint32_t* r, int cc) {
+        if (n0 + cc >= a.N || m0 + ew * 32 >= a.M || failed) return;  // boxes start inside the matrix
+        const int nbox = a.splits == 1 ? 1 : 2;
+        for (int h = 0; h < nbox; ++h) {
+          if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous box has been read
+          __syncwarp();
+          // this lane's row: 64 bytes, its 16-byte pieces in the 64-byte
+          // swizzle the store's tensor map reads (piece v at v ^ (row / 2) % 4)
+          uint4* dst = (uint4*)(stg + sbuf * 2048 + lane * 64);
+          const int sw = (lane >> 1) & 3;
+          if (a.splits == 1) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               float f[8];
@@ -249,37 +289,46 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
               w.y = pack_bf16(__float2bfloat16_rn(f[2]), __float2bfloat16_rn(f[3]));
               w.z = pack_bf16(__float2bfloat16_rn(f[4]), __float2bfloat16_rn(f[5]));
               w.w = pack_bf16(__float2bfloat16_rn(f[6]), __float2bfloat16_rn(f[7]));
-              *(uint4*)(out + 8 * v) = w;
+              dst[v ^ sw] = w;
             }
           } else {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              if (n + c < a.N) {
-                float v = __uint_as_float(r[c]);
-                if (a.bias) v += bsm[cc + c];
-                out[c] = __float2bfloat16_rn(v);
-              }
-            }
+            for (int v = 0; v < 4; ++v)
+              dst[v ^ sw] = h == 0 ? make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3])
+                                   : make_uint4(r[16 + 4 * v], r[17 + 4 * v], r[18 + 4 * v], r[19 + 4 * v]);
           }
-        } else {
-          float* out = a.partial + ((size_t)split * a.M + m) * a.N + n;
-          if (n + 32 <= a.N) {
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              *(float4*)(out + 4 * v) = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                                    __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-          } else {
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-              if (n + c < a.N) out[c] = __uint_as_float(r[c]);
+          fence_proxy_async_smem();  // the generic writes above are read by the TMA store
+          __syncwarp();
+          if (lane == 0) {
+            const uint32_t src = smem_u32(stg + sbuf * 2048);
+            if (a.splits == 1)
+              tma_store_5d(&cmap, src, n0 + cc, m0 + ew * 32, 0, 0, 0);
+            else
+              tma_store_5d(&cmap, src, n0 + cc + 16 * h, m0 + ew * 32, split, 0, 0);
+            bulk_commit_group();
           }
+          sbuf ^= 1;
         }
+      };
+      uint32_t ra[32], rb[32];
+      tmem_ld32(ra, trow);
+      tmem_wait_ld();
+#pragma unroll 1
+      for (int cc = 0; cc < BN; cc += 64) {
+        tmem_ld32(rb, trow + (uint32_t)(cc + 32));
+        emit(ra, cc);
+        tmem_wait_ld();
+        if (cc + 64 < BN) tmem_ld32(ra, trow + (uint32_t)(cc + 64));
+        emit(rb, cc + 32);
+        tmem_wait_ld();
       }
       // accumulator b is free for tile tc + 2
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(acce0 + 8 * b);
     }
+    if (lane == 0) bulk_wait_group_all();  // every store has landed before the CTA retires
+    __syncwarp();
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
@@ -379,6 +428,20 @@ cudaError_t gemm_run(bool a_kmajor, bool b_kmajor, int M, int N, int K, const vo
     e = encode_tensor_map_sw128(&bm, B, 5, b_kmajor ? dims_k : dims_n, b_kmajor ? box_k : box_n);
     if (e != cudaSuccess) return e;
   }
+  // the output: C [M][N] bf16 in 32 x 32 boxes, or the split-K partials
+  // [splits][M][N] fp32 in 16-column x 32-row boxes (one split per plane)
+  CUtensorMap cm;
+  if (tl.splits == 1) {
+    const unsigned long long dims[5] = {(unsigned long long)N, (unsigned long long)M, 1, 1, 1};
+    const unsigned int box[5] = {32, 32, 1, 1, 1};
+    e = encode_tensor_map_swizzled(&cm, C, 2, 5, dims, box, 64);
+  } else {
+    const unsigned long long dims[5] = {(unsigned long long)N, (unsigned long long)M, (unsigned long long)tl.splits,
+                                        1, 1};
+    const unsigned int box[5] = {16, 32, 1, 1, 1};
+    e = encode_tensor_map_swizzled(&cm, scratch, 4, 5, dims, box, 64);
+  }
+  if (e != cudaSuccess) return e;
   const int tiles = ((M + GM_TILE - 1) / GM_TILE) * ((N + BN - 1) / BN);
   GemmArgs g{};
   g.M = M; g.N = N; g.K = K;
@@ -389,7 +452,7 @@ cudaError_t gemm_run(bool a_kmajor, bool b_kmajor, int M, int N, int K, const vo
   g.bias = (const __nv_bfloat16*)bias;
   g.status = status;
   g.wait_limit_ns = 2000000000ull;
-  void (*k)(const CUtensorMap, const CUtensorMap, GemmArgs);
+  void (*k)(const CUtensorMap, const CUtensorMap, const CUtensorMap, GemmArgs);
   if (BN == 256)
     k = a_kmajor ? (b_kmajor ? gemm_umma_kernel<true, true, 256> : gemm_umma_kernel<true, false, 256>)
                  : (b_kmajor ? gemm_umma_kernel<false, true, 256> : gemm_umma_kernel<false, false, 256>);
@@ -403,7 +466,7 @@ cudaError_t gemm_run(bool a_kmajor, bool b_kmajor, int M, int N, int K, const vo
   // accumulators take the whole SM), never more CTAs than work units
   const int units = tiles * g.splits;
   const int ctas = units < num_sms() ? units : num_sms();
-  k<<<ctas, GM_THREADS, smem, st>>>(am, bm, g);
+  k<<<ctas, GM_THREADS, smem, st>>>(am, bm, cm, g);
   note_launch();
   if (g.splits > 1) {
     gemm_reduce_kernel<<<2 * 152, 256, 0, st>>>(scratch, (__nv_bfloat16*)C, (size_t)M * N, g.splits);

@@ -121,6 +121,10 @@ cudaError_t encode_tensor_map_bf16(void* map, const void* base, int rank,
                                    const unsigned long long* dims, const unsigned int* box);
 cudaError_t encode_tensor_map(void* map, const void* base, int elem_bytes, int rank,
                               const unsigned long long* dims, const unsigned int* box);
+// the same with the shared-memory side swizzled in spans of swizzle_bytes
+// (0, 32, 64 or 128)
+cudaError_t encode_tensor_map_swizzled(void* map, const void* base, int elem_bytes, int rank,
+                                       const unsigned long long* dims, const unsigned int* box, int swizzle_bytes);
 // bf16, 128-byte swizzle (box[0] * 2 <= 128): the layout the tcgen05 operands read
 cudaError_t encode_tensor_map_sw128(void* map, const void* base, int rank, const unsigned long long* dims,
                                     const unsigned int* box);

@@ -42,6 +42,11 @@ cudaError_t encode_tensor_map_sw128(void* map, const void* base, int rank, const
 
 cudaError_t encode_tensor_map(void* map, const void* base, int elem_bytes, int rank,
                               const unsigned long long* dims, const unsigned int* box) {
+  return encode_tensor_map_swizzled(map, base, elem_bytes, rank, dims, box, 0);
+}
+
+cudaError_t encode_tensor_map_swizzled(void* map, const void* base, int elem_bytes, int rank,
+                                       const unsigned long long* dims, const unsigned int* box, int swizzle_bytes) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn || rank < 1 || rank > 5 || (elem_bytes != 2 && elem_bytes != 4)) return cudaErrorNotSupported;
   cuuint64_t gdim[5], gstride[4];
@@ -56,8 +61,12 @@ cudaError_t encode_tensor_map(void* map, const void* base, int elem_bytes, int r
   }
   const CUtensorMapDataType ty =
       elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const CUtensorMapSwizzle sw = swizzle_bytes == 64    ? CU_TENSOR_MAP_SWIZZLE_64B
+                                : swizzle_bytes == 32  ? CU_TENSOR_MAP_SWIZZLE_32B
+                                : swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                       : CU_TENSOR_MAP_SWIZZLE_NONE;
   CUresult r = fn((CUtensorMap*)map, ty, (cuuint32_t)rank, (void*)base, gdim,
-                  gstride, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  gstride, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
