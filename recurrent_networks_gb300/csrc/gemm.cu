@@ -24,6 +24,7 @@
 
 #include <cmath>
 
+#include "colsum.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
 #include "rnn.h"
@@ -501,7 +502,9 @@ extern "C" {
 size_t rnn_input_proj_workspace_size(int BT, int I, int C) {
   if (!proj_dims_ok(BT, I, C)) return 0;
   const int s = proj_splits_bound(C, I, BT);  // dW_x: M = C, N = I, K = B T
-  return 256 + (s > 1 ? (size_t)s * C * I * sizeof(float) : 0);
+  const size_t dW_part = s > 1 ? (size_t)s * C * I * sizeof(float) : 0;
+  const size_t db_part = colsum_scratch_bytes(BT, C);  // the dbias partials, after dW_x
+  return 256 + (dW_part > db_part ? dW_part : db_part);
 }
 
 int rnn_input_proj_fwd(int BT, int I, int C, const void* x, const void* W, const void* bias, void* Wx,
@@ -537,8 +540,11 @@ int rnn_input_proj_bwd(int BT, int I, int C, const void* x, const void* W, const
     if (rc) return rc;
   }
   if (dbias) {
-    colsum_kernel<<<(C + 31) / 32, 1024, 0, st>>>((const __nv_bfloat16*)dWx, (__nv_bfloat16*)dbias, BT, C);
-    note_launch();
+    float* scratch = (float*)((char*)workspace + 256);
+    if (!colsum_bf16((const __nv_bfloat16*)dWx, (__nv_bfloat16*)dbias, BT, C, scratch, ws_bytes - 256, st)) {
+      colsum_kernel<<<(C + 31) / 32, 1024, 0, st>>>((const __nv_bfloat16*)dWx, (__nv_bfloat16*)dbias, BT, C);
+      note_launch();
+    }
     rc = cuda_status(cudaGetLastError());
   }
   return rc;

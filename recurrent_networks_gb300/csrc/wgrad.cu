@@ -7,6 +7,7 @@
 // gate factor). h_{t-1} is read from the forward's states (t > 0) or from the
 // initial states (t = 0). The plain fp32-FMA tiled version serves fp32
 // storage; bf16 storage goes through the tensor-core version further down.
+#include "colsum.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -288,73 +289,6 @@ static int wgrad_splits(int B, int T, int N, int D, int G) {
   return splits < 1 ? 1 : splits;
 }
 
-// ---- db for bf16 dr: two passes over 16-byte loads ------------------------------
-// dr is [K = B T rows][Cn = G N D columns]. Pass 1: block (x, y) sums rows
-// [y rpc, (y+1) rpc) of 256 columns (8 per thread, 8 row lanes, four rows in
-// flight per lane) into partial[y][Cn] (fp32). Pass 2 adds the partials of
-// each column in chunk order. Both orders are fixed, so db is deterministic.
-constexpr int BGV_MAX_CHUNKS = 64;
-static int bgrad_chunks(int K, int Cn) {
-  const int colblocks = (Cn + 255) / 256;
-  int c = (4 * 152 + colblocks - 1) / colblocks;  // about four blocks per SM
-  if (c > BGV_MAX_CHUNKS) c = BGV_MAX_CHUNKS;
-  if (c > (K + 31) / 32) c = (K + 31) / 32;      // at least 32 rows per chunk
-  return c < 1 ? 1 : c;
-}
-
-__global__ void __launch_bounds__(256) bgrad_partial_kernel(const __nv_bfloat16* dr, float* partial, int K, int Cn,
-                                                            int rpc) {
-  __shared__ float red[8][256];
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int c0 = blockIdx.x * 256 + tx * 8;
-  const int r0 = blockIdx.y * rpc, r1 = min(K, r0 + rpc);
-  float acc[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-  auto add = [&](const uint4& v) {
-    const __nv_bfloat16* h = (const __nv_bfloat16*)&v;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) acc[q] += __bfloat162float(h[q]);
-  };
-  if (c0 < Cn) {  // Cn is a multiple of 8: the 8 columns are all inside
-    const __nv_bfloat16* p = dr + c0;
-    int r = r0 + ty;
-    for (; r + 24 < r1; r += 32) {
-      const uint4 v0 = *(const uint4*)(p + (size_t)r * Cn), v1 = *(const uint4*)(p + (size_t)(r + 8) * Cn);
-      const uint4 v2 = *(const uint4*)(p + (size_t)(r + 16) * Cn), v3 = *(const uint4*)(p + (size_t)(r + 24) * Cn);
-      add(v0);
-      add(v1);
-      add(v2);
-      add(v3);
-    }
-    for (; r < r1; r += 8) add(*(const uint4*)(p + (size_t)r * Cn));
-  }
-#pragma unroll
-  for (int q = 0; q < 8; ++q) red[ty][tx * 8 + q] = acc[q];
-  __syncthreads();
-  if (ty == 0 && c0 < Cn) {
-    float t[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      float v = 0.0f;
-#pragma unroll
-      for (int y = 0; y < 8; ++y) v += red[y][tx * 8 + q];
-      t[q] = v;
-    }
-    float* out = partial + (size_t)blockIdx.y * Cn + c0;
-    *(float4*)out = make_float4(t[0], t[1], t[2], t[3]);
-    *(float4*)(out + 4) = make_float4(t[4], t[5], t[6], t[7]);
-  }
-}
-
-__global__ void bgrad_final_kernel(const float* partial, __nv_bfloat16* db, int Cn, int chunks) {
-  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < Cn; c += gridDim.x * blockDim.x) {
-    float v = 0.0f;
-    for (int k = 0; k < chunks; ++k) v += partial[(size_t)k * Cn + c];
-    db[c] = __float2bfloat16_rn(v);
-  }
-}
-
 size_t wgrad_scratch_bytes(int B, int T, int N, int D, int G, int dtype) {
   if (dtype != 1 || D % 8) return 0;
   int s = wgrad_splits(B, T, N, D, G);
@@ -362,7 +296,7 @@ size_t wgrad_scratch_bytes(int B, int T, int N, int D, int G, int dtype) {
   if (su > s) s = su;
   const size_t dR_part = s > 1 ? (size_t)s * G * N * D * D * sizeof(float) : 0;
   // the db partials reuse the region after the dR partials have been reduced
-  const size_t db_part = (size_t)bgrad_chunks(B * T, G * N * D) * G * N * D * sizeof(float);
+  const size_t db_part = colsum_scratch_bytes(B * T, G * N * D);
   return dR_part > db_part ? dR_part : db_part;
 }
 
@@ -371,16 +305,8 @@ size_t wgrad_scratch_bytes(int B, int T, int N, int D, int G, int dtype) {
 static cudaError_t bgrad_launch(const WgradArgs& a, cudaStream_t st) {
   if (!a.db) return cudaSuccess;
   const int K = a.B * a.T, Cn = a.G * a.N * a.D;
-  const int chunks = bgrad_chunks(K, Cn);
-  if (Cn % 8 == 0 && ((uintptr_t)a.dr & 15) == 0 && a.scratch &&
-      a.scratch_bytes >= (size_t)chunks * Cn * sizeof(float)) {
-    const int rpc = (K + chunks - 1) / chunks;
-    const int used = (K + rpc - 1) / rpc;  // chunks that hold rows
-    bgrad_partial_kernel<<<dim3((Cn + 255) / 256, used), 256, 0, st>>>((const __nv_bfloat16*)a.dr, a.scratch, K, Cn,
-                                                                       rpc);
-    note_launch();
-    bgrad_final_kernel<<<(Cn + 255) / 256, 256, 0, st>>>(a.scratch, (__nv_bfloat16*)a.db, Cn, used);
-    note_launch();
+  if (colsum_bf16((const __nv_bfloat16*)a.dr, (__nv_bfloat16*)a.db, K, Cn, a.scratch, a.scratch_bytes, st)) {
+    // dr is [K rows][G N D columns]; db[g, n, j] is column (g, n, j)
   } else {
     dim3 g2((a.D + 31) / 32, a.G * a.N);
     bgrad_kernel<__nv_bfloat16><<<g2, 32 * BG_KS, 0, st>>>(a);
