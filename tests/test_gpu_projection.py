@@ -28,9 +28,11 @@ def _close(got, ref, what):
 
 
 # (BT, I, C): ragged 128-tiles in every dimension, K shorter than one 64-chunk
-# (BT = 37 for dW), several K chunks, a dW long enough for split-K partials
+# (BT = 37 for dW), several K chunks, a dW long enough for split-K partials;
+# the last takes 128 x 256 tiles in all three GEMMs (dW split three ways)
+# with ragged edges in every dimension
 CASES = [(256, 64, 128, True), (300, 72, 200, False), (37, 128, 96, True), (2048, 256, 768, True),
-         (8192, 256, 3072, False)]
+         (8192, 256, 3072, False), (8200, 1000, 3000, True)]
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "BT%dI%dC%d%s" % (c[0], c[1], c[2], "-bias" if c[3] else ""))
