@@ -1,8 +1,9 @@
 // Column sums of a bf16 matrix [rows][cols] into bf16, in two deterministic
 // passes over 16-byte loads. Pass 1: block (x, y) sums rows [y rpc, (y+1) rpc)
 // of 256 columns (8 per thread, 8 row lanes, four rows in flight per lane)
-// into fp32 partial[y][cols]. Pass 2 adds each column's partials in chunk
-// order. Both orders are fixed, so the result does not depend on timing.
+// into fp32 partial[y][cols]. Pass 2 adds each column's partials in eight
+// interleaved lanes, then the lanes in order. Both orders are fixed, so the
+// result does not depend on timing.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -71,11 +72,23 @@ __global__ void __launch_bounds__(256) colsum_partial_kernel(const __nv_bfloat16
   }
 }
 
-__global__ void colsum_final_kernel(const float* partial, __nv_bfloat16* out, int cols, int chunks) {
-  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += gridDim.x * blockDim.x) {
-    float v = 0.0f;
-    for (int k = 0; k < chunks; ++k) v += partial[(size_t)k * cols + c];
-    out[c] = __float2bfloat16_rn(v);
+// 32 columns per block, 8 lanes each summing chunks k = lane, lane + 8, ...,
+// then the 8 lane sums in lane order
+__global__ void __launch_bounds__(256) colsum_final_kernel(const float* partial, __nv_bfloat16* out, int cols,
+                                                           int chunks) {
+  __shared__ float red[8][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + tx;
+  float v = 0.0f;
+  if (c < cols)
+    for (int k = ty; k < chunks; k += 8) v += partial[(size_t)k * cols + c];
+  red[ty][tx] = v;
+  __syncthreads();
+  if (ty == 0 && c < cols) {
+    float t = 0.0f;
+#pragma unroll
+    for (int y = 0; y < 8; ++y) t += red[y][tx];
+    out[c] = __float2bfloat16_rn(t);
   }
 }
 
@@ -92,7 +105,7 @@ inline bool colsum_bf16(const __nv_bfloat16* X, __nv_bfloat16* out, int rows, in
   const int used = (rows + rpc - 1) / rpc;  // chunks that hold rows
   colsum_partial_kernel<<<dim3((cols + 255) / 256, used), 256, 0, st>>>(X, scratch, rows, cols, rpc);
   note_launch();
-  colsum_final_kernel<<<(cols + 255) / 256, 256, 0, st>>>(scratch, out, cols, used);
+  colsum_final_kernel<<<(cols + 31) / 32, 256, 0, st>>>(scratch, out, cols, used);
   note_launch();
   return true;
 }
