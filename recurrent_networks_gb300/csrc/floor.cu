@@ -3,7 +3,8 @@
 // the C slices of the previous step (mbarrier transaction count, bounded),
 // order the staged slice for the async proxy, a CTA barrier, then one bulk
 // copy per peer (shared::cta -> shared::cluster) into the peer's next buffer,
-// issued by lane 0 of the warps in the same rotation as the forward kernel.
+// issued as in the forward kernel: lane q of warp w sends to peer
+// rank + w + q warps, with the cluster addresses computed once.
 #include <stdio.h>
 
 #include "kernels.cuh"
@@ -38,6 +39,17 @@ __global__ void __launch_bounds__(256, 1) exchange_floor_kernel(int slice_bytes,
     if (steps > 1) mbar_arrive_expect_tx(bar0 + 8, hbytes);
     if (steps > 2) mbar_arrive_expect_tx(bar0, hbytes);
   }
+  const int my_c = warp + lane * nwarps;
+  const bool sender = lane < (C + nwarps - 1) / nwarps && my_c < C;
+  uint32_t rdst0 = 0, rdst1 = 0, rbar0 = 0, rbar1 = 0;
+  if (sender) {
+    int peer = (int)rank + my_c;
+    if (peer >= C) peer -= C;
+    rdst0 = mapa_shared(smem_u32(hbuf + (size_t)rank * slice_bytes), (uint32_t)peer);
+    rdst1 = mapa_shared(smem_u32(hbuf + (size_t)C * slice_bytes + (size_t)rank * slice_bytes), (uint32_t)peer);
+    rbar0 = mapa_shared(bar0, (uint32_t)peer);
+    rbar1 = mapa_shared(bar0 + 8, (uint32_t)peer);
+  }
   bool failed = false;
   uint32_t ph0 = 0, ph1 = 0;
   const long long t0 = clock64();
@@ -50,17 +62,9 @@ __global__ void __launch_bounds__(256, 1) exchange_floor_kernel(int slice_bytes,
     }
     fence_proxy_async_smem();
     __syncthreads();
-    if (t + 1 < steps && lane == 0) {
-      const uint32_t dst = smem_u32(hbuf + (size_t)(p ^ 1) * C * slice_bytes + (size_t)rank * slice_bytes);
-      const uint32_t bar = bar0 + 8 * (p ^ 1);
-      const uint32_t src = smem_u32(stage + (size_t)p * slice_bytes);
-      for (int c = warp; c < C; c += nwarps) {
-        int peer = (int)rank + c;
-        if (peer >= C) peer -= C;
-        bulk_copy_to_peer(mapa_shared(dst, (uint32_t)peer), src, (uint32_t)slice_bytes,
-                          mapa_shared(bar, (uint32_t)peer));
-      }
-    }
+    if (t + 1 < steps && sender)  // into the peer's buffer p ^ 1
+      bulk_copy_to_peer(p ? rdst0 : rdst1, smem_u32(stage + (size_t)p * slice_bytes), (uint32_t)slice_bytes,
+                        p ? rbar0 : rbar1);
   }
   const long long t1 = clock64();
   __syncthreads();

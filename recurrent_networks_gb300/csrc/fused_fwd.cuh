@@ -143,10 +143,23 @@ __global__ void __launch_bounds__(256, 1)
 
   bool failed = false;
   uint32_t ph0 = 0, ph1 = 0;
-  // lane 0 of warp w sends this CTA's slice to the peers rank + w, rank + w +
-  // warps, ... (mod C), one bulk copy each: the copies of a step are issued by
-  // all warps side by side rather than one after another by a single warp
+  // lane q of warp w sends this CTA's slice to the peer rank + w + q warps
+  // (mod C), one bulk copy each: the copies of a step leave side by side, one
+  // instruction per warp, rather than one after another. Each sender's
+  // cluster addresses (the peer's h buffer and barrier, for both parities)
+  // are fixed for the kernel.
   const int nwarps = nthr >> 5;
+  const int my_c = warp + lane * nwarps;
+  const bool sender = !GRIDX && lane < (C + nwarps - 1) / nwarps && my_c < C;
+  uint32_t rdst0 = 0, rdst1 = 0, rbar0 = 0, rbar1 = 0;
+  if (sender) {
+    int peer = (int)rank + my_c;
+    if (peer >= C) peer -= C;
+    rdst0 = mapa_shared(smem_u32(hbuf + (size_t)rank * BC * UP), (uint32_t)peer);
+    rdst1 = mapa_shared(smem_u32(hbuf + HB + (size_t)rank * BC * UP), (uint32_t)peer);
+    rbar0 = mapa_shared(full_bar0, (uint32_t)peer);
+    rbar1 = mapa_shared(full_bar0 + 8, (uint32_t)peer);
+  }
 
   const bool tracer = a.trace && blockIdx.x == 0 && tid == 0;
 #define RNN_TRACE(k)                                                                    \
@@ -308,15 +321,8 @@ __global__ void __launch_bounds__(256, 1)
     // have landed (so their reads of stage[p] are over).
     if (GRIDX) {
       if (t + 1 < TT && tid == 0) counter_publish(a.counters + grp);
-    } else if (t + 1 < TT && lane == 0) {
-      const uint32_t dst = smem_u32(hbuf + (p ^ 1) * HB + (size_t)rank * BC * UP);
-      const uint32_t bar = full_bar0 + 8 * (p ^ 1);
-      const uint32_t src = smem_u32(stage + p * BC * UP);
-      for (int c = warp; c < C; c += nwarps) {
-        int peer = (int)rank + c;
-        if (peer >= C) peer -= C;
-        bulk_copy_to_peer(mapa_shared(dst, (uint32_t)peer), src, slice_bytes, mapa_shared(bar, (uint32_t)peer));
-      }
+    } else if (t + 1 < TT && sender) {  // into the peer's buffer p ^ 1
+      bulk_copy_to_peer(p ? rdst0 : rdst1, smem_u32(stage + p * BC * UP), slice_bytes, p ? rbar0 : rbar1);
     }
     RNN_TRACE(7)
     // Wx[:, t + NS] into the ring slot this step's update has finished reading
