@@ -86,11 +86,16 @@ __global__ void __launch_bounds__(256, 1)
   }
   // carried state gradients of this thread's (batch row, unit) pairs
   // e = tid + k * blockDim (k < FUSED_PPT), in registers for the whole scan
+  // and their (row, unit) coordinates, divided once here rather than every step
   float dsr[FUSED_PPT][S];
+  int prow[FUSED_PPT], punit[FUSED_PPT];
 #pragma unroll
-  for (int k = 0; k < FUSED_PPT; ++k)
+  for (int k = 0; k < FUSED_PPT; ++k) {
+    prow[k] = (tid + k * nthr) / U;
+    punit[k] = tid + k * nthr - prow[k] * U;
 #pragma unroll
     for (int s = 0; s < S; ++s) dsr[k][s] = 0.0f;
+  }
   // resident R fragments: A[m = row i][k = (g, j)] = R[g, n, i, u0 + j]
   uint32_t afr[MT][KTM][4];
   {
@@ -181,7 +186,7 @@ __global__ void __launch_bounds__(256, 1)
     for (int kp = 0; kp < FUSED_PPT; ++kp) {
       const int e = tid + kp * nthr;
       if (e >= nb * U) break;
-      const int b = e / U, u = e - b * U;
+      const int b = prow[kp], u = punit[kp];
       float pre[P], sp[S], sn[S], dsn[S], dx[G], dr[G], dsp[S];
 #pragma unroll
       for (int kk = 0; kk < P; ++kk) pre[kk] = tp[(b * K + kk) * U + u];

@@ -95,10 +95,15 @@ __global__ void __launch_bounds__(256, 1)
   // Each thread owns the (batch row, unit) pairs e = tid + k * blockDim
   // (k < FUSED_PPT) for the whole sequence: their carried states (fp32) and
   // biases live in registers.
+  // The pairs' (row, unit) coordinates are fixed for the kernel: divided
+  // once here, not every step.
   float csr[FUSED_PPT][S], bsr[FUSED_PPT][G];
+  int pb[FUSED_PPT], pu[FUSED_PPT];
 #pragma unroll
   for (int k = 0; k < FUSED_PPT; ++k) {
     const int e = tid + k * nthr, b = e / U, u = e - b * U;
+    pb[k] = b;
+    pu[k] = u;
     const bool own = e < nb * U;
 #pragma unroll
     for (int s = 0; s < S; ++s)
@@ -107,6 +112,10 @@ __global__ void __launch_bounds__(256, 1)
     for (int g = 0; g < G; ++g)
       bsr[k][g] = own ? __bfloat162float(bias[((size_t)g * N + n) * D + u0 + u]) : 0.0f;
   }
+
+  // the first k-tile of this warp's K slice: source block and column group
+  const int U16 = U / 16;
+  const int ktile_sblk0 = (ks * KT) / U16, ktile_j0 = ks * KT - ktile_sblk0 * U16;
 
   // resident R fragments: A[m = unit j][k = input i] = R[g, n, i, j]. Warps
   // past the (U/16) * KS that the product needs only join the cell update.
@@ -217,11 +226,16 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) acc[gi][c2][nt][q] = 0.0f;
     const uint32_t hb = smem_u32(hbuf + p * HB);
+    // k-tile kt holds inputs 16 (ks KT + kt) .. + 15, in the block of source
+    // CTA sblk at column 16 jj; both advance without a division
+    int sblk = ktile_sblk0, jj = ktile_j0;
 #pragma unroll
     for (int kt = 0; kt < KT; ++kt) {
-      const int k0 = (ks * KT + kt) * 16;
-      const int sblk = k0 / U;  // the source CTA whose block holds inputs k0 .. k0+15
-      const uint32_t blk = hb + (uint32_t)((sblk * BC * UP + k0 - sblk * U) * 2);
+      const uint32_t blk = hb + (uint32_t)((sblk * BC * UP + 16 * jj) * 2);
+      if (++jj == U16) {
+        jj = 0;
+        ++sblk;
+      }
       uint32_t bf[NT][2];
       if constexpr (NT == 1) {
         const uint32_t addr = blk + (uint32_t)(((lane & 7) * UP + ((lane >> 3) & 1) * 8) * 2);
@@ -278,7 +292,7 @@ __global__ void __launch_bounds__(256, 1)
     for (int kp = 0; kp < FUSED_PPT; ++kp) {
       const int e = tid + kp * nthr;
       if (e >= nb * U) break;
-      const int b = e / U, u = e - b * U;
+      const int b = pb[kp], u = pu[kp];
       const int q = u >> 4, r = u & 15;
       float x[G], rc[G], sn[S], pre[P];
       // all K-split partials are loaded before any is summed (independent loads)
@@ -336,7 +350,7 @@ __global__ void __launch_bounds__(256, 1)
     for (int kp = 0; kp < FUSED_PPT; ++kp) {
       const int e = tid + kp * nthr;
       if (e >= nb * U) break;
-      const int b = e / U, u = e - b * U, bg = b0 + b, j = u0 + u;
+      const int b = pb[kp], u = pu[kp], bg = b0 + b, j = u0 + u;
       if (states) {
 #pragma unroll
         for (int s = 0; s < S; ++s)
