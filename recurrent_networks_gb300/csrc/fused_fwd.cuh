@@ -113,6 +113,13 @@ __global__ void __launch_bounds__(256, 1)
       bsr[k][g] = own ? __bfloat162float(bias[((size_t)g * N + n) * D + u0 + u]) : 0.0f;
   }
 
+  // grid variant: when the block size is a multiple of the 16-byte chunks per
+  // row of h, thread tid copies column chunk tid % (D/8) of rows tid / (D/8),
+  // + nthr / (D/8), ...: its source block and offsets are fixed
+  const bool gx_fixed = GRIDX && nthr % (D / 8) == 0;
+  const int gx_b0 = tid / (D / 8), gx_db = nthr / (D / 8), gx_i = (tid - gx_b0 * (D / 8)) * 8;
+  const int gx_sblk = gx_i / U, gx_col = gx_i - gx_sblk * U;
+
   // the first k-tile of this warp's K slice: source block and column group
   const int U16 = U / 16;
   const int ktile_sblk0 = (ks * KT) / U16, ktile_j0 = ks * KT - ktile_sblk0 * U16;
@@ -186,9 +193,14 @@ __global__ void __launch_bounds__(256, 1)
         __syncthreads();
         const __nv_bfloat16* src = (const __nv_bfloat16*)a.hx + ((size_t)(p * (gridDim.x / C) + grp) * BC) * D;
         const int rc = D / 8;
-        for (int e = tid; e < nb * rc; e += nthr) {
-          const int b = e / rc, i = (e - b * rc) * 8, sblk = i / U;
-          cp_async_cg16(smem_u32(hbuf + p * HB + (sblk * BC + b) * UP + i - sblk * U), src + (size_t)b * D + i);
+        if (gx_fixed) {  // this thread's 16-byte column is the same in every row it copies
+          for (int b = gx_b0; b < nb; b += gx_db)
+            cp_async_cg16(smem_u32(hbuf + p * HB + (gx_sblk * BC + b) * UP + gx_col), src + (size_t)b * D + gx_i);
+        } else {
+          for (int e = tid; e < nb * rc; e += nthr) {
+            const int b = e / rc, i = (e - b * rc) * 8, sblk = i / U;
+            cp_async_cg16(smem_u32(hbuf + p * HB + (sblk * BC + b) * UP + i - sblk * U), src + (size_t)b * D + i);
+          }
         }
         cp_async_wait_all();
         __syncthreads();

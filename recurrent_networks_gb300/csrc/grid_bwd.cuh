@@ -90,6 +90,12 @@ __global__ void __launch_bounds__(256, 1)
   }
   __syncthreads();
 
+  // per-thread starting coordinates and strides of the two per-step loops
+  // (the gather's 16-byte chunks e = b rc + c, the cell's pairs e = b U + u)
+  const int rc = KG / 8;
+  const int g_b0 = tid / rc, g_c0 = tid - g_b0 * rc, g_db = nthr / rc, g_dc = nthr - g_db * rc;
+  const int c_b0 = tid / U, c_u0 = tid - c_b0 * U, c_db = nthr / U, c_du = nthr - c_db * U;
+
   auto issue_stage = [&](int k) {
     const int t = TT - 1 - k, s = k % FUSED_NS;
     unsigned char* st = ring + (size_t)s * L.ring_stage;
@@ -115,10 +121,15 @@ __global__ void __launch_bounds__(256, 1)
       RNN_TRACE(1)
       __syncthreads();
       const __nv_bfloat16* src = dx + ((size_t)((kk - 1) & 1) * groups + grp) * BC * KG;
-      const int rc = KG / 8;
-      for (int e = tid; e < nb * rc; e += nthr) {
-        const int b = e / rc, c = e - b * rc;
+      // chunk e = b rc + c, stepped without a division
+      for (int e = tid, b = g_b0, c = g_c0; e < nb * rc; e += nthr) {
         cp_async_cg16(smem_u32(dbuf + b * KB + c * 8), src + (size_t)b * KG + c * 8);
+        b += g_db;
+        c += g_dc;
+        if (c >= rc) {
+          c -= rc;
+          ++b;
+        }
       }
       cp_async_wait_all();
       __syncthreads();
@@ -191,8 +202,9 @@ __global__ void __launch_bounds__(256, 1)
     }
     RNN_TRACE(4)
     __nv_bfloat16* dxw = dx + ((size_t)(kk & 1) * groups + grp) * BC * KG;
-    for (int e = tid; e < nb * U; e += nthr) {
-      const int b = e / U, u = e - b * U, q = u >> 4, r = u & 15;
+    // pair e = b U + u, stepped without a division
+    for (int e = tid, b = c_b0, u = c_u0; e < nb * U; e += nthr, b += c_db + (u + c_du >= U), u = u + c_du >= U ? u + c_du - U : u + c_du) {
+      const int q = u >> 4, r = u & 15;
       float pre[P], sp[S], sn[S], dsn[S], dxg[G], dr[G], dsp[S];
 #pragma unroll
       for (int k2 = 0; k2 < P; ++k2) pre[k2] = tp[(b * K + k2) * U + u];
