@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(256, 1)
   float* ds = (float*)(smem + L.ds);
   float* s0s = (float*)(smem + L.s0);
   const uint32_t ring_bar0 = smem_u32(&bars[0]);
+  const uint32_t gath_bar = smem_u32(&bars[FUSED_NS]);  // the gather of the group's dr
   const bool has_dst = a.dstates != nullptr;
   const uint32_t stage_bytes = (uint32_t)(L.tape_bytes + (has_dst ? (size_t)S * BC * U * 2 : 0));
 
@@ -62,6 +63,7 @@ __global__ void __launch_bounds__(256, 1)
 
   if (tid == 0) {
     for (int s = 0; s < FUSED_NS; ++s) mbar_init(ring_bar0 + 8 * s, 1);
+    mbar_init(gath_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_tensormap(&tapemap);
     if (has_dst) prefetch_tensormap(&dstmap);
@@ -90,11 +92,10 @@ __global__ void __launch_bounds__(256, 1)
   }
   __syncthreads();
 
-  // per-thread starting coordinates and strides of the two per-step loops
-  // (the gather's 16-byte chunks e = b rc + c, the cell's pairs e = b U + u)
-  const int rc = KG / 8;
-  const int g_b0 = tid / rc, g_c0 = tid - g_b0 * rc, g_db = nthr / rc, g_dc = nthr - g_db * rc;
+  // per-thread starting coordinates and strides of the per-step cell loop
+  // over the pairs e = b U + u
   const int c_b0 = tid / U, c_u0 = tid - c_b0 * U, c_db = nthr / U, c_du = nthr - c_db * U;
+  uint32_t gath_par = 0u;
 
   auto issue_stage = [&](int k) {
     const int t = TT - 1 - k, s = k % FUSED_NS;
@@ -117,22 +118,23 @@ __global__ void __launch_bounds__(256, 1)
     RNN_TRACE(0)
     if (have_rec) {
       // gather dr_{t+1} of the whole group, multiply by the resident rows of R
-      if (tid == 0) counter_wait_bounded(a.counters + grp, (unsigned)(C * kk), a.wait_limit_ns, a.status, failed);
-      RNN_TRACE(1)
-      __syncthreads();
-      const __nv_bfloat16* src = dx + ((size_t)((kk - 1) & 1) * groups + grp) * BC * KG;
-      // chunk e = b rc + c, stepped without a division
-      for (int e = tid, b = g_b0, c = g_c0; e < nb * rc; e += nthr) {
-        cp_async_cg16(smem_u32(dbuf + b * KB + c * 8), src + (size_t)b * KG + c * 8);
-        b += g_db;
-        c += g_dc;
-        if (c >= rc) {
-          c -= rc;
-          ++b;
+      // one thread observes the group's step counter, then pulls the nb rows
+      // of dr (G D bf16 each) with one bulk copy per row; every thread waits
+      // for the bytes on the gather barrier
+      if (tid == 0) {
+        counter_wait_bounded(a.counters + grp, (unsigned)(C * kk), a.wait_limit_ns, a.status, failed);
+        if (!failed) {
+          const __nv_bfloat16* src = dx + ((size_t)((kk - 1) & 1) * groups + grp) * BC * KG;
+          fence_proxy_async_global();  // the peers' stores, acquired above, before the bulk reads
+          fence_proxy_async_smem();    // the last step's reads of dbuf (ordered by the barrier) before the writes
+          mbar_arrive_expect_tx(gath_bar, (uint32_t)(nb * KG * 2));
+          for (int b = 0; b < nb; ++b)
+            bulk_load_global(smem_u32(dbuf + b * KB), src + (size_t)b * KG, (uint32_t)(KG * 2), gath_bar);
         }
       }
-      cp_async_wait_all();
-      __syncthreads();
+      RNN_TRACE(1)
+      mbar_wait_bounded<false>(gath_bar, gath_par, a.wait_limit_ns, a.status, failed);
+      gath_par ^= 1u;
       RNN_TRACE(2)
       float acc[NT][4];
 #pragma unroll

@@ -91,7 +91,7 @@ struct GridBwdSmem {
   RNN_HD static GridBwdSmem make(int G, int S, int K, int D, int U, int BC, int KS) {
     GridBwdSmem m;
     size_t off = 0;
-    m.bars = FusedSmem::take(off, 8 * FUSED_NS);
+    m.bars = FusedSmem::take(off, 8 * (FUSED_NS + 1));  // the TMA ring, then the gather
     m.tape_bytes = (size_t)BC * K * U * 4;
     m.dst_off = (m.tape_bytes + 127) & ~(size_t)127;
     m.ring_stage = (m.dst_off + (size_t)S * BC * U * 2 + 127) & ~(size_t)127;

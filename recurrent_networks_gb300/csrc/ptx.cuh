@@ -161,6 +161,18 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t rdst, uint32_t src, u
       "r"(src), "r"(bytes), "r"(rbar)
       : "memory");
 }
+// Bulk copy of `bytes` (multiple of 16) from global memory into this CTA's
+// shared memory, completing its bytes on the mbarrier `bar`.
+__device__ __forceinline__ void bulk_load_global(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// Orders global-memory data this thread has acquired (written by other
+// threads through the generic proxy) before its later async-proxy reads of it.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (bulk copy / TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {
