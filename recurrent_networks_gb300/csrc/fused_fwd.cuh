@@ -35,8 +35,11 @@ __global__ void __launch_bounds__(256, 1)
   constexpr int G = FnInfo<FN>::G, S = FnInfo<FN>::S, P = FnInfo<FN>::P, K = P + S;
   constexpr int BC = 8 * NT;
   const int C = a.C, U = a.U, D = a.D, KS = a.KS, TT = a.T, N = a.N, B = a.B;
-  const int UP = U + 8;        // row stride (elements) of one source CTA's block of h
-  const int HB = C * BC * UP;  // elements of one h buffer: [C][BC][UP]
+  const int UP = U + 8;  // row stride (elements) of one source CTA's block of h
+  // one h buffer: [C][BC][UP] blocks per source CTA in a cluster; the grid
+  // variant gathers whole rows, [BC][D + 8] (one block, within the same space)
+  const int RS = GRIDX ? D + 8 : UP;
+  const int HB = GRIDX ? BC * (D + 8) : C * BC * UP;
   const uint32_t rank = GRIDX ? (uint32_t)(blockIdx.x % C) : cluster_ctarank();
   const int grp = blockIdx.x / C;
   const int n = grp % N;
@@ -90,7 +93,7 @@ __global__ void __launch_bounds__(256, 1)
   for (int e = tid; e < nb * D; e += nthr) {
     const int b = e / D, i = e - b * D, src = i / U;
     float v = s0 ? __bfloat162float(s0[((size_t)(b0 + b) * N + n) * D + i]) : 0.0f;
-    hbuf[(src * BC + b) * UP + i - src * U] = __float2bfloat16_rn(v);
+    hbuf[GRIDX ? b * RS + i : (src * BC + b) * UP + i - src * U] = __float2bfloat16_rn(v);
   }
   // Each thread owns the (batch row, unit) pairs e = tid + k * blockDim
   // (k < FUSED_PPT) for the whole sequence: their carried states (fp32) and
@@ -113,15 +116,9 @@ __global__ void __launch_bounds__(256, 1)
       bsr[k][g] = own ? __bfloat162float(bias[((size_t)g * N + n) * D + u0 + u]) : 0.0f;
   }
 
-  // grid variant: when the block size is a multiple of the 16-byte chunks per
-  // row of h, thread tid copies column chunk tid % (D/8) of rows tid / (D/8),
-  // + nthr / (D/8), ...: its source block and offsets are fixed
-  const bool gx_fixed = GRIDX && nthr % (D / 8) == 0;
-  const int gx_b0 = tid / (D / 8), gx_db = nthr / (D / 8), gx_i = (tid - gx_b0 * (D / 8)) * 8;
-  const int gx_sblk = gx_i / U, gx_col = gx_i - gx_sblk * U;
-
   // the first k-tile of this warp's K slice: source block and column group
-  const int U16 = U / 16;
+  // (the grid variant's one block holds all D inputs)
+  const int U16 = GRIDX ? D / 16 : U / 16;
   const int ktile_sblk0 = (ks * KT) / U16, ktile_j0 = ks * KT - ktile_sblk0 * U16;
 
   // resident R fragments: A[m = unit j][k = input i] = R[g, n, i, j]. Warps
@@ -188,22 +185,22 @@ __global__ void __launch_bounds__(256, 1)
     RNN_TRACE(0)
     if (t > 0) {
       if constexpr (GRIDX) {
-        // every CTA of the group published h_{t-1}; copy it from L2
-        if (tid == 0) counter_wait_bounded(a.counters + grp, (unsigned)(C * t), a.wait_limit_ns, a.status, failed);
-        __syncthreads();
-        const __nv_bfloat16* src = (const __nv_bfloat16*)a.hx + ((size_t)(p * (gridDim.x / C) + grp) * BC) * D;
-        const int rc = D / 8;
-        if (gx_fixed) {  // this thread's 16-byte column is the same in every row it copies
-          for (int b = gx_b0; b < nb; b += gx_db)
-            cp_async_cg16(smem_u32(hbuf + p * HB + (gx_sblk * BC + b) * UP + gx_col), src + (size_t)b * D + gx_i);
-        } else {
-          for (int e = tid; e < nb * rc; e += nthr) {
-            const int b = e / rc, i = (e - b * rc) * 8, sblk = i / U;
-            cp_async_cg16(smem_u32(hbuf + p * HB + (sblk * BC + b) * UP + i - sblk * U), src + (size_t)b * D + i);
+        // every CTA of the group published h_{t-1}: one thread observes the
+        // step counter and pulls the nb rows from L2 with one bulk copy each;
+        // every thread waits for the bytes
+        if (tid == 0) {
+          counter_wait_bounded(a.counters + grp, (unsigned)(C * t), a.wait_limit_ns, a.status, failed);
+          if (!failed) {
+            const __nv_bfloat16* src = (const __nv_bfloat16*)a.hx + ((size_t)(p * (gridDim.x / C) + grp) * BC) * D;
+            fence_proxy_async_global();  // the peers' stores, acquired above, before the bulk reads
+            fence_proxy_async_smem();    // the last reads of this buffer (ordered by the barrier) before the writes
+            mbar_arrive_expect_tx(full_bar0, (uint32_t)(nb * D * 2));
+            for (int b = 0; b < nb; ++b)
+              bulk_load_global(smem_u32(hbuf + p * HB + b * RS), src + (size_t)b * D, (uint32_t)(D * 2), full_bar0);
           }
         }
-        cp_async_wait_all();
-        __syncthreads();
+        mbar_wait_bounded<false>(full_bar0, ph0, a.wait_limit_ns, a.status, failed);
+        ph0 ^= 1u;
       } else {
         const uint32_t par = p ? ph1 : ph0;
         mbar_wait_bounded(full_bar0 + 8 * p, par, a.wait_limit_ns, a.status, failed);
@@ -250,13 +247,13 @@ __global__ void __launch_bounds__(256, 1)
       }
       uint32_t bf[NT][2];
       if constexpr (NT == 1) {
-        const uint32_t addr = blk + (uint32_t)(((lane & 7) * UP + ((lane >> 3) & 1) * 8) * 2);
+        const uint32_t addr = blk + (uint32_t)(((lane & 7) * RS + ((lane >> 3) & 1) * 8) * 2);
         ldmatrix_x2(addr, bf[0][0], bf[0][1]);
       } else {
 #pragma unroll
         for (int np = 0; np < NT; np += 2) {
           const int q = lane >> 3;
-          const uint32_t addr = blk + (uint32_t)((((np + (q >> 1)) * 8 + (lane & 7)) * UP + (q & 1) * 8) * 2);
+          const uint32_t addr = blk + (uint32_t)((((np + (q >> 1)) * 8 + (lane & 7)) * RS + (q & 1) * 8) * 2);
           ldmatrix_x4(addr, bf[np][0], bf[np][1], bf[np + 1][0], bf[np + 1][1]);
         }
       }
