@@ -279,9 +279,18 @@ __global__ void __launch_bounds__(ALT_THREADS) alt_bwd_step(AltArgs a, int t) {
   const size_t drsz = (size_t)B * G * N * D;
   const __nv_bfloat16* drin = (const __nv_bfloat16*)a.xbuf + (size_t)((t + 1) & 1) * drsz;
 
+  // the gate of 16-wide chunk kc of the G D inputs, by comparison (G <= 4)
+  // rather than a division by D
+  const int d16 = D / ALT_BK;
+  auto chunk_gate = [&](int kc) {
+    int g = 0;
+#pragma unroll
+    for (int q = 1; q < G; ++q) g += kc >= q * d16;
+    return g;
+  };
   auto load_r = [&](int c) {
     __nv_bfloat16* st = wbase + (c % ALT_NSTG) * Stg::ELEMS;
-    const int k0 = (cbeg + c) * ALT_BK, g = k0 / D, j0 = k0 - g * D;
+    const int kc = cbeg + c, g = chunk_gate(kc), j0 = (kc - g * d16) * ALT_BK;
     // B: R[g, n, i0 + i, j0 .. j0 + 15] for the UB units i, two pieces each
     const int i = lane >> 1, p8 = lane & 1;  // UB * 2 = 32 pieces
     const __nv_bfloat16* src = R + ((size_t)(g * N + n) * D + i0 + i) * D + j0 + p8 * 8;
@@ -289,7 +298,7 @@ __global__ void __launch_bounds__(ALT_THREADS) alt_bwd_step(AltArgs a, int t) {
   };
   auto load_dr = [&](int c) {
     __nv_bfloat16* st = wbase + (c % ALT_NSTG) * Stg::ELEMS;
-    const int k0 = (cbeg + c) * ALT_BK, g = k0 / D, j0 = k0 - g * D;
+    const int kc = cbeg + c, g = chunk_gate(kc), j0 = (kc - g * d16) * ALT_BK;
     // A: dr_{t+1}[b0 + b, g, n, j0 .. j0 + 15]
     __nv_bfloat16* as = st + Stg::B_ELEMS;
     for (int e = lane; e < BM * 2; e += 32) {
