@@ -118,13 +118,46 @@ __device__ __forceinline__ void cell_fwd(const float* x, const float* r, const f
 // dsn: total gradient reaching sn. Outputs dx (gradient of Wx), dr (gradient
 // of the recurrent branch, what dR, db and dh_{t-1} through R see) and dsp
 // (gradient of the previous states through the cell itself).
+//
+// The derivative comes in two parts: cell_bwd_act evaluates what does not
+// depend on the incoming gradient (the gate activations, from the tape), and
+// cell_bwd_grad finishes with dsn. A kernel can so evaluate the
+// transcendentals while the gradient of h is still on its way.
+constexpr int CELL_BWD_ACT = 8;
 template <int FN, bool FAST>
-__device__ __forceinline__ void cell_bwd(const float* pre, const float* sp, const float* sn,
-                                         const float* dsn, float* dx, float* dr, float* dsp) {
+__device__ __forceinline__ void cell_bwd_act(const float* pre, const float* sp, const float* sn, float* act) {
   if constexpr (FN == LSTM) {
-    float i = f_sigmoid<FAST>(pre[0]), f = f_sigmoid<FAST>(pre[1]);
-    float g = f_tanh<FAST>(pre[2]), o = f_sigmoid<FAST>(pre[3]);
-    float tc = f_tanh<FAST>(sn[1]);
+    act[0] = f_sigmoid<FAST>(pre[0]);  // i
+    act[1] = f_sigmoid<FAST>(pre[1]);  // f
+    act[2] = f_tanh<FAST>(pre[2]);     // g
+    act[3] = f_sigmoid<FAST>(pre[3]);  // o
+    act[4] = f_tanh<FAST>(sn[1]);      // tanh(c)
+  } else if constexpr (FN == GRU) {
+    act[0] = f_sigmoid<FAST>(pre[0]);                     // r
+    act[1] = f_sigmoid<FAST>(pre[1]);                     // z
+    act[2] = f_tanh<FAST>(fmaf(act[0], pre[3], pre[2]));  // n
+  } else if constexpr (FN == ELMAN) {
+    act[0] = sn[0];
+  } else {  // SLSTM and SLSTM_LS
+    const float ai = pre[0], af = pre[1];
+    const float lf = FN == SLSTM_LS ? f_logsigmoid<FAST>(af) : af;
+    const float m = sn[3], mp = sp[3];
+    act[0] = f_exp<FAST>(ai - m);                            // i'
+    act[1] = f_exp<FAST>(lf + mp - m);                       // f'
+    act[2] = f_tanh<FAST>(pre[2]);                           // z
+    act[3] = f_sigmoid<FAST>(pre[3]);                        // o
+    act[4] = 1.0f / sn[2];                                   // 1 / n
+    act[5] = sn[1] * act[4];                                 // y = c / n
+    act[6] = lf + mp >= ai ? 1.0f : 0.0f;                    // the max took the forget branch
+    act[7] = FN == SLSTM_LS ? f_sigmoid<FAST>(-af) : 1.0f;  // d log f / d a_f
+  }
+}
+
+template <int FN, bool FAST>
+__device__ __forceinline__ void cell_bwd_grad(const float* act, const float* pre, const float* sp,
+                                              const float* dsn, float* dx, float* dr, float* dsp) {
+  if constexpr (FN == LSTM) {
+    const float i = act[0], f = act[1], g = act[2], o = act[3], tc = act[4];
     float dh = dsn[0];
     float dc = fmaf(dh * o, 1.0f - tc * tc, dsn[1]);
     dx[0] = dc * g * i * (1.0f - i);
@@ -135,9 +168,8 @@ __device__ __forceinline__ void cell_bwd(const float* pre, const float* sp, cons
     dsp[0] = 0.0f;
     dsp[1] = dc * f;
   } else if constexpr (FN == GRU) {
-    float rg = f_sigmoid<FAST>(pre[0]), z = f_sigmoid<FAST>(pre[1]);
+    const float rg = act[0], z = act[1], n = act[2];
     float q = pre[3];
-    float n = f_tanh<FAST>(fmaf(rg, q, pre[2]));
     float dh = dsn[0];
     float dan = dh * (1.0f - z) * (1.0f - n * n);
     float drg = dan * q;
@@ -147,20 +179,14 @@ __device__ __forceinline__ void cell_bwd(const float* pre, const float* sp, cons
     dr[0] = dx[0]; dr[1] = dx[1]; dr[2] = dan * rg;
     dsp[0] = dh * z;
   } else if constexpr (FN == ELMAN) {
-    float h = sn[0];
+    const float h = act[0];
     dx[0] = dsn[0] * (1.0f - h * h);
     dr[0] = dx[0];
     dsp[0] = 0.0f;
   } else {  // SLSTM and SLSTM_LS (gradients through log f, then d log f / d a_f)
-    float ai = pre[0], af = pre[1], az = pre[2], ao = pre[3];
-    float cp = sp[1], np = sp[2], mp = sp[3];
-    float c = sn[1], n = sn[2], m = sn[3];
-    const float lf = FN == SLSTM_LS ? f_logsigmoid<FAST>(af) : af;
-    float ig = f_exp<FAST>(ai - m), fg = f_exp<FAST>(lf + mp - m);
-    float zt = f_tanh<FAST>(az), o = f_sigmoid<FAST>(ao);
+    const float ig = act[0], fg = act[1], zt = act[2], o = act[3], rn = act[4], y = act[5];
+    const float cp = sp[1], np = sp[2];
     float dh = dsn[0];
-    float rn = 1.0f / n;
-    float y = c * rn;
     float dy = dh * o;
     float dc = fmaf(dy, rn, dsn[1]);
     float dn = dsn[2] - dy * y * rn;
@@ -170,14 +196,22 @@ __device__ __forceinline__ void cell_bwd(const float* pre, const float* sp, cons
     float dlf = dfg * fg;
     float dmp = dlf;
     float dm = dsn[3] - dai - dlf;
-    if (lf + mp >= ai) { dlf += dm; dmp += dm; } else { dai += dm; }
-    const float daf = FN == SLSTM_LS ? dlf * f_sigmoid<FAST>(-af) : dlf;
+    if (act[6] != 0.0f) { dlf += dm; dmp += dm; } else { dai += dm; }
+    const float daf = FN == SLSTM_LS ? dlf * act[7] : dlf;
     dx[0] = dai; dx[1] = daf;
     dx[2] = dc * ig * (1.0f - zt * zt);
     dx[3] = dh * y * o * (1.0f - o);
     dr[0] = dx[0]; dr[1] = dx[1]; dr[2] = dx[2]; dr[3] = dx[3];
     dsp[0] = 0.0f; dsp[1] = dc * fg; dsp[2] = dn * fg; dsp[3] = dmp;
   }
+}
+
+template <int FN, bool FAST>
+__device__ __forceinline__ void cell_bwd(const float* pre, const float* sp, const float* sn,
+                                         const float* dsn, float* dx, float* dr, float* dsp) {
+  float act[CELL_BWD_ACT];
+  cell_bwd_act<FN, FAST>(pre, sp, sn, act);
+  cell_bwd_grad<FN, FAST>(act, pre, sp, dsn, dx, dr, dsp);
 }
 
 // ---- element access --------------------------------------------------------

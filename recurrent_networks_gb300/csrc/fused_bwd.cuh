@@ -163,13 +163,6 @@ __global__ void __launch_bounds__(256, 1)
     const int t = TT - 1 - k;
     const int pb = t & 1;  // gradient-operand buffer of this step
     RNN_TRACE(0)
-    if (t < TT - 1) {  // partial sums for dh_t arrived
-      const int bi = t & 1;
-      mbar_wait_bounded(recv_bar0 + 8 * bi, bi ? ph1 : ph0, a.wait_limit_ns, a.status, failed);
-      if (bi) ph1 ^= 1u; else ph0 ^= 1u;
-      if (tid == 0 && t - 2 >= -1) mbar_arrive_expect_tx(recv_bar0 + 8 * bi, rbytes);
-    }
-    RNN_TRACE(1)
     const int sc = k % FUSED_NS, sn_ = (k + 1) % FUSED_NS;
     const float* tp = (const float*)(ring + (size_t)sc * L.ring_stage);
     const __nv_bfloat16* dstage = (const __nv_bfloat16*)(ring + (size_t)sc * L.ring_stage + L.dst_off);
@@ -179,46 +172,65 @@ __global__ void __launch_bounds__(256, 1)
       if (t > 0)
         mbar_wait_bounded<false>(ring_bar0 + 8 * sn_, ((k + 1) / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
     }
+    // The tape, the upstream gradients and the gate activations of the step
+    // do not depend on dh_t: they are evaluated while its partial sums are
+    // still arriving.
+    float pre[FUSED_PPT][P], sp[FUSED_PPT][S], sn[FUSED_PPT][S], dsn[FUSED_PPT][S];
+    float act[FUSED_PPT][CELL_BWD_ACT];
+#pragma unroll
+    for (int kp = 0; kp < FUSED_PPT; ++kp) {
+      if (tid + kp * nthr < nb * U) {
+        const int b = prow[kp], u = punit[kp];
+#pragma unroll
+        for (int kk = 0; kk < P; ++kk) pre[kp][kk] = tp[(b * K + kk) * U + u];
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+          sn[kp][s] = tp[(b * K + P + s) * U + u];
+          sp[kp][s] = t > 0 ? tq[(b * K + P + s) * U + u] : s0s[(s * BC + b) * U + u];
+          float d = dsr[kp][s];
+          if (has_dst) d += __bfloat162float(dstage[(s * BC + b) * U + u]);
+          if (dlast && t == TT - 1) d += __bfloat162float(dlast[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u]);
+          dsn[kp][s] = d;
+        }
+        cell_bwd_act<FN, true>(pre[kp], sp[kp], sn[kp], act[kp]);
+      }
+    }
+    RNN_TRACE(1)
+    if (t < TT - 1) {  // partial sums for dh_t arrived
+      const int bi = t & 1;
+      mbar_wait_bounded(recv_bar0 + 8 * bi, bi ? ph1 : ph0, a.wait_limit_ns, a.status, failed);
+      if (bi) ph1 ^= 1u; else ph0 ^= 1u;
+      if (tid == 0 && t - 2 >= -1) mbar_arrive_expect_tx(recv_bar0 + 8 * bi, rbytes);
+    }
     RNN_TRACE(2)
     const float* rv = recv + (size_t)(t & 1) * C * U * BC;
     __nv_bfloat16* drw = drb + (size_t)pb * BC * KB;
 #pragma unroll
     for (int kp = 0; kp < FUSED_PPT; ++kp) {
-      const int e = tid + kp * nthr;
-      if (e >= nb * U) break;
-      const int b = prow[kp], u = punit[kp];
-      float pre[P], sp[S], sn[S], dsn[S], dx[G], dr[G], dsp[S];
+      if (tid + kp * nthr < nb * U) {
+        const int b = prow[kp], u = punit[kp];
+        float dx[G], dr[G], dsp[S];
+        if (t < TT - 1) {  // the C partial sums, loaded together
+          float part[FUSED_MAX_C];
+          const int bs = b ^ (4 * swz(u));
 #pragma unroll
-      for (int kk = 0; kk < P; ++kk) pre[kk] = tp[(b * K + kk) * U + u];
+          for (int c = 0; c < FUSED_MAX_C; ++c) part[c] = c < C ? rv[((size_t)c * U + u) * BC + bs] : 0.0f;
+          float acc = 0.0f;
 #pragma unroll
-      for (int s = 0; s < S; ++s) {
-        sn[s] = tp[(b * K + P + s) * U + u];
-        sp[s] = t > 0 ? tq[(b * K + P + s) * U + u] : s0s[(s * BC + b) * U + u];
-        float d = dsr[kp][s];
-        if (has_dst) d += __bfloat162float(dstage[(s * BC + b) * U + u]);
-        if (dlast && t == TT - 1) d += __bfloat162float(dlast[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u]);
-        dsn[s] = d;
+          for (int c = 0; c < FUSED_MAX_C; ++c) acc += part[c];
+          dsn[kp][0] += acc;
+        }
+        cell_bwd_grad<FN, true>(act[kp], pre[kp], sp[kp], dsn[kp], dx, dr, dsp);
+        const size_t o = (((size_t)(b0 + b) * TT + t) * G) * N * D + (size_t)n * D + u0 + u;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          if (dWx) dWx[o + (size_t)g * N * D] = __float2bfloat16_rn(dx[g]);
+          if (write_dr) dro[o + (size_t)g * N * D] = __float2bfloat16_rn(dr[g]);
+          drw[b * KB + g * U + u] = __float2bfloat16_rn(dr[g]);
+        }
+#pragma unroll
+        for (int s = 0; s < S; ++s) dsr[kp][s] = dsp[s];
       }
-      if (t < TT - 1) {  // the C partial sums, loaded together
-        float part[FUSED_MAX_C];
-        const int bs = b ^ (4 * swz(u));
-#pragma unroll
-        for (int c = 0; c < FUSED_MAX_C; ++c) part[c] = c < C ? rv[((size_t)c * U + u) * BC + bs] : 0.0f;
-        float acc = 0.0f;
-#pragma unroll
-        for (int c = 0; c < FUSED_MAX_C; ++c) acc += part[c];
-        dsn[0] += acc;
-      }
-      cell_bwd<FN, true>(pre, sp, sn, dsn, dx, dr, dsp);
-      const size_t o = (((size_t)(b0 + b) * TT + t) * G) * N * D + (size_t)n * D + u0 + u;
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        if (dWx) dWx[o + (size_t)g * N * D] = __float2bfloat16_rn(dx[g]);
-        if (write_dr) dro[o + (size_t)g * N * D] = __float2bfloat16_rn(dr[g]);
-        drw[b * KB + g * U + u] = __float2bfloat16_rn(dr[g]);
-      }
-#pragma unroll
-      for (int s = 0; s < S; ++s) dsr[kp][s] = dsp[s];
     }
     // one thread observes the TMA completion of the two stages the next step
     // reads (loaded NS - 2 or more steps ago); the barrier below orders them
