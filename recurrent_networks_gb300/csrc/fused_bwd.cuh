@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(256, 1)
           float part[FUSED_MAX_C];
           const int bs = b ^ (4 * swz(u));
 #pragma unroll
-          for (int c = 0; c < FUSED_MAX_C; ++c) part[c] = c < C ? rv[((size_t)c * U + u) * BC + bs] : 0.0f;
+          for (int c = 0; c < FUSED_MAX_C; ++c) part[c] = c < C ? rv[(c * U + u) * BC + bs] : 0.0f;
           float acc = 0.0f;
 #pragma unroll
           for (int c = 0; c < FUSED_MAX_C; ++c) acc += part[c];

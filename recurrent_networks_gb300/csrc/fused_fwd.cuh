@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(256, 1)
       const int r = lane >> 2, bc = 2 * (lane & 3);
 #pragma unroll
       for (int gi = 0; gi < GW; ++gi) {
-        float* rp = red + (size_t)((mg * KS + ks) * G + gq * GW + gi) * BC * FUSED_RED_STRIDE;
+        float* rp = red + ((mg * KS + ks) * G + gq * GW + gi) * BC * FUSED_RED_STRIDE;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           float v[4];
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(256, 1)
       for (int g = 0; g < G; ++g)
 #pragma unroll
         for (int k2 = 0; k2 < FUSED_MAX_KS; ++k2)
-          part[g][k2] = k2 < KS ? red[((size_t)((q * KS + k2) * G + g) * BC + b) * FUSED_RED_STRIDE + r] : 0.0f;
+          part[g][k2] = k2 < KS ? red[(((q * KS + k2) * G + g) * BC + b) * FUSED_RED_STRIDE + r] : 0.0f;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float v = bsr[kp][g];

@@ -128,10 +128,6 @@ __device__ __forceinline__ void counter_publish(unsigned int* ctr) {
   // observed through the barrier as well as its own
   asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
 }
-__device__ __forceinline__ void cp_async_cg16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // ---- cluster barrier --------------------------------------------------------
 __device__ __forceinline__ void cluster_sync_all() {
