@@ -197,6 +197,7 @@ GRID_CASES = [
     ("elman", 16, 21, 2, 256, dict(C=16, NT=2)),
     ("slstm", 4, 17, 1, 512, dict(C=32)),
     ("slstm_logsig", 5, 13, 1, 512, dict(C=32)),
+    ("lstm", 13, 9, 1, 512, dict(C=32, NT=2)),   # 16-row batch tile with 13 rows: ragged bulk-copy gathers
 ]
 
 
@@ -217,6 +218,30 @@ def test_grid_parity(case, monkeypatch):
     dl = torch.randn(last.shape, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).cuda()
     dWx, dR, db, ds0 = run_bwd(fn, inp, st, tape, "grid", dlast=dl)
     check_grads(fn, inp, (dWx, dR, db, ds0), dlast=dl)
+
+
+def test_grid_reuses_its_workspace(monkeypatch):
+    """Two grid forward + backward runs of different lengths on one workspace:
+    the second must not see the first's step counters or exchange rows."""
+    _restrict(monkeypatch, dict(C=16))
+    B, N, D = 5, 1, 256
+    dims_long = _lib.make_dims(B, 12, N, D, "lstm", torch.bfloat16, "grid")
+    ws = torch.empty(_lib.rnn_workspace_size(dims_long, _lib.WS_BWD), dtype=torch.uint8, device="cuda")
+    for T, seed in ((12, 61), (5, 62)):
+        inp = _inputs("lstm", (B, T, N, D), torch.bfloat16, seed=seed)
+        dims = _lib.make_dims(B, T, N, D, "lstm", torch.bfloat16, "grid")
+        st = torch.full((2, B, T, N, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        last = torch.full((2, B, 1, N, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        tape = torch.empty(_lib.rnn_tape_size(dims), dtype=torch.uint8, device="cuda")
+        _lib.rnn_fwd(dims, inp["Wx"], inp["R"], inp["b"], inp["states0"], st, last, tape, ws)
+        _lib.rnn_check_status(ws)
+        ref_st, _ = oracle_fwd("lstm", inp)
+        check_states("lstm", torch.bfloat16, st, ref_st)
+        dWx, dR, db, ds0 = (torch.full_like(inp[k], float("nan")) for k in ("Wx", "R", "b", "states0"))
+        _lib.rnn_bwd(dims, inp["Wx"], inp["R"], inp["b"], inp["states0"], st, tape, inp["dstates"], None,
+                     dWx, dR, db, ds0, ws)
+        _lib.rnn_check_status(ws)
+        check_grads("lstm", inp, (dWx, dR, db, ds0))
 
 
 def test_grid_and_cluster_forward_agree(monkeypatch):
