@@ -18,8 +18,11 @@
 // the tiles (and split-K slices), with warp-specialised roles. Warp 0 feeds a
 // TMA / mbarrier ring that runs ahead across tile boundaries, warp 1 issues the
 // MMAs, and warps 2-5 drain the accumulator. Tensor memory holds two
-// accumulators, so one tile's epilogue overlaps the next tile's MMAs.
-#include <math.h>
+// accumulators, so one tile's epilogue overlaps the next tile's MMAs. The
+// epilogue leaves through shared memory as TMA stores of 64-byte-swizzled
+// 32 x 32 boxes, clipped at the matrix edges; split-K partials leave the same
+// way and a second kernel adds them in a fixed order. dbias is a two-pass
+// column sum.
 #include <stdio.h>
 
 #include <cmath>
