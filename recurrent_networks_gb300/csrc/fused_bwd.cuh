@@ -2,8 +2,11 @@
 //
 // Reverse-time counterpart of the forward cluster kernel. One cluster of C
 // CTAs runs one head and batch group from t = T-1 down to 0; CTA c owns units
-// [c*U, (c+1)*U) and carries their state gradients (fp32, shared memory).
+// [c*U, (c+1)*U) and carries their state gradients (fp32, registers).
 // Per step:
+//   0. the tape, the upstream gradients and the gate activations of the
+//      CTA's (row, unit) pairs, which do not depend on dh_t, while its
+//      partial products are still arriving;
 //   1. dh_t[own units] = sum over the C CTAs of the fp32 partial products
 //      received for this step (plus dstates[:, t] and the carried terms);
 //   2. the cell derivative gives dWx[:, t] and the recurrent-branch gradient
