@@ -76,3 +76,28 @@ def test_plan_describe():
     rc, text = _lib.rnn_plan_describe(_lib.make_dims(8, 1024, 3, 256, "lstm", torch.float32))
     assert rc == _lib.RNN_OK and "path=" in text
     assert _lib.rnn_strerror(_lib.RNN_ENOSPC) == "workspace too small"
+
+
+def test_projection_sizes_and_host_validation():
+    """The input projection's size query and argument checks run on the host:
+    dims the TMA boxes cannot take size 0 and are rejected, as are null or
+    misaligned pointers and a short workspace, before any device work."""
+    lib = _lib.load()
+    # I and C multiples of 8 and at least 64 (16-byte rows, 64-wide boxes)
+    assert _lib.rnn_input_proj_workspace_size(8, 60, 128) == 0
+    assert _lib.rnn_input_proj_workspace_size(8, 64, 124) == 0
+    assert _lib.rnn_input_proj_workspace_size(8, 64, 56) == 0
+    assert _lib.rnn_input_proj_workspace_size(0, 64, 128) == 0
+    ok = _lib.rnn_input_proj_workspace_size(8192, 768, 3072)
+    # status word + the dbias column-sum partials (at least one row chunk of C fp32)
+    assert ok >= 256 + 3072 * 4
+    big = _lib.rnn_input_proj_workspace_size(131072, 1024, 4096)
+    assert big >= 256 + 4096 * 4
+    ws = 4096
+    assert lib.rnn_input_proj_fwd(8, 60, 128, 16, 16, None, 16, 256, ws, None) == _lib.RNN_EINVAL
+    assert lib.rnn_input_proj_fwd(8, 64, 128, None, 16, None, 16, 256, ws, None) == _lib.RNN_EINVAL
+    assert lib.rnn_input_proj_fwd(8, 64, 128, 24, 16, None, 16, 256, ws, None) == _lib.RNN_EINVAL
+    assert lib.rnn_input_proj_fwd(8, 64, 128, 16, 16, 40, 16, 256, ws, None) == _lib.RNN_EINVAL
+    assert lib.rnn_input_proj_fwd(8192, 768, 3072, 16, 16, None, 16, 256, 256, None) == _lib.RNN_ENOSPC
+    assert lib.rnn_input_proj_bwd(8, 64, 128, 16, 16, 16, 24, None, None, 256, ws, None) == _lib.RNN_EINVAL
+    assert lib.rnn_input_proj_bwd(8192, 768, 3072, 16, 16, 16, 16, 16, 16, 256, 256, None) == _lib.RNN_ENOSPC
