@@ -1,0 +1,38 @@
+"""The per-step roofline arithmetic of bench.py, checked against hand-computed
+algorithmic work for the measured workloads: forward 2 G D^2 flops and
+(G + S) D e bytes per (b, n, t); backward 4 G D^2 flops and (2S + 2G) D e
+bytes."""
+import pytest
+
+import bench
+from recurrent_networks_gb300.synth import WORKLOADS
+
+
+def per_step(k, fn, esize):
+    w = WORKLOADS[k]
+    a = bench.algorithmic(w, fn, esize)
+    return {key: v / w["T"] for key, v in a.items() if key != "units"}
+
+
+def test_lstm_d256_bench_workload():
+    # B = 8, N = 3, D = 256, G = 4, S = 2, bf16: 24 sequences per step
+    s = per_step(2, "lstm", 2)
+    assert s["fwd_bytes"] == 24 * (4 + 2) * 256 * 2 == 73728
+    assert s["fwd_flops"] == 24 * 2 * 4 * 256 * 256 == pytest.approx(12.58e6, rel=1e-3)
+    assert s["bwd_bytes"] == 24 * (2 * 2 + 2 * 4) * 256 * 2
+    assert s["bwd_flops"] == 2 * s["fwd_flops"]
+    # at the measured 6789.3 GB/s the forward step's HBM time is 10.86 ns
+    assert s["fwd_bytes"] / 6789.3e9 == pytest.approx(10.86e-9, rel=1e-3)
+
+
+def test_lstm_d1024_is_tensor_bound():
+    # B = 32, N = 1, D = 1024: 268 MFLOP per forward step, 140 ns at 1.91 PFLOP/s
+    s = per_step(5, "lstm", 2)
+    assert s["fwd_flops"] == 32 * 2 * 4 * 1024 * 1024 == pytest.approx(268.4e6, rel=1e-3)
+    assert s["fwd_flops"] / 1.9125e15 > s["fwd_bytes"] / 6789.3e9
+
+
+def test_slstm_counts_four_states():
+    s = per_step(4, "slstm", 2)
+    assert s["fwd_bytes"] == 16 * 4 * (4 + 4) * 192 * 2
+    assert s["bwd_bytes"] == 16 * 4 * (2 * 4 + 2 * 4) * 192 * 2
