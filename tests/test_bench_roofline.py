@@ -36,3 +36,23 @@ def test_slstm_counts_four_states():
     s = per_step(4, "slstm", 2)
     assert s["fwd_bytes"] == 16 * 4 * (4 + 4) * 192 * 2
     assert s["bwd_bytes"] == 16 * 4 * (2 * 4 + 2 * 4) * 192 * 2
+
+
+def test_traffic_record_follows_the_kernel_sources(monkeypatch):
+    """profiles/traffic.json's DRAM bytes are reported only while the kernel's
+    sources hash to what they were when the counters were taken."""
+    got = bench.measured_traffic("fused_bwd_kernel", "lstm_bf16_B8_T1024_N3_D256")
+    assert got is not None and got > 0
+    monkeypatch.setattr(bench, "kernel_sources_sha", lambda kernel: "0" * 64)
+    assert bench.measured_traffic("fused_bwd_kernel", "lstm_bf16_B8_T1024_N3_D256") is None
+    assert bench.measured_traffic("fused_fwd_kernel", "no_such_workload") is None
+
+
+def test_oracle_sample_is_bounded():
+    # the bench workload fits whole; the D = 1024 workload takes a time prefix
+    # over at least as many sequences as cores
+    w2, w5 = WORKLOADS[2], WORKLOADS[5]
+    assert bench.oracle_sample(w2, "lstm", 16) == (w2["B"], w2["T"])
+    rows, steps = bench.oracle_sample(w5, "lstm", 16)
+    assert rows >= 16 and 8 <= steps < w5["T"]
+    assert 3 * 2 * 4 * 1024 * 1024 * rows * steps <= 60e9
