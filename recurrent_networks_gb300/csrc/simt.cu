@@ -25,6 +25,36 @@ constexpr int SIMT_BBM = 8;  // max batch rows per CTA
 // so that consecutive threads read consecutive addresses); otherwise it is
 // read through L1 / L2. Each dot product keeps four independent partial sums.
 
+// Coordinates (g, bb, j) of a flat index e = (g * BB + bb) * D + j walked with
+// a fixed stride: the stride is split into the same digits once, and each step
+// adds digit by digit with carries, so no division runs inside the time loop.
+struct Walk3 {
+  int g, bb, j;          // the current coordinates
+  int dg, dbb, dj;       // the stride's digits
+  int BB, D;
+  __device__ __forceinline__ Walk3(int e0, int stride, int BB_, int D_) : BB(BB_), D(D_) {
+    g = e0 / (BB * D);
+    bb = (e0 - g * BB * D) / D;
+    j = e0 - (g * BB + bb) * D;
+    dg = stride / (BB * D);
+    dbb = (stride - dg * BB * D) / D;
+    dj = stride - (dg * BB + dbb) * D;
+  }
+  __device__ __forceinline__ void next() {
+    j += dj;
+    if (j >= D) {
+      j -= D;
+      ++bb;
+    }
+    bb += dbb;
+    if (bb >= BB) {
+      bb -= BB;
+      ++g;
+    }
+    g += dg;
+  }
+};
+
 template <int FN, typename T>
 __global__ void __launch_bounds__(256) simt_fwd_kernel(SimtArgs a) {
   constexpr int G = FnInfo<FN>::G, S = FnInfo<FN>::S, P = FnInfo<FN>::P, K = P + S;
@@ -67,12 +97,14 @@ __global__ void __launch_bounds__(256) simt_fwd_kernel(SimtArgs a) {
     for (int g = 0; g < G; ++g) xnext[g] = ldf(Wx + (((size_t)(b0 + bb) * TT + 0) * G + g) * N * D + (size_t)n * D + j);
   }
 
+  const Walk3 walk0(threadIdx.x, blockDim.x, BB, D);  // this thread's first index, divided once
   for (int t = 0; t < TT; ++t) {
     const float* hin = hop + (t & 1) * BS * D;
     float* hout = hop + ((t + 1) & 1) * BS * D;
     // phase A: the G * BB * D dot products of the step
-    for (int e = threadIdx.x; e < G * BB * D; e += blockDim.x) {
-      const int g = e / (BB * D), r = e - g * BB * D, bb = r / D, j = r - bb * D;
+    Walk3 wa = walk0;
+    for (int e = threadIdx.x; e < G * BB * D; e += blockDim.x, wa.next()) {
+      const int g = wa.g, bb = wa.bb, j = wa.j;
       const float* hv = hin + bb * D;
       float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
       int i = 0;
@@ -99,8 +131,9 @@ __global__ void __launch_bounds__(256) simt_fwd_kernel(SimtArgs a) {
     }
     __syncthreads();
     // phase B: the cell update of every (batch row, unit) pair
-    for (int e = threadIdx.x; e < BB * D; e += blockDim.x) {
-      const int bb = e / D, j = e - bb * D, b = b0 + bb;
+    Walk3 wb = walk0;
+    for (int e = threadIdx.x; e < BB * D; e += blockDim.x, wb.next()) {
+      const int bb = wb.bb, j = wb.j, b = b0 + bb;
       float x[G], r[G], sp[S], sn[S], pre[P];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -176,8 +209,8 @@ __global__ void __launch_bounds__(256) simt_bwd_kernel(SimtArgs a) {
   // thread's first pair are loaded one step ahead
   const int e0 = threadIdx.x;
   float npre[P], nsn[S], nsp[S], nup[S];
-  auto fetch = [&](int tt, int e, float* pre, float* sn, float* sp, float* up) {
-    const int bb = e / D, j = e - bb * D, b = b0 + bb;
+  auto fetch = [&](int tt, int bb, int j, float* pre, float* sn, float* sp, float* up) {
+    const int b = b0 + bb;
     const float* tp = a.tape + (((size_t)tt * B + b) * N + n) * K * D + j;
 #pragma unroll
     for (int k = 0; k < P; ++k) pre[k] = tp[k * D];
@@ -199,13 +232,16 @@ __global__ void __launch_bounds__(256) simt_bwd_kernel(SimtArgs a) {
       up[s] = d;
     }
   };
-  if (e0 < BB * D && TT > 0) fetch(TT - 1, e0, npre, nsn, nsp, nup);
+  const int bb0 = e0 / D, j00 = e0 - bb0 * D;
+  if (e0 < BB * D && TT > 0) fetch(TT - 1, bb0, j00, npre, nsn, nsp, nup);
 
+  const Walk3 walk0(threadIdx.x, blockDim.x, BB, D);  // this thread's first index, divided once
   for (int t = TT - 1; t >= 0; --t) {
     // phase A: cell derivative of every pair; dh_t gathers the G partials of
     // the later step first
-    for (int e = threadIdx.x; e < BB * D; e += blockDim.x) {
-      const int bb = e / D, j = e - bb * D, b = b0 + bb;
+    Walk3 wc = walk0;
+    for (int e = threadIdx.x; e < BB * D; e += blockDim.x, wc.next()) {
+      const int bb = wc.bb, j = wc.j, b = b0 + bb;
       float hsum = 0.0f;
 #pragma unroll
       for (int g = 0; g < G; ++g) hsum += part[(g * BS + bb) * D + j];
@@ -215,9 +251,9 @@ __global__ void __launch_bounds__(256) simt_bwd_kernel(SimtArgs a) {
         for (int k = 0; k < P; ++k) pre[k] = npre[k];
 #pragma unroll
         for (int s = 0; s < S; ++s) { sn[s] = nsn[s]; sp[s] = nsp[s]; up[s] = nup[s]; }
-        if (t > 0) fetch(t - 1, e0, npre, nsn, nsp, nup);
+        if (t > 0) fetch(t - 1, bb0, j00, npre, nsn, nsp, nup);
       } else {
-        fetch(t, e, pre, sn, sp, up);
+        fetch(t, bb, j, pre, sn, sp, up);
       }
 #pragma unroll
       for (int s = 0; s < S; ++s) {
@@ -238,8 +274,9 @@ __global__ void __launch_bounds__(256) simt_bwd_kernel(SimtArgs a) {
     }
     __syncthreads();
     // phase B: part[g][bb][i] = sum_j dr[g][bb][j] R[g, n, i, j]
-    for (int e = threadIdx.x; e < G * BB * D; e += blockDim.x) {
-      const int g = e / (BB * D), r = e - g * BB * D, bb = r / D, i = r - bb * D;
+    Walk3 wd = walk0;
+    for (int e = threadIdx.x; e < G * BB * D; e += blockDim.x, wd.next()) {
+      const int g = wd.g, bb = wd.bb, i = wd.j;
       const float* dv = drs + (g * BS + bb) * D;
       float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
       int j = 0;
