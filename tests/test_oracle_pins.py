@@ -300,51 +300,81 @@ class _Bf16OperandBranch(torch.autograd.Function):
         return dyb @ W.T, hb.T @ dyb, dyb.sum(0)
 
 
-@pytest.mark.parametrize("fn", ["lstm", "elman"])
+def _torch_cell_step(fn, x, branch, sp, D):
+    """One step of each cell written with torch operations, for autograd.
+    x: the input pre-activations [B, G*D]; branch: the recurrent branch
+    h.R + b [B, G*D]; sp: the previous states (list of [B, D]). GRU applies
+    the reset gate to the whole recurrent branch of n (bias included); sLSTM
+    takes the max of the stabiliser with torch.where, so a tie sends the whole
+    derivative to the forget branch."""
+    if fn == "lstm":
+        a = x + branch
+        i, f, g, o = a.split(D, dim=1)
+        c = torch.sigmoid(f) * sp[1] + torch.sigmoid(i) * torch.tanh(g)
+        return [torch.sigmoid(o) * torch.tanh(c), c]
+    if fn == "gru":
+        xr, xz, xn = x.split(D, dim=1)
+        qr, qz, qn = branch.split(D, dim=1)
+        r, z = torch.sigmoid(xr + qr), torch.sigmoid(xz + qz)
+        nn_ = torch.tanh(xn + r * qn)
+        return [(1 - z) * nn_ + z * sp[0]]
+    if fn == "elman":
+        return [torch.tanh(x + branch)]
+    ai, af, az, ao = (x + branch).split(D, dim=1)
+    lf = af if fn == "slstm" else torch.nn.functional.logsigmoid(af)
+    mp = sp[3]
+    m = torch.where(lf + mp >= ai, lf + mp, ai)
+    ig, fg = torch.exp(ai - m), torch.exp(lf + mp - m)
+    c = fg * sp[1] + ig * torch.tanh(az)
+    n = fg * sp[2] + ig
+    return [torch.sigmoid(ao) * c / n, c, n, m]
+
+
+@pytest.mark.parametrize("fn", FNS)
 def test_bf16_operand_mode_against_torch_autograd(fn):
     """The oracle's bfloat16 mode equals torch autograd of the same cell with a
-    bfloat16-operand recurrent matmul (gates and derivatives by torch)."""
+    bfloat16-operand recurrent matmul (cell and derivatives by torch). For GRU
+    the operand of the backward contraction is the gradient reaching the
+    recurrent branch, r * dn_pre for gate n, not dWx_n = dn_pre: autograd
+    delivers exactly that to the branch, so a rounding applied to the wrong
+    quantity fails here."""
     B, T, N, D = 3, 8, 1, 6
     G, S = oracle.GATES[fn], oracle.STATES[fn]
     Wx, R, b, s0 = rand_problem(fn, B, T, N, D, seed=17, rscale=1.5)
     rng = np.random.default_rng(2)
     dst = rng.normal(size=(S, B, T, N, D))
-    states, _ = oracle.fwd(fn, Wx, R, b, s0, round_bf16=True)
-    dWx, dR, db, ds0 = oracle.bwd(fn, Wx, R, b, s0, dst, round_bf16=True)
+    dl = rng.normal(size=(S, B, 1, N, D))
+    states, last = oracle.fwd(fn, Wx, R, b, s0, round_bf16=True)
+    dWx, dR, db, ds0 = oracle.bwd(fn, Wx, R, b, s0, dst, dl, round_bf16=True)
     plain, _ = oracle.fwd(fn, Wx, R, b, s0)
     assert np.abs(plain - states).max() > 1e-6  # the mode changes the result
+    pdWx, pdR, _, _ = oracle.bwd(fn, Wx, R, b, s0, dst, dl)
+    assert np.abs(pdR - dR).max() > 1e-6
 
     x = torch.from_numpy(Wx[:, :, :, 0, :].copy()).requires_grad_(True)        # [B,T,G,D]
     W = torch.from_numpy(R[:, 0].transpose(1, 0, 2).reshape(D, G * D).copy()).requires_grad_(True)
     bb = torch.from_numpy(b[:, 0].reshape(G * D).copy()).requires_grad_(True)
-    h = torch.from_numpy(s0[0, :, 0, 0].copy()).requires_grad_(True)
-    c = torch.from_numpy(s0[1, :, 0, 0].copy()).requires_grad_(True) if fn == "lstm" else None
-    h0, c0 = h, c
-    hs, cs = [], []
+    init = [torch.from_numpy(s0[s, :, 0, 0].copy()).requires_grad_(True) for s in range(S)]
+    sp = list(init)
+    seq = [[] for _ in range(S)]
     for t in range(T):
-        a = x[:, t].reshape(B, G * D) + _Bf16OperandBranch.apply(h, W, bb)
-        if fn == "lstm":
-            i, f, g, o = a.split(D, dim=1)
-            c = torch.sigmoid(f) * c + torch.sigmoid(i) * torch.tanh(g)
-            h = torch.sigmoid(o) * torch.tanh(c)
-            cs.append(c)
-        else:
-            h = torch.tanh(a)
-        hs.append(h)
-    H = torch.stack(hs, 1)
-    loss = (H * torch.from_numpy(dst[0, :, :, 0])).sum()
-    np.testing.assert_allclose(states[0, :, :, 0], H.detach().numpy(), rtol=1e-12, atol=1e-13)
-    if fn == "lstm":
-        Cs = torch.stack(cs, 1)
-        loss = loss + (Cs * torch.from_numpy(dst[1, :, :, 0])).sum()
+        branch = _Bf16OperandBranch.apply(sp[0], W, bb)
+        sp = _torch_cell_step(fn, x[:, t].reshape(B, G * D), branch, sp, D)
+        for s in range(S):
+            seq[s].append(sp[s])
+    loss = 0.0
+    for s in range(S):
+        Hs = torch.stack(seq[s], 1)  # [B,T,D]
+        np.testing.assert_allclose(states[s, :, :, 0], Hs.detach().numpy(), rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(last[s, :, 0, 0], sp[s].detach().numpy(), rtol=1e-12, atol=1e-13)
+        loss = loss + (Hs * torch.from_numpy(dst[s, :, :, 0])).sum() + (sp[s] * torch.from_numpy(dl[s, :, 0, 0])).sum()
     loss.backward()
     np.testing.assert_allclose(dWx[:, :, :, 0], x.grad.numpy(), rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(dR[:, 0], W.grad.numpy().reshape(D, G, D).transpose(1, 0, 2),
                                rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(db[:, 0], bb.grad.numpy().reshape(G, D), rtol=1e-10, atol=1e-12)
-    np.testing.assert_allclose(ds0[0, :, 0, 0], h0.grad.numpy(), rtol=1e-10, atol=1e-12)
-    if fn == "lstm":
-        np.testing.assert_allclose(ds0[1, :, 0, 0], c0.grad.numpy(), rtol=1e-10, atol=1e-12)
+    for s in range(S):
+        np.testing.assert_allclose(ds0[s, :, 0, 0], init[s].grad.numpy(), rtol=1e-10, atol=1e-12)
 
 
 # ------------------------------------------------------- input projection oracle
