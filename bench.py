@@ -4,8 +4,12 @@
 A step is one pass of the whole hot path over one batch of synthetic input:
 the forward scan (writing states and the backward's tape) followed by the
 backward through time (reverse scan, dWx, dstates0, and the dR / db
-reduction). Default workload: LSTM, bf16 storage / fp32 arithmetic, B=8,
-T=1024, N=3 heads, D=256 (the FlashRNN announcement's usage example).
+reduction). Default workload: the largest one-GPU configuration, LSTM, bf16
+storage / fp32 arithmetic, B=32, T=4096, N=1 head, D=1024 (R = 8 MB, larger
+than one thread-block cluster holds: the cooperative grid kernels). The same
+line carries `target_config`: the per-step roofline fractions of the LSTM fp32
+B=2 T=16 N=1 D=32 workload, the configuration the >= 50% forward / >= 35%
+backward target is stated on, measured in the same run.
 
 Prints ONE JSON line (rank 0). value = timesteps*batch per second of the
 forward + backward step, summed over all ranks (weak scaling: every rank runs
@@ -40,7 +44,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--workload", type=int, default=5, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--function", default=None, help="override the workload's cell (workload 3: gru|elman)")
     ap.add_argument("--path", default="auto", choices=["auto", "fused", "alternating", "simt", "grid"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -50,6 +54,8 @@ def parse():
                          "on the workload's B*T rows instead of the scan")
     ap.add_argument("--proj-shape", default=None, metavar="ROWS,I,C",
                     help="with --input-proj: time this projection shape instead of the workload's")
+    ap.add_argument("--no-target-config", action="store_true",
+                    help="skip the per-step roofline fractions of the LSTM fp32 B=2 T=16 D=32 workload")
     ap.add_argument("--trace", action="store_true",
                     help="print the per-phase cycle medians of the persistent scan kernels (rnn_trace) "
                          "instead of the bench line")
@@ -170,11 +176,11 @@ def kernel_sources_sha(kernel):
     return h.hexdigest()
 
 
-def measured_traffic(kernel, workload):
+def measured_traffic(kernel, workload, path=None):
     """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
     summary (profiles/traffic.json), or None when absent or when the kernel's
     sources changed since the counters were taken."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    p = path or os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     rec = json.load(open(p)).get(f"{kernel}@{workload}")
@@ -196,6 +202,67 @@ def aggregate(total_ms, fwd_ms, world, units_per_rank, steps, device=None):
     value = world * units_per_rank / (ms_per_step / 1e3)
     fwd_value = world * units_per_rank / (fwd / steps / 1e3) if fwd > 0 else 0.0
     return ms_per_step, value, fwd_value
+
+
+def target_config_fracs(dev, steps=50, warmup=5, index=1):
+    """The per-step roofline fractions of one workload's scan kernels (default:
+    LSTM fp32 B=2 T=16 N=1 D=32), as the metric defines them: the forward's
+    roofline max(F / P_tensor, bytes / BW_HBM) over its T steps, divided by the
+    forward scan kernel's CUDA-event time, and the same for the backward scan
+    kernel. Timed after the main measurement, with the L2 flushed before every
+    step outside the event windows; the medians over `steps` steps."""
+    from recurrent_networks_gb300 import _lib
+    from recurrent_networks_gb300.synth import WORKLOADS, workload_inputs
+    w = WORKLOADS[index]
+    fn = w["fns"][0]
+    B, T, N, D, dtype = w["B"], w["T"], w["N"], w["D"], w["dtype"]
+    esize = 2 if dtype == torch.bfloat16 else 4
+    inp = {k: (v.to(dev) if v is not None else None) for k, v in workload_inputs(index, function=fn).items()}
+    S = _lib.rnn_num_states(fn)
+    dims = _lib.make_dims(B, T, N, D, fn, dtype, "auto")
+    _, plan_f = _lib.rnn_plan_describe(dims, False)
+    _, plan_b = _lib.rnn_plan_describe(dims, True)
+    states = torch.empty((S, B, T, N, D), dtype=dtype, device=dev)
+    last = torch.empty((S, B, 1, N, D), dtype=dtype, device=dev)
+    tape = torch.empty(_lib.rnn_tape_size(dims), dtype=torch.uint8, device=dev)
+    ws = torch.empty(_lib.rnn_workspace_size(dims, _lib.WS_BWD), dtype=torch.uint8, device=dev)
+    dWx, dR, db, ds0 = (torch.empty_like(inp[k]) for k in ("Wx", "R", "b", "states0"))
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    ev = {k: torch.cuda.Event(enable_timing=True) for k in ("f0", "f1", "b0", "b1", "s0", "s1")}
+    for e in ev.values():
+        e.record()
+    _lib.rnn_profile_events(0, ev["f0"], ev["f1"])
+    _lib.rnn_profile_events(1, ev["b0"], ev["b1"])
+    tf, tb, ts = [], [], []
+    for k in range(warmup + steps):
+        flush.zero_()
+        ev["s0"].record()
+        _lib.rnn_fwd(dims, inp["Wx"], inp["R"], inp["b"], inp["states0"], states, last, tape, ws)
+        _lib.rnn_bwd(dims, inp["Wx"], inp["R"], inp["b"], inp["states0"], states, tape, inp["dstates"], None,
+                     dWx, dR, db, ds0, ws)
+        ev["s1"].record()
+        ev["s1"].synchronize()
+        if k >= warmup:
+            tf.append(ev["f0"].elapsed_time(ev["f1"]))
+            tb.append(ev["b0"].elapsed_time(ev["b1"]))
+            ts.append(ev["s0"].elapsed_time(ev["s1"]))
+    _lib.rnn_check_status(ws)
+    _lib.rnn_profile_events(0, None, None)
+    _lib.rnn_profile_events(1, None, None)
+    pk = peaks()
+    alg = algorithmic(w, fn, esize)
+    roof_f = max(alg["fwd_flops"] / (pk["bf16"] * 1e12), alg["fwd_bytes"] / (pk["hbm"] * 1e9))
+    roof_b = max(alg["bwd_flops"] / (pk["bf16"] * 1e12), alg["bwd_bytes"] / (pk["hbm"] * 1e9))
+    f_ms, b_ms, s_ms = statistics.median(tf), statistics.median(tb), statistics.median(ts)
+    return {"workload": w["name"], "plan_fwd": plan_f, "plan_bwd": plan_b,
+            "target": "forward >= 0.50, backward >= 0.35 of the per-step roofline",
+            "fwd_frac": roof_f / (f_ms / 1e3), "bwd_frac": roof_b / (b_ms / 1e3),
+            "fwd_roof_ns_per_step": roof_f / T * 1e9, "bwd_roof_ns_per_step": roof_b / T * 1e9,
+            "fwd_kernel_ms": f_ms, "bwd_kernel_ms": b_ms, "step_ms": s_ms,
+            "fwd_ns_per_timestep": f_ms * 1e6 / T, "bwd_ns_per_timestep": b_ms * 1e6 / T,
+            "value": B * T / (s_ms / 1e3), "unit": UNIT, "steps": steps,
+            "peaks": f"{pk['source']} (MEASURED_PEAKS.json: bf16 burst for the tensor term, HBM copy)",
+            "l2": "flushed before every step, outside the event windows"}
 
 
 def host_cores():
@@ -504,6 +571,11 @@ def main():
             "what": f"h exchange alone: cluster of {C}, {slice_bytes} B bulk copy to each peer per step",
             "cycles_per_step": cyc, "ns_per_step": fl_ns, "status": st_fl,
             "fwd_step_over_floor": (f_ms * 1e6 / T) / fl_ns if fl_ns > 0 else None}
+
+    # ---- the configuration the per-step roofline target is stated on (LSTM fp32
+    # B=2 T=16 N=1 D=32), measured in this run after the main measurement
+    if not args.no_target_config and args.workload != 1:
+        result["target_config"] = target_config_fracs(dev)
 
     # ---- e2e through the C ABI with host buffers (pinned), copies inside the window.
     # Every step copies its inputs host -> device and all its outputs device ->

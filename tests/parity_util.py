@@ -13,16 +13,30 @@ Tolerances (stated once, used by every parity test):
                 L2-normwise relative ||g - g*|| / ||g*|| <= 2e-2 and cosine
                 >= 0.9995 for every cell, and normwise-max relative <= 2e-2 for
                 the cells whose gradient is continuous (LSTM, GRU, Elman).
-                sLSTM is exempt from the max-norm bound: the derivative of its
-                stabiliser max(a_f + m, a_i) jumps at ties, and bf16 rounding of
-                h (plus fp32 summation order) moves near-ties to the other branch,
-                which changes single elements of dWx by O(|dm|) and, through the
-                carried dm, earlier steps too. The L2 / cosine bounds therefore
-                widen to 1.5x the oracle's own distance between its bf16-operand
-                and plain-fp64 gradients whenever that is larger: 3-5% L2 for
-                sLSTM at D = 192..512, ~0.1% for LSTM (check_grads).
+  Calibrated widening, with a fixed ceiling. Over long sequences the rounding
+                of h to bf16 alone moves sLSTM's integrating states and its
+                gradients: the bounds above widen to 1.5x the oracle's own
+                distance between its bf16-operand and plain-fp64 results when
+                that is larger, but never past the ceilings CEIL: c, n, m
+                within 0.25 * max(1, |ref|); gradients L2 <= 8e-2 and cosine
+                >= 0.995.
+  sLSTM element-wise bound away from stabiliser ties. The derivative of the
+                stabiliser max(log f + m, a_i) jumps where the two branches
+                tie; bf16 rounding of h and fp32 summation order move
+                near-ties to the other branch, which changes the gate
+                gradients of that unit by O(|dm|) at the tie step and, through
+                the carried dm, at the earlier steps until the input branch
+                wins clearly (there dm is absorbed into a_i's gradient). The
+                elements of dWx and dstates0 in such a backward cone of a
+                near-tie (|log f + m_{t-1} - a_i| < TIE_MARGIN, computed from
+                the oracle's own bf16-operand forward) are left out; every
+                other element must meet the normwise-max bound 2e-2, as must
+                dR and db, which sum over all steps.
 """
 from __future__ import annotations
+
+import json
+import os
 
 import numpy as np
 import torch
@@ -34,6 +48,19 @@ TOL = {
     torch.float32: dict(h=1e-4, states=1e-4, states_rel=False, grad=1e-3, cos=None),
     torch.bfloat16: dict(h=3e-2, states=3e-2, states_rel=True, grad=2e-2, cos=0.9995),
 }
+# fixed ceilings of the calibrated (widened) bf16 bounds
+CEIL = dict(states=0.25, grad_l2=8e-2, cos=0.995)
+# |log f + m_{t-1} - a_i| below which an sLSTM step counts as a near-tie
+TIE_MARGIN = 5e-2
+
+
+def _log(rec):
+    """Appends one comparison record to the JSON-lines file named by the
+    environment variable RNN_PARITY_LOG (a diagnostic; off by default)."""
+    path = os.environ.get("RNN_PARITY_LOG")
+    if path:
+        with open(path, "a") as fh:
+            fh.write(json.dumps(rec) + "\n")
 
 
 def run_fwd(fn, inp, path="auto", want_tape=True, stream=None):
@@ -86,9 +113,13 @@ def check_states(fn, dtype, got, ref, what="states", calib=None):
         e = np.abs(got[s] - ref[s]) / den
         m = e.max() if e.size else 0.0
         bound = tol["states"]
+        cal = None
         if calib is not None and e.size:
-            bound = max(bound, 1.5 * float((np.abs(calib[s] - ref[s]) / den).max()))
+            cal = float((np.abs(calib[s] - ref[s]) / den).max())
+            bound = min(CEIL["states"], max(bound, 1.5 * cal))
+        _log(dict(kind="state", fn=fn, what=what, s=s, err=float(m), calib=cal, bound=bound))
         assert m <= bound, f"{fn} {what} state {s}: err {m:.3g} > {bound:.3g}"
+    _log(dict(kind="state", fn=fn, what=what, s=0, err=float(err_h), bound=tol["h"]))
     return err_h
 
 
@@ -121,22 +152,69 @@ def check_grad(name, dtype, got, ref):
     return rel
 
 
-def check_grads(fn, inp, got, dlast=None):
+def _bf16_np(x):
+    """binary32 then bfloat16 (round to nearest even), as the oracle's
+    bfloat16-operand mode rounds h."""
+    return torch.from_numpy(np.ascontiguousarray(x)).float().bfloat16().double().numpy()
+
+
+def slstm_tie_cone(fn, inp, margin=TIE_MARGIN):
+    """Backward cones of the sLSTM stabiliser's near-ties, from the oracle's
+    own bfloat16-operand forward. Returns (mask [B,T,N,D], mask0 [B,N,D]):
+    mask marks the (row, step, unit) whose gate gradients a branch flip at a
+    near-tie can change; mask0 the units whose flip reaches dstates0.
+
+    At step t the stabiliser is m_t = max(log f + m_{t-1}, a_i). Its margin
+    log f + m_{t-1} - a_i (>= 0: forget branch) within `margin` of zero is a
+    near-tie. A flip there reroutes dm_t; the reroute travels to dm_{t-1}
+    through the forget branch and stops at the first step whose input branch
+    wins clearly, where dm is absorbed into a_i's gradient (that step is
+    still in the cone)."""
+    f64 = lambda v: None if v is None else (v.detach().cpu().double().numpy() if hasattr(v, "detach")
+                                            else np.asarray(v, dtype=np.float64))
+    Wx, R, b, s0 = (f64(inp[k]) for k in ("Wx", "R", "b", "states0"))
+    B, T, G, N, D = Wx.shape
+    if s0 is None:
+        s0 = np.zeros((4, B, 1, N, D))
+    st, _ = oracle.fwd(fn, Wx, R, b, s0, round_bf16=True)
+    h_prev = _bf16_np(np.concatenate([s0[0], st[0][:, :-1]], axis=1))      # [B,T,N,D]
+    m_prev = np.concatenate([s0[3], st[3][:, :-1]], axis=1)
+    a_i = Wx[:, :, 0] + np.einsum("btni,nij->btnj", h_prev, R[0]) + b[0]
+    a_f = Wx[:, :, 1] + np.einsum("btni,nij->btnj", h_prev, R[1]) + b[1]
+    lf = a_f if fn == "slstm" else np.minimum(a_f, 0.0) - np.log1p(np.exp(-np.abs(a_f)))
+    mar = lf + m_prev - a_i
+    near = np.abs(mar) < margin
+    mask = np.zeros((B, T, N, D), dtype=bool)
+    active = np.zeros((B, N, D), dtype=bool)
+    for t in range(T - 1, -1, -1):
+        active |= near[:, t]
+        mask[:, t] = active
+        active &= ~((~near[:, t]) & (mar[:, t] < 0.0))
+    return mask, active
+
+
+def check_grads(fn, inp, got, dlast=None, ref=None, plain=None, label=""):
     """All four gradients (dWx, dR, db, dstates0) of the CUDA path against the
     oracle. fp32: the TOL bounds against the plain oracle. bf16: against the
     oracle's bfloat16-operand mode; the L2 / cosine bounds widen to 1.5x the
     distance between the oracle's own bf16-operand and plain-fp64 gradients
     when that is larger (the gradient's sensitivity to bf16 rounding of h: a
-    few percent for sLSTM, whose stabiliser max flips branch at near-ties,
-    ~0.1% for LSTM)."""
+    few percent for sLSTM, ~0.1% for LSTM), never past CEIL. sLSTM meets the
+    normwise-max bound outside the near-tie cones (slstm_tie_cone).
+    ref / plain: precomputed oracle gradients (bf16-operand mode / plain), or
+    None to run the oracle here; plain = False skips the widening."""
     names = ("dWx", "dR", "db", "dstates0")
     dtype = inp["Wx"].dtype
-    ref = oracle_bwd(fn, inp, dlast=dlast)
-    plain = oracle_bwd(fn, inp, dlast=dlast, round_bf16=False) if dtype == torch.bfloat16 else None
+    if ref is None:
+        ref = oracle_bwd(fn, inp, dlast=dlast)
+    if plain is None and dtype == torch.bfloat16:
+        plain = oracle_bwd(fn, inp, dlast=dlast, round_bf16=False)
+    slstm = fn.startswith("slstm")
+    cone = slstm_tie_cone(fn, inp) if (slstm and dtype == torch.bfloat16) else None
     for k, (name, g) in enumerate(zip(names, got)):
         if g is None:
             continue
-        if plain is None:
+        if dtype == torch.float32:
             check_grad(f"{fn} {name}", dtype, g, ref[k])
             continue
         tol = TOL[dtype]
@@ -145,12 +223,28 @@ def check_grads(fn, inp, got, dlast=None):
         if np.abs(ref[k]).max() == 0:
             assert np.abs(arr).max() == 0, f"{fn} {name}: expected zeros"
             continue
-        _, l2_s, cos_s = grad_errors(plain[k], ref[k])
+        l2_tol, cos_tol, l2_s, cos_s = tol["grad"], tol["cos"], None, None
+        if plain is not None and plain is not False:
+            _, l2_s, cos_s = grad_errors(plain[k], ref[k])
+            l2_tol = min(CEIL["grad_l2"], max(tol["grad"], 1.5 * l2_s))
+            cos_tol = max(CEIL["cos"], min(tol["cos"], 1.0 - 1.5 * (1.0 - cos_s)))
         rel, l2, cos = grad_errors(arr, ref[k])
-        l2_tol = max(tol["grad"], 1.5 * l2_s)
-        cos_tol = min(tol["cos"], 1.0 - 1.5 * (1.0 - cos_s))
-        if not fn.startswith("slstm"):
-            assert rel <= tol["grad"], f"{fn} {name}: normwise-max relative err {rel:.3g} > {tol['grad']}"
+        rec = dict(kind="grad", fn=fn, name=name, label=label, rel=rel, l2=l2, cos=cos, l2_s=l2_s,
+                   cos_s=cos_s, l2_tol=l2_tol, cos_tol=cos_tol)
+        rel_checked = rel
+        if cone is not None and name in ("dWx", "dstates0"):
+            if name == "dWx":
+                m = np.broadcast_to(cone[0][:, :, None], arr.shape)          # [B,T,G,N,D]
+            else:
+                m = np.broadcast_to(cone[1][None, :, None], arr.shape)       # [S,B,1,N,D]
+            keep = ~m
+            err = np.abs(arr - ref[k])
+            rel_checked = float(err[keep].max() / np.abs(ref[k]).max()) if keep.any() else 0.0
+            rec.update(masked_frac=float(m.mean()), rel_unmasked=rel_checked)
+        _log(rec)
+        assert rel_checked <= tol["grad"], \
+            f"{fn} {name}: normwise-max relative err {rel_checked:.3g} > {tol['grad']}" + \
+            (" (outside the near-tie cones)" if cone is not None and name in ("dWx", "dstates0") else "")
         assert l2 <= l2_tol, f"{fn} {name}: L2-normwise relative err {l2:.3g} > {l2_tol:.3g}"
         assert cos >= cos_tol, f"{fn} {name}: cosine {cos:.6f} < {cos_tol:.6f}"
 

@@ -38,14 +38,19 @@ def test_slstm_counts_four_states():
     assert s["bwd_bytes"] == 16 * 4 * (2 * 4 + 2 * 4) * 192 * 2
 
 
-def test_traffic_record_follows_the_kernel_sources(monkeypatch):
-    """profiles/traffic.json's DRAM bytes are reported only while the kernel's
+def test_traffic_record_follows_the_kernel_sources(monkeypatch, tmp_path):
+    """A traffic record's DRAM bytes are reported only while the kernel's
     sources hash to what they were when the counters were taken."""
-    got = bench.measured_traffic("fused_bwd_kernel", "lstm_bf16_B8_T1024_N3_D256")
-    assert got is not None and got > 0
+    import json
+    rec = tmp_path / "traffic.json"
+    key = "fused_bwd_kernel@lstm_bf16_B8_T1024_N3_D256"
+    rec.write_text(json.dumps({key: {"dram_bytes_per_launch": 2.0e8,
+                                     "sources_sha256": bench.kernel_sources_sha("fused_bwd_kernel")}}))
+    got = bench.measured_traffic("fused_bwd_kernel", "lstm_bf16_B8_T1024_N3_D256", path=str(rec))
+    assert got == 2.0e8
     monkeypatch.setattr(bench, "kernel_sources_sha", lambda kernel: "0" * 64)
-    assert bench.measured_traffic("fused_bwd_kernel", "lstm_bf16_B8_T1024_N3_D256") is None
-    assert bench.measured_traffic("fused_fwd_kernel", "no_such_workload") is None
+    assert bench.measured_traffic("fused_bwd_kernel", "lstm_bf16_B8_T1024_N3_D256", path=str(rec)) is None
+    assert bench.measured_traffic("fused_fwd_kernel", "no_such_workload", path=str(rec)) is None
 
 
 def test_oracle_sample_is_bounded():

@@ -189,6 +189,38 @@ def test_fused_backward_parity(case, monkeypatch):
     assert d1 <= 2e-2, d1
 
 
+# tape = NULL: the backward rebuilds the tape inside its workspace by running the
+# same forward kernels (the gate recompute), on the bf16 cluster and grid paths
+RECOMPUTE_CASES = [
+    ("fused", "lstm", 5, 19, 1, 256, dict(C=16)),
+    ("fused", "gru", 9, 20, 3, 48, dict(C=3)),
+    ("fused", "slstm", 5, 29, 2, 96, dict(C=3)),
+    ("grid", "lstm", 3, 9, 1, 1024, dict(C=64)),
+    ("grid", "gru", 9, 19, 2, 128, dict(C=8)),
+    ("grid", "slstm_logsig", 5, 13, 1, 512, dict(C=32)),
+]
+
+
+@pytest.mark.parametrize("case", RECOMPUTE_CASES,
+                         ids=lambda c: "%s-%s-B%dT%dN%dD%d-" % c[:6] + "-".join(f"{k}{v}" for k, v in c[6].items()))
+def test_backward_recomputes_tape_bf16(case, monkeypatch):
+    path, fn, B, T, N, D, restr = case
+    _restrict(monkeypatch, restr)
+    inp = _inputs(fn, (B, T, N, D), torch.bfloat16, seed=1100 + B + T + D)
+    dims = _lib.make_dims(B, T, N, D, fn, torch.bfloat16, path)
+    for bwd in (False, True):
+        rc, desc = _lib.rnn_plan_describe(dims, bwd)
+        assert rc == 0 and f"path={path}" in desc, desc
+    st, last, tape = run_fwd(fn, inp, path)
+    dl = torch.randn(last.shape, generator=torch.Generator().manual_seed(8)).to(torch.bfloat16).cuda()
+    got = run_bwd(fn, inp, st, None, path, dlast=dl)
+    check_grads(fn, inp, got, dlast=dl)
+    # the rebuilt tape is the forward's tape: the gradients equal those taken with it
+    with_tape = run_bwd(fn, inp, st, tape, path, dlast=dl)
+    for name, a, b in zip(("dWx", "dR", "db", "dstates0"), got, with_tape):
+        assert torch.equal(a, b), f"{name} differs between the rebuilt and the stored tape"
+
+
 # ---------------------------------------------------------------- grid kernels
 GRID_CASES = [
     ("lstm", 5, 23, 1, 256, dict(C=16)),

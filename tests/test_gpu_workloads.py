@@ -2,37 +2,35 @@
 benchmark times (the planner's automatic choice: cluster kernels for D <= 256,
 the cooperative grid kernels for D = 1024).
 
-Batch rows are independent sequences. So the oracle runs on a sample of
-them (the first and the last batch row, every head, all T steps), and the
-matching slices of the GPU's full-batch outputs must agree with it within
-tests/parity_util.py's tolerances. dR and db sum over every batch row; they
-are checked by a property that holds at any size: they equal the fp32
-contraction of the GPU's own h_{t-1} with its own recurrent-branch
-gradients (dr = dWx for LSTM and sLSTM)."""
+The fp64 oracle runs on every batch row, every head and every step, on all
+host cores, and every output of the CUDA path is compared with it element by
+element: states and last states against the plain oracle, the four gradients
+(dWx, dR, db, dstates0) against its bfloat16-operand mode, with the bounds of
+tests/parity_util.py. dR and db sum over all B*T (row, step) pairs, so this is
+the check of the full-size weight-gradient GEMM and column sums against the
+definition, not against the GPU's own intermediate values."""
+import os
+
 import numpy as np
 import pytest
 import torch
 
+from oracle import oracle
 from recurrent_networks_gb300 import _lib
 from recurrent_networks_gb300.synth import WORKLOADS, workload_inputs
 
-from parity_util import check_grads, check_states, oracle_fwd, run_bwd, run_fwd
+from parity_util import check_grads, check_states, run_bwd, run_fwd
 
 pytestmark = pytest.mark.gpu
 
 CASES = [(2, "lstm"), (3, "gru"), (3, "elman"), (4, "slstm"), (5, "lstm")]
 
 
-def _rows(inp, rows):
-    out = {}
-    for k, v in inp.items():
-        if v is None or k in ("R", "b"):
-            out[k] = v
-        elif k == "Wx":
-            out[k] = v[rows]
-        else:  # [S, B, ...]
-            out[k] = v[:, rows]
-    return out
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"w{c[0]}-{c[1]}")
@@ -40,33 +38,29 @@ def test_workload_full_size(case):
     k, fn = case
     w = WORKLOADS[k]
     B, T, N, D = w["B"], w["T"], w["N"], w["D"]
-    inp = workload_inputs(k, function=fn, device="cuda")
+    bf16 = w["dtype"] == torch.bfloat16
+    host = workload_inputs(k, function=fn)
+    inp = {key: (v.cuda() if v is not None else None) for key, v in host.items()}
     dims = _lib.make_dims(B, T, N, D, fn, w["dtype"], "auto")
     rc, plan = _lib.rnn_plan_describe(dims)
     assert rc == 0 and ("path=fused" in plan or "path=grid" in plan), plan
     st, last, tape = run_fwd(fn, inp, "auto")
-    rows = [0, B - 1]
-    sub = _rows(inp, rows)
-    ref_st, ref_last = oracle_fwd(fn, sub, nthreads=8)
-    cal_st, cal_last = oracle_fwd(fn, sub, nthreads=8, round_bf16=True) if w["dtype"] == torch.bfloat16 else (None, None)
-    check_states(fn, w["dtype"], st[:, rows], ref_st, calib=cal_st)
-    check_states(fn, w["dtype"], last[:, rows], ref_last, "last", calib=cal_last)
+    nt = _cores()
+    ref_st, ref_last = oracle.fwd(fn, host["Wx"], host["R"], host["b"], host["states0"], nthreads=nt)
+    # the bf16-operand states calibrate the long-sequence bounds of sLSTM's c, n, m
+    cal_st, cal_last = (oracle.fwd(fn, host["Wx"], host["R"], host["b"], host["states0"], nthreads=nt,
+                                   round_bf16=True) if (bf16 and fn.startswith("slstm")) else (None, None))
+    check_states(fn, w["dtype"], st, ref_st, calib=cal_st)
+    check_states(fn, w["dtype"], last, ref_last, "last", calib=cal_last)
+    del ref_st, cal_st
     if not w["backward"]:
         return
-    dWx, dR, db, ds0 = run_bwd(fn, inp, st, tape, "auto")
-    check_grads(fn, sub, (dWx[rows], None, None, ds0[:, rows]))
-    # dR[g, n] = sum_{b,t} h_{t-1}[b, n, :]^T dr[b, t, g, n, :], db = sum dr
-    h = st[0].float()                                          # [B, T, N, D]
-    hprev = torch.cat([inp["states0"][0].float(), h[:, :-1]], dim=1)  # [B, T, N, D]
-    dr = dWx.float()                                           # [B, T, G, N, D]
-    G = dr.shape[2]
-    for g in range(G):
-        for n in range(N):
-            ref = hprev[:, :, n, :].reshape(B * T, D).t() @ dr[:, :, g, n, :].reshape(B * T, D)
-            got = dR[g, n].float()
-            rel = ((got - ref).norm() / ref.norm()).item()
-            assert rel <= 1e-2, (g, n, rel)
-    ref_db = dr.sum(dim=(0, 1))
-    rel = ((db.float() - ref_db).norm() / ref_db.norm()).item()
-    assert rel <= 1e-2, rel
-    assert np.isfinite(dR.float().cpu().numpy()).all()
+    got = run_bwd(fn, inp, st, tape, "auto")
+    ref = oracle.bwd(fn, host["Wx"], host["R"], host["b"], host["states0"], host["dstates"], nthreads=nt,
+                     round_bf16=bf16)
+    # the widening of the bf16 bounds needs the plain gradients too: only sLSTM
+    # has a distance between the two modes above the base bounds
+    plain = (oracle.bwd(fn, host["Wx"], host["R"], host["b"], host["states0"], host["dstates"], nthreads=nt)
+             if (bf16 and fn.startswith("slstm")) else False)
+    check_grads(fn, host, got, ref=ref, plain=plain, label=w["name"])
+    assert np.isfinite(got[1].float().cpu().numpy()).all()
