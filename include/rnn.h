@@ -83,7 +83,11 @@ int rnn_num_states(int function); /* S, or -1 */
 size_t rnn_tape_size(const rnn_dims_t *dims);
 
 /* Bytes of scratch the call of the given kind needs (a multiple of 256;
- * at least 256). 0 for invalid dims. */
+ * at least 256). 0 for invalid dims. The caller allocates it: the usage
+ * example of the FlashRNN announcement passes every tensor in ("a functional
+ * structure, none of the parameters are tied to the flashrnn function"), and
+ * this library keeps that contract for its scratch too. The size depends on
+ * the plan chosen for the current device. */
 size_t rnn_workspace_size(const rnn_dims_t *dims, int kind);
 
 /*
@@ -104,7 +108,10 @@ int rnn_fwd(const rnn_dims_t *dims, const void *Wx, const void *R, const void *b
 
 /*
  * Backward through time of rnn_fwd (the gradient of sum(states*dstates) +
- * sum(last*dlast) with respect to every input).
+ * sum(last*dlast) with respect to every input). The FlashRNN announcement's
+ * usage example creates Wx, R, b and the initial states with
+ * requires_grad=True: these four gradients are what its flashrnn call
+ * returns through autograd.
  *   Wx, R, b, states0  the forward's inputs (states0 may be NULL = zeros)
  *   states             the forward's output [S,B,T,N,D]
  *   tape               the tape rnn_fwd wrote for these inputs, or NULL to have
@@ -134,13 +141,21 @@ int rnn_bwd(const rnn_dims_t *dims, const void *Wx, const void *R, const void *b
  * held by every GPU that loads it until the process exits. It holds the status
  * word and, for GRU or when dWx is NULL, the recurrent-branch gradients
  * (B*T*G*N*D elements of the storage type): problems whose need exceeds the
- * array (256 bytes + those gradients) return RNN_ENOSPC before any work.
+ * array (256 bytes + those gradients) return RNN_ENOSPC before any work. The
+ * rest of the array holds the weight gradient's split-K partial sums when they
+ * fit; when they do not, dR is computed without splitting K, so dR and db may
+ * differ from rnn_bwd's in the order of their fp32 sums (not beyond rounding).
+ * Paths: only the cluster kernels and the plain kernel run here. An explicit
+ * RNN_PATH_GRID or RNN_PATH_ALTERNATING returns RNN_EUNSUPPORTED (their
+ * exchange buffers would need workspace); under RNN_PATH_AUTO a problem whose
+ * plan is one of those runs on the plain kernel instead.
  * The first call on a device looks the array's device address up (once per
  * device); make that first call before any stream capture. Every call shares
  * the array and keeps the last call's contents: calls whose work overlaps on
  * the GPU (different streams or threads) race; calls on one stream are safe.
- * Device-side wait time-outs of this entry point are not reported.
- * Errors: RNN_EINVAL, RNN_EUNSUPPORTED, RNN_ENOSPC, RNN_ECUDA.
+ * Device-side wait time-outs are recorded in the array's status word (cleared
+ * at the start of every call) and read by rnn_bwd_noalloc_status.
+ * Errors: RNN_EINVAL (as rnn_bwd), RNN_EUNSUPPORTED, RNN_ENOSPC, RNN_ECUDA.
  */
 #define RNN_BWD_NOALLOC_SCRATCH_BYTES (16u << 20)
 int rnn_bwd_noalloc(const rnn_dims_t *dims, const void *Wx, const void *R, const void *b,
@@ -148,14 +163,39 @@ int rnn_bwd_noalloc(const rnn_dims_t *dims, const void *Wx, const void *R, const
                     const void *dstates, const void *dlast, void *dWx, void *dR, void *db,
                     void *dstates0, void *stream);
 
+/* Status of the most recent rnn_bwd_noalloc call on the current device (no
+ * counterpart on the pages): synchronises `stream`, reads and clears the
+ * status word of the library's fixed scratch array. Returns RNN_OK,
+ * RNN_ETIMEOUT (a device-side wait of that call ran out; its results are not
+ * valid) or RNN_ECUDA. */
+int rnn_bwd_noalloc_status(void *stream);
+
 /* Synchronises `stream`, reads and clears the device status word that kernels
- * running on `workspace` recorded. Returns RNN_OK, RNN_ETIMEOUT or RNN_ECUDA. */
+ * running on `workspace` recorded. Returns RNN_OK, RNN_ETIMEOUT or RNN_ECUDA.
+ * (The pages have no device-side error path; the status-code convention --
+ * validation errors returned before any work, the empty-batch error, T = 0 as
+ * a copy of the initial state -- follows the precedent of ruDNN 0.2.1,
+ * src/kda/prepared.rs, prepare_chunk_kda.) */
 int rnn_check_status(void *workspace, void *stream);
 
 /* Writes a one-line description of the plan chosen for dims (path, cluster
  * size, tiles) or the reason none fits into buf (NUL-terminated, truncated to
- * len). Returns RNN_OK, RNN_EINVAL or RNN_EUNSUPPORTED. */
+ * len). Returns RNN_OK, RNN_EINVAL or RNN_EUNSUPPORTED. The plan is the
+ * solution of an integer constraint problem over the tile and cluster sizes
+ * (divisibility, warp, register and shared-memory limits, cluster
+ * co-residency on the current device), the role the FlashRNN announcement's
+ * overview gives its ConstrINT tuner ("hardware limits written as equalities,
+ * inequalities and divisibility constraints"). */
 int rnn_plan_describe(const rnn_dims_t *dims, int for_backward, char *buf, size_t len);
+
+/* Planning for a stated device (for the planner's tests and what-if sizing):
+ * with sms > 0, every later plan uses these limits -- sms SMs (1 .. 4096),
+ * smem_per_cta bytes of shared memory per CTA (1024 .. 1048576) and clusters
+ * of at most max_cluster CTAs (1 .. 16) -- instead of the current device's,
+ * and co-residency is judged from the SM count alone. sms <= 0 returns to the
+ * current device. Process-global; launches on a device smaller than the stated
+ * one fail. Returns RNN_OK or RNN_EINVAL. */
+int rnn_plan_set_limits(int sms, int smem_per_cta, int max_cluster);
 
 const char *rnn_strerror(int status);
 

@@ -20,7 +20,8 @@ WS_FWD, WS_BWD, WS_BWD_RECOMPUTE = 0, 1, 2
 
 EXPORTS = ["rnn_num_gates", "rnn_num_states", "rnn_tape_size", "rnn_workspace_size", "rnn_fwd",
            "rnn_bwd", "rnn_check_status", "rnn_plan_describe", "rnn_strerror", "rnn_kernel_launches",
-           "rnn_profile_events", "rnn_bwd_noalloc", "rnn_trace", "rnn_debug_inject_wait"]
+           "rnn_profile_events", "rnn_bwd_noalloc", "rnn_bwd_noalloc_status", "rnn_trace",
+           "rnn_debug_inject_wait", "rnn_plan_set_limits"]
 
 
 class RnnError(RuntimeError):
@@ -56,12 +57,14 @@ def load(path: str | None = None):
             lib.rnn_bwd.argtypes = [dp] + [vp] * 13 + [sz, vp]
             lib.rnn_check_status.argtypes = [vp, vp]
             lib.rnn_plan_describe.argtypes = [dp, i, ctypes.c_char_p, sz]
+            lib.rnn_plan_set_limits.argtypes = [i, i, i]
             lib.rnn_strerror.argtypes = [i]
             lib.rnn_strerror.restype = ctypes.c_char_p
             lib.rnn_kernel_launches.argtypes = []
             lib.rnn_kernel_launches.restype = ctypes.c_ulonglong
             lib.rnn_profile_events.argtypes = [i, vp, vp]
             lib.rnn_bwd_noalloc.argtypes = [dp] + [vp] * 13
+            lib.rnn_bwd_noalloc_status.argtypes = [vp]
             lib.rnn_trace.argtypes = [vp, i, i]
             lib.rnn_debug_inject_wait.argtypes = [i, ctypes.c_ulonglong]
             lib.rnn_exchange_floor.argtypes = [i, i, i, vp, vp]
@@ -142,6 +145,12 @@ def rnn_plan_describe(dims: Dims, for_backward: bool = False) -> tuple[int, str]
     return rc, buf.value.decode()
 
 
+def rnn_plan_set_limits(sms: int = 0, smem_per_cta: int = 227 * 1024, max_cluster: int = 16) -> int:
+    """Plan for a stated device (sms > 0) or the current one (sms <= 0)."""
+    return _check(load().rnn_plan_set_limits(int(sms), int(smem_per_cta), int(max_cluster)),
+                  "rnn_plan_set_limits")
+
+
 def rnn_strerror(status: int) -> str:
     return load().rnn_strerror(status).decode()
 
@@ -166,6 +175,11 @@ def rnn_bwd_noalloc(dims: Dims, Wx, R, b, states0, states, tape, dstates, dlast,
                                 _p(tape), _p(dstates), _p(dlast), _p(dWx), _p(dR), _p(db), _p(dstates0),
                                 _stream(stream))
     return _check(rc, "rnn_bwd_noalloc")
+
+
+def rnn_bwd_noalloc_status(stream=None) -> int:
+    """Status of the last rnn_bwd_noalloc call on the current device (synchronises)."""
+    return _check(load().rnn_bwd_noalloc_status(_stream(stream)), "rnn_bwd_noalloc_status")
 
 
 def rnn_trace(buf=None, t0: int = 0, steps: int = 0) -> int:

@@ -5,7 +5,10 @@
 #include <string.h>
 
 #include <atomic>
+#include <map>
 #include <mutex>
+#include <string>
+#include <tuple>
 #include <vector>
 
 #include "kernels.cuh"
@@ -59,6 +62,94 @@ cudaError_t set_nonportable_cluster(const void* func) {
   return e;
 }
 
+// ---- device limits of the planner ------------------------------------------
+namespace {
+constexpr int kMaxDev = 64;
+std::mutex g_lim_mu;
+bool g_lim_known[kMaxDev] = {};
+DeviceLimits g_lim[kMaxDev];
+bool g_lim_override = false;
+DeviceLimits g_lim_forced;
+// co-resident clusters per (device, cell, direction, shape)
+std::map<std::tuple<int, int, int, int, int, int, int, int, int, size_t>, int> g_cap;
+
+int capacity_cb(int fn, bool bwd, const FusedShape& fs) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  const auto key = std::make_tuple(dev, fn, (int)bwd, fs.C, fs.NT, fs.KT, fs.MT, (int)fs.allg, fs.warps, fs.smem);
+  {
+    std::lock_guard<std::mutex> lock(g_lim_mu);
+    auto it = g_cap.find(key);
+    if (it != g_cap.end()) return it->second;
+  }
+  const int cap = fused_capacity(fn, bwd, fs);
+  if (cap >= 0) {
+    std::lock_guard<std::mutex> lock(g_lim_mu);
+    g_cap[key] = cap;
+  }
+  return cap;
+}
+}  // namespace
+
+int cluster_capacity_of(const void* func, const FusedShape& sh) {
+  if (set_smem_attr(func, sh.smem) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return -1;
+  }
+  if (sh.C > 8 && set_nonportable_cluster(func) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;  // the device refuses clusters above the portable size
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sh.C);
+  cfg.blockDim = dim3(sh.warps * 32);
+  cfg.dynamicSmemBytes = sh.smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = sh.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, func, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return -1;
+  }
+  return clusters;
+}
+
+// The limits the planner uses: forced ones (rnn_plan_set_limits), else those
+// of the current device (SM count, opt-in shared memory per block, cluster
+// co-residency asked per candidate), else the GB300 defaults when no device
+// can be asked (a size query on a host without a GPU).
+DeviceLimits device_limits() {
+  std::lock_guard<std::mutex> lock(g_lim_mu);
+  if (g_lim_override) return g_lim_forced;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    (void)cudaGetLastError();
+    return DeviceLimits{};
+  }
+  if (!g_lim_known[dev]) {
+    DeviceLimits l;
+    int sms = 0, smem = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess || sms < 1) {
+      (void)cudaGetLastError();
+      return DeviceLimits{};
+    }
+    l.sms = sms;
+    l.smem_per_cta = (size_t)smem;
+    l.cluster_capacity = capacity_cb;
+    g_lim[dev] = l;
+    g_lim_known[dev] = true;
+  }
+  return g_lim[dev];
+}
+
+int device_sms() { return device_limits().sms; }
+
 // Optional events recorded around the scan kernel (rnn_profile_events).
 static cudaEvent_t g_prof[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};
 static void prof_mark(int which, int edge, cudaStream_t st) {
@@ -72,7 +163,7 @@ struct Sizes {
   size_t esize, wx, r, bias, st, st0, tape, dr;
 };
 
-static bool dims_ok(const rnn_dims_t* d) {
+bool dims_ok(const rnn_dims_t* d) {
   return d && d->B >= 1 && d->T >= 0 && d->N >= 1 && d->D >= 1 && d->function >= 0 &&
          d->function <= 4 && (d->dtype == RNN_F32 || d->dtype == RNN_BF16) && d->path >= 0 &&
          d->path <= 4 && (size_t)d->B * d->N * d->D < ((size_t)1 << 40);
@@ -125,9 +216,42 @@ static int cuda_status(cudaError_t e) {
   return RNN_ECUDA;
 }
 
+// Plans are cached per (dims, direction, device, limits in force, planner
+// restriction variables): the enumeration and its co-residency queries run
+// once per shape, not on every call.
+namespace {
+std::mutex g_plan_mu;
+std::map<std::string, std::pair<int, Plan>> g_plans;
+}  // namespace
+
 static int choose(const rnn_dims_t* d, bool bwd, Plan* plan) {
-  PlanRequest q{d->B, d->T, d->N, d->D, d->function, d->dtype, d->path, bwd};
-  return plan_select(q, plan);
+  const DeviceLimits lim = device_limits();
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    dev = -1;
+  }
+  char key[320];
+  int n = snprintf(key, sizeof(key), "%d %d %d %d %d %d %d %d | %d %d %d %zu %d |", d->B, d->T, d->N, d->D,
+                   d->function, d->dtype, d->path, (int)bwd, dev, lim.sms, lim.max_cluster, lim.smem_per_cta,
+                   lim.cluster_capacity != nullptr);
+  for (const char* v : {"RNN_PLAN_C", "RNN_PLAN_NT", "RNN_PLAN_KT", "RNN_PLAN_MT", "RNN_PLAN_ALLG"}) {
+    const char* e = getenv(v);
+    if (n > 0 && n < (int)sizeof(key)) n += snprintf(key + n, sizeof(key) - n, " %s", e ? e : "-");
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    auto it = g_plans.find(key);
+    if (it != g_plans.end()) {
+      *plan = it->second.second;
+      return it->second.first;
+    }
+  }
+  PlanRequest q{d->B, d->T, d->N, d->D, d->function, d->dtype, d->path, bwd, &lim};
+  const int rc = plan_select(q, plan);
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  g_plans[key] = std::make_pair(rc, *plan);
+  return rc;
 }
 
 // Grid path scratch inside the workspace (after the 256-byte status word):
@@ -151,6 +275,7 @@ static void alt_scratch(const rnn_dims_t* d, char* ws, bool bwd, AltArgs* a) {
 
 // Upper bound of every device-side wait.
 static unsigned long long g_wait_limit_ns = 2000000000ull;
+unsigned long long wait_limit_ns() { return g_wait_limit_ns; }
 
 // Phase trace of the persistent kernels (rnn_trace).
 static unsigned long long* g_trace_buf = nullptr;
@@ -394,6 +519,24 @@ int rnn_check_status(void* workspace, void* stream) {
     if (e != cudaSuccess) return cuda_status(e);
     return RNN_ETIMEOUT;
   }
+  return RNN_OK;
+}
+
+int rnn_plan_set_limits(int sms, int smem_per_cta, int max_cluster) {
+  std::lock_guard<std::mutex> lock(g_lim_mu);
+  if (sms <= 0) {
+    g_lim_override = false;
+    return RNN_OK;
+  }
+  if (sms > 4096 || smem_per_cta < 1024 || smem_per_cta > (1 << 20) || max_cluster < 1 || max_cluster > 16)
+    return RNN_EINVAL;
+  DeviceLimits l;
+  l.sms = sms;
+  l.smem_per_cta = (size_t)smem_per_cta;
+  l.max_cluster = max_cluster;
+  l.cluster_capacity = nullptr;  // a stated device: co-residency from the SM count alone
+  g_lim_forced = l;
+  g_lim_override = true;
   return RNN_OK;
 }
 

@@ -17,7 +17,7 @@ namespace {  // each including translation unit has its own copy of the kernels
 constexpr int COLSUM_MAX_CHUNKS = 64;
 inline int colsum_chunks(int rows, int cols) {
   const int colblocks = (cols + 255) / 256;
-  int c = (4 * 152 + colblocks - 1) / colblocks;  // about four blocks per SM
+  int c = (4 * device_sms() + colblocks - 1) / colblocks;  // about four blocks per SM
   if (c > COLSUM_MAX_CHUNKS) c = COLSUM_MAX_CHUNKS;
   if (c > (rows + 31) / 32) c = (rows + 31) / 32;  // at least 32 rows per chunk
   return c < 1 ? 1 : c;

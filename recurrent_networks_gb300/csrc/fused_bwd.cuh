@@ -399,4 +399,17 @@ cudaError_t fused_bwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStrea
   return e;
 }
 
+// Clusters of the backward cluster kernel of shape `sh` that the current
+// device holds at once, -1 if the device cannot be asked.
+template <int FN>
+int fused_bwd_capacity(const FusedShape& sh) {
+  void (*k)(const CUtensorMap, const CUtensorMap, FusedArgs) = nullptr;
+#define RNN_FUSED_BWD_PICK(NT_, MT_) \
+  if (sh.NT == NT_ && sh.MT == MT_) k = fused_bwd_kernel<FN, NT_, MT_>;
+  RNN_FUSED_BWD_PICK(1, 1) RNN_FUSED_BWD_PICK(1, 2) RNN_FUSED_BWD_PICK(2, 1) RNN_FUSED_BWD_PICK(2, 2)
+#undef RNN_FUSED_BWD_PICK
+  if (!k) return 0;
+  return cluster_capacity_of((const void*)k, sh);
+}
+
 }  // namespace rnn

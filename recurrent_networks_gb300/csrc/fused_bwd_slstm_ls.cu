@@ -3,4 +3,5 @@
 
 namespace rnn {
 template cudaError_t fused_bwd_launch<SLSTM_LS>(const FusedShape&, const FusedArgs&, cudaStream_t);
+template int fused_bwd_capacity<SLSTM_LS>(const FusedShape&);
 }  // namespace rnn

@@ -467,6 +467,23 @@ template <int FN>
 cudaError_t fused_fwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream_t st) {
   return fwd_launch<FN, false>(sh, a, st);
 }
+
+// Clusters of the forward cluster kernel of shape `sh` that the current device
+// holds at once (cudaOccupancyMaxActiveClusters), -1 if the device cannot be
+// asked. The planner's co-residency constraint.
+template <int FN>
+int fused_fwd_capacity(const FusedShape& sh) {
+  void (*k)(const CUtensorMap, FusedArgs) = nullptr;
+#define RNN_FUSED_PICK(NT_, KT_, AG_) \
+  if (sh.NT == NT_ && sh.KT == KT_ && sh.allg == AG_) k = fused_fwd_kernel<FN, NT_, KT_, AG_, false>;
+  RNN_FUSED_PICK(1, 4, false) RNN_FUSED_PICK(1, 6, false) RNN_FUSED_PICK(1, 8, false)
+  RNN_FUSED_PICK(1, 12, false) RNN_FUSED_PICK(1, 16, false)
+  RNN_FUSED_PICK(1, 2, true) RNN_FUSED_PICK(1, 3, true) RNN_FUSED_PICK(1, 4, true)
+  RNN_FUSED_PICK(2, 2, true) RNN_FUSED_PICK(2, 3, true) RNN_FUSED_PICK(2, 4, true)
+#undef RNN_FUSED_PICK
+  if (!k) return 0;
+  return cluster_capacity_of((const void*)k, sh);
+}
 template <int FN>
 cudaError_t grid_fwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream_t st) {
   return fwd_launch<FN, true>(sh, a, st);

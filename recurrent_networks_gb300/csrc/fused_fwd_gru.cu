@@ -5,4 +5,5 @@
 namespace rnn {
 template cudaError_t fused_fwd_launch<GRU>(const FusedShape&, const FusedArgs&, cudaStream_t);
 template cudaError_t grid_fwd_launch<GRU>(const FusedShape&, const FusedArgs&, cudaStream_t);
+template int fused_fwd_capacity<GRU>(const FusedShape&);
 }  // namespace rnn

@@ -5,4 +5,5 @@
 namespace rnn {
 template cudaError_t fused_fwd_launch<LSTM>(const FusedShape&, const FusedArgs&, cudaStream_t);
 template cudaError_t grid_fwd_launch<LSTM>(const FusedShape&, const FusedArgs&, cudaStream_t);
+template int fused_fwd_capacity<LSTM>(const FusedShape&);
 }  // namespace rnn

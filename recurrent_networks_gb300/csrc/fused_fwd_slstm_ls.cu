@@ -5,4 +5,5 @@
 namespace rnn {
 template cudaError_t fused_fwd_launch<SLSTM_LS>(const FusedShape&, const FusedArgs&, cudaStream_t);
 template cudaError_t grid_fwd_launch<SLSTM_LS>(const FusedShape&, const FusedArgs&, cudaStream_t);
+template int fused_fwd_capacity<SLSTM_LS>(const FusedShape&);
 }  // namespace rnn

@@ -367,18 +367,9 @@ __global__ void colsum_kernel(const __nv_bfloat16* X, __nv_bfloat16* out, int ro
   }
 }
 
-int num_sms() {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
-  }
-  return sms;
-}
 
 // Tile width and split-K count of one GEMM, from a small cost model of the
-// persistent kernel on 152 SMs: the time is the number of waves of work units
+// persistent kernel on the device's SMs: the time is the number of waves of work units
 // times one unit's MMA cycles (128 x BN x 64 per k-chunk at about 2300 MACs
 // per cycle and SM; a 128-wide tile at 85% of a 256-wide one's rate), plus,
 // with split-K, the fp32 partials written and read back (8 bytes per output
@@ -387,7 +378,7 @@ struct Tiling {
   int BN, splits, kps;
 };
 Tiling choose_tiling(int M, int N, int K, bool split_ok) {
-  const int sms = 152, nchunk = (K + GM_BK - 1) / GM_BK;
+  const int sms = device_sms(), nchunk = (K + GM_BK - 1) / GM_BK;
   Tiling best{N >= 256 ? 256 : 128, 1, nchunk};
   double best_cost = 1e300;
   for (int BN = 256; BN >= 128; BN -= 128) {
@@ -455,7 +446,7 @@ cudaError_t gemm_run(bool a_kmajor, bool b_kmajor, int M, int N, int K, const vo
   g.partial = scratch;
   g.bias = (const __nv_bfloat16*)bias;
   g.status = status;
-  g.wait_limit_ns = 2000000000ull;
+  g.wait_limit_ns = wait_limit_ns();
   void (*k)(const CUtensorMap, const CUtensorMap, const CUtensorMap, GemmArgs);
   if (BN == 256)
     k = a_kmajor ? (b_kmajor ? gemm_umma_kernel<true, true, 256> : gemm_umma_kernel<true, false, 256>)
@@ -469,11 +460,11 @@ cudaError_t gemm_run(bool a_kmajor, bool b_kmajor, int M, int N, int K, const vo
   // persistent: one CTA per SM (the shared-memory ring and the two
   // accumulators take the whole SM), never more CTAs than work units
   const int units = tiles * g.splits;
-  const int ctas = units < num_sms() ? units : num_sms();
+  const int ctas = units < device_sms() ? units : device_sms();
   k<<<ctas, GM_THREADS, smem, st>>>(am, bm, cm, g);
   note_launch();
   if (g.splits > 1) {
-    gemm_reduce_kernel<<<2 * 152, 256, 0, st>>>(scratch, (__nv_bfloat16*)C, (size_t)M * N, g.splits);
+    gemm_reduce_kernel<<<2 * device_sms(), 256, 0, st>>>(scratch, (__nv_bfloat16*)C, (size_t)M * N, g.splits);
     note_launch();
   }
   return cudaGetLastError();

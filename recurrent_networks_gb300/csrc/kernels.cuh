@@ -11,6 +11,9 @@ namespace rnn {
 // Counts kernel launches for rnn_kernel_launches(); every launcher calls it.
 void note_launch(int count = 1);
 
+// The upper bound (ns) every device-side wait of the library's kernels uses.
+unsigned long long wait_limit_ns();
+
 // cudaFuncSetAttribute, called once per (device, kernel) for the largest
 // dynamic shared memory requested so far (and once for the non-portable
 // cluster size): the runtime call costs microseconds of host time that a
@@ -111,6 +114,15 @@ cudaError_t alt_fwd_run(int fn, const AltArgs& a, cudaStream_t st);
 cudaError_t alt_bwd_run(int fn, const AltArgs& a, cudaStream_t st);
 
 struct FusedShape;
+// Clusters of kernel `func` (the cluster kernel of shape `sh`) the current
+// device holds at once: sets the kernel's shared-memory and cluster-size
+// attributes and asks cudaOccupancyMaxActiveClusters. -1 when the device
+// cannot be asked (no device, or the query failed).
+int cluster_capacity_of(const void* func, const FusedShape& sh);
+// The same for the cluster kernels of one cell (the planner's callback).
+int fused_capacity(int fn, bool bwd, const FusedShape& sh);
+// SM count of the current device; the GB300's 152 when no device can be asked.
+int device_sms();
 cudaError_t fused_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st);
 cudaError_t grid_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st);
 cudaError_t grid_bwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st);

@@ -3,11 +3,12 @@
 //
 // The backward normally needs caller-provided workspace: a status word and,
 // for GRU (or when dWx is not requested), a buffer for the recurrent-branch
-// gradients that the weight-gradient pass reads. Here that scratch is a
-// file-scope __device__ array of fixed size instead. Every GPU that loads the
-// library holds the array until the process exits. Every call shares it, so
-// calls whose work overlaps on the GPU (two streams, or two threads) race on
-// it; calls on one stream run one after another and are safe.
+// gradients that the weight-gradient pass reads, plus optional split-K
+// partial sums. Here that scratch is a file-scope __device__ array of fixed
+// size instead. Every GPU that loads the library holds the array until the
+// process exits. Every call shares it, so calls whose work overlaps on the GPU
+// (two streams, or two threads) race on it; calls on one stream run one after
+// another and are safe.
 #include <mutex>
 
 #include "kernels.cuh"
@@ -16,8 +17,11 @@
 
 namespace rnn {
 
+bool dims_ok(const rnn_dims_t* d);  // api.cu: the argument bounds every entry point shares
+
 // [0, 256): device status word of the bounded waits; [256, ...): recurrent-
-// branch gradients [B][T][G][N][D] in the storage type.
+// branch gradients [B][T][G][N][D] in the storage type when needed, then
+// whatever is left serves as the weight gradient's split-K scratch.
 static __device__ __align__(256) unsigned char g_bwd_scratch[RNN_BWD_NOALLOC_SCRATCH_BYTES];
 
 namespace {
@@ -45,6 +49,7 @@ int scratch_address(void** out) {
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 }  // namespace rnn
@@ -55,18 +60,20 @@ extern "C" int rnn_bwd_noalloc(const rnn_dims_t* d, const void* Wx, const void* 
                                const void* states0, const void* states, const void* tape,
                                const void* dstates, const void* dlast, void* dWx, void* dR, void* db,
                                void* dstates0, void* stream) {
-  if (!d || d->B < 1 || d->T < 0 || d->N < 1 || d->D < 1 || d->function < 0 || d->function > 3 ||
-      (d->dtype != RNN_F32 && d->dtype != RNN_BF16) || d->path < 0 || d->path > 3)
-    return RNN_EINVAL;
+  if (!dims_ok(d)) return RNN_EINVAL;
   if (!R || !b || (d->T > 0 && (!Wx || !states || !tape))) return RNN_EINVAL;
   const void* ptrs[] = {Wx, R, b, states0, states, tape, dstates, dlast, dWx, dR, db, dstates0};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return RNN_EINVAL;
+  // the cluster and plain kernels need no scratch beyond dr; the grid and
+  // alternating paths need exchange buffers that this entry point does not hold
+  if (d->path == RNN_PATH_GRID || d->path == RNN_PATH_ALTERNATING) return RNN_EUNSUPPORTED;
   const int G = fn_gates(d->function), S = fn_states(d->function);
   const size_t e = d->dtype == RNN_BF16 ? 2 : 4;
   const size_t wx_elems = (size_t)d->B * d->T * G * d->N * d->D;
   const bool need_dr = d->function == RNN_GRU || !dWx;
-  const size_t need = kStatusBytes + (need_dr ? wx_elems * e : 0);
+  const size_t dr_bytes = need_dr ? align256(wx_elems * e) : 0;
+  const size_t need = kStatusBytes + dr_bytes;
   if (need > (size_t)RNN_BWD_NOALLOC_SCRATCH_BYTES) return RNN_ENOSPC;  // problem too large for the static scratch
 
   void* scratch = nullptr;
@@ -91,6 +98,14 @@ extern "C" int rnn_bwd_noalloc(const rnn_dims_t* d, const void* Wx, const void* 
   PlanRequest q{d->B, d->T, d->N, d->D, d->function, d->dtype, d->path, true};
   rc = plan_select(q, &plan);
   if (rc != RNN_OK) return rc;
+  if (plan.path == RNN_PATH_GRID || plan.path == RNN_PATH_ALTERNATING) {
+    // AUTO chose a path whose exchange buffers live in a workspace: the plain
+    // kernel computes the same backward with no scratch beyond dr
+    PlanRequest qs = q;
+    qs.path = RNN_PATH_SIMT;
+    rc = plan_select(qs, &plan);
+    if (rc != RNN_OK) return rc;
+  }
   void* drbuf = need_dr ? (void*)(base + kStatusBytes) : dWx;
   cudaError_t ce = cudaErrorInvalidValue;
   if (plan.path == RNN_PATH_SIMT) {
@@ -106,7 +121,7 @@ extern "C" int rnn_bwd_noalloc(const rnn_dims_t* d, const void* Wx, const void* 
     f.R = R; f.s0 = states0; f.tape = (float*)tape;
     f.dstates = dstates; f.dlast = dlast; f.dWx = dWx; f.dr = drbuf; f.ds0 = dstates0;
     f.status = (unsigned int*)base;
-    f.wait_limit_ns = 2000000000ull;
+    f.wait_limit_ns = wait_limit_ns();
     ce = fused_bwd_run(d->function, plan.fs, f, st);
   } else {
     return RNN_EUNSUPPORTED;
@@ -114,7 +129,31 @@ extern "C" int rnn_bwd_noalloc(const rnn_dims_t* d, const void* Wx, const void* 
   if (ce != cudaSuccess) return RNN_ECUDA;
   if (dR || db) {
     WgradArgs g{d->B, d->T, d->N, d->D, G, states, states0, drbuf, dR, db};
+    // the rest of the array holds the split-K partial sums when they fit;
+    // otherwise the weight-gradient pass runs without splitting K
+    const size_t used = kStatusBytes + dr_bytes;
+    g.scratch = (float*)(base + used);
+    g.scratch_bytes = (size_t)RNN_BWD_NOALLOC_SCRATCH_BYTES - used;
+    g.status = (unsigned int*)base;
+    g.wait_limit_ns = wait_limit_ns();
     if (wgrad_run(d->dtype, g, st) != cudaSuccess) return RNN_ECUDA;
+  }
+  return RNN_OK;
+}
+
+extern "C" int rnn_bwd_noalloc_status(void* stream) {
+  void* scratch = nullptr;
+  int rc = scratch_address(&scratch);
+  if (rc != RNN_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned int h = 0;
+  cudaError_t e = cudaMemcpyAsync(&h, scratch, sizeof(h), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return RNN_ECUDA;
+  if (h != STATUS_OK) {
+    e = cudaMemsetAsync(scratch, 0, sizeof(h), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    return e == cudaSuccess ? RNN_ETIMEOUT : RNN_ECUDA;
   }
   return RNN_OK;
 }

@@ -16,6 +16,20 @@ static int gates_of(int fn) { return fn == 0 ? 4 : fn == 1 ? 3 : fn == 2 ? 1 : 4
 static int states_of(int fn) { return fn == 0 ? 2 : fn == 1 ? 1 : fn == 2 ? 1 : 4; }
 
 static const int kClusterSizes[] = {1, 2, 3, 4, 6, 8, 12, 16};
+static const DeviceLimits kDefaultLimits;
+
+static const DeviceLimits& limits_of(const PlanRequest& q) { return q.lim ? *q.lim : kDefaultLimits; }
+
+// Waves of clusters the device runs the groups in: the co-resident cluster
+// count when the device reports it, else CTAs over SMs. Returns 0 when the
+// device cannot hold even one cluster of this shape (the point is infeasible).
+static int cluster_waves(const PlanRequest& q, const DeviceLimits& lim, const FusedShape& fs, int groups) {
+  int cap = lim.cluster_capacity ? lim.cluster_capacity(q.fn, q.bwd, fs) : -1;
+  if (cap == 0) return 0;
+  if (cap < 0) cap = lim.sms / fs.C;
+  if (cap < 1) return 0;
+  return (groups + cap - 1) / cap;
+}
 static const int kNT[] = {1, 2};
 // instantiated k-tiles per warp of the forward cluster kernel: a warp holds
 // all G gate tiles over a short K (allg) or one gate tile over a long K
@@ -65,8 +79,11 @@ bool fused_fwd_feasible(const PlanRequest& q, int C, int NT, int KT, bool allg, 
   if (pairs < 1) pairs = 1;
   double cyc = 900.0 + 10.0 * GW * KT * NT + 28.0 * KT / CH + 14.0 * G * KS * pairs + 250.0 * pairs +
                (C > 1 ? 600.0 : 0.0);
-  const int ctas = groups * C;
-  cyc *= (ctas + lim.sms - 1) / lim.sms;
+  FusedShape fs;
+  fs.C = C; fs.U = U; fs.NT = NT; fs.KT = KT; fs.KS = KS; fs.allg = allg; fs.warps = warps; fs.smem = L.total;
+  const int waves = cluster_waves(q, lim, fs, groups);
+  if (waves < 1) return false;
+  cyc *= waves;
   if (out) {
     *out = Plan{};
     out->path = RNN_PATH_FUSED;
@@ -94,7 +111,7 @@ static bool env_admits(const char* name, int v) {
 }
 
 static int fused_fwd_plan(const PlanRequest& q, Plan* best) {
-  DeviceLimits lim;
+  const DeviceLimits& lim = limits_of(q);
   int found = 0;
   for (int C : kClusterSizes)
     for (int ag = 0; ag < 2; ++ag)
@@ -152,8 +169,11 @@ bool fused_bwd_feasible(const PlanRequest& q, int C, int NT, int MT, const Devic
   if (pairs < 1) pairs = 1;
   const double mma = (double)MT * KTA * NT;
   double cyc = 900.0 + 18.0 * mma + (160.0 + 4.0 * C) * pairs + 25.0 * MT * NT + (C > 1 ? 150.0 : 0.0);
-  const int ctas = groups * C;
-  cyc *= (ctas + lim.sms - 1) / lim.sms;
+  FusedShape fs;
+  fs.C = C; fs.U = U; fs.NT = NT; fs.MT = MT; fs.KT = KTA; fs.warps = warps; fs.smem = L.total;
+  const int waves = cluster_waves(q, lim, fs, groups);
+  if (waves < 1) return false;
+  cyc *= waves;
   if (out) {
     *out = Plan{};
     out->path = RNN_PATH_FUSED;
@@ -172,7 +192,7 @@ bool fused_bwd_feasible(const PlanRequest& q, int C, int NT, int MT, const Devic
 }
 
 static int fused_bwd_plan(const PlanRequest& q, Plan* best) {
-  DeviceLimits lim;
+  const DeviceLimits& lim = limits_of(q);
   int found = 0;
   for (int C : kClusterSizes)
     for (int NT : kNT)
@@ -255,7 +275,7 @@ bool grid_feasible(const PlanRequest& q, int C, int NT, int KT, const DeviceLimi
 }
 
 static int grid_plan(const PlanRequest& q, Plan* best) {
-  DeviceLimits lim;
+  const DeviceLimits& lim = limits_of(q);
   int found = 0;
   const int* kts = q.bwd ? kGridBwdKT : kGridFwdKT;
   const int nkt = q.bwd ? 4 : 3;
@@ -361,10 +381,10 @@ void plan_describe(const Plan& p, int rc, char* buf, size_t len) {
   }
   const char* names[] = {"auto", "fused", "alternating", "simt", "grid"};
   snprintf(buf, len,
-           "path=%s C=%d U=%d NT=%d KT=%d KS=%d warps=%d groups=%d regs_R=%d smem=%zu scratch=%zu "
-           "model_ns=%.0f candidates=%d",
-           names[(p.path >= 0 && p.path <= 4) ? p.path : 0], p.fs.C, p.fs.U, p.fs.NT, p.fs.KT, p.fs.KS, p.fs.warps, p.groups, p.regs_R,
-           p.fs.smem, p.scratch_bytes, p.model_ns, p.candidates);
+           "path=%s C=%d U=%d NT=%d KT=%d KS=%d MT=%d allg=%d warps=%d groups=%d regs_R=%d smem=%zu "
+           "scratch=%zu model_ns=%.1f candidates=%d",
+           names[(p.path >= 0 && p.path <= 4) ? p.path : 0], p.fs.C, p.fs.U, p.fs.NT, p.fs.KT, p.fs.KS, p.fs.MT,
+           (int)p.fs.allg, p.fs.warps, p.groups, p.regs_R, p.fs.smem, p.scratch_bytes, p.model_ns, p.candidates);
 }
 
 }  // namespace rnn

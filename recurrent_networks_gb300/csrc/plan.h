@@ -9,18 +9,26 @@
 
 namespace rnn {
 
-struct PlanRequest {
-  int B, T, N, D, fn, dtype, path;
-  bool bwd;
-};
-
-// Limits of one GB300 SM / GPU that the constraints use.
+// Limits of the GPU that the constraints use. The defaults are a GB300's
+// (152 SMs, 227 KB of opt-in shared memory per CTA, clusters of up to 16 CTAs
+// with the non-portable size); the library fills them from the current device.
 struct DeviceLimits {
   int sms = 152;
   int max_cluster = 16;       // non-portable cluster size limit
   size_t smem_per_cta = 227 * 1024;
   int regs_per_thread = 255;  // launch bounds: 256 threads, 1 CTA per SM
   int max_warps = 8;
+  // Clusters of the cluster kernel for (fn, backward, shape) that the device
+  // can hold at once (cudaOccupancyMaxActiveClusters), or -1 when unknown (no
+  // device to ask). 0 makes the candidate infeasible; a positive count sets the
+  // number of waves the model charges. nullptr: not asked.
+  int (*cluster_capacity)(int fn, bool bwd, const FusedShape& fs) = nullptr;
+};
+
+struct PlanRequest {
+  int B, T, N, D, fn, dtype, path;
+  bool bwd;
+  const DeviceLimits* lim = nullptr;  // nullptr: the GB300 defaults above
 };
 
 struct Plan {
@@ -38,6 +46,8 @@ struct Plan {
 // (exposed for tests): returns true and fills *out when every constraint holds.
 bool fused_fwd_feasible(const PlanRequest& q, int C, int NT, int KT, bool allg, const DeviceLimits& lim,
                         Plan* out);
+bool fused_bwd_feasible(const PlanRequest& q, int C, int NT, int MT, const DeviceLimits& lim, Plan* out);
+bool grid_feasible(const PlanRequest& q, int C, int NT, int KT, const DeviceLimits& lim, Plan* out);
 
 // Alternating path (csrc/alt.cu): whether the unit tiles divide D, and the
 // workspace its ping-pong and carried-state buffers take.

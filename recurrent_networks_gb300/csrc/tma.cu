@@ -104,6 +104,22 @@ cudaError_t fused_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cuda
 }
 
 template <int FN>
+int fused_fwd_capacity(const FusedShape&);
+template <int FN>
+int fused_bwd_capacity(const FusedShape&);
+
+int fused_capacity(int fn, bool bwd, const FusedShape& sh) {
+  switch (fn) {
+    case LSTM: return bwd ? fused_bwd_capacity<LSTM>(sh) : fused_fwd_capacity<LSTM>(sh);
+    case GRU: return bwd ? fused_bwd_capacity<GRU>(sh) : fused_fwd_capacity<GRU>(sh);
+    case ELMAN: return bwd ? fused_bwd_capacity<ELMAN>(sh) : fused_fwd_capacity<ELMAN>(sh);
+    case SLSTM: return bwd ? fused_bwd_capacity<SLSTM>(sh) : fused_fwd_capacity<SLSTM>(sh);
+    case SLSTM_LS: return bwd ? fused_bwd_capacity<SLSTM_LS>(sh) : fused_fwd_capacity<SLSTM_LS>(sh);
+  }
+  return 0;
+}
+
+template <int FN>
 cudaError_t grid_fwd_launch(const FusedShape&, const FusedArgs&, cudaStream_t);
 template <int FN>
 cudaError_t grid_bwd_launch(const FusedShape&, const FusedArgs&, cudaStream_t);

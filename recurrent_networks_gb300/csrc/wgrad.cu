@@ -282,7 +282,7 @@ __global__ void wgrad_reduce_kernel(WgradArgs a, int splits) {
 static int wgrad_splits(int B, int T, int N, int D, int G) {
   const int tiles = ((D + WM_BN - 1) / WM_BN) * ((D + WM_BM - 1) / WM_BM) * G * N;
   const int K = B * T;
-  int splits = (2 * 152 + tiles - 1) / tiles;  // aim at two CTAs per SM
+  int splits = (2 * device_sms() + tiles - 1) / tiles;  // aim at two CTAs per SM
   const int max_by_k = (K + 255) / 256;           // keep >= 256 rows of K per split
   if (splits > max_by_k) splits = max_by_k;
   if (splits > 32) splits = 32;
@@ -324,7 +324,7 @@ cudaError_t wgrad_run(int dtype, const WgradArgs& a, cudaStream_t st) {
     const cudaError_t e = wgrad_umma_run(a, su, st);
     if (e == cudaSuccess) {
       if (su > 1) {
-        wgrad_reduce_kernel<<<2 * 152, 256, 0, st>>>(a, su);
+        wgrad_reduce_kernel<<<2 * device_sms(), 256, 0, st>>>(a, su);
         note_launch();
       }
       return bgrad_launch(a, st);
@@ -347,7 +347,7 @@ cudaError_t wgrad_run(int dtype, const WgradArgs& a, cudaStream_t st) {
   wgrad_mma_kernel<<<grid, 256, smem, st>>>(a, splits, kchunk);
   note_launch();
   if (splits > 1) {
-    wgrad_reduce_kernel<<<2 * 152, 256, 0, st>>>(a, splits);
+    wgrad_reduce_kernel<<<2 * device_sms(), 256, 0, st>>>(a, splits);
     note_launch();
   }
   return bgrad_launch(a, st);

@@ -205,7 +205,7 @@ bool wgrad_umma_supported(const WgradArgs& a) { return a.dR && a.D % 8 == 0 && a
 int wgrad_umma_splits(int B, int T, int N, int D, int G) {
   const int tiles = ((D + UM_TILE - 1) / UM_TILE) * ((D + UM_TILE - 1) / UM_TILE) * G * N;
   const int Q = B * ((T + UM_BK - 1) / UM_BK) + (B + UM_BK - 1) / UM_BK;
-  int splits = (152 + tiles - 1) / tiles;  // about one wave of 152 SMs
+  int splits = (device_sms() + tiles - 1) / tiles;  // about one wave of the SMs
   if (splits > Q / 4) splits = Q / 4;      // keep at least 4 k-tiles per split
   if (splits > 32) splits = 32;
   return splits < 1 ? 1 : splits;
