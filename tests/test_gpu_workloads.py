@@ -48,10 +48,12 @@ def test_workload_full_size(case):
     nt = _cores()
     ref_st, ref_last = oracle.fwd(fn, host["Wx"], host["R"], host["b"], host["states0"], nthreads=nt)
     # the bf16-operand states calibrate the long-sequence bounds of sLSTM's c, n, m
+    # (and h past the 1024 steps the stated bound covers)
     cal_st, cal_last = (oracle.fwd(fn, host["Wx"], host["R"], host["b"], host["states0"], nthreads=nt,
-                                   round_bf16=True) if (bf16 and fn.startswith("slstm")) else (None, None))
+                                   round_bf16=True) if (bf16 and (fn.startswith("slstm") or T > 1024))
+                        else (None, None))
     check_states(fn, w["dtype"], st, ref_st, calib=cal_st)
-    check_states(fn, w["dtype"], last, ref_last, "last", calib=cal_last)
+    check_states(fn, w["dtype"], last, ref_last, "last", calib=cal_last, t0=T - 1)
     del ref_st, cal_st
     if not w["backward"]:
         return
