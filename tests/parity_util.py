@@ -22,8 +22,12 @@ Tolerances (stated once, used by every parity test):
                 gradients: the bounds above widen to 1.5x the oracle's own
                 distance between its bf16-operand and plain-fp64 results when
                 that is larger, but never past the ceilings CEIL: c, n, m
-                within 0.25 * max(1, |ref|); gradients L2 <= 8e-2 and cosine
-                >= 0.995.
+                within 0.75 * max(1, |ref|); gradients L2 <= 8e-2 and cosine
+                >= 0.995. (sLSTM's c, n and m integrate: m sums log f along
+                runs of forget-branch steps and c, n scale with exp(-m), so
+                over 2048 steps the oracle's own bf16-operand c, n, m move
+                32%, 24% and 46% of max(1, |x|) from its plain ones, while h
+                and c/n, which the stabiliser does not change, stay close.)
   sLSTM element-wise bound away from stabiliser ties. The derivative of the
                 stabiliser max(log f + m, a_i) jumps where the two branches
                 tie; bf16 rounding of h and fp32 summation order move
@@ -55,7 +59,7 @@ TOL = {
     torch.bfloat16: dict(h=3e-2, states=3e-2, states_rel=True, grad=2e-2, cos=0.9995),
 }
 # fixed ceilings of the calibrated (widened) bf16 bounds
-CEIL = dict(states=0.25, h=0.1, grad_l2=8e-2, cos=0.995)
+CEIL = dict(states=0.75, h=0.1, grad_l2=8e-2, cos=0.995)
 # steps over which the stated bf16 bound on h holds as stated
 H_STATED_STEPS = 1024
 # |log f + m_{t-1} - a_i| below which an sLSTM step counts as a near-tie
