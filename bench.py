@@ -54,6 +54,9 @@ def parse():
                          "on the workload's B*T rows instead of the scan")
     ap.add_argument("--proj-shape", default=None, metavar="ROWS,I,C",
                     help="with --input-proj: time this projection shape instead of the workload's")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="run the workload with this T instead of its own (profiling captures of a smaller "
+                         "case); the line's workload name records it")
     ap.add_argument("--no-target-config", action="store_true",
                     help="skip the per-step roofline fractions of the LSTM fp32 B=2 T=16 D=32 workload")
     ap.add_argument("--trace", action="store_true",
@@ -378,7 +381,9 @@ def run_reference(args, w, fn):
 def main():
     args = parse()
     from recurrent_networks_gb300.synth import WORKLOADS
-    w = WORKLOADS[args.workload]
+    w = dict(WORKLOADS[args.workload])
+    if args.seq_len:
+        w.update(T=args.seq_len, name=f"{w['name']}_seq{args.seq_len}")
     fn = args.function or w["fns"][0]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -408,6 +413,9 @@ def main():
     B, T, N, D = w["B"], w["T"], w["N"], w["D"]
     backward = w["backward"]
     host = workload_inputs(args.workload, function=fn, with_grads=backward)
+    if args.seq_len:  # a time prefix of the workload's inputs
+        host = {k: (None if v is None else v[:, :T].contiguous() if k == "Wx" else
+                    v[:, :, :T].contiguous() if k == "dstates" else v) for k, v in host.items()}
     inp = {k: (v.to(dev) if v is not None else None) for k, v in host.items()}
     S = _lib.rnn_num_states(fn)
     dims = _lib.make_dims(B, T, N, D, fn, dtype, args.path)
