@@ -580,6 +580,23 @@ def main():
             "cycles_per_step": cyc, "ns_per_step": fl_ns, "status": st_fl,
             "fwd_step_over_floor": (f_ms * 1e6 / T) / fl_ns if fl_ns > 0 else None}
 
+    if plan_f.startswith("path=grid"):
+        pf = dict(kv.split("=") for kv in plan_f.split()[1:] if "=" in kv)
+        C, NT, groups = int(pf["C"]), int(pf["NT"]), int(pf["groups"])
+        rows = min(B, 8 * NT)
+        scratch = torch.empty(2 * groups * rows * D * 2 + 4096, dtype=torch.uint8, device=dev)
+        fl = torch.zeros(2, dtype=torch.int64, device=dev)
+        _lib.rnn_exchange_floor_grid(C, groups, rows, D, 2000, scratch, fl)
+        torch.cuda.synchronize()
+        cyc, st_fl = (int(x) for x in fl.cpu().tolist())
+        mhz = result["clocks"].get("sm_mhz") or 2070.0
+        fl_ns = cyc / mhz * 1e3
+        result["latency_floor"] = {
+            "what": f"h exchange alone through L2: {groups} groups of {C} CTAs, {rows} rows of {D} bf16 pulled per "
+                    f"step after a release/acquire step counter",
+            "cycles_per_step": cyc, "ns_per_step": fl_ns, "status": st_fl,
+            "fwd_step_over_floor": (f_ms * 1e6 / T) / fl_ns if fl_ns > 0 else None}
+
     # ---- the configuration the per-step roofline target is stated on (LSTM fp32
     # B=2 T=16 N=1 D=32), measured in this run after the main measurement
     if not args.no_target_config and args.workload != 1:

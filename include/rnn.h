@@ -273,6 +273,23 @@ int rnn_input_proj_bwd(int BT, int I, int C, const void *x, const void *W, const
  * or RNN_ECUDA. */
 int rnn_exchange_floor(int C, int slice_bytes, int steps, void *out, void *stream);
 
+/* Latency floor of the grid kernels' exchange through L2 (a measurement aid).
+ * Runs `groups` groups of C CTAs (a cooperative launch, one CTA per SM) whose
+ * steps hold only the forward grid kernel's h exchange: each CTA stores its
+ * D / C units of h for `rows` batch rows (2-byte stores), one release increment
+ * of the group's step counter after a CTA barrier, then the next step's
+ * acquire wait on the counter (bounded, 2 s) and the pull of the group's rows
+ * from L2 with one bulk copy per row, for `steps` (2 .. 1e6) steps. C >= 1,
+ * groups >= 1, rows 1 .. 32, D 8 .. 4096 with D % 8 == 0 and D % C == 0.
+ * scratch: device memory owned by the caller, 256-byte aligned, of at least
+ * 2*groups*rows*D*2 bytes rounded up to 256, plus 256 + 4*groups bytes (the
+ * exchange buffers and counters). Writes to out[0] the clock64 cycles per step
+ * seen by CTA 0 and to out[1] the status (0 = ok, 1 = a wait ran out).
+ * Asynchronous on `stream`. Returns RNN_OK, RNN_EINVAL, RNN_ENOSPC,
+ * RNN_EUNSUPPORTED (the CTAs cannot all be resident) or RNN_ECUDA. */
+int rnn_exchange_floor_grid(int C, int groups, int rows, int D, int steps, void *scratch, size_t scratch_bytes,
+                            void *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

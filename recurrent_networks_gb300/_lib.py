@@ -68,6 +68,7 @@ def load(path: str | None = None):
             lib.rnn_trace.argtypes = [vp, i, i]
             lib.rnn_debug_inject_wait.argtypes = [i, ctypes.c_ulonglong]
             lib.rnn_exchange_floor.argtypes = [i, i, i, vp, vp]
+            lib.rnn_exchange_floor_grid.argtypes = [i, i, i, i, i, vp, sz, vp, vp]
             lib.rnn_input_proj_workspace_size.argtypes = [i, i, i]
             lib.rnn_input_proj_workspace_size.restype = sz
             lib.rnn_input_proj_fwd.argtypes = [i, i, i] + [vp] * 5 + [sz, vp]
@@ -200,6 +201,16 @@ def rnn_exchange_floor(C: int, slice_bytes: int, steps: int, out, stream=None) -
     tensor of >= 2 int64: cycles per step of CTA 0, then the status."""
     return _check(load().rnn_exchange_floor(int(C), int(slice_bytes), int(steps), _p(out), _stream(stream)),
                   "rnn_exchange_floor")
+
+
+def rnn_exchange_floor_grid(C: int, groups: int, rows: int, D: int, steps: int, scratch, out, stream=None) -> int:
+    """Runs the grid kernels' L2 exchange alone (groups x C CTAs, `rows` batch
+    rows of D units) for `steps` steps; `scratch` is a device uint8 tensor for
+    the exchange buffers and counters, `out` >= 2 int64: cycles per step of
+    CTA 0, then the status."""
+    return _check(load().rnn_exchange_floor_grid(int(C), int(groups), int(rows), int(D), int(steps), _p(scratch),
+                                                 scratch.numel() * scratch.element_size(), _p(out), _stream(stream)),
+                  "rnn_exchange_floor_grid")
 
 
 def rnn_input_proj_workspace_size(BT: int, I: int, C: int) -> int:

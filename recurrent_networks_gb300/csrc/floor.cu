@@ -72,11 +72,110 @@ __global__ void __launch_bounds__(256, 1) exchange_floor_kernel(int slice_bytes,
   if (rank == 0 && tid == 0) out[0] = (unsigned long long)((t1 - t0) / steps);
 }
 
+// Latency floor of the grid kernels' L2 exchange: the forward grid kernel's
+// steps with the product and the cell taken out. C CTAs per group, `groups`
+// groups, one CTA per SM (cooperative launch). Each step t > 0: one thread
+// waits until the group's step counter reaches C t (acquire), fences the
+// proxies and pulls the group's `rows` rows of h_{t-1} (D bf16 each) from L2
+// with one bulk copy per row; every thread waits for the bytes. Then every
+// CTA stores its U = D / C units of h_t for each row (2-byte stores, as the
+// cell does), a CTA barrier, and one release increment of the counter.
+__global__ void __launch_bounds__(256, 1) grid_floor_kernel(int C, int D, int rows, int steps, unsigned short* hx,
+                                                          unsigned int* counters, unsigned long long* out) {
+  extern __shared__ __align__(128) unsigned char gf_smem[];
+  const int U = D / C, grp = blockIdx.x / C, r = blockIdx.x % C, groups = gridDim.x / C;
+  const int tid = threadIdx.x;
+  uint64_t* bar = (uint64_t*)gf_smem;
+  unsigned short* hbuf = (unsigned short*)(gf_smem + 128);  // [rows][D + 8]
+  unsigned int* status = (unsigned int*)(out + 1);
+  const unsigned long long limit = 2000000000ull;
+  const uint32_t bar0 = smem_u32(bar);
+  if (tid == 0) {
+    mbar_init(bar0, 1);
+    fence_mbar_init_cluster();
+  }
+  __syncthreads();
+  bool failed = false;
+  uint32_t ph = 0;
+  unsigned x = 0;
+  const long long t0 = clock64();
+  for (int t = 0; t < steps; ++t) {
+    const int p = t & 1;
+    if (t > 0) {
+      if (tid == 0) {
+        counter_wait_bounded(counters + grp, (unsigned)(C * t), limit, status, failed);
+        if (!failed) {
+          const unsigned short* src = hx + ((size_t)(p * groups + grp) * rows) * D;
+          fence_proxy_async_global();
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(bar0, (uint32_t)(rows * D * 2));
+          for (int b = 0; b < rows; ++b)
+            bulk_load_global(smem_u32(hbuf + b * (D + 8)), src + (size_t)b * D, (uint32_t)(D * 2), bar0);
+        }
+      }
+      mbar_wait_bounded<false>(bar0, ph, limit, status, failed);
+      ph ^= 1u;
+      x += hbuf[tid % (rows * (D + 8))];  // the pulled row is read, as the product reads it
+    }
+    if (t + 1 < steps) {
+      unsigned short* dst = hx + ((size_t)((p ^ 1) * groups + grp) * rows) * D;
+      for (int e = tid; e < rows * U; e += blockDim.x) {
+        const int b = e / U, u = e - b * U;
+        dst[(size_t)b * D + r * U + u] = (unsigned short)(t + x);
+      }
+    }
+    __syncthreads();
+    if (t + 1 < steps && tid == 0) counter_publish(counters + grp);
+  }
+  const long long t1 = clock64();
+  if (blockIdx.x == 0 && tid == 0) out[0] = (unsigned long long)((t1 - t0) / steps) + (x == 0xffffffffu);
+}
+
 }  // namespace
 
 }  // namespace rnn
 
 using namespace rnn;
+
+extern "C" int rnn_exchange_floor_grid(int C, int groups, int rows, int D, int steps, void* scratch,
+                                       size_t scratch_bytes, void* out, void* stream) {
+  if (C < 1 || groups < 1 || rows < 1 || rows > 32 || D < 8 || D > 4096 || D % 8 || D % C || steps < 2 ||
+      steps > 1000000 || !scratch || ((uintptr_t)scratch & 255u) || !out || ((uintptr_t)out & 7u))
+    return RNN_EINVAL;
+  const size_t hx_bytes = ((size_t)2 * groups * rows * D * 2 + 255) & ~(size_t)255;
+  if (scratch_bytes < hx_bytes + 256 + (size_t)groups * 4) return RNN_ENOSPC;
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned short* hx = (unsigned short*)scratch;
+  unsigned int* counters = (unsigned int*)((char*)scratch + hx_bytes);
+  // at least as much shared memory as the forward grid kernel, so one CTA runs per SM
+  size_t smem = 128 + (size_t)rows * (D + 8) * 2;
+  if (smem < 100 * 1024) smem = 100 * 1024;
+  cudaError_t e = cudaMemsetAsync(out, 0, 16, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(counters, 0, (size_t)groups * 4, st);
+  if (e == cudaSuccess) e = set_smem_attr((const void*)grid_floor_kernel, smem);
+  int per_sm = 0;
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, grid_floor_kernel, 256, smem);
+  if (e == cudaSuccess && per_sm * device_sms() < groups * C) return RNN_EUNSUPPORTED;
+  if (e == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(groups * C);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, grid_floor_kernel, C, D, rows, steps, hx, counters, (unsigned long long*)out);
+    note_launch();
+  }
+  if (e != cudaSuccess) {
+    fprintf(stderr, "librnn_gb300: CUDA error: %s\n", cudaGetErrorString(e));
+    return RNN_ECUDA;
+  }
+  return RNN_OK;
+}
 
 extern "C" int rnn_exchange_floor(int C, int slice_bytes, int steps, void* out, void* stream) {
   if (C < 1 || C > 16 || slice_bytes < 16 || slice_bytes > 4096 || slice_bytes % 16 || steps < 2 ||

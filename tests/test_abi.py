@@ -101,3 +101,15 @@ def test_projection_sizes_and_host_validation():
     assert lib.rnn_input_proj_fwd(8192, 768, 3072, 16, 16, None, 16, 256, 256, None) == _lib.RNN_ENOSPC
     assert lib.rnn_input_proj_bwd(8, 64, 128, 16, 16, 16, 24, None, None, 256, ws, None) == _lib.RNN_EINVAL
     assert lib.rnn_input_proj_bwd(8192, 768, 3072, 16, 16, 16, 16, 16, 16, 256, 256, None) == _lib.RNN_ENOSPC
+
+
+def test_grid_exchange_floor_validates_on_host():
+    lib = _lib.load()
+    out = ctypes.c_void_p(4096)
+    scratch = ctypes.c_void_p(1 << 20)
+    # D not a multiple of C, too many rows, a misaligned scratch, a short scratch
+    assert lib.rnn_exchange_floor_grid(3, 1, 8, 256, 10, scratch, 1 << 20, out, None) == _lib.RNN_EINVAL
+    assert lib.rnn_exchange_floor_grid(16, 1, 33, 256, 10, scratch, 1 << 20, out, None) == _lib.RNN_EINVAL
+    assert lib.rnn_exchange_floor_grid(16, 1, 8, 256, 10, ctypes.c_void_p((1 << 20) + 16), 1 << 20, out,
+                                       None) == _lib.RNN_EINVAL
+    assert lib.rnn_exchange_floor_grid(16, 1, 8, 256, 10, scratch, 1024, out, None) == _lib.RNN_ENOSPC

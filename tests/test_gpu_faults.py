@@ -67,3 +67,20 @@ def test_exchange_floor_runs_and_reports():
     assert cyc[16] > cyc[2], cyc
     with pytest.raises(_lib.RnnError):
         _lib.rnn_exchange_floor(17, 384, 500, out)
+
+
+def test_grid_exchange_floor_runs_and_reports():
+    """The grid kernels' L2 exchange alone completes with status 0; two groups
+    of 64 CTAs pulling 16 rows of 1024 units take longer per step than one
+    group of 16 CTAs pulling 8 rows of 256."""
+    out = torch.zeros(2, dtype=torch.int64, device="cuda")
+    scratch = torch.empty(2 * 2 * 16 * 1024 * 2 + 4096, dtype=torch.uint8, device="cuda")
+    cyc = {}
+    for C, groups, rows, D in ((16, 1, 8, 256), (64, 2, 16, 1024)):
+        _lib.rnn_exchange_floor_grid(C, groups, rows, D, 500, scratch, out)
+        torch.cuda.synchronize()
+        v = out.cpu().tolist()
+        assert v[1] == 0, v
+        assert 100 < v[0] < 1_000_000, v
+        cyc[D] = v[0]
+    assert cyc[1024] > cyc[256], cyc
