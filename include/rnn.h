@@ -210,7 +210,8 @@ unsigned long long rnn_kernel_launches(void);
  * thread-safe. Returns RNN_OK or RNN_EINVAL. */
 int rnn_profile_events(int which, void *before, void *after);
 
-/* Diagnostic phase trace of the persistent kernels (cluster and grid paths).
+/* Diagnostic phase trace of the persistent kernels (cluster and grid paths)
+ * and of the plain kernels.
  * Registers a device buffer of 8 * steps unsigned 64-bit words, or NULL to
  * stop. Kernels launched afterwards have CTA 0, thread 0 write clock64() at
  * eight phase points of the steps [t0, t0 + steps) of their processing order
@@ -221,8 +222,12 @@ int rnn_profile_events(int which, void *before, void *after);
  * staged, 3 cell derivative done, 4 after the CTA barrier, 5 partial products
  * computed, 6 partials sent. Grid backward phases: 0 step start, 1 step
  * counter reached, 2 dr gathered, 3 dh reduced, 4 tape staged, 5 cell
- * derivative done, 6 published. Process-global, not thread-safe; returns
- * RNN_OK or RNN_EINVAL. */
+ * derivative done, 6 published. Plain forward: 0 step start, 1 products
+ * written, 2 after the CTA barrier, 5 cell inputs loaded, 6 cell done, 3
+ * outputs stored, 4 after the CTA barrier. Plain backward: 0 step start, 1
+ * cell derivative done, 2 after the CTA barrier, 3 products written, 4 after
+ * the CTA barrier. Process-global, not thread-safe; returns RNN_OK or
+ * RNN_EINVAL. */
 int rnn_trace(void *buf, int t0, int steps);
 
 /* Fault injection for tests of the device-side time-out path. With step >= 0,

@@ -301,6 +301,7 @@ static int run_forward(const rnn_dims_t* d, const Plan& plan, const void* Wx, co
   a.B = d->B; a.T = d->T; a.N = d->N; a.D = d->D;
   a.Wx = Wx; a.R = R; a.bias = b; a.s0 = s0;
   a.states = states; a.last = last; a.tape = tape;
+  a.trace = g_trace_buf; a.trace_t0 = g_trace_t0; a.trace_steps = g_trace_steps;
   int rc = RNN_EUNSUPPORTED;
   prof_mark(0, 0, st);
   switch (plan.path) {
@@ -447,6 +448,7 @@ int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
   SimtArgs a{};
   a.B = d->B; a.T = d->T; a.N = d->N; a.D = d->D;
   a.R = R; a.s0 = states0; a.tape = (float*)tp;
+  a.trace = g_trace_buf; a.trace_t0 = g_trace_t0; a.trace_steps = g_trace_steps;
   // the recurrent-branch gradient equals dWx except for the GRU candidate gate:
   // reuse dWx as the weight-gradient operand when it is there
   void* drbuf = (d->function != RNN_GRU && dWx) ? dWx : (void*)(ws + w.dr);
@@ -455,6 +457,11 @@ int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
   prof_mark(1, 0, st);
   switch (plan.path) {
     case RNN_PATH_SIMT:
+      if ((dR || db) && simt_fuses_wgrad(d->function, d->B, d->T, d->D)) {
+        a.fuse_wgrad = 1;  // dR and db from the backward kernel itself
+        a.dR = dR;
+        a.db = db;
+      }
       rc = cuda_status(simt_run(d->function, d->dtype, a, true, st));
       break;
     case RNN_PATH_FUSED: {
@@ -495,7 +502,7 @@ int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
   }
   prof_mark(1, 1, st);
   if (rc) return rc;
-  if (dR || db) {
+  if ((dR || db) && !a.fuse_wgrad) {
     WgradArgs g{d->B, d->T, d->N, d->D, z.G, states, states0, drbuf, dR, db};
     g.scratch = (float*)(ws + w.wg);
     g.scratch_bytes = w.tape - w.wg;

@@ -37,9 +37,21 @@ struct SimtArgs {
   void* dWx;
   void* dr;  // bwd: recurrent-branch gradients [B,T,G,N,D] (storage type)
   void* ds0;
+  // bwd: dR and db computed by the backward kernel itself (simt_fuses_wgrad)
+  int fuse_wgrad = 0;
+  void* dR = nullptr;
+  void* db = nullptr;
+  // optional phase trace (rnn_trace): CTA 0, thread 0 writes clock64() at the
+  // phase points of steps [trace_t0, trace_t0 + trace_steps) (processing order)
+  unsigned long long* trace = nullptr;
+  int trace_t0 = 0, trace_steps = 0;
 };
 
 int simt_supported(int fn, int B, int D, bool bwd);
+// Whether the plain backward computes dR and db itself: one CTA holds every
+// batch row of a head, the problem is small (G D^2 B T <= 2^21) and the
+// steps' recurrent-branch gradients and h_{t-1} fit in shared memory.
+bool simt_fuses_wgrad(int fn, int B, int T, int D);
 cudaError_t simt_run(int fn, int dtype, const SimtArgs& a, bool bwd, cudaStream_t st);
 
 // dR[g,n,i,j] = sum_{b,t} hprev[b,t,n,i] dr[b,t,g,n,j];  db[g,n,j] = sum_{b,t} dr[b,t,g,n,j]
