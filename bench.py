@@ -120,10 +120,13 @@ def proj_bench(args, w, fn, dev, _lib):
 
 def phase_trace(step_fn, backward, T):
     """Median clock64 cycles between the phase points of the persistent
-    kernels (CTA 0, thread 0), over up to 200 steps after the first 10."""
+    kernels (CTA 0, thread 0), over up to 200 steps after the first 10.
+    Points 8-11 of the forward kernels lie inside phases: 8 the cell's inputs
+    summed, 9 the cell computed, 10 h staged or stored, 11 the states and tape
+    stores issued."""
     from recurrent_networks_gb300 import _lib
     steps = max(1, min(200, T - 20))
-    buf = torch.zeros(8 * steps, dtype=torch.int64, device="cuda")
+    buf = torch.zeros(16 * steps, dtype=torch.int64, device="cuda")
     out = {}
     for which in (("fwd", "bwd") if backward else ("fwd",)):
         buf.zero_()
@@ -131,12 +134,20 @@ def phase_trace(step_fn, backward, T):
         step_fn(which)
         torch.cuda.synchronize()
         _lib.rnn_trace(None)
-        tr = buf.view(steps, 8).cpu().tolist()
+        tr = buf.view(steps, 16).cpu().tolist()
         phases = {}
         for p in range(1, 8):
             d = [r[p] - r[p - 1] for r in tr if r[p] and r[p - 1]]
             if d:
                 phases[f"{p - 1}->{p}"] = statistics.median(d)
+        # the finer points inside a phase, each against the nearest earlier point
+        for p in range(8, 16):
+            prev = {8: 4, 9: 8, 10: 9, 11: 7}.get(p)
+            if prev is None:
+                continue
+            d = [r[p] - r[prev] for r in tr if r[p] and r[prev]]
+            if d:
+                phases[f"{prev}->{p}"] = statistics.median(d)
         per = [tr[i + 1][0] - tr[i][0] for i in range(steps - 1) if tr[i + 1][0] and tr[i][0]]
         out[which] = {"step_cycles": statistics.median(per) if per else None, "phase_cycles": phases}
     return out

@@ -184,8 +184,8 @@ def rnn_bwd_noalloc_status(stream=None) -> int:
 
 
 def rnn_trace(buf=None, t0: int = 0, steps: int = 0) -> int:
-    """Registers a device tensor of >= 8*steps int64 for the persistent kernels'
-    phase trace (clock64 at eight points of steps [t0, t0+steps)), or None."""
+    """Registers a device tensor of >= 16*steps int64 for the persistent kernels'
+    phase trace (clock64 at up to sixteen points of steps [t0, t0+steps)), or None."""
     return _check(load().rnn_trace(_p(buf), int(t0), int(steps)), "rnn_trace")
 
 

@@ -116,6 +116,27 @@ __global__ void __launch_bounds__(256, 1)
       bsr[k][g] = own ? __bfloat162float(bias[((size_t)g * N + n) * D + u0 + u]) : 0.0f;
   }
 
+  // per pair, fixed for the kernel: the offset of its K-split partial sums
+  // (k2 = 0, g = 0) in red, of its Wx in a ring stage, of its h in the grid's
+  // exchange buffer, and its states / tape output pointers at t = 0 (advanced
+  // by a fixed stride per step): no index arithmetic inside the time loop
+  const int red_sk = G * BC * FUSED_RED_STRIDE;  // red stride of the K slice k2
+  constexpr int RED_SG = BC * FUSED_RED_STRIDE;   // red stride of the gate g
+  const int groups = gridDim.x / C;
+  const size_t hx_par = (size_t)groups * BC * D;  // grid exchange buffer stride of the step parity
+  int red_off[FUSED_PPT], hx_off[FUSED_PPT];
+  __nv_bfloat16* st_ptr[FUSED_PPT];
+  float* tp_ptr[FUSED_PPT];
+  const size_t st_sstride = (size_t)B * TT * N * D, tp_tstride = (size_t)B * N * K * D;
+#pragma unroll
+  for (int k = 0; k < FUSED_PPT; ++k) {
+    const int b = pb[k], u = pu[k], bg = b0 + b, j = u0 + u;
+    red_off[k] = (((u >> 4) * KS * G) * BC + b) * FUSED_RED_STRIDE + (u & 15);
+    hx_off[k] = (grp * BC + b) * D + j;
+    st_ptr[k] = states ? states + ((size_t)bg * TT) * N * D + (size_t)n * D + j : nullptr;
+    tp_ptr[k] = a.tape ? a.tape + ((size_t)bg * N + n) * K * D + j : nullptr;
+  }
+
   // the first k-tile of this warp's K slice: source block and column group
   // (the grid variant's one block holds all D inputs)
   const int U16 = GRIDX ? D / 16 : U / 16;
@@ -177,7 +198,7 @@ __global__ void __launch_bounds__(256, 1)
   const bool tracer = a.trace && blockIdx.x == 0 && tid == 0;
 #define RNN_TRACE(k)                                                                    \
   if (tracer && t >= a.trace_t0 && t < a.trace_t0 + a.trace_steps)                      \
-    a.trace[(size_t)(t - a.trace_t0) * 8 + (k)] = (unsigned long long)clock64();
+    a.trace[(size_t)(t - a.trace_t0) * 16 + (k)] = (unsigned long long)clock64();
 
   // ---- time loop -------------------------------------------------------------
   for (int t = 0; t < TT; ++t) {
@@ -191,7 +212,7 @@ __global__ void __launch_bounds__(256, 1)
         if (tid == 0) {
           counter_wait_bounded(a.counters + grp, (unsigned)(C * t), a.wait_limit_ns, a.status, failed);
           if (!failed) {
-            const __nv_bfloat16* src = (const __nv_bfloat16*)a.hx + ((size_t)(p * (gridDim.x / C) + grp) * BC) * D;
+            const __nv_bfloat16* src = (const __nv_bfloat16*)a.hx + p * hx_par + (size_t)grp * BC * D;
             fence_proxy_async_global();  // the peers' stores, acquired above, before the bulk reads
             fence_proxy_async_smem();    // the last reads of this buffer (ordered by the barrier) before the writes
             mbar_arrive_expect_tx(full_bar0, (uint32_t)(nb * D * 2));
@@ -301,37 +322,39 @@ __global__ void __launch_bounds__(256, 1)
     for (int kp = 0; kp < FUSED_PPT; ++kp) {
       const int e = tid + kp * nthr;
       if (e >= nb * U) break;
-      const int b = pb[kp], u = pu[kp];
-      const int q = u >> 4, r = u & 15;
+      const int u = pu[kp];
       float x[G], rc[G], sn[S], pre[P];
       // all K-split partials are loaded before any is summed (independent loads)
       float part[G][FUSED_MAX_KS];
+      const float* rp = red + red_off[kp];
 #pragma unroll
-      for (int g = 0; g < G; ++g)
+      for (int k2 = 0; k2 < FUSED_MAX_KS; ++k2) {
 #pragma unroll
-        for (int k2 = 0; k2 < FUSED_MAX_KS; ++k2)
-          part[g][k2] = k2 < KS ? red[(((q * KS + k2) * G + g) * BC + b) * FUSED_RED_STRIDE + r] : 0.0f;
+        for (int g = 0; g < G; ++g) part[g][k2] = k2 < KS ? rp[g * RED_SG] : 0.0f;
+        rp += red_sk;
+      }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float v = bsr[kp][g];
 #pragma unroll
         for (int k2 = 0; k2 < FUSED_MAX_KS; ++k2) v += part[g][k2];
         rc[g] = v;
-        x[g] = __bfloat162float(wxt[(b * G + g) * U + u]);
+        x[g] = __bfloat162float(wxt[(pb[kp] * G + g) * U + u]);
       }
+      if (kp == 0) RNN_TRACE(8)
       cell_fwd<FN, true>(x, rc, csr[kp], sn, pre);
-      const int j = u0 + u;
+      if (kp == 0) RNN_TRACE(9)
 #pragma unroll
       for (int s = 0; s < S; ++s) csr[kp][s] = sn[s];
 #pragma unroll
       for (int k2 = 0; k2 < P; ++k2) prk[kp][k2] = pre[k2];
       if constexpr (GRIDX) {
         if (t + 1 < TT)
-          ((__nv_bfloat16*)a.hx)[((size_t)((p ^ 1) * (gridDim.x / C) + grp) * BC + b) * D + j] =
-              __float2bfloat16_rn(sn[0]);
+          ((__nv_bfloat16*)a.hx)[(size_t)hx_off[kp] + (p ^ 1) * hx_par] = __float2bfloat16_rn(sn[0]);
       } else {
-        stage[(p * BC + b) * UP + u] = __float2bfloat16_rn(sn[0]);
+        stage[(p * BC + pb[kp]) * UP + u] = __float2bfloat16_rn(sn[0]);
       }
+      if (kp == 0) RNN_TRACE(10)
     }
     RNN_TRACE(5)
     if constexpr (!GRIDX) fence_proxy_async_smem();  // the staged slice is read by bulk copies
@@ -359,20 +382,21 @@ __global__ void __launch_bounds__(256, 1)
     for (int kp = 0; kp < FUSED_PPT; ++kp) {
       const int e = tid + kp * nthr;
       if (e >= nb * U) break;
-      const int b = pb[kp], u = pu[kp], bg = b0 + b, j = u0 + u;
-      if (states) {
+      if (st_ptr[kp]) {
 #pragma unroll
-        for (int s = 0; s < S; ++s)
-          states[(((size_t)s * B + bg) * TT + t) * N * D + (size_t)n * D + j] = __float2bfloat16_rn(csr[kp][s]);
+        for (int s = 0; s < S; ++s) st_ptr[kp][s * st_sstride] = __float2bfloat16_rn(csr[kp][s]);
+        st_ptr[kp] += (size_t)N * D;
       }
-      if (a.tape) {
-        float* tp = a.tape + (((size_t)t * B + bg) * N + n) * K * D + j;
+      if (tp_ptr[kp]) {
+        float* tp = tp_ptr[kp];
 #pragma unroll
         for (int k2 = 0; k2 < P; ++k2) tp[k2 * D] = prk[kp][k2];
 #pragma unroll
         for (int s = 0; s < S; ++s) tp[(P + s) * D] = csr[kp][s];
+        tp_ptr[kp] += tp_tstride;
       }
     }
+    RNN_TRACE(11)
   }
 #undef RNN_TRACE
 

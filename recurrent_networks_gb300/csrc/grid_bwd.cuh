@@ -96,6 +96,13 @@ __global__ void __launch_bounds__(256, 1)
   // over the pairs e = b U + u
   const int c_b0 = tid / U, c_u0 = tid - c_b0 * U, c_db = nthr / U, c_du = nthr - c_db * U;
   uint32_t gath_par = 0u;
+  // the thread's first pair, fixed for the kernel: the offset of its K-split
+  // partial sums in red and of its gradients in dWx / dr at t = 0 (a step
+  // moves them by G N D): no index arithmetic in the time loop for it
+  const int red_off0 = ((c_u0 >> 4) * KS * BC + c_b0) * FUSED_RED_STRIDE + (c_u0 & 15);
+  const int red_sk = BC * FUSED_RED_STRIDE;
+  const size_t o_first = ((size_t)(b0 + c_b0) * TT * G) * N * D + (size_t)n * D + u0 + c_u0;
+  const size_t o_step = (size_t)G * N * D;
 
   auto issue_stage = [&](int k) {
     const int t = TT - 1 - k, s = k % FUSED_NS;
@@ -111,7 +118,7 @@ __global__ void __launch_bounds__(256, 1)
   const bool tracer = a.trace && blockIdx.x == 0 && tid == 0;
 #define RNN_TRACE(p)                                                                    \
   if (tracer && kk >= a.trace_t0 && kk < a.trace_t0 + a.trace_steps)                    \
-    a.trace[(size_t)(kk - a.trace_t0) * 8 + (p)] = (unsigned long long)clock64();
+    a.trace[(size_t)(kk - a.trace_t0) * 16 + (p)] = (unsigned long long)clock64();
   for (int kk = 0; kk <= TT; ++kk) {
     const int t = TT - 1 - kk;
     const bool have_rec = kk > 0;
@@ -206,7 +213,7 @@ __global__ void __launch_bounds__(256, 1)
     __nv_bfloat16* dxw = dx + ((size_t)(kk & 1) * groups + grp) * BC * KG;
     // pair e = b U + u, stepped without a division
     for (int e = tid, b = c_b0, u = c_u0; e < nb * U; e += nthr, b += c_db + (u + c_du >= U), u = u + c_du >= U ? u + c_du - U : u + c_du) {
-      const int q = u >> 4, r = u & 15;
+      const bool first = e == tid;
       float pre[P], sp[S], sn[S], dsn[S], dxg[G], dr[G], dsp[S];
 #pragma unroll
       for (int k2 = 0; k2 < P; ++k2) pre[k2] = tp[(b * K + k2) * U + u];
@@ -221,14 +228,15 @@ __global__ void __launch_bounds__(256, 1)
       }
       if (have_rec) {  // the K-split partials, loaded together
         float part[FUSED_MAX_KS];
+        const float* rp = red + (first ? red_off0 : (((u >> 4) * KS * BC + b) * FUSED_RED_STRIDE + (u & 15)));
 #pragma unroll
-        for (int k2 = 0; k2 < FUSED_MAX_KS; ++k2)
-          part[k2] = k2 < KS ? red[((size_t)(q * KS + k2) * BC + b) * FUSED_RED_STRIDE + r] : 0.0f;
+        for (int k2 = 0; k2 < FUSED_MAX_KS; ++k2) part[k2] = k2 < KS ? rp[k2 * red_sk] : 0.0f;
 #pragma unroll
         for (int k2 = 0; k2 < FUSED_MAX_KS; ++k2) dsn[0] += part[k2];
       }
       cell_bwd<FN, true>(pre, sp, sn, dsn, dxg, dr, dsp);
-      const size_t o = (((size_t)(b0 + b) * TT + t) * G) * N * D + (size_t)n * D + u0 + u;
+      const size_t o = first ? o_first + (size_t)t * o_step
+                             : (((size_t)(b0 + b) * TT + t) * G) * N * D + (size_t)n * D + u0 + u;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         if (dWx) dWx[o + (size_t)g * N * D] = __float2bfloat16_rn(dxg[g]);

@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(256) simt_fwd_kernel(SimtArgs a) {
   const bool tracer = a.trace && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0;
 #define RNN_TRACE(k)                                                               \
   if (tracer && t >= a.trace_t0 && t < a.trace_t0 + a.trace_steps)                 \
-    a.trace[(size_t)(t - a.trace_t0) * 8 + (k)] = (unsigned long long)clock64();
+    a.trace[(size_t)(t - a.trace_t0) * 16 + (k)] = (unsigned long long)clock64();
   for (int t = 0; t < TT; ++t) {
     RNN_TRACE(0)
     const float* hin = hop + (t & 1) * BS * D;
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(256) simt_bwd_kernel(SimtArgs a) {
   const bool tracer = a.trace && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0;
 #define RNN_TRACE(k)                                                                   \
   if (tracer && TT - 1 - t >= a.trace_t0 && TT - 1 - t < a.trace_t0 + a.trace_steps)    \
-    a.trace[(size_t)(TT - 1 - t - a.trace_t0) * 8 + (k)] = (unsigned long long)clock64();
+    a.trace[(size_t)(TT - 1 - t - a.trace_t0) * 16 + (k)] = (unsigned long long)clock64();
   for (int t = TT - 1; t >= 0; --t) {
     RNN_TRACE(0)
     // phase A: cell derivative of every pair; dh_t gathers the G partials of
