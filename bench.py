@@ -350,15 +350,21 @@ def cpu_oracle_step(fn, inp, nthreads, rows, steps, backward=True):
     return time.perf_counter() - t0
 
 
-def oracle_sample(w, fn, cores):
-    """(batch rows, time steps) of the workload that make one oracle step about
-    20-60 s of CPU work: all rows when they fit, else a time prefix over at
+# fp64 flops of the oracle per sample: the CPU baseline of the bench line takes
+# about 15 s on the GPU machine's 16 host cores; each step of the reference arm
+# (--impl reference, 20 + 3 steps by default) about 1.5 s
+ORACLE_BUDGET_BASELINE = 700e9
+ORACLE_BUDGET_REFERENCE_STEP = 60e9
+
+
+def oracle_sample(w, fn, cores, budget=ORACLE_BUDGET_BASELINE):
+    """(batch rows, time steps) of the workload that make one oracle run about
+    `budget` fp64 flops: all rows when they fit, else a time prefix over at
     least `cores` sequences. The metric is per (row, step), so the sample's
     rate stands for the workload's."""
     from recurrent_networks_gb300.synth import GATES
     G, D, T, N, B = GATES[fn], w["D"], w["T"], w["N"], w["B"]
     per_row_step = (3.0 if w["backward"] else 1.0) * 2.0 * G * D * D * N  # fwd (+ bwd), fp64 loops
-    budget = 60e9
     if per_row_step * B * T <= budget:
         return B, T
     rows = min(B, max(1, -(-cores // N)))
@@ -370,7 +376,7 @@ def run_reference(args, w, fn):
     from recurrent_networks_gb300.synth import workload_inputs
     cores = host_cores()
     inp = workload_inputs(args.workload, function=fn, with_grads=True)
-    rows, steps = oracle_sample(w, fn, cores)
+    rows, steps = oracle_sample(w, fn, cores, ORACLE_BUDGET_REFERENCE_STEP)
     times = []
     for k in range(args.warmup + args.steps):
         dt = cpu_oracle_step(fn, inp, cores, rows, steps, w["backward"])

@@ -58,6 +58,7 @@ def test_oracle_sample_is_bounded():
     # over at least as many sequences as cores
     w2, w5 = WORKLOADS[2], WORKLOADS[5]
     assert bench.oracle_sample(w2, "lstm", 16) == (w2["B"], w2["T"])
-    rows, steps = bench.oracle_sample(w5, "lstm", 16)
-    assert rows >= 16 and 8 <= steps < w5["T"]
-    assert 3 * 2 * 4 * 1024 * 1024 * rows * steps <= 60e9
+    for budget in (bench.ORACLE_BUDGET_BASELINE, bench.ORACLE_BUDGET_REFERENCE_STEP):
+        rows, steps = bench.oracle_sample(w5, "lstm", 16, budget)
+        assert rows >= 16 and 8 <= steps < w5["T"]
+        assert 3 * 2 * 4 * 1024 * 1024 * rows * steps <= budget
