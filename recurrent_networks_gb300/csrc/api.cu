@@ -226,8 +226,8 @@ std::map<std::string, std::pair<int, Plan>> g_plans;
 
 static int choose(const rnn_dims_t* d, bool bwd, Plan* plan) {
   const DeviceLimits lim = device_limits();
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
+  int dev = -1;  // stated limits (no device query) or no device: -1
+  if (lim.cluster_capacity && cudaGetDevice(&dev) != cudaSuccess) {
     (void)cudaGetLastError();
     dev = -1;
   }

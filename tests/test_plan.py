@@ -10,7 +10,8 @@ checked on the CPU through the C ABI:
 - requests no point satisfies return RNN_EUNSUPPORTED with a reason;
 - a stated device (fewer SMs, smaller clusters, less shared memory) removes
   exactly the points its limits exclude;
-- the latency model orders the measured cluster sizes as the measurements do.
+- the latency model orders the measured cluster sizes as the measurements do,
+  and its choice is the fastest point of a timed sweep of every feasible plan.
 """
 import itertools
 import os
@@ -318,3 +319,24 @@ def test_bad_limits_are_rejected():
     assert lib.rnn_plan_set_limits(152, 100, 16) == _lib.RNN_EINVAL
     assert lib.rnn_plan_set_limits(152, 227 * 1024, 17) == _lib.RNN_EINVAL
     assert lib.rnn_plan_set_limits(0, 0, 0) == _lib.RNN_OK
+
+
+# The fastest plan of a timed sweep of every feasible cluster plan on one GB300
+# (profiles/planner_sweep_cluster_scan.md): the planner's unrestricted choice
+# must be that point.
+MEASURED_BEST = [
+    # (cell, B, N, D, backward, C, NT, KT or MT)
+    ("lstm", 8, 3, 256, False, 16, 1, 8),
+    ("lstm", 8, 3, 256, True, 16, 1, 2),
+    ("slstm", 16, 4, 192, False, 12, 1, 6),
+    ("slstm", 16, 4, 192, True, 12, 1, 2),
+]
+
+
+@pytest.mark.parametrize("case", MEASURED_BEST, ids=lambda c: "%s-D%d-%s" % (c[0], c[3], "bwd" if c[4] else "fwd"))
+def test_choice_is_the_measured_fastest_plan(planner, case):
+    fn, B, N, D, bwd, C, NT, X = case
+    rc, desc = planner(fn, B, N, D, "fused", bwd)
+    assert rc == 0
+    p = _parse(desc)
+    assert (int(p["C"]), int(p["NT"]), int(p["MT"] if bwd else p["KT"])) == (C, NT, X), desc
