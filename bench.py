@@ -620,18 +620,24 @@ def main():
         result["target_config"] = target_config_fracs(dev)
 
     # ---- e2e through the C ABI with host buffers (pinned), copies inside the window.
-    # Every step copies its inputs host -> device and all its outputs device ->
-    # host; the copies of one step overlap the compute of the neighbouring
-    # steps (two buffer sets, a host-to-device and a device-to-host stream),
-    # as a training loop prefetching its next batch would run it.
+    # Every step copies all its inputs host -> device (Wx, R, b, the initial
+    # states and the upstream gradients) and reads its result device -> host:
+    # the parameter gradients dR and db, the initial-state gradients and the
+    # last states (the forward alone: the states and the last states). The
+    # per-step states and dWx stay on the device, where the neighbouring layers
+    # of a model consume them. The copies of one step overlap the compute of
+    # the neighbouring steps (two buffer sets, a host-to-device and a
+    # device-to-host stream), as a training loop prefetching its next batch
+    # would run it.
     if not args.no_e2e:
         hin = [{k: v.pin_memory() for k, v in host.items() if v is not None} for _ in range(2)]
         dev_in = [{k: torch.empty_like(v, device=dev) for k, v in hin[0].items()} for _ in range(2)]
         out0 = [states, last] + ([dWx, dR, db, ds0] if backward else [])
         outs = [out0, [torch.empty_like(o) for o in out0]]
-        hout = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in out0] for _ in range(2)]
+        read = [1, 3, 4, 5] if backward else [0, 1]  # which outputs are the step's result read back
+        hout = [[torch.empty(out0[r].shape, dtype=out0[r].dtype, pin_memory=True) for r in read] for _ in range(2)]
         h2d = sum(v.numel() * v.element_size() for v in hin[0].values())
-        d2h = sum(o.numel() * o.element_size() for o in out0)
+        d2h = sum(out0[r].numel() * out0[r].element_size() for r in read)
         cs = torch.cuda.current_stream()
         hs, ds = torch.cuda.Stream(), torch.cuda.Stream()
         ev_h2d = [torch.cuda.Event() for _ in range(2)]
@@ -659,8 +665,8 @@ def main():
             ev_done[i].record(cs)
             with torch.cuda.stream(ds):
                 ds.wait_event(ev_done[i])
-                for t_dev, t_host in zip(o, hout[i]):
-                    t_host.copy_(t_dev, non_blocking=True)
+                for r, t_host in zip(read, hout[i]):
+                    t_host.copy_(o[r], non_blocking=True)
                 ev_out[i].record(ds)
 
         for k in range(args.warmup):
@@ -683,8 +689,11 @@ def main():
             e2e_ms = float(t[0])
         result["e2e"] = {"value": world * B * T / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                          "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                         "copies": "every step: all inputs host->device, all outputs device->host (pinned), "
-                                   "overlapped with the neighbouring steps' compute on two copy streams"}
+                         "copies": "every step: all inputs host->device; the result device->host: "
+                                   + ("dR, db, dstates0 and the last states" if backward else
+                                      "the states and the last states")
+                                   + " (pinned), overlapped with the neighbouring steps' compute on two copy "
+                                     "streams; the per-step states and dWx stay on the device"}
 
     # ---- the oracle on the host cores (rank 0, N=1 only), bounded sample
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
