@@ -155,7 +155,9 @@ cudaError_t encode_tensor_map_sw128(void* map, const void* base, int rank, const
 // dR on the 5th-generation tensor cores (bf16, D % 8 == 0); the caller adds db.
 bool wgrad_umma_supported(const WgradArgs& a);
 int wgrad_umma_splits(int B, int T, int N, int D, int G);
-cudaError_t wgrad_umma_run(const WgradArgs& a, int splits, cudaStream_t st);
+// splits: asked for on entry; on return the count launched (K-tiles are dealt
+// out evenly, which can leave fewer splits), the number of partials to reduce.
+cudaError_t wgrad_umma_run(const WgradArgs& a, int& splits, cudaStream_t st);
 cudaError_t fused_bwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st);
 
 }  // namespace rnn

@@ -1,6 +1,9 @@
 // Weight gradient of the recurrent branch on the 5th-generation tensor cores:
 //   dR[g, n] (D x D) = Hprev^T dr,   K = B T (+ B rows for the initial state)
-// one 128 x 128 output tile per CTA, the fp32 accumulator in tensor memory.
+// one 128 x BN output tile per CTA (BN = 128, 192 or 256 columns: the head
+// size rounded up to 64, at most 256), the fp32 accumulator in tensor memory.
+// Wider tiles read each row block of h once per BN columns instead of per 128,
+// and a head of 192 units needs no padded columns.
 //
 // Operands stream in by TMA with the 128-byte swizzle, k-rows of 64 units
 // (128 bytes) per box, which is the MN-major canonical layout tcgen05 reads
@@ -13,7 +16,8 @@
 // rows past T read zeros on both sides. The initial state enters as extra
 // k-tiles whose rows run over b: A = states0[0, b, n, :], B = dr[b, 0, g, n, :].
 //
-// Warp roles: thread 0 issues the TMA loads into a ring of 4 stages, thread 32
+// Warp roles: thread 0 issues the TMA loads into a ring of stages (as many as
+// 192 KB hold: 6 for BN = 128, 4 for 192 and 256), thread 32
 // issues the MMAs (4 per stage, K = 16 each) and releases each stage with
 // tcgen05.commit; after the last stage all four warps read the accumulator
 // (warp w owns TMEM lanes 32w .. 32w+31 = tile rows) and write dR, or fp32
@@ -25,10 +29,20 @@ namespace rnn {
 
 namespace {
 
-constexpr int UM_TILE = 128, UM_BK = 64, UM_STAGES = 4;
+constexpr int UM_TILE = 128, UM_BK = 64;           // tile rows (i), k-rows per stage
 constexpr int UM_BOX_BYTES = 64 * 128;              // one 64 x 64 bf16 box, 128-byte rows
-constexpr int UM_STAGE_BYTES = 4 * UM_BOX_BYTES;    // A: two unit halves, B: two unit halves
-constexpr int UM_SMEM = UM_STAGES * UM_STAGE_BYTES + 1024 + 256;  // + alignment slack, barriers
+
+// The tile width for head size D: the columns rounded up to 64, at most 256.
+inline int um_bn(int D) { return D <= 128 ? 128 : (D <= 192 ? 192 : 256); }
+
+template <int BN>
+struct UmCfg {
+  static constexpr int NB = BN / 64;                            // B boxes per stage
+  static constexpr int STAGE_BYTES = (2 + NB) * UM_BOX_BYTES;   // A: two 64-unit halves, B: NB
+  static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;  // + alignment slack, barriers
+  static constexpr int TCOLS = BN <= 128 ? 128 : 256;           // tensor-memory columns (a power of two)
+};
 
 __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t addr) {
   // start address, leading byte offset = stride of the 64-unit halves (8 KB),
@@ -51,10 +65,13 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+template <int BN>
 __global__ void __launch_bounds__(128, 1)
     wgrad_umma_kernel(const __grid_constant__ CUtensorMap amain, const __grid_constant__ CUtensorMap as0,
                       const __grid_constant__ CUtensorMap bmain, const __grid_constant__ CUtensorMap bs0,
                       WgradArgs a, int splits, int kps, int tpb, int s0_tiles) {
+  using Cfg = UmCfg<BN>;
+  constexpr int UM_STAGES = Cfg::STAGES, UM_STAGE_BYTES = Cfg::STAGE_BYTES, NB = Cfg::NB;
   extern __shared__ unsigned char um_raw[];
   unsigned char* sm = (unsigned char*)(((uintptr_t)um_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + UM_STAGES * UM_STAGE_BYTES);  // full[4], empty[4], acc
@@ -63,7 +80,7 @@ __global__ void __launch_bounds__(128, 1)
                  accb = smem_u32(&bars[2 * UM_STAGES]);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int D = a.D, N = a.N, G = a.G;
-  const int j0 = blockIdx.x * UM_TILE, i0 = blockIdx.y * UM_TILE;
+  const int j0 = blockIdx.x * BN, i0 = blockIdx.y * UM_TILE;
   const int gn = blockIdx.z / splits, split = blockIdx.z - gn * splits;
   const int g = gn / N, n = gn - g * N;
   const int Q = a.B * tpb + s0_tiles;
@@ -80,7 +97,8 @@ __global__ void __launch_bounds__(128, 1)
     prefetch_tensormap(&bmain);
   }
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" ::"r"(smem_u32(tslot))
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                 "n"(Cfg::TCOLS)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -105,22 +123,22 @@ __global__ void __launch_bounds__(128, 1)
       const int q = q0 + it;
       if (q < a.B * tpb) {
         const int b = q / tpb, t0 = (q - b * tpb) * UM_BK;
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < 2; ++h)
           tma_load_5d(smem_u32(As + h * UM_BOX_BYTES), &amain, fb, i0 + 64 * h, n, t0 - 1, b, 0);
+        for (int h = 0; h < NB; ++h)
           tma_load_5d(smem_u32(Bs + h * UM_BOX_BYTES), &bmain, fb, j0 + 64 * h, n, g, t0, b);
-        }
       } else {
         const int bb = (q - a.B * tpb) * UM_BK;
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < 2; ++h)
           tma_load_5d(smem_u32(As + h * UM_BOX_BYTES), &as0, fb, i0 + 64 * h, n, bb, 0, 0);
+        for (int h = 0; h < NB; ++h)
           tma_load_5d(smem_u32(Bs + h * UM_BOX_BYTES), &bs0, fb, j0 + 64 * h, n, g, 0, bb);
-        }
       }
     }
   } else if (tid == 32) {  // ---- MMA issuer
-    // kind::f16 descriptor: f32 accumulator, bf16 A and B, both MN-major, N = M = 128
+    // kind::f16 descriptor: f32 accumulator, bf16 A and B, both MN-major, M = 128, N = BN
     const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) |
-                           ((uint32_t)(UM_TILE >> 3) << 17) | ((uint32_t)(UM_TILE >> 4) << 24);
+                           ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(UM_TILE >> 4) << 24);
     for (int it = 0; it < nq; ++it) {
       const int s = it % UM_STAGES;
       mbar_wait_bounded<false>(full0 + 8 * s, (it / UM_STAGES) & 1, a.wait_limit_ns, a.status, failed);
@@ -141,7 +159,7 @@ __global__ void __launch_bounds__(128, 1)
   mbar_wait_bounded<false>(accb, 0, a.wait_limit_ns, a.status, failed);
   tc_fence_after();
   const int i = i0 + warp * 32 + lane;
-  for (int c0 = 0; c0 < UM_TILE; c0 += 32) {
+  for (int c0 = 0; c0 < BN; c0 += 32) {
     uint32_t r[32];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -195,7 +213,8 @@ __global__ void __launch_bounds__(128, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(tmem) : "memory");
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(Cfg::TCOLS) : "memory");
 }
 
 }  // namespace
@@ -203,15 +222,26 @@ __global__ void __launch_bounds__(128, 1)
 bool wgrad_umma_supported(const WgradArgs& a) { return a.dR && a.D % 8 == 0 && a.D >= 64 && a.B * a.T > 0; }
 
 int wgrad_umma_splits(int B, int T, int N, int D, int G) {
-  const int tiles = ((D + UM_TILE - 1) / UM_TILE) * ((D + UM_TILE - 1) / UM_TILE) * G * N;
+  // Split K so that the waves of CTAs (one per SM) divide evenly: a split
+  // count s costs ceil(tiles s / SMs) / s of the unsplit tile time, plus the
+  // fp32 partials written and reduced (s D^2 words per head, each way).
+  const int bn = um_bn(D);
+  const int tiles = ((D + bn - 1) / bn) * ((D + UM_TILE - 1) / UM_TILE) * G * N;
   const int Q = B * ((T + UM_BK - 1) / UM_BK) + (B + UM_BK - 1) / UM_BK;
-  int splits = (device_sms() + tiles - 1) / tiles;  // about one wave of the SMs
-  if (splits > Q / 4) splits = Q / 4;      // keep at least 4 k-tiles per split
-  if (splits > 32) splits = 32;
-  return splits < 1 ? 1 : splits;
+  const int sms = device_sms();
+  const double tile_s = 2.0 * UM_TILE * bn * UM_BK * (double)Q / 1.0e13;  // one tile, all of K, on one SM
+  const double part_s = 2.0 * 4.0 * G * N * (double)D * D / 6.0e12;       // one split's partials, out and back
+  int best = 1;
+  double best_t = 1e30;
+  const int smax = Q / 4 < 32 ? Q / 4 : 32;  // keep at least 4 k-tiles per split
+  for (int s = 1; s <= (smax < 1 ? 1 : smax); ++s) {
+    const double t = (double)((tiles * s + sms - 1) / sms) * tile_s / s + (s > 1 ? s * part_s + 3e-6 : 0.0);
+    if (t < best_t * 0.98) best = s, best_t = t;  // a split must gain 2% to be taken
+  }
+  return best;
 }
 
-cudaError_t wgrad_umma_run(const WgradArgs& a, int splits, cudaStream_t st) {
+cudaError_t wgrad_umma_run(const WgradArgs& a, int& splits, cudaStream_t st) {
   const int tpb = (a.T + UM_BK - 1) / UM_BK;
   const int s0_tiles = a.s0 ? (a.B + UM_BK - 1) / UM_BK : 0;
   const int Q = a.B * tpb + s0_tiles;
@@ -240,10 +270,14 @@ cudaError_t wgrad_umma_run(const WgradArgs& a, int splits, cudaStream_t st) {
     e = encode_tensor_map_sw128(&bs0, a.dr, 5, dims, box_b);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = set_smem_attr((const void*)wgrad_umma_kernel, (size_t)UM_SMEM);
+  const int bn = um_bn(a.D);
+  void (*k)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, WgradArgs, int, int, int, int) =
+      bn == 128 ? wgrad_umma_kernel<128> : bn == 192 ? wgrad_umma_kernel<192> : wgrad_umma_kernel<256>;
+  const int smem = bn == 128 ? UmCfg<128>::SMEM : bn == 192 ? UmCfg<192>::SMEM : UmCfg<256>::SMEM;
+  cudaError_t e = set_smem_attr((const void*)k, (size_t)smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((a.D + UM_TILE - 1) / UM_TILE, (a.D + UM_TILE - 1) / UM_TILE, a.G * a.N * splits);
-  wgrad_umma_kernel<<<grid, 128, UM_SMEM, st>>>(amain, as0, bmain, bs0, a, splits, kps, tpb, s0_tiles);
+  const dim3 grid((a.D + bn - 1) / bn, (a.D + UM_TILE - 1) / UM_TILE, a.G * a.N * splits);
+  k<<<grid, 128, smem, st>>>(amain, as0, bmain, bs0, a, splits, kps, tpb, s0_tiles);
   note_launch();
   return cudaGetLastError();
 }
