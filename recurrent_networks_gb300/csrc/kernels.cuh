@@ -152,6 +152,11 @@ cudaError_t encode_tensor_map_swizzled(void* map, const void* base, int elem_byt
 // bf16, 128-byte swizzle (box[0] * 2 <= 128): the layout the tcgen05 operands read
 cudaError_t encode_tensor_map_sw128(void* map, const void* base, int rank, const unsigned long long* dims,
                                     const unsigned int* box);
+// The same with explicit byte strides of dimensions 1 .. rank-1 (any order:
+// a dimension may step by less than the one before it), so that one box can
+// gather several 64-element slabs of a row into consecutive 8 KB blocks.
+cudaError_t encode_tensor_map_sw128_strided(void* map, const void* base, int rank, const unsigned long long* dims,
+                                            const unsigned long long* strides, const unsigned int* box);
 // dR on the 5th-generation tensor cores (bf16, D % 8 == 0); the caller adds db.
 bool wgrad_umma_supported(const WgradArgs& a);
 int wgrad_umma_splits(int B, int T, int N, int D, int G);

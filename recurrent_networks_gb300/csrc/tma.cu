@@ -40,6 +40,24 @@ cudaError_t encode_tensor_map_sw128(void* map, const void* base, int rank, const
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t encode_tensor_map_sw128_strided(void* map, const void* base, int rank, const unsigned long long* dims,
+                                            const unsigned long long* strides, const unsigned int* box) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn || rank < 2 || rank > 5 || box[0] * 2 > 128) return cudaErrorNotSupported;
+  cuuint64_t gdim[5], gstride[4];
+  cuuint32_t bdim[5], estr[5];
+  for (int d = 0; d < rank; ++d) {
+    gdim[d] = dims[d];
+    bdim[d] = box[d];
+    estr[d] = 1;
+    if (d > 0) gstride[d - 1] = strides[d - 1];
+  }
+  CUresult r = fn((CUtensorMap*)map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, (void*)base, gdim, gstride,
+                  bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t encode_tensor_map(void* map, const void* base, int elem_bytes, int rank,
                               const unsigned long long* dims, const unsigned int* box) {
   return encode_tensor_map_swizzled(map, base, elem_bytes, rank, dims, box, 0);

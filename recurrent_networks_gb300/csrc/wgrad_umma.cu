@@ -65,7 +65,7 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-template <int BN>
+template <int BN, bool BLK>
 __global__ void __launch_bounds__(128, 1)
     wgrad_umma_kernel(const __grid_constant__ CUtensorMap amain, const __grid_constant__ CUtensorMap as0,
                       const __grid_constant__ CUtensorMap bmain, const __grid_constant__ CUtensorMap bs0,
@@ -123,16 +123,26 @@ __global__ void __launch_bounds__(128, 1)
       const int q = q0 + it;
       if (q < a.B * tpb) {
         const int b = q / tpb, t0 = (q - b * tpb) * UM_BK;
-        for (int h = 0; h < 2; ++h)
-          tma_load_5d(smem_u32(As + h * UM_BOX_BYTES), &amain, fb, i0 + 64 * h, n, t0 - 1, b, 0);
-        for (int h = 0; h < NB; ++h)
-          tma_load_5d(smem_u32(Bs + h * UM_BOX_BYTES), &bmain, fb, j0 + 64 * h, n, g, t0, b);
+        if (BLK) {  // one box per operand: the 64-unit slabs land 8 KB apart
+          tma_load_5d(smem_u32(As), &amain, fb, 0, t0 - 1, i0 / 64, n, b);
+          tma_load_5d(smem_u32(Bs), &bmain, fb, 0, t0, j0 / 64, g * N + n, b);
+        } else {
+          for (int h = 0; h < 2; ++h)
+            tma_load_5d(smem_u32(As + h * UM_BOX_BYTES), &amain, fb, i0 + 64 * h, n, t0 - 1, b, 0);
+          for (int h = 0; h < NB; ++h)
+            tma_load_5d(smem_u32(Bs + h * UM_BOX_BYTES), &bmain, fb, j0 + 64 * h, n, g, t0, b);
+        }
       } else {
         const int bb = (q - a.B * tpb) * UM_BK;
-        for (int h = 0; h < 2; ++h)
-          tma_load_5d(smem_u32(As + h * UM_BOX_BYTES), &as0, fb, i0 + 64 * h, n, bb, 0, 0);
-        for (int h = 0; h < NB; ++h)
-          tma_load_5d(smem_u32(Bs + h * UM_BOX_BYTES), &bs0, fb, j0 + 64 * h, n, g, 0, bb);
+        if (BLK) {
+          tma_load_5d(smem_u32(As), &as0, fb, 0, bb, i0 / 64, n, 0);
+          tma_load_5d(smem_u32(Bs), &bs0, fb, 0, bb, j0 / 64, g * N + n, 0);
+        } else {
+          for (int h = 0; h < 2; ++h)
+            tma_load_5d(smem_u32(As + h * UM_BOX_BYTES), &as0, fb, i0 + 64 * h, n, bb, 0, 0);
+          for (int h = 0; h < NB; ++h)
+            tma_load_5d(smem_u32(Bs + h * UM_BOX_BYTES), &bs0, fb, j0 + 64 * h, n, g, 0, bb);
+        }
       }
     }
   } else if (tid == 32) {  // ---- MMA issuer
@@ -249,30 +259,62 @@ cudaError_t wgrad_umma_run(const WgradArgs& a, int& splits, cudaStream_t st) {
   splits = (Q + kps - 1) / kps;  // every split has at least one k-tile
   CUtensorMap amain, as0, bmain, bs0;
   const unsigned long long D = a.D, N = a.N, T = a.T, B = a.B, G = a.G;
-  {  // states[0] as (D, N, T, B): rows of 64 steps of one batch row
-    const unsigned long long dims[5] = {D, N, T, B, 1};
-    const unsigned int box[5] = {64, 1, UM_BK, 1, 1};
-    cudaError_t e = encode_tensor_map_sw128(&amain, a.states, 5, dims, box);
-    if (e != cudaSuccess) return e;
-  }
-  {  // states0[0] as (D, N, B): rows over the batch
-    const unsigned long long dims[5] = {D, N, B, 1, 1};
-    const unsigned int box[5] = {64, 1, UM_BK, 1, 1};
-    cudaError_t e = encode_tensor_map_sw128(&as0, a.s0 ? a.s0 : a.states, 5, dims, box);
-    if (e != cudaSuccess) return e;
-  }
-  {  // dr as (D, N, G, T, B): rows of 64 steps, or rows over the batch at t = 0
-    const unsigned long long dims[5] = {D, N, G, T, B};
-    const unsigned int box_t[5] = {64, 1, 1, UM_BK, 1};
-    const unsigned int box_b[5] = {64, 1, 1, 1, UM_BK};
-    cudaError_t e = encode_tensor_map_sw128(&bmain, a.dr, 5, dims, box_t);
-    if (e != cudaSuccess) return e;
-    e = encode_tensor_map_sw128(&bs0, a.dr, 5, dims, box_b);
-    if (e != cudaSuccess) return e;
-  }
   const int bn = um_bn(a.D);
+  // With D a multiple of 64, one box per operand and stage gathers the tile's
+  // 64-unit slabs (dimension 2, 128 bytes apart in memory) into consecutive
+  // 8 KB blocks: 2 TMA copies per stage instead of 2 + BN / 64.
+  const bool blk = a.D % 64 == 0;
+  if (blk) {
+    const unsigned int box_a[5] = {64, UM_BK, 2, 1, 1};
+    const unsigned int box_b[5] = {64, UM_BK, (unsigned)bn / 64, 1, 1};
+    {  // states[0] (B, T, N, D) as (unit, t, slab, n, b)
+      const unsigned long long dims[5] = {64, T, D / 64, N, B};
+      const unsigned long long str[4] = {N * D * 2, 128, D * 2, T * N * D * 2};
+      cudaError_t e = encode_tensor_map_sw128_strided(&amain, a.states, 5, dims, str, box_a);
+      if (e != cudaSuccess) return e;
+    }
+    {  // states0[0] (B, N, D) as (unit, b, slab, n)
+      const unsigned long long dims[5] = {64, B, D / 64, N, 1};
+      const unsigned long long str[4] = {N * D * 2, 128, D * 2, B * N * D * 2};
+      cudaError_t e = encode_tensor_map_sw128_strided(&as0, a.s0 ? a.s0 : a.states, 5, dims, str, box_a);
+      if (e != cudaSuccess) return e;
+    }
+    {  // dr (B, T, G, N, D) as (unit, t, slab, g n, b), and as (unit, b, slab, g n, t)
+      const unsigned long long dims_t[5] = {64, T, D / 64, G * N, B};
+      const unsigned long long str_t[4] = {G * N * D * 2, 128, D * 2, T * G * N * D * 2};
+      cudaError_t e = encode_tensor_map_sw128_strided(&bmain, a.dr, 5, dims_t, str_t, box_b);
+      if (e != cudaSuccess) return e;
+      const unsigned long long dims_b[5] = {64, B, D / 64, G * N, T};
+      const unsigned long long str_b[4] = {T * G * N * D * 2, 128, D * 2, G * N * D * 2};
+      e = encode_tensor_map_sw128_strided(&bs0, a.dr, 5, dims_b, str_b, box_b);
+      if (e != cudaSuccess) return e;
+    }
+  } else {
+    {  // states[0] as (D, N, T, B): rows of 64 steps of one batch row
+      const unsigned long long dims[5] = {D, N, T, B, 1};
+      const unsigned int box[5] = {64, 1, UM_BK, 1, 1};
+      cudaError_t e = encode_tensor_map_sw128(&amain, a.states, 5, dims, box);
+      if (e != cudaSuccess) return e;
+    }
+    {  // states0[0] as (D, N, B): rows over the batch
+      const unsigned long long dims[5] = {D, N, B, 1, 1};
+      const unsigned int box[5] = {64, 1, UM_BK, 1, 1};
+      cudaError_t e = encode_tensor_map_sw128(&as0, a.s0 ? a.s0 : a.states, 5, dims, box);
+      if (e != cudaSuccess) return e;
+    }
+    {  // dr as (D, N, G, T, B): rows of 64 steps, or rows over the batch at t = 0
+      const unsigned long long dims[5] = {D, N, G, T, B};
+      const unsigned int box_t[5] = {64, 1, 1, UM_BK, 1};
+      const unsigned int box_b[5] = {64, 1, 1, 1, UM_BK};
+      cudaError_t e = encode_tensor_map_sw128(&bmain, a.dr, 5, dims, box_t);
+      if (e != cudaSuccess) return e;
+      e = encode_tensor_map_sw128(&bs0, a.dr, 5, dims, box_b);
+      if (e != cudaSuccess) return e;
+    }
+  }
   void (*k)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, WgradArgs, int, int, int, int) =
-      bn == 128 ? wgrad_umma_kernel<128> : bn == 192 ? wgrad_umma_kernel<192> : wgrad_umma_kernel<256>;
+      blk ? (bn == 128 ? wgrad_umma_kernel<128, true> : bn == 192 ? wgrad_umma_kernel<192, true> : wgrad_umma_kernel<256, true>)
+          : (bn == 128 ? wgrad_umma_kernel<128, false> : bn == 192 ? wgrad_umma_kernel<192, false> : wgrad_umma_kernel<256, false>);
   const int smem = bn == 128 ? UmCfg<128>::SMEM : bn == 192 ? UmCfg<192>::SMEM : UmCfg<256>::SMEM;
   cudaError_t e = set_smem_attr((const void*)k, (size_t)smem);
   if (e != cudaSuccess) return e;

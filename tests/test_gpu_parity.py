@@ -357,12 +357,15 @@ def test_auto_takes_alternating_when_r_does_not_fit():
 
 
 # ------------------------------------------------- weight gradients (tcgen05)
-@pytest.mark.parametrize("case", [("lstm", 3, 200, 2, 192), ("gru", 70, 9, 1, 64), ("slstm", 2, 130, 1, 320)],
+@pytest.mark.parametrize("case", [("lstm", 3, 200, 2, 192), ("gru", 70, 9, 1, 64), ("slstm", 2, 130, 1, 320),
+                                  ("elman", 5, 100, 3, 136), ("lstm", 4, 70, 2, 200)],
                          ids=lambda c: "%s-B%dT%dN%dD%d" % c)
 def test_weight_gradient_tiles(case):
-    """dR and db through the tensor-memory GEMM: ragged 128-unit tiles (D = 192,
-    320), runs of steps that end inside a 64-step tile (T = 200, 130, 9), a batch
-    wider than one 64-row initial-state tile (B = 70), split-K partial sums."""
+    """dR and db through the tensor-memory GEMM: ragged tiles (D = 192, 320 with
+    128 x 192 and 128 x 256 tiles), runs of steps that end inside a 64-step tile
+    (T = 200, 130, 9, 100, 70), a batch wider than one 64-row initial-state tile
+    (B = 70), split-K partial sums; D = 136 and 200 (not multiples of 64) take
+    one TMA box per 64-unit slab instead of one gathered box per operand."""
     fn, B, T, N, D = case
     inp = _inputs(fn, (B, T, N, D), torch.bfloat16, seed=1500 + B + T + D)
     st, last, tape = run_fwd(fn, inp, "simt")
