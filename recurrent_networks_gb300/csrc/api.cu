@@ -188,10 +188,11 @@ static Sizes sizes_of(const rnn_dims_t* d) {
 
 static bool aligned(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-// Workspace layout: [status 256 B][path scratch][dr buffer (bwd)][split-K partials of
-// the weight gradients (bwd)][tape (bwd recompute)]
+// Workspace layout: [status 256 B][path scratch][dr buffer (bwd)][db partials of the
+// persistent backward kernels (bwd)][split-K partials of the weight gradients
+// (bwd)][tape (bwd recompute)]
 struct WsLayout {
-  size_t status, path, dr, wg, tape, total;
+  size_t status, path, dr, dbp, wg, tape, total;
 };
 
 static WsLayout ws_layout(const rnn_dims_t* d, int kind, const Plan& plan) {
@@ -202,6 +203,8 @@ static WsLayout ws_layout(const rnn_dims_t* d, int kind, const Plan& plan) {
   size_t off = w.path + align256(plan.scratch_bytes);
   w.dr = off;
   if (kind != RNN_WS_FWD) off += align256(z.dr);
+  w.dbp = off;  // [ceil(B / 8) batch blocks][G][N][D] fp32: enough for any block height
+  if (kind != RNN_WS_FWD) off += align256((size_t)((d->B + 7) / 8) * z.bias * sizeof(float));
   w.wg = off;
   if (kind != RNN_WS_FWD) off += align256(wgrad_scratch_bytes(d->B, d->T, d->N, d->D, z.G, d->dtype));
   w.tape = off;
@@ -454,6 +457,7 @@ int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
   void* drbuf = (d->function != RNN_GRU && dWx) ? dWx : (void*)(ws + w.dr);
   a.dstates = dstates; a.dlast = dlast; a.dWx = dWx; a.dr = drbuf; a.ds0 = dstates0;
   rc = RNN_EUNSUPPORTED;
+  int dbp_blocks = 0;  // > 0: the scan kernel left db partials at ws + w.dbp
   prof_mark(1, 0, st);
   switch (plan.path) {
     case RNN_PATH_SIMT:
@@ -472,6 +476,10 @@ int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
       f.dstates = dstates; f.dlast = dlast; f.dWx = dWx; f.dr = drbuf; f.ds0 = dstates0;
       f.status = (unsigned int*)ws;
       f.wait_limit_ns = g_wait_limit_ns;
+      if (db && d->dtype == RNN_BF16) {  // db summed inside the kernel, per batch block
+        f.dbp = (float*)(ws + w.dbp);
+        dbp_blocks = (d->B + 8 * plan.fs.NT - 1) / (8 * plan.fs.NT);
+      }
       with_trace(&f);
       rc = cuda_status(fused_bwd_run(d->function, plan.fs, f, st));
       break;
@@ -484,6 +492,10 @@ int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
       f.dstates = dstates; f.dlast = dlast; f.dWx = dWx; f.dr = drbuf; f.ds0 = dstates0;
       f.status = (unsigned int*)ws;
       f.wait_limit_ns = g_wait_limit_ns;
+      if (db && d->dtype == RNN_BF16) {  // db summed inside the kernel, per batch block
+        f.dbp = (float*)(ws + w.dbp);
+        dbp_blocks = (d->B + 8 * plan.fs.NT - 1) / (8 * plan.fs.NT);
+      }
       with_trace(&f);
       grid_scratch(d, plan, ws, true, &f);
       rc = cuda_status(cudaMemsetAsync(f.counters, 0, (size_t)plan.groups * sizeof(unsigned), st));
@@ -508,6 +520,10 @@ int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
     g.scratch_bytes = w.tape - w.wg;
     g.status = (unsigned int*)ws;
     g.wait_limit_ns = g_wait_limit_ns;
+    if (dbp_blocks > 0) {
+      g.dbp = (const float*)(ws + w.dbp);
+      g.dbp_blocks = dbp_blocks;
+    }
     rc = cuda_status(wgrad_run(d->dtype, g, st));
   }
   return rc;

@@ -48,6 +48,8 @@ __global__ void __launch_bounds__(256, 1)
   float* red = (float*)(smem + L.red);
   float* ds = (float*)(smem + L.ds);
   float* s0s = (float*)(smem + L.s0);
+  float* dbs = (float*)(smem + L.dbs);  // [G][BC][U]: the pairs' sums of dr over the steps
+  const bool with_db = a.dbp != nullptr;
   const uint32_t ring_bar0 = smem_u32(&bars[0]);
   const uint32_t gath_bar = smem_u32(&bars[FUSED_NS]);  // the gather of the group's dr
   const bool has_dst = a.dstates != nullptr;
@@ -76,6 +78,8 @@ __global__ void __launch_bounds__(256, 1)
     s0s[e] = v;
     ds[e] = 0.0f;
   }
+  if (with_db)
+    for (int e = tid; e < G * BC * U; e += nthr) dbs[e] = 0.0f;
   // resident fragments: A[m = own row i][k = (g, j)] = R[g, n, i, j]
   uint32_t afr[KT][4];
   {
@@ -115,6 +119,7 @@ __global__ void __launch_bounds__(256, 1)
     for (int k = 0; k < FUSED_NS - 1 && k < TT; ++k) issue_stage(k);
 
   bool failed = false;
+  float dbv[G];  // the first pair's dr of the step, for db
   const bool tracer = a.trace && blockIdx.x == 0 && tid == 0;
 #define RNN_TRACE(p)                                                                    \
   if (tracer && kk >= a.trace_t0 && kk < a.trace_t0 + a.trace_steps)                    \
@@ -243,6 +248,17 @@ __global__ void __launch_bounds__(256, 1)
         if (write_dr) dro[o + (size_t)g * N * D] = __float2bfloat16_rn(dr[g]);
         dxw[(size_t)b * KG + g * D + u0 + u] = __float2bfloat16_rn(dr[g]);
       }
+      // db: the pair's own running sum (the pair stays with this thread); the
+      // first pair's is added after the step is published, off the step's path
+      if (with_db) {
+        if (first) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) dbv[g] = dr[g];
+        } else {
+#pragma unroll
+          for (int g = 0; g < G; ++g) dbs[(g * BC + b) * U + u] += dr[g];
+        }
+      }
 #pragma unroll
       for (int s = 0; s < S; ++s) ds[(s * BC + b) * U + u] = dsp[s];
     }
@@ -250,8 +266,20 @@ __global__ void __launch_bounds__(256, 1)
     __syncthreads();
     if (tid == 0) counter_publish(a.counters + grp);
     RNN_TRACE(6)
+    if (with_db && tid < nb * U)
+#pragma unroll
+      for (int g = 0; g < G; ++g) dbs[(g * BC + c_b0) * U + c_u0] += dbv[g];
   }
 #undef RNN_TRACE
+  // db partial of the batch block: the column sums over its rows, in row order
+  // (every pair's last update was ordered before the last step's barrier)
+  if (with_db)
+    for (int e = tid; e < G * U; e += nthr) {
+      const int g = e / U, u = e - g * U;
+      float v = 0.0f;
+      for (int b = 0; b < nb; ++b) v += dbs[(g * BC + b) * U + u];
+      a.dbp[(((size_t)(grp / N) * G + g) * N + n) * D + u0 + u] = v;
+    }
 }
 
 template <int FN>

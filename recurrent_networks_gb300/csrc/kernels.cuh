@@ -65,6 +65,10 @@ struct WgradArgs {
   void* db;  // may be null
   float* scratch = nullptr;  // optional: split-K partial sums (wgrad_scratch_bytes)
   size_t scratch_bytes = 0;
+  // optional: db already summed by the backward scan kernel per batch block,
+  // fp32 [dbp_blocks][G][N][D]; db is then their sum in block order
+  const float* dbp = nullptr;
+  int dbp_blocks = 0;
   unsigned int* status = nullptr;  // device status word for the bounded waits (may be null)
   unsigned long long wait_limit_ns = 2000000000ull;
 };
@@ -87,6 +91,9 @@ struct FusedArgs {
   void* dWx;
   void* dr;
   void* ds0;
+  // optional (backward): fp32 [B / BC blocks][G][N][D], each CTA's column
+  // sums of dr over its batch block and all steps (db partials)
+  float* dbp = nullptr;
   unsigned int* status;  // device status word (bounded waits)
   unsigned long long wait_limit_ns;
   // grid mode (cooperative persistent kernel): h exchange buffers

@@ -65,7 +65,7 @@ struct FusedSmem {
 constexpr int FUSED_BWD_MAX_KTA = 8;  // k-tiles G*U/16 a CTA may own
 
 struct FusedBwdSmem {
-  size_t bars, ring, ring_stage, tape_bytes, dst_off, recv, drb, ds, s0, total;
+  size_t bars, ring, ring_stage, tape_bytes, dst_off, recv, drb, ds, s0, dbs, total;
   RNN_HD static FusedBwdSmem make(int G, int S, int K, int U, int BC, int C) {
     FusedBwdSmem m;
     size_t off = 0;
@@ -78,6 +78,7 @@ struct FusedBwdSmem {
     m.drb = FusedSmem::take(off, (size_t)2 * BC * (G * U + 8) * 2);
     m.ds = off;  // the carried gradients are held in registers
     m.s0 = FusedSmem::take(off, (size_t)S * BC * U * 4);
+    m.dbs = FusedSmem::take(off, (size_t)G * BC * U * 4);  // db sums of the CTA's pairs
     m.total = off;
     return m;
   }
@@ -87,7 +88,7 @@ struct FusedBwdSmem {
 // recurrent-branch gradients of the whole group ([BC][G D + 8] bf16), the
 // K-split partial sums, and the carried and initial states.
 struct GridBwdSmem {
-  size_t bars, ring, ring_stage, tape_bytes, dst_off, dbuf, red, ds, s0, total;
+  size_t bars, ring, ring_stage, tape_bytes, dst_off, dbuf, red, ds, s0, dbs, total;
   RNN_HD static GridBwdSmem make(int G, int S, int K, int D, int U, int BC, int KS) {
     GridBwdSmem m;
     size_t off = 0;
@@ -100,6 +101,7 @@ struct GridBwdSmem {
     m.red = FusedSmem::take(off, (size_t)(U / 16) * KS * BC * FUSED_RED_STRIDE * 4);
     m.ds = FusedSmem::take(off, (size_t)S * BC * U * 4);
     m.s0 = FusedSmem::take(off, (size_t)S * BC * U * 4);
+    m.dbs = FusedSmem::take(off, (size_t)G * BC * U * 4);  // db sums of the CTA's pairs
     m.total = off;
     return m;
   }

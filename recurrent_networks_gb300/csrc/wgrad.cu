@@ -300,10 +300,26 @@ size_t wgrad_scratch_bytes(int B, int T, int N, int D, int G, int dtype) {
   return dR_part > db_part ? dR_part : db_part;
 }
 
-// db after the tensor-core dR: the column sums of dr (two passes when the
-// scratch and alignment allow, else one block per 32 columns).
+// db from the backward scan kernel's per-batch-block sums, added in block order.
+__global__ void db_blocks_kernel(const float* __restrict__ dbp, int blocks, int cols, __nv_bfloat16* __restrict__ db) {
+  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += gridDim.x * blockDim.x) {
+    float v = 0.0f;
+    for (int k = 0; k < blocks; ++k) v += dbp[(size_t)k * cols + c];
+    db[c] = __float2bfloat16_rn(v);
+  }
+}
+
+// db after the tensor-core dR: the sum of the scan kernel's block partials
+// when it left them, else the column sums of dr (two passes when the scratch
+// and alignment allow, else one block per 32 columns).
 static cudaError_t bgrad_launch(const WgradArgs& a, cudaStream_t st) {
   if (!a.db) return cudaSuccess;
+  if (a.dbp && a.dbp_blocks > 0) {
+    const int cols = a.G * a.N * a.D;
+    db_blocks_kernel<<<(cols + 255) / 256, 256, 0, st>>>(a.dbp, a.dbp_blocks, cols, (__nv_bfloat16*)a.db);
+    note_launch();
+    return cudaGetLastError();
+  }
   const int K = a.B * a.T, Cn = a.G * a.N * a.D;
   if (colsum_bf16((const __nv_bfloat16*)a.dr, (__nv_bfloat16*)a.db, K, Cn, a.scratch, a.scratch_bytes, st)) {
     // dr is [K rows][G N D columns]; db[g, n, j] is column (g, n, j)

@@ -67,6 +67,7 @@ def _bwd_smem(G, S, K, U, BC, C):
     off = _take(off, 2 * C * U * BC * 4)               # received partial sums of dh
     off = _take(off, 2 * BC * (G * U + 8) * 2)         # own dr, bf16
     off = _take(off, S * BC * U * 4)                   # initial states
+    off = _take(off, G * BC * U * 4)                   # running db sums of the pairs
     return off
 
 
@@ -77,6 +78,7 @@ def _grid_bwd_smem(G, S, K, D, U, BC, KS):
     off = _take(off, (U // 16) * KS * BC * RED_STRIDE * 4)
     off = _take(off, S * BC * U * 4)
     off = _take(off, S * BC * U * 4)
+    off = _take(off, G * BC * U * 4)                   # running db sums of the pairs
     return off
 
 
