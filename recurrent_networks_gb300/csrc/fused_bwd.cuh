@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(256, 1)
   auto swz = [](int u) { return NT == 1 ? ((u >> 2) & 1) : ((u >> 1) & 3); };
   __nv_bfloat16* drb = (__nv_bfloat16*)(smem + L.drb);  // [2][BC][KB]
   float* s0s = (float*)(smem + L.s0);   // [S][BC][U]
-  float* dbs = (float*)(smem + L.dbs);  // [G][BC][U]: the pairs' sums of dr over the steps
+  float* dbs = (float*)(smem + L.dbs);  // [G][BC][U]: the pairs' sums of dr, gathered at the end
   const bool with_db = a.dbp != nullptr;
   const uint32_t recv_bar0 = smem_u32(&bars[0]);
   const uint32_t ring_bar0 = smem_u32(&bars[2]);
@@ -89,8 +89,6 @@ __global__ void __launch_bounds__(256, 1)
     if (b < nb && s0) v = __bfloat162float(s0[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u]);
     s0s[e] = v;
   }
-  if (with_db)
-    for (int e = tid; e < G * BC * U; e += nthr) dbs[e] = 0.0f;
   // carried state gradients of this thread's (batch row, unit) pairs
   // e = tid + k * blockDim (k < FUSED_PPT), in registers for the whole scan
   // and their (row, unit) coordinates, divided once here rather than every step
@@ -151,7 +149,11 @@ __global__ void __launch_bounds__(256, 1)
   }
 
   bool failed = false;
-  float dbv[FUSED_PPT][G];      // the pairs' dr of the step, for db
+  float dbv[FUSED_PPT][G];      // the pairs' running sums of dr over the steps (db)
+#pragma unroll
+  for (int kp = 0; kp < FUSED_PPT; ++kp)
+#pragma unroll
+    for (int g = 0; g < G; ++g) dbv[kp][g] = 0.0f;
   uint32_t ph0 = 0u, ph1 = 0u;  // phase parity of the two partial-sum barriers
   const int q4 = lane & 3, r8 = lane >> 2;
   // each lane always sends row i = (warp*MT + mt)*16 + r8 (+8 on odd lanes):
@@ -244,9 +246,9 @@ __global__ void __launch_bounds__(256, 1)
           if (write_dr) dro[o + (size_t)g * N * D] = __float2bfloat16_rn(dr[g]);
           drw[b * KB + g * U + u] = __float2bfloat16_rn(dr[g]);
         }
-        if (with_db)  // db: added to the pair's running sum once the partials are sent
+        if (with_db)  // db: the pair's running sum (the pair stays with this thread)
 #pragma unroll
-          for (int g = 0; g < G; ++g) dbv[kp][g] = dr[g];
+          for (int g = 0; g < G; ++g) dbv[kp][g] += dr[g];
 #pragma unroll
         for (int s = 0; s < S; ++s) dsr[kp][s] = dsp[s];
       }
@@ -325,12 +327,6 @@ __global__ void __launch_bounds__(256, 1)
         }
     }
     RNN_TRACE(6)
-    if (with_db)  // db: each pair's running sum (the pair stays with this thread)
-#pragma unroll
-      for (int kp = 0; kp < FUSED_PPT; ++kp)
-        if (tid + kp * nthr < nb * U)
-#pragma unroll
-          for (int g = 0; g < G; ++g) dbs[(g * BC + prow[kp]) * U + punit[kp]] += dbv[kp][g];
     // tape and upstream gradients of step k + NS into the ring slot this
     // step's derivative has finished reading
     if (tid == nthr - 32 && k + FUSED_NS < TT) issue_stage(k + FUSED_NS);
@@ -359,6 +355,12 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
   }
+  if (with_db)
+#pragma unroll
+    for (int kp = 0; kp < FUSED_PPT; ++kp)
+      if (tid + kp * nthr < nb * U)
+#pragma unroll
+        for (int g = 0; g < G; ++g) dbs[(g * BC + prow[kp]) * U + punit[kp]] = dbv[kp][g];
   __syncthreads();
   // db partial of the batch block: the column sums over its rows, in row order
   if (with_db)
