@@ -21,6 +21,7 @@
 #include <cuda.h>
 
 #include "kernels.cuh"
+#include "grid_place.cuh"
 #include "layout.h"
 #include "ptx.cuh"
 
@@ -40,8 +41,14 @@ __global__ void __launch_bounds__(256, 1)
   // variant gathers whole rows, [BC][D + 8] (one block, within the same space)
   const int RS = GRIDX ? D + 8 : UP;
   const int HB = GRIDX ? BC * (D + 8) : C * BC * UP;
-  const uint32_t rank = GRIDX ? (uint32_t)(blockIdx.x % C) : cluster_ctarank();
-  const int grp = blockIdx.x / C;
+  extern __shared__ __align__(128) unsigned char smem[];
+  int2 place = make_int2((int)(blockIdx.x / C), 0);
+  if constexpr (GRIDX) {
+    place = grid_place(a, C, (int*)smem);
+    if (place.x < 0) return;  // a spare CTA of a die-placed launch
+  }
+  const uint32_t rank = GRIDX ? (uint32_t)place.y : cluster_ctarank();
+  const int grp = place.x;
   const int n = grp % N;
   const int b0 = (grp / N) * BC;
   const int nb = min(BC, B - b0);
@@ -57,7 +64,6 @@ __global__ void __launch_bounds__(256, 1)
   const int mg = warp / (GQ * KS), wrem = warp - mg * (GQ * KS);
   const int gq = wrem / KS, ks = wrem - gq * KS;
 
-  extern __shared__ __align__(128) unsigned char smem[];
   const FusedSmem L = FusedSmem::make(G, S, D, U, BC, KS);
   uint64_t* bars = (uint64_t*)(smem + L.bars);  // [0,1]: h full; [2..]: Wx ring
   __nv_bfloat16* wxs = (__nv_bfloat16*)(smem + L.wx);
@@ -122,7 +128,7 @@ __global__ void __launch_bounds__(256, 1)
   // by a fixed stride per step): no index arithmetic inside the time loop
   const int red_sk = G * BC * FUSED_RED_STRIDE;  // red stride of the K slice k2
   constexpr int RED_SG = BC * FUSED_RED_STRIDE;   // red stride of the gate g
-  const int groups = gridDim.x / C;
+  const int groups = N * ((B + BC - 1) / BC);
   const size_t hx_par = (size_t)groups * BC * D;  // grid exchange buffer stride of the step parity
   int red_off[FUSED_PPT], hx_off[FUSED_PPT];
   __nv_bfloat16* st_ptr[FUSED_PPT];
@@ -195,7 +201,7 @@ __global__ void __launch_bounds__(256, 1)
     rbar1 = mapa_shared(full_bar0 + 8, (uint32_t)peer);
   }
 
-  const bool tracer = a.trace && blockIdx.x == 0 && tid == 0;
+  const bool tracer = a.trace && grp == 0 && rank == 0 && tid == 0;
 #define RNN_TRACE(k)                                                                    \
   if (tracer && t >= a.trace_t0 && t < a.trace_t0 + a.trace_steps)                      \
     a.trace[(size_t)(t - a.trace_t0) * 16 + (k)] = (unsigned long long)clock64();
@@ -210,7 +216,7 @@ __global__ void __launch_bounds__(256, 1)
         // step counter and pulls the nb rows from L2 with one bulk copy each;
         // every thread waits for the bytes
         if (tid == 0) {
-          counter_wait_bounded(a.counters + grp, (unsigned)(C * t), a.wait_limit_ns, a.status, failed);
+          counter_wait_bounded(group_counter(a, grp), (unsigned)(C * t), a.wait_limit_ns, a.status, failed);
           if (!failed) {
             const __nv_bfloat16* src = (const __nv_bfloat16*)a.hx + p * hx_par + (size_t)grp * BC * D;
             fence_proxy_async_global();  // the peers' stores, acquired above, before the bulk reads
@@ -235,7 +241,7 @@ __global__ void __launch_bounds__(256, 1)
     // completion; the barrier after the product orders it for every thread
     if (tid == nthr - 1)
       mbar_wait_bounded<false>(wx_bar0 + 8 * ws, (t / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
-    if (t == a.inject_step && blockIdx.x == 0) {
+    if (t == a.inject_step && grp == 0 && rank == 0) {
       // injected fault: a wait that nothing ends runs out and records
       // STATUS_TIMEOUT; the exchange protocol itself is left untouched
       bool inj_failed = false;
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(256, 1)
     // needs every peer's h_{t+1}, which in turn needed this step's copies to
     // have landed (so their reads of stage[p] are over).
     if (GRIDX) {
-      if (t + 1 < TT && tid == 0) counter_publish(a.counters + grp);
+      if (t + 1 < TT && tid == 0) counter_publish(group_counter(a, grp));
     } else if (t + 1 < TT && sender) {  // into the peer's buffer p ^ 1
       bulk_copy_to_peer(p ? rdst0 : rdst1, smem_u32(stage + p * BC * UP), slice_bytes, p ? rbar0 : rbar1);
     }
@@ -453,6 +459,7 @@ cudaError_t fwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream_t st
     if (e != cudaSuccess) return e;
   }
   const int groups = a.N * ((a.B + 8 * sh.NT - 1) / (8 * sh.NT));
+  FusedArgs args = a;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(groups * sh.C);
   cfg.blockDim = dim3(sh.warps * 32);
@@ -468,6 +475,10 @@ cudaError_t fwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream_t st
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (per_sm * sms < groups * sh.C) return cudaErrorCooperativeLaunchTooLarge;
+    // die placement holds one CTA per SM, so that each die's ticket counts
+    // exactly its SMs; otherwise groups by block index
+    if (args.die_of_sm && per_sm == 1 && args.launch_ctas == sms) cfg.gridDim = dim3(sms);
+    else args.die_of_sm = nullptr;
   } else {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = sh.C;
@@ -482,7 +493,7 @@ cudaError_t fwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream_t st
     if (e != cudaSuccess) return e;
     if (clusters < 1) return cudaErrorInvalidConfiguration;
   }
-  e = cudaLaunchKernelEx(&cfg, k, map, a);
+  e = cudaLaunchKernelEx(&cfg, k, map, args);
   note_launch();
   return e;
 }

@@ -18,6 +18,7 @@
 #include <cuda.h>
 
 #include "kernels.cuh"
+#include "grid_place.cuh"
 #include "layout.h"
 #include "ptx.cuh"
 
@@ -31,7 +32,10 @@ __global__ void __launch_bounds__(256, 1)
   constexpr int BC = 8 * NT;
   const int C = a.C, U = a.U, D = a.D, KS = a.KS, TT = a.T, N = a.N, B = a.B;
   const int KG = G * D, KB = KG + 8;
-  const int rank = blockIdx.x % C, grp = blockIdx.x / C, groups = gridDim.x / C;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int2 place = grid_place(a, C, (int*)smem);
+  if (place.x < 0) return;  // a spare CTA of a die-placed launch
+  const int rank = place.y, grp = place.x, groups = N * ((B + BC - 1) / BC);
   const int n = grp % N;
   const int b0 = (grp / N) * BC;
   const int nb = min(BC, B - b0);
@@ -40,7 +44,6 @@ __global__ void __launch_bounds__(256, 1)
   const int warp = tid >> 5, lane = tid & 31;
   const int mg = warp / KS, ks = warp - mg * KS;
 
-  extern __shared__ __align__(128) unsigned char smem[];
   const GridBwdSmem L = GridBwdSmem::make(G, S, K, D, U, BC, KS);
   uint64_t* bars = (uint64_t*)(smem + L.bars);
   unsigned char* ring = smem + L.ring;
@@ -120,7 +123,7 @@ __global__ void __launch_bounds__(256, 1)
 
   bool failed = false;
   float dbv[G];  // the first pair's dr of the step, for db
-  const bool tracer = a.trace && blockIdx.x == 0 && tid == 0;
+  const bool tracer = a.trace && grp == 0 && rank == 0 && tid == 0;
 #define RNN_TRACE(p)                                                                    \
   if (tracer && kk >= a.trace_t0 && kk < a.trace_t0 + a.trace_steps)                    \
     a.trace[(size_t)(kk - a.trace_t0) * 16 + (p)] = (unsigned long long)clock64();
@@ -134,7 +137,7 @@ __global__ void __launch_bounds__(256, 1)
       // of dr (G D bf16 each) with one bulk copy per row; every thread waits
       // for the bytes on the gather barrier
       if (tid == 0) {
-        counter_wait_bounded(a.counters + grp, (unsigned)(C * kk), a.wait_limit_ns, a.status, failed);
+        counter_wait_bounded(group_counter(a, grp), (unsigned)(C * kk), a.wait_limit_ns, a.status, failed);
         if (!failed) {
           const __nv_bfloat16* src = dx + ((size_t)((kk - 1) & 1) * groups + grp) * BC * KG;
           fence_proxy_async_global();  // the peers' stores, acquired above, before the bulk reads
@@ -264,7 +267,7 @@ __global__ void __launch_bounds__(256, 1)
     }
     RNN_TRACE(5)
     __syncthreads();
-    if (tid == 0) counter_publish(a.counters + grp);
+    if (tid == 0) counter_publish(group_counter(a, grp));
     RNN_TRACE(6)
     if (with_db && tid < nb * U)
 #pragma unroll
@@ -319,8 +322,13 @@ cudaError_t grid_bwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (per_sm * sms < groups * sh.C) return cudaErrorCooperativeLaunchTooLarge;
+  FusedArgs args = a;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(groups * sh.C);
+  // die placement holds one CTA per SM, so that each die's ticket counts
+  // exactly its SMs; otherwise groups by block index
+  if (args.die_of_sm && per_sm == 1 && args.launch_ctas == sms) cfg.gridDim = dim3(sms);
+  else args.die_of_sm = nullptr;
   cfg.blockDim = dim3(sh.warps * 32);
   cfg.dynamicSmemBytes = sh.smem;
   cfg.stream = st;
@@ -329,7 +337,7 @@ cudaError_t grid_bwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, k, tmap, dmap, a);
+  e = cudaLaunchKernelEx(&cfg, k, tmap, dmap, args);
   note_launch();
   return e;
 }

@@ -76,6 +76,17 @@ struct WgradArgs {
 size_t wgrad_scratch_bytes(int B, int T, int N, int D, int G, int dtype);
 cudaError_t wgrad_run(int dtype, const WgradArgs& a, cudaStream_t st);
 
+constexpr int FUSED_MAX_GROUP_CTR = 16;  // groups whose counter word FusedArgs::ctr_word places
+
+// One-time measurements of the GPU's two dies (dies.cu): the SM count on
+// each die (false when the device shows no two-die structure or cannot be
+// measured now), the device table of the die of each SM id, and the home
+// die of each 1 KB block of `region` (measured on stream `st` once per
+// address; false while `st` is capturing or when the homes are unclear).
+bool die_counts(int dev, int count[2], int* sms);
+const signed char* die_table_device();
+bool block_homes(int dev, unsigned* region, int nblocks, cudaStream_t st, signed char* home);
+
 // Arguments of the persistent cluster kernels (bf16 storage).
 struct FusedArgs {
   int B, T, N, D, C, U, KS;
@@ -97,9 +108,19 @@ struct FusedArgs {
   unsigned int* status;  // device status word (bounded waits)
   unsigned long long wait_limit_ns;
   // grid mode (cooperative persistent kernel): h exchange buffers
-  // [2][groups][BC][D] and one step counter per group, zeroed before launch
+  // [2][groups][BC][D] and one step counter per group, zeroed before launch;
+  // group g's counter is word ctr_word[g] of `counters` (g < 16), word g above
   void* hx = nullptr;
   unsigned int* counters = nullptr;
+  int ctr_word[16] = {0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15};
+  // die placement (grid mode, optional): with die_of_sm set (the SM-id ->
+  // die table) the launch holds one CTA per SM; groups [die_grp0[d],
+  // die_grp0[d] + die_ngrp[d]) run on die d, a CTA taking its (group, rank)
+  // from ticket d (zeroed before launch), and the spare CTAs leave
+  const signed char* die_of_sm = nullptr;
+  unsigned int* tickets = nullptr;
+  int die_grp0[2] = {0, 0}, die_ngrp[2] = {0, 0};
+  int launch_ctas = 0;  // die placement: CTAs launched (the SM count)
   // optional phase trace (rnn_trace): CTA 0, thread 0 writes clock64() at 8
   // phase points of steps [trace_t0, trace_t0 + trace_steps) (processing order)
   unsigned long long* trace = nullptr;

@@ -268,7 +268,9 @@ bool grid_feasible(const PlanRequest& q, int C, int NT, int KT, const DeviceLimi
     out->fs.smem = smem;
     out->groups = groups;
     out->regs_R = 4 * KT;
-    out->scratch_bytes = align256((size_t)2 * groups * BC * klen * 2) + align256((size_t)groups * 4);
+    // the exchange buffers, then the step counters and die tickets
+    out->scratch_bytes = align256((size_t)2 * groups * BC * klen * 2) +
+                         align256(GRID_CTR_BYTES + (size_t)groups * 4);
     out->model_ns = cyc / 1.9;
   }
   return true;

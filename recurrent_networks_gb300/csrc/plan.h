@@ -9,6 +9,13 @@
 
 namespace rnn {
 
+// The grid kernels' counter region in the workspace: 16 blocks of 1 KB (under
+// die placement a group's counter sits at the start of a block whose L2 home
+// is on the group's die), then one line of die tickets; 1 KB of alignment
+// slack in front.
+constexpr int GRID_CTR_BLOCKS = 16;
+constexpr size_t GRID_CTR_BYTES = (size_t)(GRID_CTR_BLOCKS + 1) * 1024 + 256;
+
 // Limits of the GPU that the constraints use. The defaults are a GB300's
 // (152 SMs, 227 KB of opt-in shared memory per CTA, clusters of up to 16 CTAs
 // with the non-portable size); the library fills them from the current device.
