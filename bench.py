@@ -190,6 +190,17 @@ def kernel_sources_sha(kernel):
     return h.hexdigest()
 
 
+def placement():
+    """How the grid kernels place their batch groups on the GPU's dies."""
+    from recurrent_networks_gb300 import _lib
+    if os.environ.get("RNN_DIE_PLACEMENT", "1").startswith("0"):
+        return "groups by block index (RNN_DIE_PLACEMENT=0)"
+    layout = _lib.rnn_die_layout()
+    if layout is None:
+        return "groups by block index (no two-die structure measured)"
+    return "grid groups on one die each (%d + %d SMs), step counters homed on the group's die" % layout
+
+
 def measured_traffic(kernel, workload, path=None):
     """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
     summary (profiles/traffic.json), or None when absent or when the kernel's
@@ -567,7 +578,7 @@ def main():
               "config": {"workload": w["name"], "function": fn, "B": B, "T": T, "N": N, "D": D,
                          "backward": backward, "plan_fwd": plan_f, "plan_bwd": plan_b,
                          "l2": "flushed (256 MiB write) before every step, outside the event window",
-                         "parallelism": f"replicas x{world}"},
+                         "parallelism": f"replicas x{world}", "placement": placement()},
               "fwd_value": fwd_value, "fwd_ms": fwd_tot / args.steps,
               "warm_l2": {"value": B * T / (warm_ms / 1e3), "ms_per_step": warm_ms, "steps": nwarm,
                           "note": "this rank, steps back to back without the flush"},
@@ -601,7 +612,7 @@ def main():
         pf = dict(kv.split("=") for kv in plan_f.split()[1:] if "=" in kv)
         C, NT, groups = int(pf["C"]), int(pf["NT"]), int(pf["groups"])
         rows = min(B, 8 * NT)
-        scratch = torch.empty(2 * groups * rows * D * 2 + 4096, dtype=torch.uint8, device=dev)
+        scratch = torch.empty(2 * groups * rows * D * 2 + 32768, dtype=torch.uint8, device=dev)
         fl = torch.zeros(2, dtype=torch.int64, device=dev)
         _lib.rnn_exchange_floor_grid(C, groups, rows, D, 2000, scratch, fl)
         torch.cuda.synchronize()
@@ -610,7 +621,8 @@ def main():
         fl_ns = cyc / mhz * 1e3
         result["latency_floor"] = {
             "what": f"h exchange alone through L2: {groups} groups of {C} CTAs, {rows} rows of {D} bf16 pulled per "
-                    f"step after a release/acquire step counter",
+                    f"step after a release/acquire step counter; CTAs placed as the grid kernels place theirs "
+                    f"({placement()})",
             "cycles_per_step": cyc, "ns_per_step": fl_ns, "status": st_fl,
             "fwd_step_over_floor": (f_ms * 1e6 / T) / fl_ns if fl_ns > 0 else None}
 

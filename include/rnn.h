@@ -197,6 +197,24 @@ int rnn_plan_describe(const rnn_dims_t *dims, int for_backward, char *buf, size_
  * one fail. Returns RNN_OK or RNN_EINVAL. */
 int rnn_plan_set_limits(int sms, int smem_per_cta, int max_cluster);
 
+/* The GPU's two dies as the grid kernels see them (no counterpart in the
+ * pages: a placement aid of this implementation). A GB300 is two dies, each
+ * with its own L2; the cooperative grid kernels put each batch group's CTAs
+ * on one die and the group's step counter in a 1 KB block of the workspace
+ * whose L2 home is on that die, which keeps the per-step exchange's L2 round
+ * trips on the die. The SM-to-die map is measured once per device with L2
+ * flag round trips (about 15 ms, on an internal stream, at the first grid
+ * launch or here), and the home die of the workspace's counter blocks once
+ * per workspace address on the caller's stream (a host synchronisation; a
+ * stream that is capturing skips it, and that launch groups CTAs by block
+ * index). Writes the number of SMs on each die (die 0 holds the SM of the
+ * measurement's first CTA) and returns RNN_OK, or RNN_EUNSUPPORTED when the
+ * current device shows no two-die structure or cannot be measured (grid
+ * kernels then group CTAs by block index). RNN_DIE_PLACEMENT=0 in the
+ * environment turns the placement off for later launches. Either pointer may
+ * be NULL. */
+int rnn_die_layout(int *sms_die0, int *sms_die1);
+
 const char *rnn_strerror(int status);
 
 /* Number of CUDA kernels this library has enqueued since it was loaded
@@ -289,10 +307,13 @@ int rnn_exchange_floor(int C, int slice_bytes, int steps, void *out, void *strea
  * acquire wait on the counter (bounded, 2 s) and the pull of the group's rows
  * from L2 with one bulk copy per row, for `steps` (2 .. 1e6) steps. C >= 1,
  * groups >= 1, rows 1 .. 32, D 8 .. 4096 with D % 8 == 0 and D % C == 0.
+ * The CTAs are placed as the grid kernels place theirs (each group on one die
+ * with its counter homed there, see rnn_die_layout), or by block index.
  * scratch: device memory owned by the caller, 256-byte aligned, of at least
- * 2*groups*rows*D*2 bytes rounded up to 256, plus 256 + 4*groups bytes (the
- * exchange buffers and counters). Writes to out[0] the clock64 cycles per step
- * seen by CTA 0 and to out[1] the status (0 = ok, 1 = a wait ran out).
+ * 2*groups*rows*D*2 bytes rounded up to 256, plus 17664 bytes (the exchange
+ * buffers, then a 1 KB-aligned region of 16 KB of counter blocks and the die
+ * tickets). Writes to out[0] the clock64 cycles per step seen by the first
+ * CTA of group 0 and to out[1] the status (0 = ok, 1 = a wait ran out).
  * Asynchronous on `stream`. Returns RNN_OK, RNN_EINVAL, RNN_ENOSPC,
  * RNN_EUNSUPPORTED (the CTAs cannot all be resident) or RNN_ECUDA. */
 int rnn_exchange_floor_grid(int C, int groups, int rows, int D, int steps, void *scratch, size_t scratch_bytes,

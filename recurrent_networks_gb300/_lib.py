@@ -21,7 +21,7 @@ WS_FWD, WS_BWD, WS_BWD_RECOMPUTE = 0, 1, 2
 EXPORTS = ["rnn_num_gates", "rnn_num_states", "rnn_tape_size", "rnn_workspace_size", "rnn_fwd",
            "rnn_bwd", "rnn_check_status", "rnn_plan_describe", "rnn_strerror", "rnn_kernel_launches",
            "rnn_profile_events", "rnn_bwd_noalloc", "rnn_bwd_noalloc_status", "rnn_trace",
-           "rnn_debug_inject_wait", "rnn_plan_set_limits"]
+           "rnn_debug_inject_wait", "rnn_plan_set_limits", "rnn_die_layout"]
 
 
 class RnnError(RuntimeError):
@@ -58,6 +58,7 @@ def load(path: str | None = None):
             lib.rnn_check_status.argtypes = [vp, vp]
             lib.rnn_plan_describe.argtypes = [dp, i, ctypes.c_char_p, sz]
             lib.rnn_plan_set_limits.argtypes = [i, i, i]
+            lib.rnn_die_layout.argtypes = [ctypes.POINTER(i), ctypes.POINTER(i)]
             lib.rnn_strerror.argtypes = [i]
             lib.rnn_strerror.restype = ctypes.c_char_p
             lib.rnn_kernel_launches.argtypes = []
@@ -150,6 +151,17 @@ def rnn_plan_set_limits(sms: int = 0, smem_per_cta: int = 227 * 1024, max_cluste
     """Plan for a stated device (sms > 0) or the current one (sms <= 0)."""
     return _check(load().rnn_plan_set_limits(int(sms), int(smem_per_cta), int(max_cluster)),
                   "rnn_plan_set_limits")
+
+
+def rnn_die_layout():
+    """(SMs on die 0, SMs on die 1) as the grid kernels place their groups, or
+    None when the device shows no two-die structure (see include/rnn.h)."""
+    a, b = ctypes.c_int(0), ctypes.c_int(0)
+    rc = load().rnn_die_layout(ctypes.byref(a), ctypes.byref(b))
+    if rc == RNN_EUNSUPPORTED:
+        return None
+    _check(rc, "rnn_die_layout")
+    return a.value, b.value
 
 
 def rnn_strerror(status: int) -> str:

@@ -282,42 +282,18 @@ static size_t grid_counter_bytes(const Plan& plan) {
 // die of the GPU and its step counter in a block homed on that die, so that
 // the exchange's L2 round trips stay on the die (about 1750 cycles each
 // instead of about 3000 when a leg crosses). Off (groups by block index) when
-// the dies cannot be measured, a group does not fit a die, the stream is
-// capturing before the counter region was measured, or RNN_DIE_PLACEMENT=0.
+// die_plan declines.
 static void grid_die_setup(const Plan& plan, cudaStream_t st, FusedArgs* f) {
-  const char* env = getenv("RNN_DIE_PLACEMENT");
-  const bool off = env && env[0] == '0';
-  const int groups = plan.groups, C = plan.fs.C;
-  if (off || groups > FUSED_MAX_GROUP_CTR || groups > GRID_CTR_BLOCKS) return;
-  int dev = 0, cnt[2] = {0, 0}, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || !die_counts(dev, cnt, &sms)) return;
-  // the split of the groups over the two dies closest to even that fits
-  int g0 = -1;
-  for (int k = 0; k <= groups; ++k)
-    if (k * C <= cnt[0] && (groups - k) * C <= cnt[1] && (g0 < 0 || abs(2 * k - groups) < abs(2 * g0 - groups))) g0 = k;
-  if (g0 < 0) return;
-  signed char home[GRID_CTR_BLOCKS];
-  if (!block_homes(dev, f->counters, GRID_CTR_BLOCKS, st, home)) return;
-  bool used[GRID_CTR_BLOCKS] = {};
-  int word[FUSED_MAX_GROUP_CTR];
-  for (int g = 0; g < groups; ++g) {
-    const int d = g < g0 ? 0 : 1;
-    int k = 0;
-    while (k < GRID_CTR_BLOCKS && (used[k] || home[k] != d)) ++k;
-    if (k == GRID_CTR_BLOCKS) return;  // no free block homed on that die
-    used[k] = true;
-    word[g] = k * 256;
-  }
-  const signed char* table = die_table_device();
-  if (!table) return;
-  for (int g = 0; g < groups; ++g) f->ctr_word[g] = word[g];
-  f->die_of_sm = table;
+  DiePlan p;
+  if (!die_plan(plan.groups, plan.fs.C, f->counters, st, &p)) return;
+  for (int g = 0; g < plan.groups; ++g) f->ctr_word[g] = p.ctr_word[g];
+  f->die_of_sm = p.table;
   f->tickets = f->counters + GRID_CTR_BLOCKS * 256;
-  f->die_grp0[0] = 0;
-  f->die_ngrp[0] = g0;
-  f->die_grp0[1] = g0;
-  f->die_ngrp[1] = groups - g0;
-  f->launch_ctas = sms;
+  for (int d = 0; d < 2; ++d) {
+    f->die_grp0[d] = p.grp0[d];
+    f->die_ngrp[d] = p.ngrp[d];
+  }
+  f->launch_ctas = p.sms;
 }
 
 // Alternating path scratch inside the workspace: the bf16 ping-pong buffer,
@@ -597,6 +573,15 @@ int rnn_check_status(void* workspace, void* stream) {
     if (e != cudaSuccess) return cuda_status(e);
     return RNN_ETIMEOUT;
   }
+  return RNN_OK;
+}
+
+int rnn_die_layout(int* sms_die0, int* sms_die1) {
+  int dev = 0, cnt[2] = {0, 0}, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RNN_ECUDA;
+  if (!die_counts(dev, cnt, &sms)) return RNN_EUNSUPPORTED;
+  if (sms_die0) *sms_die0 = cnt[0];
+  if (sms_die1) *sms_die1 = cnt[1];
   return RNN_OK;
 }
 

@@ -17,6 +17,7 @@
 // its step counter homed there (api.cu). Every wait is bounded; a timed-out
 // or ambiguous measurement leaves die placement off.
 #include <cuda_runtime.h>
+#include <stdlib.h>
 
 #include <map>
 #include <mutex>
@@ -24,6 +25,7 @@
 #include <vector>
 
 #include "kernels.cuh"
+#include "plan.h"
 #include "ptx.cuh"
 
 namespace rnn {
@@ -285,6 +287,39 @@ bool block_homes(int dev, unsigned* region, int nblocks, cudaStream_t st, signed
     if (it->second[k] < 0) return false;
     home[k] = it->second[k];
   }
+  return true;
+}
+
+bool die_plan(int groups, int C, unsigned* ctr_region, cudaStream_t st, DiePlan* out) {
+  const char* env = getenv("RNN_DIE_PLACEMENT");
+  if ((env && env[0] == '0') || groups < 1 || groups > FUSED_MAX_GROUP_CTR || groups > GRID_CTR_BLOCKS) return false;
+  int dev = 0, cnt[2] = {0, 0}, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || !die_counts(dev, cnt, &sms)) return false;
+  // the split of the groups over the two dies closest to even that fits
+  int g0 = -1;
+  for (int k = 0; k <= groups; ++k)
+    if (k * C <= cnt[0] && (groups - k) * C <= cnt[1] && (g0 < 0 || abs(2 * k - groups) < abs(2 * g0 - groups))) g0 = k;
+  if (g0 < 0) return false;
+  signed char home[GRID_CTR_BLOCKS];
+  if (!block_homes(dev, ctr_region, GRID_CTR_BLOCKS, st, home)) return false;
+  bool used[GRID_CTR_BLOCKS] = {};
+  DiePlan p;
+  for (int g = 0; g < groups; ++g) {
+    const int d = g < g0 ? 0 : 1;
+    int k = 0;
+    while (k < GRID_CTR_BLOCKS && (used[k] || home[k] != d)) ++k;
+    if (k == GRID_CTR_BLOCKS) return false;  // no free block homed on that die
+    used[k] = true;
+    p.ctr_word[g] = k * 256;
+  }
+  p.table = die_table_device();
+  if (!p.table) return false;
+  p.grp0[0] = 0;
+  p.ngrp[0] = g0;
+  p.grp0[1] = g0;
+  p.ngrp[1] = groups - g0;
+  p.sms = sms;
+  *out = p;
   return true;
 }
 

@@ -7,7 +7,9 @@
 // rank + w + q warps, with the cluster addresses computed once.
 #include <stdio.h>
 
+#include "grid_place.cuh"
 #include "kernels.cuh"
+#include "plan.h"
 #include "ptx.cuh"
 #include "rnn.h"
 
@@ -80,10 +82,14 @@ __global__ void __launch_bounds__(256, 1) exchange_floor_kernel(int slice_bytes,
 // with one bulk copy per row; every thread waits for the bytes. Then every
 // CTA stores its U = D / C units of h_t for each row (2-byte stores, as the
 // cell does), a CTA barrier, and one release increment of the counter.
-__global__ void __launch_bounds__(256, 1) grid_floor_kernel(int C, int D, int rows, int steps, unsigned short* hx,
-                                                          unsigned int* counters, unsigned long long* out) {
+__global__ void __launch_bounds__(256, 1) grid_floor_kernel(int D, int rows, int steps, int groups, unsigned short* hx,
+                                                          FusedArgs pl, unsigned long long* out) {
   extern __shared__ __align__(128) unsigned char gf_smem[];
-  const int U = D / C, grp = blockIdx.x / C, r = blockIdx.x % C, groups = gridDim.x / C;
+  const int C = pl.C;
+  const int2 place = grid_place(pl, C, (int*)gf_smem);  // as the grid kernels place their CTAs
+  if (place.x < 0) return;
+  const int U = D / C, grp = place.x, r = place.y;
+  unsigned int* ctr = group_counter(pl, grp);
   const int tid = threadIdx.x;
   uint64_t* bar = (uint64_t*)gf_smem;
   unsigned short* hbuf = (unsigned short*)(gf_smem + 128);  // [rows][D + 8]
@@ -103,7 +109,7 @@ __global__ void __launch_bounds__(256, 1) grid_floor_kernel(int C, int D, int ro
     const int p = t & 1;
     if (t > 0) {
       if (tid == 0) {
-        counter_wait_bounded(counters + grp, (unsigned)(C * t), limit, status, failed);
+        counter_wait_bounded(ctr, (unsigned)(C * t), limit, status, failed);
         if (!failed) {
           const unsigned short* src = hx + ((size_t)(p * groups + grp) * rows) * D;
           fence_proxy_async_global();
@@ -125,10 +131,10 @@ __global__ void __launch_bounds__(256, 1) grid_floor_kernel(int C, int D, int ro
       }
     }
     __syncthreads();
-    if (t + 1 < steps && tid == 0) counter_publish(counters + grp);
+    if (t + 1 < steps && tid == 0) counter_publish(ctr);
   }
   const long long t1 = clock64();
-  if (blockIdx.x == 0 && tid == 0) out[0] = (unsigned long long)((t1 - t0) / steps) + (x == 0xffffffffu);
+  if (grp == 0 && r == 0 && tid == 0) out[0] = (unsigned long long)((t1 - t0) / steps) + (x == 0xffffffffu);
 }
 
 }  // namespace
@@ -143,15 +149,30 @@ extern "C" int rnn_exchange_floor_grid(int C, int groups, int rows, int D, int s
       steps > 1000000 || !scratch || ((uintptr_t)scratch & 255u) || !out || ((uintptr_t)out & 7u))
     return RNN_EINVAL;
   const size_t hx_bytes = ((size_t)2 * groups * rows * D * 2 + 255) & ~(size_t)255;
-  if (scratch_bytes < hx_bytes + 256 + (size_t)groups * 4) return RNN_ENOSPC;
+  if (scratch_bytes < hx_bytes + GRID_CTR_BYTES) return RNN_ENOSPC;
   cudaStream_t st = (cudaStream_t)stream;
   unsigned short* hx = (unsigned short*)scratch;
-  unsigned int* counters = (unsigned int*)((char*)scratch + hx_bytes);
+  FusedArgs pl{};
+  pl.C = C;
+  pl.counters = (unsigned int*)(((uintptr_t)scratch + hx_bytes + 1023) & ~(uintptr_t)1023);
+  // the grid kernels' die placement, when they would use it
+  DiePlan dp;
+  const bool die = die_plan(groups, C, pl.counters, st, &dp);
+  if (die) {
+    for (int g = 0; g < groups; ++g) pl.ctr_word[g] = dp.ctr_word[g];
+    pl.die_of_sm = dp.table;
+    pl.tickets = pl.counters + GRID_CTR_BLOCKS * 256;
+    for (int d = 0; d < 2; ++d) {
+      pl.die_grp0[d] = dp.grp0[d];
+      pl.die_ngrp[d] = dp.ngrp[d];
+    }
+  }
   // at least as much shared memory as the forward grid kernel, so one CTA runs per SM
   size_t smem = 128 + (size_t)rows * (D + 8) * 2;
   if (smem < 100 * 1024) smem = 100 * 1024;
+  const size_t ctr_bytes = (groups > GRID_CTR_BLOCKS * 256 ? (size_t)groups : (size_t)GRID_CTR_BLOCKS * 256) * 4 + 256;
   cudaError_t e = cudaMemsetAsync(out, 0, 16, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(counters, 0, (size_t)groups * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(pl.counters, 0, ctr_bytes, st);
   if (e == cudaSuccess) e = set_smem_attr((const void*)grid_floor_kernel, smem);
   int per_sm = 0;
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, grid_floor_kernel, 256, smem);
@@ -159,6 +180,8 @@ extern "C" int rnn_exchange_floor_grid(int C, int groups, int rows, int D, int s
   if (e == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(groups * C);
+    if (die && per_sm == 1 && dp.sms == device_sms()) cfg.gridDim = dim3(dp.sms);
+    else pl.die_of_sm = nullptr;
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -167,7 +190,7 @@ extern "C" int rnn_exchange_floor_grid(int C, int groups, int rows, int D, int s
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, grid_floor_kernel, C, D, rows, steps, hx, counters, (unsigned long long*)out);
+    e = cudaLaunchKernelEx(&cfg, grid_floor_kernel, D, rows, steps, groups, hx, pl, (unsigned long long*)out);
     note_launch();
   }
   if (e != cudaSuccess) {

@@ -86,6 +86,20 @@ constexpr int FUSED_MAX_GROUP_CTR = 16;  // groups whose counter word FusedArgs:
 bool die_counts(int dev, int count[2], int* sms);
 const signed char* die_table_device();
 bool block_homes(int dev, unsigned* region, int nblocks, cudaStream_t st, signed char* home);
+// Die placement of `groups` groups of C CTAs whose step counters live in the
+// 16 1 KB blocks of `ctr_region` (1 KB aligned): groups [0, ngrp[0]) on die
+// 0, the rest on die 1, the split closest to even that fits each die; each
+// group's counter at the start of a block homed on its die (word ctr_word[g]
+// of the region); launched as one CTA per SM (sms). False (block-index
+// placement) when RNN_DIE_PLACEMENT=0, the dies or the homes cannot be
+// measured, or the groups do not fit.
+struct DiePlan {
+  const signed char* table = nullptr;
+  int grp0[2] = {0, 0}, ngrp[2] = {0, 0};
+  int ctr_word[16] = {};
+  int sms = 0;
+};
+bool die_plan(int groups, int C, unsigned* ctr_region, cudaStream_t st, DiePlan* out);
 
 // Arguments of the persistent cluster kernels (bf16 storage).
 struct FusedArgs {

@@ -74,7 +74,7 @@ def test_grid_exchange_floor_runs_and_reports():
     of 64 CTAs pulling 16 rows of 1024 units take longer per step than one
     group of 16 CTAs pulling 8 rows of 256."""
     out = torch.zeros(2, dtype=torch.int64, device="cuda")
-    scratch = torch.empty(2 * 2 * 16 * 1024 * 2 + 4096, dtype=torch.uint8, device="cuda")
+    scratch = torch.empty(2 * 2 * 16 * 1024 * 2 + 32768, dtype=torch.uint8, device="cuda")
     cyc = {}
     for C, groups, rows, D in ((16, 1, 8, 256), (64, 2, 16, 1024)):
         _lib.rnn_exchange_floor_grid(C, groups, rows, D, 500, scratch, out)

@@ -252,6 +252,30 @@ def test_grid_parity(case, monkeypatch):
     check_grads(fn, inp, (dWx, dR, db, ds0), dlast=dl)
 
 
+def test_grid_die_placement_changes_nothing(monkeypatch):
+    """The grid kernels' die placement (each batch group's CTAs on one die of
+    the GPU, its step counter homed in L2 there) only moves CTAs between SMs:
+    states and gradients are bitwise those of the block-index placement, and
+    both match the oracle."""
+    layout = _lib.rnn_die_layout()
+    if layout is None:
+        pytest.skip("the device shows no two-die structure")
+    assert min(layout) > 0 and sum(layout) == torch.cuda.get_device_properties(0).multi_processor_count
+    _restrict(monkeypatch, dict(C=32, NT=2))
+    fn, B, T, N, D = "lstm", 20, 33, 2, 512  # 2 heads x 2 batch blocks: 4 groups of 32 CTAs
+    inp = _inputs(fn, (B, T, N, D), torch.bfloat16, seed=4242)
+    outs = {}
+    for mode in ("1", "0"):
+        monkeypatch.setenv("RNN_DIE_PLACEMENT", mode)
+        st, last, tape = run_fwd(fn, inp, "grid")
+        outs[mode] = (st, last) + tuple(run_bwd(fn, inp, st, tape, "grid"))
+    for name, a, b in zip(("states", "last", "dWx", "dR", "db", "dstates0"), outs["1"], outs["0"]):
+        assert torch.equal(a, b), f"{name} differs between the die and the block-index placement"
+    ref_st, _ = oracle_fwd(fn, inp)
+    check_states(fn, torch.bfloat16, outs["1"][0], ref_st)
+    check_grads(fn, inp, outs["1"][2:])
+
+
 def test_grid_reuses_its_workspace(monkeypatch):
     """Two grid forward + backward runs of different lengths on one workspace:
     the second must not see the first's step counters or exchange rows."""
