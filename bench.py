@@ -121,9 +121,9 @@ def proj_bench(args, w, fn, dev, _lib):
 def phase_trace(step_fn, backward, T):
     """Median clock64 cycles between the phase points of the persistent
     kernels (CTA 0, thread 0), over up to 200 steps after the first 10.
-    Points 8-11 of the forward kernels lie inside phases: 8 the cell's inputs
-    summed, 9 the cell computed, 10 h staged or stored, 11 the states and tape
-    stores issued."""
+    Point 11 of the forward kernels (the states and tape stores issued) is
+    reported against point 7; points 8-10 (inside the cell) are reported when
+    a kernel build records them."""
     from recurrent_networks_gb300 import _lib
     steps = max(1, min(200, T - 20))
     buf = torch.zeros(16 * steps, dtype=torch.int64, device="cuda")

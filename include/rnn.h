@@ -235,10 +235,9 @@ int rnn_profile_events(int which, void *before, void *after);
  * up to sixteen phase points of the steps [t0, t0 + steps) of their processing order
  * (the backward processes t = T-1 first). Forward phases: 0 step start,
  * 1 h_{t-1} available, 2 partial products written, 3 after the CTA barrier,
- * 4 Wx[t] staged, 5 cell update done, 6 after the CTA barrier, 7 h_t sent;
- * inside phase 4-5: 8 the cell's inputs summed, 9 the cell computed, 10 h
- * staged (cluster) or stored to L2 (grid); 11 the states and tape stores
- * issued.
+ * 4 Wx[t] staged, 5 cell update done, 6 after the CTA barrier, 7 h_t sent,
+ * 11 the states and tape stores issued (points 8-10 are not recorded: inside
+ * the cell's loop they cost up to a tenth of the forward step).
  * Cluster backward phases: 0 step start, 1 partial dh available, 2 tape
  * staged, 3 cell derivative done, 4 after the CTA barrier, 5 partial products
  * computed, 6 partials sent. Grid backward phases: 0 step start, 1 step

@@ -347,9 +347,7 @@ __global__ void __launch_bounds__(256, 1)
         rc[g] = v;
         x[g] = __bfloat162float(wxt[(pb[kp] * G + g) * U + u]);
       }
-      if (kp == 0) RNN_TRACE(8)
       cell_fwd<FN, true>(x, rc, csr[kp], sn, pre);
-      if (kp == 0) RNN_TRACE(9)
 #pragma unroll
       for (int s = 0; s < S; ++s) csr[kp][s] = sn[s];
 #pragma unroll
@@ -360,7 +358,6 @@ __global__ void __launch_bounds__(256, 1)
       } else {
         stage[(p * BC + pb[kp]) * UP + u] = __float2bfloat16_rn(sn[0]);
       }
-      if (kp == 0) RNN_TRACE(10)
     }
     RNN_TRACE(5)
     if constexpr (!GRIDX) fence_proxy_async_smem();  // the staged slice is read by bulk copies
