@@ -94,21 +94,13 @@ __global__ void __launch_bounds__(256, 1)
   // and their (row, unit) coordinates, divided once here rather than every step
   float dsr[FUSED_PPT][S];
   int prow[FUSED_PPT], punit[FUSED_PPT];
-  // and, fixed for the kernel, the offset of their received partial sums
-  // (peer 0) in a receive buffer and of their gradients in dWx / dr at t = 0
-  int rv_off[FUSED_PPT];
-  size_t o_first[FUSED_PPT];
-  const size_t o_step = (size_t)G * N * D;
 #pragma unroll
   for (int k = 0; k < FUSED_PPT; ++k) {
     prow[k] = (tid + k * nthr) / U;
     punit[k] = tid + k * nthr - prow[k] * U;
-    rv_off[k] = punit[k] * BC + (prow[k] ^ (4 * swz(punit[k])));
-    o_first[k] = ((size_t)(b0 + prow[k]) * TT * G) * N * D + (size_t)n * D + u0 + punit[k];
 #pragma unroll
     for (int s = 0; s < S; ++s) dsr[k][s] = 0.0f;
   }
-  const int rv_sc = U * BC;  // receive-buffer stride of the peer
   // resident R fragments: A[m = row i][k = (g, j)] = R[g, n, i, u0 + j]
   uint32_t afr[MT][KTM][4];
   {
@@ -230,16 +222,16 @@ __global__ void __launch_bounds__(256, 1)
         float dx[G], dr[G], dsp[S];
         if (t < TT - 1) {  // the C partial sums, loaded together
           float part[FUSED_MAX_C];
-          const float* rp = rv + rv_off[kp];
+          const int bs = b ^ (4 * swz(u));
 #pragma unroll
-          for (int c = 0; c < FUSED_MAX_C; ++c) part[c] = c < C ? rp[c * rv_sc] : 0.0f;
+          for (int c = 0; c < FUSED_MAX_C; ++c) part[c] = c < C ? rv[(c * U + u) * BC + bs] : 0.0f;
           float acc = 0.0f;
 #pragma unroll
           for (int c = 0; c < FUSED_MAX_C; ++c) acc += part[c];
           dsn[kp][0] += acc;
         }
         cell_bwd_grad<FN, true>(act[kp], pre[kp], sp[kp], dsn[kp], dx, dr, dsp);
-        const size_t o = o_first[kp] + (size_t)t * o_step;
+        const size_t o = (((size_t)(b0 + b) * TT + t) * G) * N * D + (size_t)n * D + u0 + u;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           if (dWx) dWx[o + (size_t)g * N * D] = __float2bfloat16_rn(dx[g]);
