@@ -272,7 +272,28 @@ __global__ void __launch_bounds__(256) wgrad_mma_kernel(WgradArgs a, int splits,
 // Sums the split-K partials in order and rounds to bf16.
 __global__ void wgrad_reduce_kernel(WgradArgs a, int splits) {
   const size_t total = (size_t)a.G * a.N * a.D * a.D;
-  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  const size_t first = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (total % 4 == 0) {  // four elements per thread: 16-byte loads of every partial, all in flight
+    const size_t quads = total / 4;
+    const float4* p = (const float4*)a.scratch;
+    for (size_t e = first; e < quads; e += stride) {
+      float4 s = p[e];
+      for (int k = 1; k < splits; ++k) {
+        const float4 v = p[(size_t)k * quads + e];
+        s.x += v.x;
+        s.y += v.y;
+        s.z += v.z;
+        s.w += v.w;
+      }
+      uint2 o;
+      o.x = pack_bf16(__float2bfloat16_rn(s.x), __float2bfloat16_rn(s.y));
+      o.y = pack_bf16(__float2bfloat16_rn(s.z), __float2bfloat16_rn(s.w));
+      ((uint2*)a.dR)[e] = o;
+    }
+    return;
+  }
+  for (size_t e = first; e < total; e += stride) {
     float s = 0.0f;
     for (int k = 0; k < splits; ++k) s += a.scratch[(size_t)k * total + e];
     ((__nv_bfloat16*)a.dR)[e] = __float2bfloat16_rn(s);
