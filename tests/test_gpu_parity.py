@@ -276,6 +276,51 @@ def test_grid_die_placement_changes_nothing(monkeypatch):
     check_grads(fn, inp, outs["1"][2:])
 
 
+def test_grid_path_in_a_cuda_graph(monkeypatch):
+    """A forward and backward on the grid kernels captured into a CUDA graph
+    and replayed give the eager results bit for bit: with the workspace's
+    counter blocks measured before the capture (die placement inside the
+    graph), and with a fresh workspace, whose capture skips the measurement
+    (groups by block index)."""
+    _restrict(monkeypatch, dict(C=32, NT=2))
+    fn, B, T, N, D = "lstm", 20, 17, 2, 512
+    inp = _inputs(fn, (B, T, N, D), torch.bfloat16, seed=4343)
+    dims = _lib.make_dims(B, T, N, D, fn, torch.bfloat16, "grid")
+    S = _lib.rnn_num_states(fn)
+
+    def buffers():
+        return dict(states=torch.empty((S, B, T, N, D), dtype=torch.bfloat16, device="cuda"),
+                    last=torch.empty((S, B, 1, N, D), dtype=torch.bfloat16, device="cuda"),
+                    tape=torch.empty(_lib.rnn_tape_size(dims), dtype=torch.uint8, device="cuda"),
+                    ws=torch.empty(_lib.rnn_workspace_size(dims, _lib.WS_BWD), dtype=torch.uint8, device="cuda"),
+                    dWx=torch.empty_like(inp["Wx"]), dR=torch.empty_like(inp["R"]),
+                    db=torch.empty_like(inp["b"]), ds0=torch.empty_like(inp["states0"]))
+
+    def step(o):
+        _lib.rnn_fwd(dims, inp["Wx"], inp["R"], inp["b"], inp["states0"], o["states"], o["last"], o["tape"], o["ws"])
+        _lib.rnn_bwd(dims, inp["Wx"], inp["R"], inp["b"], inp["states0"], o["states"], o["tape"], inp["dstates"],
+                     None, o["dWx"], o["dR"], o["db"], o["ds0"], o["ws"])
+
+    names = ("states", "last", "dWx", "dR", "db", "ds0")
+    eager = buffers()
+    step(eager)
+    torch.cuda.synchronize()
+    _lib.rnn_check_status(eager["ws"])
+    for fresh in (False, True):
+        o = buffers() if fresh else eager
+        ref = {k: eager[k].clone() for k in names}
+        for k in names:
+            o[k].fill_(float("nan"))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(o)
+        g.replay()
+        torch.cuda.synchronize()
+        _lib.rnn_check_status(o["ws"])
+        for k in names:
+            assert torch.equal(o[k], ref[k]), f"{k} differs after replay (fresh workspace: {fresh})"
+
+
 def test_grid_reuses_its_workspace(monkeypatch):
     """Two grid forward + backward runs of different lengths on one workspace:
     the second must not see the first's step counters or exchange rows."""
