@@ -14,6 +14,7 @@
 
 #include "kernels.cuh"
 #include "plan.h"
+#include "umma.cuh"
 #include "rnn.h"
 
 namespace rnn {
@@ -207,7 +208,13 @@ static WsLayout ws_layout(const rnn_dims_t* d, int kind, const Plan& plan) {
   w.dbp = off;  // [ceil(B / 8) batch blocks][G][N][D] fp32: enough for any block height
   if (kind != RNN_WS_FWD) off += align256((size_t)((d->B + 7) / 8) * z.bias * sizeof(float));
   w.wg = off;
-  if (kind != RNN_WS_FWD) off += align256(wgrad_scratch_bytes(d->B, d->T, d->N, d->D, z.G, d->dtype));
+  if (kind != RNN_WS_FWD) {
+    size_t wg = wgrad_scratch_bytes(d->B, d->T, d->N, d->D, z.G, d->dtype);
+    // dR beside the grid backward: one fp32 partial per chunk
+    const size_t beside = d->dtype == RNN_BF16 && d->D % 64 == 0 && d->D >= 256
+                              ? (size_t)DR_BESIDE_CHUNKS * z.r * sizeof(float) : 0;
+    off += align256(wg > beside ? wg : beside);
+  }
   w.tape = off;
   if (kind == RNN_WS_BWD_RECOMPUTE) off += align256(z.tape);
   w.total = off;
@@ -294,6 +301,44 @@ static void grid_die_setup(const Plan& plan, cudaStream_t st, FusedArgs* f) {
     f->die_ngrp[d] = p.ngrp[d];
   }
   f->launch_ctas = p.sms;
+}
+
+// dR beside the grid backward (dr_beside.cuh): the launch's spare CTAs take
+// the tiles of chunks of steps the scan has finished, so that after the scan
+// only the sum of the chunks' partials is left. Chunks of 64-step tiles in
+// the scan's order, shrinking toward t = 0 (6 : 4 : 3 : 2 : 1), so that the
+// chunk still open when the scan ends is short. Off when RNN_DR_BESIDE=0,
+// for fp32, D not a multiple of 64 or under 256, fewer than 16 tiles of
+// steps, fewer than 8 spare SMs, or a workspace without room.
+static bool dr_beside_setup(const rnn_dims_t* d, const Plan& plan, const Sizes& z, const void* states,
+                            const void* states0, void* drbuf, void* dR, char* slots, size_t slot_bytes,
+                            FusedArgs* f, UmmaMaps* dm) {
+  const char* env = getenv("RNN_DR_BESIDE");
+  if ((env && env[0] == '0') || !dR || d->dtype != RNN_BF16 || d->D % 64 || d->D < 256) return false;
+  const int nt = (d->T + UM_BK - 1) / UM_BK;
+  if (nt < 16 || plan.groups * plan.fs.C + 8 > device_sms()) return false;
+  if ((size_t)DR_BESIDE_CHUNKS * z.r * sizeof(float) > slot_bytes) return false;
+  static const int weight[DR_BESIDE_CHUNKS] = {6, 4, 3, 2, 1};
+  int left = nt, hi = nt;
+  for (int c = 0; c < DR_BESIDE_CHUNKS; ++c) {
+    int n = c + 1 < DR_BESIDE_CHUNKS ? (nt * weight[c] + 8) / 16 : left;
+    if (n < 1) n = 1;
+    if (n > left - (DR_BESIDE_CHUNKS - 1 - c)) n = left - (DR_BESIDE_CHUNKS - 1 - c);
+    f->drw.tt_n[c] = n;
+    f->drw.tt_lo[c] = hi - n;
+    hi -= n;
+    left -= n;
+  }
+  WgradArgs wa{d->B, d->T, d->N, d->D, z.G, states, states0, drbuf, dR, nullptr};
+  if (umma_encode_maps(wa, 256, true, dm) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  f->drw.nc = DR_BESIDE_CHUNKS;
+  f->drw.s0_tiles = states0 ? (d->B + UM_BK - 1) / UM_BK : 0;
+  f->drw.slots = (float*)slots;
+  f->drw.next = f->counters + GRID_CTR_BLOCKS * 256 + 32;  // in the tickets' line, zeroed with the counters
+  return true;
 }
 
 // Alternating path scratch inside the workspace: the bf16 ping-pong buffer,
@@ -488,6 +533,7 @@ int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
   a.dstates = dstates; a.dlast = dlast; a.dWx = dWx; a.dr = drbuf; a.ds0 = dstates0;
   rc = RNN_EUNSUPPORTED;
   int dbp_blocks = 0;  // > 0: the scan kernel left db partials at ws + w.dbp
+  int dr_parts = 0;    // > 0: the scan kernel left dR as that many fp32 partials at ws + w.wg
   prof_mark(1, 0, st);
   switch (plan.path) {
     case RNN_PATH_SIMT:
@@ -529,8 +575,20 @@ int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
       with_trace(&f);
       grid_scratch(d, plan, ws, true, &f);
       grid_die_setup(plan, st, &f);
+      UmmaMaps dm;
+      bool beside = dr_beside_setup(d, plan, z, states, states0, drbuf, dR, ws + w.wg, w.tape - w.wg, &f, &dm);
       rc = cuda_status(cudaMemsetAsync(f.counters, 0, grid_counter_bytes(plan), st));
-      if (rc == RNN_OK) rc = cuda_status(grid_bwd_run(d->function, plan.fs, f, st));
+      if (rc == RNN_OK) {
+        cudaError_t e = grid_bwd_run(d->function, plan.fs, f, st, beside ? &dm : nullptr);
+        if (e == cudaErrorNotSupported && beside) {  // no spare CTAs after all: dR after the scan
+          (void)cudaGetLastError();
+          f.drw.nc = 0;
+          beside = false;
+          e = grid_bwd_run(d->function, plan.fs, f, st);
+        }
+        rc = cuda_status(e);
+      }
+      if (beside) dr_parts = f.drw.nc;
       break;
     }
     case RNN_PATH_ALTERNATING: {
@@ -555,7 +613,7 @@ int rnn_bwd(const rnn_dims_t* d, const void* Wx, const void* R, const void* b,
       g.dbp = (const float*)(ws + w.dbp);
       g.dbp_blocks = dbp_blocks;
     }
-    rc = cuda_status(wgrad_run(d->dtype, g, st));
+    rc = cuda_status(dr_parts > 0 ? wgrad_sum_partials(g, dr_parts, st) : wgrad_run(d->dtype, g, st));
   }
   return rc;
 }

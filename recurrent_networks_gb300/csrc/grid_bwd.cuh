@@ -18,6 +18,7 @@
 #include <cuda.h>
 
 #include "kernels.cuh"
+#include "dr_beside.cuh"
 #include "grid_place.cuh"
 #include "layout.h"
 #include "ptx.cuh"
@@ -27,14 +28,17 @@ namespace rnn {
 template <int FN, int NT, int KT>
 __global__ void __launch_bounds__(256, 1)
     grid_bwd_kernel(const __grid_constant__ CUtensorMap tapemap, const __grid_constant__ CUtensorMap dstmap,
-                    FusedArgs a) {
+                    FusedArgs a, const __grid_constant__ UmmaMaps dmaps) {
   constexpr int G = FnInfo<FN>::G, S = FnInfo<FN>::S, P = FnInfo<FN>::P, K = P + S;
   constexpr int BC = 8 * NT;
   const int C = a.C, U = a.U, D = a.D, KS = a.KS, TT = a.T, N = a.N, B = a.B;
   const int KG = G * D, KB = KG + 8;
   extern __shared__ __align__(128) unsigned char smem[];
   const int2 place = grid_place(a, C, (int*)smem);
-  if (place.x < 0) return;  // a spare CTA of a die-placed launch
+  if (place.x < 0) {  // a spare CTA: dR beside the scan, when asked for
+    dr_beside(a, dmaps, G, smem);
+    return;
+  }
   const int rank = place.y, grp = place.x, groups = N * ((B + BC - 1) / BC);
   const int n = grp % N;
   const int b0 = (grp / N) * BC;
@@ -283,12 +287,18 @@ __global__ void __launch_bounds__(256, 1)
       for (int b = 0; b < nb; ++b) v += dbs[(g * BC + b) * U + u];
       a.dbp[(((size_t)(grp / N) * G + g) * N + n) * D + u0 + u] = v;
     }
+  if (a.drw.nc > 0) {  // the scan is over: take the dR units still left
+    __syncthreads();   // every thread is done with the shared memory the worker reuses
+    dr_beside(a, dmaps, G, smem);
+  }
 }
 
+// dmaps: the dR operand maps when a.drw.nc > 0 (dR beside the scan, which
+// needs one CTA per SM: cudaErrorNotSupported, before any launch, otherwise).
 template <int FN>
-cudaError_t grid_bwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream_t st) {
+cudaError_t grid_bwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream_t st, const UmmaMaps* dmaps) {
   constexpr int S = FnInfo<FN>::S, K = FnInfo<FN>::P + FnInfo<FN>::S;
-  void (*k)(const CUtensorMap, const CUtensorMap, FusedArgs) = nullptr;
+  void (*k)(const CUtensorMap, const CUtensorMap, FusedArgs, const UmmaMaps) = nullptr;
 #define RNN_GRID_BWD_PICK(NT_, KT_) \
   if (sh.NT == NT_ && sh.KT == KT_) k = grid_bwd_kernel<FN, NT_, KT_>;
   RNN_GRID_BWD_PICK(1, 8) RNN_GRID_BWD_PICK(1, 16) RNN_GRID_BWD_PICK(1, 24) RNN_GRID_BWD_PICK(1, 32)
@@ -329,6 +339,12 @@ cudaError_t grid_bwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream
   // exactly its SMs; otherwise groups by block index
   if (args.die_of_sm && per_sm == 1 && args.launch_ctas == sms) cfg.gridDim = dim3(sms);
   else args.die_of_sm = nullptr;
+  // dR beside the scan runs on the spare CTAs of a launch of one CTA per SM
+  if (args.drw.nc > 0) {
+    if (per_sm != 1 || !dmaps || sms <= groups * sh.C || sh.smem < (size_t)DRB_MIN_SMEM) return cudaErrorNotSupported;
+    cfg.gridDim = dim3(sms);
+  }
+  args.groups = groups;
   cfg.blockDim = dim3(sh.warps * 32);
   cfg.dynamicSmemBytes = sh.smem;
   cfg.stream = st;
@@ -337,7 +353,9 @@ cudaError_t grid_bwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, k, tmap, dmap, args);
+  UmmaMaps none;
+  memset(&none, 0, sizeof(none));
+  e = cudaLaunchKernelEx(&cfg, k, tmap, dmap, args, dmaps ? *dmaps : none);
   note_launch();
   return e;
 }

@@ -2,5 +2,5 @@
 #include "grid_bwd.cuh"
 
 namespace rnn {
-template cudaError_t grid_bwd_launch<SLSTM_LS>(const FusedShape&, const FusedArgs&, cudaStream_t);
+template cudaError_t grid_bwd_launch<SLSTM_LS>(const FusedShape&, const FusedArgs&, cudaStream_t, const UmmaMaps*);
 }  // namespace rnn

@@ -12,6 +12,7 @@ namespace rnn {
 __device__ __forceinline__ int2 grid_place(const FusedArgs& a, int C, int* scratch) {
   if (threadIdx.x == 0) {
     int2 p = make_int2((int)(blockIdx.x / C), (int)(blockIdx.x % C));
+    if (a.groups > 0 && (int)blockIdx.x >= a.groups * C) p = make_int2(-1, -1);  // a spare CTA
     if (a.die_of_sm) {
       unsigned sm;
       asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));

@@ -75,6 +75,9 @@ struct WgradArgs {
 // Bytes of split-K scratch the tensor-core weight-gradient pass can use.
 size_t wgrad_scratch_bytes(int B, int T, int N, int D, int G, int dtype);
 cudaError_t wgrad_run(int dtype, const WgradArgs& a, cudaStream_t st);
+// dR as the sum of `parts` fp32 partials [parts][G][N][D][D] at a.scratch
+// (added in part order), then db: for dR computed beside the backward scan.
+cudaError_t wgrad_sum_partials(const WgradArgs& a, int parts, cudaStream_t st);
 
 constexpr int FUSED_MAX_GROUP_CTR = 16;  // groups whose counter word FusedArgs::ctr_word places
 
@@ -135,6 +138,18 @@ struct FusedArgs {
   unsigned int* tickets = nullptr;
   int die_grp0[2] = {0, 0}, die_ngrp[2] = {0, 0};
   int launch_ctas = 0;  // die placement: CTAs launched (the SM count)
+  int groups = 0;       // grid mode: the launch's batch groups (CTAs past groups x C are spare)
+  // dR beside the backward scan (grid mode, optional, dr_beside.cuh): chunk
+  // c covers the 64-step tiles [tt_lo[c], tt_lo[c] + tt_n[c]) in the scan's
+  // order (from t = T-1 down; the last chunk holds t = 0 and the
+  // initial-state k-tiles), its fp32 partial of dR at slots + c G N D D
+  struct {
+    int nc = 0;  // chunks; 0 = off
+    int tt_lo[8] = {}, tt_n[8] = {};
+    int s0_tiles = 0;
+    float* slots = nullptr;
+    unsigned int* next = nullptr;  // the unit counter, zeroed before launch
+  } drw;
   // optional phase trace (rnn_trace): CTA 0, thread 0 writes clock64() at 8
   // phase points of steps [trace_t0, trace_t0 + trace_steps) (processing order)
   unsigned long long* trace = nullptr;
@@ -179,7 +194,10 @@ int fused_capacity(int fn, bool bwd, const FusedShape& sh);
 int device_sms();
 cudaError_t fused_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st);
 cudaError_t grid_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st);
-cudaError_t grid_bwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st);
+struct UmmaMaps;
+// dmaps: the dR operand maps when a.drw.nc > 0 (see dr_beside.cuh)
+cudaError_t grid_bwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st,
+                         const UmmaMaps* dmaps = nullptr);
 
 // Encodes a tiled TMA descriptor for a dense row-major bf16 tensor whose
 // dims[0] is innermost; box[] gives the tile. No swizzle, zero fill.

@@ -15,6 +15,8 @@ namespace rnn {
 // slack in front.
 constexpr int GRID_CTR_BLOCKS = 16;
 constexpr size_t GRID_CTR_BYTES = (size_t)(GRID_CTR_BLOCKS + 1) * 1024 + 256;
+// Chunks of steps whose dR the grid backward's spare CTAs compute beside the scan.
+constexpr int DR_BESIDE_CHUNKS = 5;
 
 // Limits of the GPU that the constraints use. The defaults are a GB300's
 // (152 SMs, 227 KB of opt-in shared memory per CTA, clusters of up to 16 CTAs

@@ -140,7 +140,7 @@ int fused_capacity(int fn, bool bwd, const FusedShape& sh) {
 template <int FN>
 cudaError_t grid_fwd_launch(const FusedShape&, const FusedArgs&, cudaStream_t);
 template <int FN>
-cudaError_t grid_bwd_launch(const FusedShape&, const FusedArgs&, cudaStream_t);
+cudaError_t grid_bwd_launch(const FusedShape&, const FusedArgs&, cudaStream_t, const UmmaMaps*);
 
 cudaError_t grid_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st) {
   switch (fn) {
@@ -153,13 +153,13 @@ cudaError_t grid_fwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaS
   return cudaErrorInvalidValue;
 }
 
-cudaError_t grid_bwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st) {
+cudaError_t grid_bwd_run(int fn, const FusedShape& sh, const FusedArgs& a, cudaStream_t st, const UmmaMaps* dmaps) {
   switch (fn) {
-    case LSTM: return grid_bwd_launch<LSTM>(sh, a, st);
-    case GRU: return grid_bwd_launch<GRU>(sh, a, st);
-    case ELMAN: return grid_bwd_launch<ELMAN>(sh, a, st);
-    case SLSTM: return grid_bwd_launch<SLSTM>(sh, a, st);
-    case SLSTM_LS: return grid_bwd_launch<SLSTM_LS>(sh, a, st);
+    case LSTM: return grid_bwd_launch<LSTM>(sh, a, st, dmaps);
+    case GRU: return grid_bwd_launch<GRU>(sh, a, st, dmaps);
+    case ELMAN: return grid_bwd_launch<ELMAN>(sh, a, st, dmaps);
+    case SLSTM: return grid_bwd_launch<SLSTM>(sh, a, st, dmaps);
+    case SLSTM_LS: return grid_bwd_launch<SLSTM_LS>(sh, a, st, dmaps);
   }
   return cudaErrorInvalidValue;
 }

@@ -352,6 +352,16 @@ static cudaError_t bgrad_launch(const WgradArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+cudaError_t wgrad_sum_partials(const WgradArgs& a, int parts, cudaStream_t st) {
+  if (a.dR) {
+    wgrad_reduce_kernel<<<2 * device_sms(), 256, 0, st>>>(a, parts);
+    note_launch();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return bgrad_launch(a, st);
+}
+
 cudaError_t wgrad_run(int dtype, const WgradArgs& a, cudaStream_t st) {
   if (dtype != 1 || a.D % 8 || !a.dR) return dtype == 1 ? wgrad_launch<__nv_bfloat16>(a, st) : wgrad_launch<float>(a, st);
   if (wgrad_umma_supported(a)) {  // tcgen05 GEMM, accumulator in tensor memory

@@ -24,46 +24,11 @@
 // split-K partials that wgrad_reduce_kernel sums in a fixed order.
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "umma.cuh"
 
 namespace rnn {
 
 namespace {
-
-constexpr int UM_TILE = 128, UM_BK = 64;           // tile rows (i), k-rows per stage
-constexpr int UM_BOX_BYTES = 64 * 128;              // one 64 x 64 bf16 box, 128-byte rows
-
-// The tile width for head size D: the columns rounded up to 64, at most 256.
-inline int um_bn(int D) { return D <= 128 ? 128 : (D <= 192 ? 192 : 256); }
-
-template <int BN>
-struct UmCfg {
-  static constexpr int NB = BN / 64;                            // B boxes per stage
-  static constexpr int STAGE_BYTES = (2 + NB) * UM_BOX_BYTES;   // A: two 64-unit halves, B: NB
-  static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;  // + alignment slack, barriers
-  static constexpr int TCOLS = BN <= 128 ? 128 : 256;           // tensor-memory columns (a power of two)
-};
-
-__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t addr) {
-  // start address, leading byte offset = stride of the 64-unit halves (8 KB),
-  // stride byte offset = stride of the 8-row groups (1 KB), version 1,
-  // layout: 128-byte swizzle
-  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)(UM_BOX_BYTES >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         (1ull << 46) | (2ull << 61);
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t tmem, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t accum) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem),
-      "l"(ad), "l"(bd), "r"(idesc), "r"(accum)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 template <int BN, bool BLK>
 __global__ void __launch_bounds__(128, 1)
@@ -251,66 +216,74 @@ int wgrad_umma_splits(int B, int T, int N, int D, int G) {
   return best;
 }
 
-cudaError_t wgrad_umma_run(const WgradArgs& a, int& splits, cudaStream_t st) {
-  const int tpb = (a.T + UM_BK - 1) / UM_BK;
-  const int s0_tiles = a.s0 ? (a.B + UM_BK - 1) / UM_BK : 0;
-  const int Q = a.B * tpb + s0_tiles;
-  const int kps = (Q + splits - 1) / splits;
-  splits = (Q + kps - 1) / kps;  // every split has at least one k-tile
-  CUtensorMap amain, as0, bmain, bs0;
+cudaError_t umma_encode_maps(const WgradArgs& a, int bn, bool blk, UmmaMaps* m) {
   const unsigned long long D = a.D, N = a.N, T = a.T, B = a.B, G = a.G;
-  const int bn = um_bn(a.D);
   // With D a multiple of 64, one box per operand and stage gathers the tile's
   // 64-unit slabs (dimension 2, 128 bytes apart in memory) into consecutive
   // 8 KB blocks: 2 TMA copies per stage instead of 2 + BN / 64.
-  const bool blk = a.D % 64 == 0;
   if (blk) {
     const unsigned int box_a[5] = {64, UM_BK, 2, 1, 1};
     const unsigned int box_b[5] = {64, UM_BK, (unsigned)bn / 64, 1, 1};
     {  // states[0] (B, T, N, D) as (unit, t, slab, n, b)
       const unsigned long long dims[5] = {64, T, D / 64, N, B};
       const unsigned long long str[4] = {N * D * 2, 128, D * 2, T * N * D * 2};
-      cudaError_t e = encode_tensor_map_sw128_strided(&amain, a.states, 5, dims, str, box_a);
+      cudaError_t e = encode_tensor_map_sw128_strided(&m->amain, a.states, 5, dims, str, box_a);
       if (e != cudaSuccess) return e;
     }
     {  // states0[0] (B, N, D) as (unit, b, slab, n)
       const unsigned long long dims[5] = {64, B, D / 64, N, 1};
       const unsigned long long str[4] = {N * D * 2, 128, D * 2, B * N * D * 2};
-      cudaError_t e = encode_tensor_map_sw128_strided(&as0, a.s0 ? a.s0 : a.states, 5, dims, str, box_a);
+      cudaError_t e = encode_tensor_map_sw128_strided(&m->as0, a.s0 ? a.s0 : a.states, 5, dims, str, box_a);
       if (e != cudaSuccess) return e;
     }
     {  // dr (B, T, G, N, D) as (unit, t, slab, g n, b), and as (unit, b, slab, g n, t)
       const unsigned long long dims_t[5] = {64, T, D / 64, G * N, B};
       const unsigned long long str_t[4] = {G * N * D * 2, 128, D * 2, T * G * N * D * 2};
-      cudaError_t e = encode_tensor_map_sw128_strided(&bmain, a.dr, 5, dims_t, str_t, box_b);
+      cudaError_t e = encode_tensor_map_sw128_strided(&m->bmain, a.dr, 5, dims_t, str_t, box_b);
       if (e != cudaSuccess) return e;
       const unsigned long long dims_b[5] = {64, B, D / 64, G * N, T};
       const unsigned long long str_b[4] = {T * G * N * D * 2, 128, D * 2, G * N * D * 2};
-      e = encode_tensor_map_sw128_strided(&bs0, a.dr, 5, dims_b, str_b, box_b);
+      e = encode_tensor_map_sw128_strided(&m->bs0, a.dr, 5, dims_b, str_b, box_b);
       if (e != cudaSuccess) return e;
     }
   } else {
     {  // states[0] as (D, N, T, B): rows of 64 steps of one batch row
       const unsigned long long dims[5] = {D, N, T, B, 1};
       const unsigned int box[5] = {64, 1, UM_BK, 1, 1};
-      cudaError_t e = encode_tensor_map_sw128(&amain, a.states, 5, dims, box);
+      cudaError_t e = encode_tensor_map_sw128(&m->amain, a.states, 5, dims, box);
       if (e != cudaSuccess) return e;
     }
     {  // states0[0] as (D, N, B): rows over the batch
       const unsigned long long dims[5] = {D, N, B, 1, 1};
       const unsigned int box[5] = {64, 1, UM_BK, 1, 1};
-      cudaError_t e = encode_tensor_map_sw128(&as0, a.s0 ? a.s0 : a.states, 5, dims, box);
+      cudaError_t e = encode_tensor_map_sw128(&m->as0, a.s0 ? a.s0 : a.states, 5, dims, box);
       if (e != cudaSuccess) return e;
     }
     {  // dr as (D, N, G, T, B): rows of 64 steps, or rows over the batch at t = 0
       const unsigned long long dims[5] = {D, N, G, T, B};
       const unsigned int box_t[5] = {64, 1, 1, UM_BK, 1};
       const unsigned int box_b[5] = {64, 1, 1, 1, UM_BK};
-      cudaError_t e = encode_tensor_map_sw128(&bmain, a.dr, 5, dims, box_t);
+      cudaError_t e = encode_tensor_map_sw128(&m->bmain, a.dr, 5, dims, box_t);
       if (e != cudaSuccess) return e;
-      e = encode_tensor_map_sw128(&bs0, a.dr, 5, dims, box_b);
+      e = encode_tensor_map_sw128(&m->bs0, a.dr, 5, dims, box_b);
       if (e != cudaSuccess) return e;
     }
+  }
+  return cudaSuccess;
+}
+
+cudaError_t wgrad_umma_run(const WgradArgs& a, int& splits, cudaStream_t st) {
+  const int tpb = (a.T + UM_BK - 1) / UM_BK;
+  const int s0_tiles = a.s0 ? (a.B + UM_BK - 1) / UM_BK : 0;
+  const int Q = a.B * tpb + s0_tiles;
+  const int kps = (Q + splits - 1) / splits;
+  splits = (Q + kps - 1) / kps;  // every split has at least one k-tile
+  const int bn = um_bn(a.D);
+  const bool blk = a.D % 64 == 0;
+  UmmaMaps m;
+  {
+    const cudaError_t e = umma_encode_maps(a, bn, blk, &m);
+    if (e != cudaSuccess) return e;
   }
   void (*k)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, WgradArgs, int, int, int, int) =
       blk ? (bn == 128 ? wgrad_umma_kernel<128, true> : bn == 192 ? wgrad_umma_kernel<192, true> : wgrad_umma_kernel<256, true>)
@@ -319,7 +292,7 @@ cudaError_t wgrad_umma_run(const WgradArgs& a, int& splits, cudaStream_t st) {
   cudaError_t e = set_smem_attr((const void*)k, (size_t)smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((a.D + bn - 1) / bn, (a.D + UM_TILE - 1) / UM_TILE, a.G * a.N * splits);
-  k<<<grid, 128, smem, st>>>(amain, as0, bmain, bs0, a, splits, kps, tpb, s0_tiles);
+  k<<<grid, 128, smem, st>>>(m.amain, m.as0, m.bmain, m.bs0, a, splits, kps, tpb, s0_tiles);
   note_launch();
   return cudaGetLastError();
 }
