@@ -323,11 +323,14 @@ cudaError_t grid_bwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream
   } else {
     dmap = tmap;
   }
-  cudaError_t e = set_smem_attr((const void*)k, (size_t)sh.smem);
+  // dR beside the scan needs room for its TMA ring: the launch then holds at
+  // least that much shared memory (the scan uses its own part of it)
+  const size_t smem = a.drw.nc > 0 && sh.smem < (size_t)DRB_MIN_SMEM ? (size_t)DRB_MIN_SMEM : (size_t)sh.smem;
+  cudaError_t e = set_smem_attr((const void*)k, smem);
   if (e != cudaSuccess) return e;
   const int groups = a.N * ((a.B + (int)BC - 1) / (int)BC);
   int per_sm = 0, dev = 0, sms = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, sh.warps * 32, sh.smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, sh.warps * 32, smem);
   if (e != cudaSuccess) return e;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -341,12 +344,12 @@ cudaError_t grid_bwd_launch(const FusedShape& sh, const FusedArgs& a, cudaStream
   else args.die_of_sm = nullptr;
   // dR beside the scan runs on the spare CTAs of a launch of one CTA per SM
   if (args.drw.nc > 0) {
-    if (per_sm != 1 || !dmaps || sms <= groups * sh.C || sh.smem < (size_t)DRB_MIN_SMEM) return cudaErrorNotSupported;
+    if (per_sm != 1 || !dmaps || sms <= groups * sh.C) return cudaErrorNotSupported;
     cfg.gridDim = dim3(sms);
   }
   args.groups = groups;
   cfg.blockDim = dim3(sh.warps * 32);
-  cfg.dynamicSmemBytes = sh.smem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;

@@ -276,6 +276,27 @@ def test_grid_die_placement_changes_nothing(monkeypatch):
     check_grads(fn, inp, outs["1"][2:])
 
 
+def test_grid_dr_beside_the_scan(monkeypatch):
+    """dR computed by the grid backward's spare CTAs beside the scan (chunks of
+    64-step tiles, a ragged last tile, the initial-state rows, two heads and two
+    batch blocks) matches the oracle, and the dR GEMM after the scan within a
+    bf16 rounding; the other gradients do not depend on where dR is computed."""
+    _restrict(monkeypatch, dict(C=16, NT=2))
+    fn, B, T, N, D = "lstm", 20, 16 * 64 + 37, 2, 256
+    inp = _inputs(fn, (B, T, N, D), torch.bfloat16, seed=4545)
+    st, last, tape = run_fwd(fn, inp, "grid")
+    got = {}
+    for mode in ("1", "0"):
+        monkeypatch.setenv("RNN_DR_BESIDE", mode)
+        got[mode] = run_bwd(fn, inp, st, tape, "grid")
+    check_grads(fn, inp, got["1"])
+    for name, a, b in zip(("dWx", "db", "dstates0"), (got["1"][0], got["1"][2], got["1"][3]),
+                          (got["0"][0], got["0"][2], got["0"][3])):
+        assert torch.equal(a, b), f"{name} depends on where dR is computed"
+    a, b = got["1"][1].float(), got["0"][1].float()
+    assert (a - b).abs().max().item() <= 1e-2 * b.abs().max().item()
+
+
 def test_grid_path_in_a_cuda_graph(monkeypatch):
     """A forward and backward on the grid kernels captured into a CUDA graph
     and replayed give the eager results bit for bit: with the workspace's
