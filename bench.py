@@ -175,9 +175,10 @@ def algorithmic(w, fn, esize):
 
 
 KERNEL_SOURCES = {
-    "fused_fwd_kernel": ["fused_fwd.cuh", "cells.cuh", "ptx.cuh", "layout.h", "kernels.cuh"],
+    "fused_fwd_kernel": ["fused_fwd.cuh", "cells.cuh", "ptx.cuh", "layout.h", "kernels.cuh", "grid_place.cuh"],
     "fused_bwd_kernel": ["fused_bwd.cuh", "cells.cuh", "ptx.cuh", "layout.h", "kernels.cuh"],
-    "grid_bwd_kernel": ["grid_bwd.cuh", "cells.cuh", "ptx.cuh", "layout.h", "kernels.cuh"],
+    "grid_bwd_kernel": ["grid_bwd.cuh", "cells.cuh", "ptx.cuh", "layout.h", "kernels.cuh", "grid_place.cuh",
+                        "dr_beside.cuh", "umma.cuh"],
 }
 
 
