@@ -316,7 +316,8 @@ static bool dr_beside_setup(const rnn_dims_t* d, const Plan& plan, const Sizes& 
   const char* env = getenv("RNN_DR_BESIDE");
   if ((env && env[0] == '0') || !dR || d->dtype != RNN_BF16 || d->D % 64 || d->D < 256) return false;
   const int nt = (d->T + UM_BK - 1) / UM_BK;
-  if (nt < 16 || plan.groups * plan.fs.C + 8 > device_sms()) return false;
+  // the worker runs on four warps (TMEM lanes and a 128-thread barrier)
+  if (nt < 16 || plan.fs.warps < 4 || plan.groups * plan.fs.C + 8 > device_sms()) return false;
   if ((size_t)DR_BESIDE_CHUNKS * z.r * sizeof(float) > slot_bytes) return false;
   static const int weight[DR_BESIDE_CHUNKS] = {6, 4, 3, 2, 1};
   int left = nt, hi = nt;

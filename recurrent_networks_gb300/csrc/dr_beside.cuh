@@ -67,7 +67,12 @@ __device__ __forceinline__ bool worker_sync_or(bool flag) {
 // reuse from its second KB on (every thread is done with it).
 static __device__ __noinline__ void dr_beside(const FusedArgs& a, const UmmaMaps& mp, int G, unsigned char* smem) {
   const int tid = threadIdx.x;
-  if (tid >= 128 || a.drw.nc <= 0) return;
+  if (a.drw.nc <= 0) return;
+  if (blockDim.x < 128) {  // the host asks for workers only with four warps or more
+    if (tid == 0 && a.status) atomicExch(a.status, 1u);
+    return;
+  }
+  if (tid >= 128) return;
   uint32_t smem_bytes;
   asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(smem_bytes));
   const int warp = tid >> 5, lane = tid & 31;
