@@ -276,13 +276,15 @@ def test_grid_die_placement_changes_nothing(monkeypatch):
     check_grads(fn, inp, outs["1"][2:])
 
 
-def test_grid_dr_beside_the_scan(monkeypatch):
+@pytest.mark.parametrize("fn", ["lstm", "gru"])
+def test_grid_dr_beside_the_scan(fn, monkeypatch):
     """dR computed by the grid backward's spare CTAs beside the scan (chunks of
     64-step tiles, a ragged last tile, the initial-state rows, two heads and two
-    batch blocks) matches the oracle, and the dR GEMM after the scan within a
-    bf16 rounding; the other gradients do not depend on where dR is computed."""
+    batch blocks; GRU's recurrent-branch gradient in its own buffer) matches the
+    oracle, and the dR GEMM after the scan within a bf16 rounding; the other
+    gradients do not depend on where dR is computed."""
     _restrict(monkeypatch, dict(C=16, NT=2))
-    fn, B, T, N, D = "lstm", 20, 16 * 64 + 37, 2, 256
+    B, T, N, D = 20, 16 * 64 + 37, 2, 256
     inp = _inputs(fn, (B, T, N, D), torch.bfloat16, seed=4545)
     st, last, tape = run_fwd(fn, inp, "grid")
     got = {}
