@@ -135,6 +135,37 @@ __global__ void __launch_bounds__(256, 1)
     const int t = TT - 1 - kk;
     const bool have_rec = kk > 0;
     RNN_TRACE(0)
+    const int sc = kk % FUSED_NS, sn_ = (kk + 1) % FUSED_NS;
+    const float* tp = (const float*)(ring + (size_t)sc * L.ring_stage);
+    const __nv_bfloat16* dstage = (const __nv_bfloat16*)(ring + (size_t)sc * L.ring_stage + L.dst_off);
+    const float* tq = (const float*)(ring + (size_t)sn_ * L.ring_stage);
+    // The first pair's tape, upstream gradients and gate activations do not
+    // depend on dh: evaluated while the step counter and the gathered dr are
+    // still outstanding (thread 0 after issuing the gather).
+    float f_pre[P], f_sp[S], f_dsn[S], f_act[CELL_BWD_ACT];
+    auto first_pair_inputs = [&]() {
+      if (kk < TT && tid < nb * U) {
+        mbar_wait_bounded<false>(ring_bar0 + 8 * sc, (kk / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
+        if (t > 0)
+          mbar_wait_bounded<false>(ring_bar0 + 8 * sn_, ((kk + 1) / FUSED_NS) & 1, a.wait_limit_ns, a.status,
+                                   failed);
+        const int b = c_b0, u = c_u0;
+        float f_sn[S];
+#pragma unroll
+        for (int k2 = 0; k2 < P; ++k2) f_pre[k2] = tp[(b * K + k2) * U + u];
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+          f_sn[s] = tp[(b * K + P + s) * U + u];
+          f_sp[s] = t > 0 ? tq[(b * K + P + s) * U + u] : s0s[(s * BC + b) * U + u];
+          float d = ds[(s * BC + b) * U + u];
+          if (has_dst) d += __bfloat162float(dstage[(s * BC + b) * U + u]);
+          if (dlast && t == TT - 1) d += __bfloat162float(dlast[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u]);
+          f_dsn[s] = d;
+        }
+        cell_bwd_act<FN, true>(f_pre, f_sp, f_sn, f_act);
+      }
+    };
+    if (!have_rec) first_pair_inputs();
     if (have_rec) {
       // gather dr_{t+1} of the whole group, multiply by the resident rows of R
       // one thread observes the group's step counter, then pulls the nb rows
@@ -152,6 +183,7 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
       RNN_TRACE(1)
+      first_pair_inputs();
       mbar_wait_bounded<false>(gath_bar, gath_par, a.wait_limit_ns, a.status, failed);
       gath_par ^= 1u;
       RNN_TRACE(2)
@@ -212,31 +244,32 @@ __global__ void __launch_bounds__(256, 1)
 
     // ---- the cell derivative of step t -----------------------------------------
     if (tid == 0 && kk + FUSED_NS - 1 < TT) issue_stage(kk + FUSED_NS - 1);
-    const int sc = kk % FUSED_NS, sn_ = (kk + 1) % FUSED_NS;
-    const float* tp = (const float*)(ring + (size_t)sc * L.ring_stage);
-    const __nv_bfloat16* dstage = (const __nv_bfloat16*)(ring + (size_t)sc * L.ring_stage + L.dst_off);
-    const float* tq = (const float*)(ring + (size_t)sn_ * L.ring_stage);
-    if (tid < nb * U) {
-      mbar_wait_bounded<false>(ring_bar0 + 8 * sc, (kk / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
-      if (t > 0)
-        mbar_wait_bounded<false>(ring_bar0 + 8 * sn_, ((kk + 1) / FUSED_NS) & 1, a.wait_limit_ns, a.status, failed);
-    }
     RNN_TRACE(4)
     __nv_bfloat16* dxw = dx + ((size_t)(kk & 1) * groups + grp) * BC * KG;
     // pair e = b U + u, stepped without a division
     for (int e = tid, b = c_b0, u = c_u0; e < nb * U; e += nthr, b += c_db + (u + c_du >= U), u = u + c_du >= U ? u + c_du - U : u + c_du) {
       const bool first = e == tid;
-      float pre[P], sp[S], sn[S], dsn[S], dxg[G], dr[G], dsp[S];
+      float pre[P], sp[S], sn[S], dsn[S], dxg[G], dr[G], dsp[S], act[CELL_BWD_ACT];
+      if (first) {  // evaluated at the start of the step
 #pragma unroll
-      for (int k2 = 0; k2 < P; ++k2) pre[k2] = tp[(b * K + k2) * U + u];
+        for (int k2 = 0; k2 < P; ++k2) pre[k2] = f_pre[k2];
 #pragma unroll
-      for (int s = 0; s < S; ++s) {
-        sn[s] = tp[(b * K + P + s) * U + u];
-        sp[s] = t > 0 ? tq[(b * K + P + s) * U + u] : s0s[(s * BC + b) * U + u];
-        float d = ds[(s * BC + b) * U + u];
-        if (has_dst) d += __bfloat162float(dstage[(s * BC + b) * U + u]);
-        if (dlast && t == TT - 1) d += __bfloat162float(dlast[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u]);
-        dsn[s] = d;
+        for (int s = 0; s < S; ++s) sp[s] = f_sp[s], dsn[s] = f_dsn[s];
+#pragma unroll
+        for (int k2 = 0; k2 < CELL_BWD_ACT; ++k2) act[k2] = f_act[k2];
+      } else {
+#pragma unroll
+        for (int k2 = 0; k2 < P; ++k2) pre[k2] = tp[(b * K + k2) * U + u];
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+          sn[s] = tp[(b * K + P + s) * U + u];
+          sp[s] = t > 0 ? tq[(b * K + P + s) * U + u] : s0s[(s * BC + b) * U + u];
+          float d = ds[(s * BC + b) * U + u];
+          if (has_dst) d += __bfloat162float(dstage[(s * BC + b) * U + u]);
+          if (dlast && t == TT - 1) d += __bfloat162float(dlast[(((size_t)s * B + b0 + b) * N + n) * D + u0 + u]);
+          dsn[s] = d;
+        }
+        cell_bwd_act<FN, true>(pre, sp, sn, act);
       }
       if (have_rec) {  // the K-split partials, loaded together
         float part[FUSED_MAX_KS];
@@ -246,7 +279,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int k2 = 0; k2 < FUSED_MAX_KS; ++k2) dsn[0] += part[k2];
       }
-      cell_bwd<FN, true>(pre, sp, sn, dsn, dxg, dr, dsp);
+      cell_bwd_grad<FN, true>(act, pre, sp, dsn, dxg, dr, dsp);
       const size_t o = first ? o_first + (size_t)t * o_step
                              : (((size_t)(b0 + b) * TT + t) * G) * N * D + (size_t)n * D + u0 + u;
 #pragma unroll
