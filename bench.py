@@ -638,13 +638,15 @@ def main():
     # the parameter gradients dR and db, the initial-state gradients and the
     # last states (the forward alone: the states and the last states). The
     # per-step states and dWx stay on the device, where the neighbouring layers
-    # of a model consume them. The copies of one step overlap the compute of
-    # the neighbouring steps (two buffer sets, a host-to-device and a
-    # device-to-host stream), as a training loop prefetching its next batch
-    # would run it.
+    # of a model consume them. The copies overlap the compute, as a training
+    # loop prefetching its batches would run them: the inputs in three buffer
+    # sets (a step's inputs are copied while the two steps before it compute,
+    # so one slow host-to-device copy does not stall the next step), the
+    # outputs in two, on a host-to-device and a device-to-host stream.
     if not args.no_e2e:
-        hin = [{k: v.pin_memory() for k, v in host.items() if v is not None} for _ in range(2)]
-        dev_in = [{k: torch.empty_like(v, device=dev) for k, v in hin[0].items()} for _ in range(2)]
+        NIN = 3
+        hin = [{k: v.pin_memory() for k, v in host.items() if v is not None} for _ in range(NIN)]
+        dev_in = [{k: torch.empty_like(v, device=dev) for k, v in hin[0].items()} for _ in range(NIN)]
         out0 = [states, last] + ([dWx, dR, db, ds0] if backward else [])
         outs = [out0, [torch.empty_like(o) for o in out0]]
         read = [1, 3, 4, 5] if backward else [0, 1]  # which outputs are the step's result read back
@@ -653,34 +655,35 @@ def main():
         d2h = sum(out0[r].numel() * out0[r].element_size() for r in read)
         cs = torch.cuda.current_stream()
         hs, ds = torch.cuda.Stream(), torch.cuda.Stream()
-        ev_h2d = [torch.cuda.Event() for _ in range(2)]
+        ev_h2d = [torch.cuda.Event() for _ in range(NIN)]
+        ev_free = [torch.cuda.Event() for _ in range(NIN)]  # the compute is done with an input set
         ev_done = [torch.cuda.Event() for _ in range(2)]
         ev_out = [torch.cuda.Event() for _ in range(2)]
-        for i in range(2):
-            ev_done[i].record(cs)
-            ev_out[i].record(cs)
+        for e in ev_free + ev_done + ev_out:
+            e.record(cs)
 
         def e2e_step(k):
-            i = k % 2
+            i, j = k % NIN, k % 2
             with torch.cuda.stream(hs):
-                hs.wait_event(ev_done[i])  # the compute of step k-2 is done with dev_in[i]
+                hs.wait_event(ev_free[i])  # the compute of step k-3 is done with dev_in[i]
                 for key, v in hin[i].items():
                     dev_in[i][key].copy_(v, non_blocking=True)
                 ev_h2d[i].record(hs)
             cs.wait_event(ev_h2d[i])
-            cs.wait_event(ev_out[i])  # step k-2's outputs have reached the host
-            o = outs[i]
+            cs.wait_event(ev_out[j])  # step k-2's outputs have reached the host
+            o = outs[j]
             x = dev_in[i]
             _lib.rnn_fwd(dims, x["Wx"], x["R"], x["b"], x["states0"], o[0], o[1], tape, ws)
             if backward:
                 _lib.rnn_bwd(dims, x["Wx"], x["R"], x["b"], x["states0"], o[0], tape, x["dstates"], None,
                              o[2], o[3], o[4], o[5], ws)
-            ev_done[i].record(cs)
+            ev_free[i].record(cs)
+            ev_done[j].record(cs)
             with torch.cuda.stream(ds):
-                ds.wait_event(ev_done[i])
-                for r, t_host in zip(read, hout[i]):
+                ds.wait_event(ev_done[j])
+                for r, t_host in zip(read, hout[j]):
                     t_host.copy_(o[r], non_blocking=True)
-                ev_out[i].record(ds)
+                ev_out[j].record(ds)
 
         for k in range(args.warmup):
             e2e_step(k)
@@ -705,8 +708,9 @@ def main():
                          "copies": "every step: all inputs host->device; the result device->host: "
                                    + ("dR, db, dstates0 and the last states" if backward else
                                       "the states and the last states")
-                                   + " (pinned), overlapped with the neighbouring steps' compute on two copy "
-                                     "streams; the per-step states and dWx stay on the device"}
+                                   + " (pinned), overlapped with the compute on two copy streams (inputs "
+                                     "copied up to two steps ahead, three input buffer sets); the per-step "
+                                     "states and dWx stay on the device"}
 
     # ---- the oracle on the host cores (rank 0, N=1 only), bounded sample
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
