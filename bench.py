@@ -121,7 +121,7 @@ def proj_bench(args, w, fn, dev, _lib):
 def phase_trace(step_fn, backward, T):
     """Median clock64 cycles between the phase points of the persistent
     kernels (CTA 0, thread 0), over up to 200 steps after the first 10.
-    Point 11 of the forward kernels (the states and tape stores issued) is
+    Point 11 of the forward kernels (the step's tail: states and tape stores) is
     reported against point 7; points 8-10 (inside the cell) are reported when
     a kernel build records them."""
     from recurrent_networks_gb300 import _lib

@@ -236,13 +236,16 @@ int rnn_profile_events(int which, void *before, void *after);
  * (the backward processes t = T-1 first). Forward phases: 0 step start,
  * 1 h_{t-1} available, 2 partial products written, 3 after the CTA barrier,
  * 4 Wx[t] staged, 5 cell update done, 6 after the CTA barrier, 7 h_t sent,
- * 11 the states and tape stores issued (points 8-10 are not recorded: inside
- * the cell's loop they cost up to a tenth of the forward step).
- * Cluster backward phases: 0 step start, 1 partial dh available, 2 tape
- * staged, 3 cell derivative done, 4 after the CTA barrier, 5 partial products
- * computed, 6 partials sent. Grid backward phases: 0 step start, 1 step
- * counter reached, 2 dr gathered, 3 dh reduced, 4 tape staged, 5 cell
- * derivative done, 6 published. Plain forward: 0 step start, 1 products
+ * 11 the step's tail done (the states and tape stores issued; thread 0 of the
+ * grid kernel issues its own at the next step, after that step's pull)
+ * (points 8-10 are not recorded: inside the cell's loop they cost up to a
+ * tenth of the forward step).
+ * Cluster backward phases: 0 step start, 1 tape staged and the gate
+ * activations evaluated, 2 partial dh available, 3 cell derivative done, 4
+ * after the CTA barrier, 5 partial products computed, 6 partials sent. Grid
+ * backward phases: 0 step start, 1 step counter reached and the gather of dr
+ * issued, 2 the first pair's tape and activations evaluated and dr gathered,
+ * 3 dh reduced, 4 tape staged, 5 cell derivative done, 6 published. Plain forward: 0 step start, 1 products
  * written, 2 after the CTA barrier, 5 cell inputs loaded, 6 cell done, 3
  * outputs stored, 4 after the CTA barrier. Plain backward: 0 step start, 1
  * cell derivative done, 2 after the CTA barrier, 3 products written, 4 after

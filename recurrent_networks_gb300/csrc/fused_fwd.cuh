@@ -201,6 +201,32 @@ __global__ void __launch_bounds__(256, 1)
     rbar1 = mapa_shared(full_bar0 + 8, (uint32_t)peer);
   }
 
+  float prk[FUSED_PPT][P];  // pre-activations kept for the tape, written after the exchange
+  // the states and tape of a step, off the exchange's critical path
+  auto store_pair_outputs = [&]() {
+#pragma unroll
+    for (int kp = 0; kp < FUSED_PPT; ++kp) {
+      const int e = tid + kp * nthr;
+      if (e >= nb * U) break;
+      if (st_ptr[kp]) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) st_ptr[kp][s * st_sstride] = __float2bfloat16_rn(csr[kp][s]);
+        st_ptr[kp] += (size_t)N * D;
+      }
+      if (tp_ptr[kp]) {
+        float* tp = tp_ptr[kp];
+#pragma unroll
+        for (int k2 = 0; k2 < P; ++k2) tp[k2 * D] = prk[kp][k2];
+#pragma unroll
+        for (int s = 0; s < S; ++s) tp[(P + s) * D] = csr[kp][s];
+        tp_ptr[kp] += tp_tstride;
+      }
+    }
+  };
+  // the grid variant's thread 0 observes the step counter: it writes its own
+  // pairs' states and tape of step t - 1 after issuing step t's pull
+  const bool defer_stores = GRIDX && tid == 0;
+
   const bool tracer = a.trace && grp == 0 && rank == 0 && tid == 0;
 #define RNN_TRACE(k)                                                                    \
   if (tracer && t >= a.trace_t0 && t < a.trace_t0 + a.trace_steps)                      \
@@ -225,6 +251,7 @@ __global__ void __launch_bounds__(256, 1)
             for (int b = 0; b < nb; ++b)
               bulk_load_global(smem_u32(hbuf + p * HB + b * RS), src + (size_t)b * D, (uint32_t)(D * 2), full_bar0);
           }
+          store_pair_outputs();  // step t - 1's, while the rows are in flight
         }
         mbar_wait_bounded<false>(full_bar0, ph0, a.wait_limit_ns, a.status, failed);
         ph0 ^= 1u;
@@ -323,7 +350,6 @@ __global__ void __launch_bounds__(256, 1)
     // ---- epilogue: gate assembly and cell update, one (batch row, unit) pair per thread
     const __nv_bfloat16* wxt = wxs + ws * wx_stage_elems;
     RNN_TRACE(4)
-    float prk[FUSED_PPT][P];  // pre-activations kept for the tape, written after the exchange
 #pragma unroll
     for (int kp = 0; kp < FUSED_PPT; ++kp) {
       const int e = tid + kp * nthr;
@@ -380,25 +406,9 @@ __global__ void __launch_bounds__(256, 1)
       mbar_arrive_expect_tx(wx_bar0 + 8 * ws, wxbytes);
       tma_load_5d(smem_u32(wxs + ws * wx_stage_elems), &wxmap, wx_bar0 + 8 * ws, u0, n, 0, ts, b0);
     }
-    // states and tape of this step, off the exchange's critical path
-#pragma unroll
-    for (int kp = 0; kp < FUSED_PPT; ++kp) {
-      const int e = tid + kp * nthr;
-      if (e >= nb * U) break;
-      if (st_ptr[kp]) {
-#pragma unroll
-        for (int s = 0; s < S; ++s) st_ptr[kp][s * st_sstride] = __float2bfloat16_rn(csr[kp][s]);
-        st_ptr[kp] += (size_t)N * D;
-      }
-      if (tp_ptr[kp]) {
-        float* tp = tp_ptr[kp];
-#pragma unroll
-        for (int k2 = 0; k2 < P; ++k2) tp[k2 * D] = prk[kp][k2];
-#pragma unroll
-        for (int s = 0; s < S; ++s) tp[(P + s) * D] = csr[kp][s];
-        tp_ptr[kp] += tp_tstride;
-      }
-    }
+    // states and tape of this step (thread 0 of the grid variant: at the next
+    // step, after its pull is issued)
+    if (!defer_stores || t + 1 == TT) store_pair_outputs();
     RNN_TRACE(11)
   }
 #undef RNN_TRACE
