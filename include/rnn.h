@@ -215,6 +215,26 @@ int rnn_plan_set_limits(int sms, int smem_per_cta, int max_cluster);
  * be NULL. */
 int rnn_die_layout(int *sms_die0, int *sms_die1);
 
+/* The die placement for stated measurements instead of the current device's
+ * (no GPU needed: for tests and what-if use, as rnn_plan_set_limits is for
+ * the planner). sm_lat[0..nsm) are the L2 flag round trips from the
+ * measuring CTA to every CTA of a one-CTA-per-SM launch, entry 0 being the
+ * measuring CTA itself; blk_lat[0..nblocks) the round trips between two CTAs
+ * of die 0 on each 1 KB block of the counter region (nblocks <= 16). Each set
+ * splits at the midpoint of its fastest and slowest entry when the slowest
+ * is at least 1.3 times the fastest (else the measurement is not trusted);
+ * the fast side is die 0. `groups` batch groups of C CTAs are split over the
+ * dies as evenly as fits, groups 0 .. g0-1 on die 0; each group's step
+ * counter goes in the first unused block homed on its die. Writes the SMs
+ * per die, g0 and each group's counter word offset (block index x 256), any
+ * pointer of which may be NULL. Returns RNN_OK; RNN_EUNSUPPORTED when a
+ * measurement is not trusted, no split fits or a die has too few blocks
+ * homed on it; RNN_EINVAL for groups outside 1..16, C < 1, nsm outside
+ * 2..4096, nblocks outside 1..16 or a NULL latency array. */
+int rnn_die_plan_for(int groups, int C, const unsigned long long *sm_lat, int nsm,
+                     const unsigned long long *blk_lat, int nblocks, int *sms_die0, int *sms_die1,
+                     int *groups_die0, int *ctr_words);
+
 const char *rnn_strerror(int status);
 
 /* Number of CUDA kernels this library has enqueued since it was loaded

@@ -21,7 +21,7 @@ WS_FWD, WS_BWD, WS_BWD_RECOMPUTE = 0, 1, 2
 EXPORTS = ["rnn_num_gates", "rnn_num_states", "rnn_tape_size", "rnn_workspace_size", "rnn_fwd",
            "rnn_bwd", "rnn_check_status", "rnn_plan_describe", "rnn_strerror", "rnn_kernel_launches",
            "rnn_profile_events", "rnn_bwd_noalloc", "rnn_bwd_noalloc_status", "rnn_trace",
-           "rnn_debug_inject_wait", "rnn_plan_set_limits", "rnn_die_layout"]
+           "rnn_debug_inject_wait", "rnn_plan_set_limits", "rnn_die_layout", "rnn_die_plan_for"]
 
 
 class RnnError(RuntimeError):
@@ -59,6 +59,8 @@ def load(path: str | None = None):
             lib.rnn_plan_describe.argtypes = [dp, i, ctypes.c_char_p, sz]
             lib.rnn_plan_set_limits.argtypes = [i, i, i]
             lib.rnn_die_layout.argtypes = [ctypes.POINTER(i), ctypes.POINTER(i)]
+            ull_p = ctypes.POINTER(ctypes.c_ulonglong)
+            lib.rnn_die_plan_for.argtypes = [i, i, ull_p, i, ull_p, i] + [ctypes.POINTER(i)] * 4
             lib.rnn_strerror.argtypes = [i]
             lib.rnn_strerror.restype = ctypes.c_char_p
             lib.rnn_kernel_launches.argtypes = []
@@ -162,6 +164,24 @@ def rnn_die_layout():
         return None
     _check(rc, "rnn_die_layout")
     return a.value, b.value
+
+
+def rnn_die_plan_for(groups: int, C: int, sm_lat, blk_lat):
+    """The die placement for stated L2 round trips (no GPU needed): sm_lat from
+    the measuring CTA to every CTA (entry 0 itself), blk_lat on each 1 KB
+    counter block. Returns (SMs on die 0, SMs on die 1, groups on die 0, each
+    group's counter word), or None when the measurements are not trusted or no
+    placement fits."""
+    sm = (ctypes.c_ulonglong * len(sm_lat))(*[int(v) for v in sm_lat])
+    bl = (ctypes.c_ulonglong * len(blk_lat))(*[int(v) for v in blk_lat])
+    d0, d1, g0 = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    words = (ctypes.c_int * max(1, int(groups)))()
+    rc = load().rnn_die_plan_for(int(groups), int(C), sm, len(sm_lat), bl, len(blk_lat), ctypes.byref(d0),
+                                 ctypes.byref(d1), ctypes.byref(g0), words)
+    if rc == RNN_EUNSUPPORTED:
+        return None
+    _check(rc, "rnn_die_plan_for")
+    return d0.value, d1.value, g0.value, list(words[:groups])
 
 
 def rnn_strerror(status: int) -> str:

@@ -12,6 +12,7 @@
 #include <tuple>
 #include <vector>
 
+#include "dies.h"
 #include "kernels.cuh"
 #include "plan.h"
 #include "umma.cuh"
@@ -641,6 +642,28 @@ int rnn_die_layout(int* sms_die0, int* sms_die1) {
   if (!die_counts(dev, cnt, &sms)) return RNN_EUNSUPPORTED;
   if (sms_die0) *sms_die0 = cnt[0];
   if (sms_die1) *sms_die1 = cnt[1];
+  return RNN_OK;
+}
+
+int rnn_die_plan_for(int groups, int C, const unsigned long long* sm_lat, int nsm,
+                     const unsigned long long* blk_lat, int nblocks, int* sms_die0, int* sms_die1,
+                     int* groups_die0, int* ctr_words) {
+  if (groups < 1 || groups > GRID_CTR_BLOCKS || groups > FUSED_MAX_GROUP_CTR || C < 1 || !sm_lat || nsm < 2 ||
+      nsm > 4096 || !blk_lat || nblocks < 1 || nblocks > GRID_CTR_BLOCKS)
+    return RNN_EINVAL;
+  std::vector<signed char> die(nsm);
+  int cnt[2] = {0, 0};
+  if (!classify_sms(sm_lat, nsm, die.data(), cnt)) return RNN_EUNSUPPORTED;
+  if (sms_die0) *sms_die0 = cnt[0];
+  if (sms_die1) *sms_die1 = cnt[1];
+  const int g0 = die_split_groups(groups, C, cnt);
+  signed char home[GRID_CTR_BLOCKS];
+  int words[GRID_CTR_BLOCKS];
+  if (g0 < 0 || !classify_blocks(blk_lat, nblocks, home) || !die_assign_counters(groups, g0, home, nblocks, words))
+    return RNN_EUNSUPPORTED;
+  if (groups_die0) *groups_die0 = g0;
+  if (ctr_words)
+    for (int g = 0; g < groups; ++g) ctr_words[g] = words[g];
   return RNN_OK;
 }
 

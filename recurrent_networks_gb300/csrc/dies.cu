@@ -24,11 +24,63 @@
 #include <utility>
 #include <vector>
 
+#include "dies.h"
 #include "kernels.cuh"
 #include "plan.h"
 #include "ptx.cuh"
 
 namespace rnn {
+
+// ---- the placement's decisions, from the measured round trips (host only) ----
+
+// two clusters of latencies: the split point, or 0 when the gap is too small
+// to trust (fast/slow ratio under 1.3)
+unsigned long long split_point(const unsigned long long* v, int n) {
+  if (n < 1) return 0;
+  unsigned long long lo = ~0ull, hi = 0;
+  for (int k = 0; k < n; ++k) lo = v[k] < lo ? v[k] : lo, hi = v[k] > hi ? v[k] : hi;
+  if (lo == 0 || hi * 10 < lo * 13) return 0;
+  return (lo + hi) / 2;
+}
+
+bool classify_sms(const unsigned long long* lat, int n, signed char* die, int count[2]) {
+  if (n < 2) return false;
+  const unsigned long long thr = split_point(lat + 1, n - 1);
+  if (!thr) return false;
+  count[0] = count[1] = 0;
+  for (int k = 0; k < n; ++k) {
+    die[k] = (k == 0 || lat[k] < thr) ? 0 : 1;
+    ++count[die[k]];
+  }
+  return true;
+}
+
+bool classify_blocks(const unsigned long long* lat, int n, signed char* home) {
+  const unsigned long long thr = split_point(lat, n);
+  for (int k = 0; k < n; ++k) home[k] = thr ? (lat[k] < thr ? 0 : 1) : -1;
+  return thr != 0;
+}
+
+int die_split_groups(int groups, int C, const int cnt[2]) {
+  int g0 = -1;
+  for (int k = 0; k <= groups; ++k)
+    if (k * C <= cnt[0] && (groups - k) * C <= cnt[1] && (g0 < 0 || abs(2 * k - groups) < abs(2 * g0 - groups))) g0 = k;
+  return g0;
+}
+
+bool die_assign_counters(int groups, int g0, const signed char* home, int nblocks, int* ctr_word) {
+  bool used[GRID_CTR_BLOCKS] = {};
+  if (nblocks > GRID_CTR_BLOCKS) return false;
+  for (int g = 0; g < groups; ++g) {
+    const int d = g < g0 ? 0 : 1;
+    int k = 0;
+    while (k < nblocks && (used[k] || home[k] != d)) ++k;
+    if (k == nblocks) return false;  // no free block homed on that die
+    used[k] = true;
+    ctr_word[g] = k * 256;
+  }
+  return true;
+}
 
 namespace {
 
@@ -151,15 +203,6 @@ bool capturing(cudaStream_t st) {
   return s != cudaStreamCaptureStatusNone;
 }
 
-// two clusters of latencies: the split point, or 0 when the gap is too small
-// to trust (fast/slow ratio under 1.3)
-unsigned long long split_point(std::vector<unsigned long long> v) {
-  if (v.empty()) return 0;
-  unsigned long long lo = ~0ull, hi = 0;
-  for (unsigned long long x : v) lo = x < lo ? x : lo, hi = x > hi ? x : hi;
-  if (lo == 0 || hi * 10 < lo * 13) return 0;
-  return (lo + hi) / 2;
-}
 
 cudaError_t calibrate_dies(int dev, DieState& s) {
   int sms = 0, coop = 0;
@@ -200,16 +243,14 @@ cudaError_t calibrate_dies(int dev, DieState& s) {
     cudaStreamDestroy(st);
     if (r != cudaSuccess) return r;
     if (err) return cudaErrorTimeout;
-    const unsigned long long thr = split_point(std::vector<unsigned long long>(lat.begin() + 1, lat.end()));
-    if (!thr) return cudaErrorNotSupported;
+    std::vector<signed char> die(sms);
+    int count[2] = {0, 0};
+    if (!classify_sms(lat.data(), sms, die.data(), count)) return cudaErrorNotSupported;
     signed char table[256];
     for (int i = 0; i < 256; ++i) table[i] = -1;
-    int count[2] = {0, 0};
     for (int k = 0; k < sms; ++k) {
       if (smid[k] < 0 || smid[k] > 255 || table[smid[k]] != -1) return cudaErrorNotSupported;
-      const int d = (k == 0 || lat[k] < thr) ? 0 : 1;
-      table[smid[k]] = (signed char)d;
-      ++count[d];
+      table[smid[k]] = die[k];
     }
     r = cudaMemcpyToSymbol(g_die_table, table, sizeof(table));
     if (r != cudaSuccess) return r;
@@ -277,10 +318,8 @@ bool block_homes(int dev, unsigned* region, int nblocks, cudaStream_t st, signed
       return r;
     });
     std::vector<signed char> h(nblocks, -1);
-    const unsigned long long thr = (e == cudaSuccess && !err) ? split_point(lat) : 0;
+    if (e == cudaSuccess && !err) classify_blocks(lat.data(), nblocks, h.data());
     if (e != cudaSuccess) (void)cudaGetLastError();
-    if (thr)
-      for (int k = 0; k < nblocks; ++k) h[k] = lat[k] < thr ? 0 : 1;
     it = s.homes.emplace(key, h).first;  // a failed measurement is remembered as unknown homes
   }
   for (int k = 0; k < nblocks; ++k) {
@@ -296,22 +335,12 @@ bool die_plan(int groups, int C, unsigned* ctr_region, cudaStream_t st, DiePlan*
   int dev = 0, cnt[2] = {0, 0}, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || !die_counts(dev, cnt, &sms)) return false;
   // the split of the groups over the two dies closest to even that fits
-  int g0 = -1;
-  for (int k = 0; k <= groups; ++k)
-    if (k * C <= cnt[0] && (groups - k) * C <= cnt[1] && (g0 < 0 || abs(2 * k - groups) < abs(2 * g0 - groups))) g0 = k;
+  const int g0 = die_split_groups(groups, C, cnt);
   if (g0 < 0) return false;
   signed char home[GRID_CTR_BLOCKS];
   if (!block_homes(dev, ctr_region, GRID_CTR_BLOCKS, st, home)) return false;
-  bool used[GRID_CTR_BLOCKS] = {};
   DiePlan p;
-  for (int g = 0; g < groups; ++g) {
-    const int d = g < g0 ? 0 : 1;
-    int k = 0;
-    while (k < GRID_CTR_BLOCKS && (used[k] || home[k] != d)) ++k;
-    if (k == GRID_CTR_BLOCKS) return false;  // no free block homed on that die
-    used[k] = true;
-    p.ctr_word[g] = k * 256;
-  }
+  if (!die_assign_counters(groups, g0, home, GRID_CTR_BLOCKS, p.ctr_word)) return false;
   p.table = die_table_device();
   if (!p.table) return false;
   p.grp0[0] = 0;
