@@ -103,8 +103,9 @@ bool fused_fwd_feasible(const PlanRequest& q, int C, int NT, int KT, bool allg, 
 }
 
 // Optional restriction of the search (tests and tuning sweeps): the
-// environment variables RNN_PLAN_C, RNN_PLAN_NT and RNN_PLAN_KT, when set,
-// admit only candidates with that value.
+// environment variables RNN_PLAN_C, RNN_PLAN_NT, RNN_PLAN_KT, RNN_PLAN_MT
+// (backward) and RNN_PLAN_ALLG (forward: 1 for the all-gates warp mapping),
+// when set, admit only candidates with that value.
 static bool env_admits(const char* name, int v) {
   const char* s = getenv(name);
   return !s || !*s || atoi(s) == v;
