@@ -62,3 +62,24 @@ def test_oracle_sample_is_bounded():
         rows, steps = bench.oracle_sample(w5, "lstm", 16, budget)
         assert rows >= 16 and 8 <= steps < w5["T"]
         assert 3 * 2 * 4 * 1024 * 1024 * rows * steps <= budget
+
+
+@pytest.mark.parametrize("kernel,main", [("fused_fwd_kernel", "fused_fwd.cuh"), ("fused_bwd_kernel", "fused_bwd.cuh"),
+                                         ("grid_bwd_kernel", "grid_bwd.cuh")])
+def test_traffic_record_hashes_every_source_of_its_kernel(kernel, main):
+    """A DRAM-traffic record counts as current only while the hash of its
+    kernel's sources is unchanged: that list must hold every local header the
+    kernel's code includes, directly or not, or an edit could leave a stale
+    record looking current."""
+    import os
+    import re
+    csrc = os.path.join(bench.ROOT, "recurrent_networks_gb300", "csrc")
+    seen, todo = set(), [main]
+    while todo:
+        f = todo.pop()
+        path = os.path.join(csrc, f)
+        if f in seen or not os.path.exists(path):
+            continue
+        seen.add(f)
+        todo += re.findall(r'#include\s+"([^"]+)"', open(path).read())
+    assert seen <= set(bench.KERNEL_SOURCES[kernel]), sorted(seen - set(bench.KERNEL_SOURCES[kernel]))
