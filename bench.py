@@ -384,6 +384,15 @@ def oracle_sample(w, fn, cores, budget=ORACLE_BUDGET_BASELINE):
     return rows, steps
 
 
+def workload_config(w, fn, world):
+    """The `config` both arms print: the workload and how a step is timed."""
+    return {"workload": w["name"], "function": fn, "B": w["B"], "T": w["T"], "N": w["N"], "D": w["D"],
+            "backward": w["backward"],
+            "l2": "GPU arm: flushed (256 MiB write) before every step, outside the event window; "
+                  "host arm: no flush",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, w, fn):
     from recurrent_networks_gb300.synth import workload_inputs
     cores = host_cores()
@@ -401,7 +410,7 @@ def run_reference(args, w, fn):
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": w["name"], "function": fn},
+            "data": "synthetic", "config": workload_config(w, fn, args.gpus),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -576,10 +585,8 @@ def main():
               "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
               "vs_baseline": None, "dtype": "bf16" if dtype == torch.bfloat16 else "f32",
               "data": "synthetic",
-              "config": {"workload": w["name"], "function": fn, "B": B, "T": T, "N": N, "D": D,
-                         "backward": backward, "plan_fwd": plan_f, "plan_bwd": plan_b,
-                         "l2": "flushed (256 MiB write) before every step, outside the event window",
-                         "parallelism": f"replicas x{world}", "placement": placement()},
+              "config": workload_config(w, fn, world),
+              "plan": {"fwd": plan_f, "bwd": plan_b, "placement": placement()},
               "fwd_value": fwd_value, "fwd_ms": fwd_tot / args.steps,
               "warm_l2": {"value": B * T / (warm_ms / 1e3), "ms_per_step": warm_ms, "steps": nwarm,
                           "note": "this rank, steps back to back without the flush"},
